@@ -54,10 +54,10 @@ def f32_to_f16_bits(a) -> np.ndarray:
 
 
 def gen_codes(rng: np.random.Generator, fmt: str, rows: int, cols: int) -> np.ndarray:
-    """Uniform integer codes [rows, cols] (int32): unsigned for affine, -8..7 for W4A16."""
+    """Uniform integer codes [rows, cols]: uint8 for affine, int8 in -8..7 for W4A16."""
     if fmt == "w4a16_g128":
-        return rng.integers(-8, 8, size=(rows, cols), dtype=np.int32)
-    return rng.integers(0, 1 << BITS[fmt], size=(rows, cols), dtype=np.int32)
+        return rng.integers(-8, 8, size=(rows, cols), dtype=np.int8)
+    return rng.integers(0, 1 << BITS[fmt], size=(rows, cols), dtype=np.uint8)
 
 
 def gen_scales(rng, fmt: str, rows: int, cols: int, sigma: float | None = None) -> np.ndarray:
@@ -97,7 +97,7 @@ class QMatrix:
     fmt: str
     rows: int
     cols: int
-    codes: np.ndarray | None = None      # int32 [rows, cols] for quantised formats
+    codes: np.ndarray | None = None      # uint8/int8 [rows, cols] for quantised formats
     values: np.ndarray | None = None     # float32 (f32) or uint16 bits (bf16/f16)
     scales: np.ndarray | None = None     # uint16 fp16 bits [rows, cols/G]
     biases: np.ndarray | None = None     # uint16 fp16 bits [rows, cols/G] or None

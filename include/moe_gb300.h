@@ -1,0 +1,248 @@
+/*
+ * moe_gb300.h -- C ABI of the routed-expert MoE layer over low-bit
+ * affine-quantised weights (hand-written sm_103a CUDA kernels).
+ *
+ * The layer (qwen3_5 MoE 35B-A3B family: hidden 2048, 256 experts, top-8,
+ * expert intermediate 512) is defined by these passages, cited by page title
+ * and section:
+ *   [803-gate]  "qwen3_5_moe on native CUDA with 3-bit routed experts ... #803",
+ *               comment "Progress on the 4-bit gate", paragraph "What is in it":
+ *               fp32 logits over the experts and the shared-expert gate row;
+ *               top-k by logit with ties to the lower id; weights exp(l - l_top)
+ *               over the k; the shared expert as one more slot weighted by
+ *               sigmoid(gate); the slots' fma sum rounded once; experts with a
+ *               SwiGLU epilogue.
+ *   [803-run]   same issue, Description, "What I want to run": MLX affine
+ *               quantisation in groups of 64 -- routed experts 3-bit, the rest
+ *               4-bit, router and shared-expert gate 8-bit.
+ *   [w4a16]     "Sage-1.5-W4A16" model card, "Model details" / "Recipe":
+ *               int4 symmetric weights, group 128, no zero point, fp16 compute.
+ *   [1329]      "Sage-A1.5 (qwen3_5 MoE 35B-A3B) on the XPU backend ... #1329",
+ *               Proposal: 256 experts with top-8, grouped MoE decode.
+ *   [547-win]   "Native server: --backend xpu for Nemotron on Intel Arc",
+ *               update comment: a one-row window equals the decode step bit
+ *               for bit; 512-row prefill windows.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller (for example
+ *     allocated through PyTorch).  The library never allocates device memory.
+ *   - Every call is asynchronous on the caller's cudaStream_t (0 = legacy
+ *     default stream) and returns a moe_status.  Arguments are validated on
+ *     the host before any launch; on an error nothing is launched and
+ *     moe_last_error() names the offending argument or format.
+ *   - Matrices are row-major [rows, cols] = [out, in]; quantisation groups run
+ *     along cols (the reduction dimension).
+ *   - Activations are bf16 or fp16 ([T, hidden]); internal arithmetic is fp32.
+ *   - Pointers must be 16-byte aligned.
+ *   - Scratch lives in a caller-provided workspace (moe_workspace_bytes);
+ *     initialise it once with moe_workspace_init.  Calls that share a
+ *     workspace must be ordered on one stream.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* null pointer, bad shape, k > E, ... */
+  MOE_ERR_UNSUPPORTED_FORMAT = 2,  /* a width/format this library does not read */
+  MOE_ERR_WORKSPACE = 3,           /* workspace missing or too small */
+  MOE_ERR_CUDA = 4,                /* a CUDA runtime call failed */
+  MOE_ERR_TIMEOUT = 5,             /* a bounded device-side wait gave up */
+  MOE_ERR_MISALIGNED = 6           /* a pointer is not 16-byte aligned */
+} moe_status;
+
+/* Storage formats.  Quantised formats hold packed codes in little-endian
+ * uint32 words plus fp16 scales [rows, cols/G] (and fp16 biases for affine):
+ *   AFFINE8_G64  MLX affine 8-bit, 4 codes per word, code i at bits [8i, 8i+8)
+ *   AFFINE4_G64  MLX affine 4-bit, 8 codes per word, code i at bits [4i, 4i+4)
+ *   AFFINE3_G64  MLX affine 3-bit: each row is one LSB-first bit stream, code
+ *                c at stream bits [3c, 3c+3) (codes may straddle two words;
+ *                32 codes fill 3 words exactly)
+ *     affine dequantisation: w = scale * q + bias, q unsigned   [803-run]
+ *   W4A16_SYM_G128  compressed-tensors pack-quantized int4: 8 nibbles per
+ *                word LSB-first, stored u = q + 8 (q in -8..7), w = scale * q,
+ *                no bias                                          [w4a16]
+ */
+typedef enum moe_format {
+  MOE_FMT_F32 = 0,
+  MOE_FMT_BF16 = 1,
+  MOE_FMT_F16 = 2,
+  MOE_FMT_AFFINE8_G64 = 3,
+  MOE_FMT_AFFINE4_G64 = 4,
+  MOE_FMT_AFFINE3_G64 = 5,
+  MOE_FMT_W4A16_SYM_G128 = 6
+} moe_format;
+
+/* One matrix [rows, cols] in any format.  For F32/BF16/F16 qweight holds the
+ * values and scales/biases are NULL; biases is NULL for W4A16. */
+typedef struct moe_qmatrix {
+  int32_t fmt;
+  int32_t rows;
+  int32_t cols;
+  int32_t reserved;
+  const void* qweight;
+  const void* scales;
+  const void* biases;
+} moe_qmatrix;
+
+/* n_experts experts in one quantised format, stacked contiguously:
+ *   w13 [E][2*inter][hidden] : gate rows 0..inter-1, then up rows
+ *   w2  [E][hidden][inter]   : down projection
+ * with s13/b13 and s2/b2 their fp16 scales/biases ([E][rows][cols/G]).  */
+typedef struct moe_expert_bank {
+  int32_t fmt;
+  int32_t n_experts;
+  int32_t inter;
+  int32_t hidden;
+  const void* w13;
+  const void* s13;
+  const void* b13;
+  const void* w2;
+  const void* s2;
+  const void* b2;
+} moe_expert_bank;
+
+/* flags of moe_experts_forward / moe_layer_forward */
+#define MOE_FLAG_FORCE_DECODE 1   /* use the decode (grouped GEMV) kernels at any T */
+
+/* Decode path is taken for n_tokens <= MOE_DECODE_MAX_TOKENS. */
+#define MOE_DECODE_MAX_TOKENS 32
+
+/* Human-readable name of a status; never NULL. */
+const char* moe_status_string(moe_status s);
+
+/* Detail of the last error returned on this host thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Bytes of workspace needed for calls with up to max_tokens tokens and the
+ * given shape.  Returns 0 on invalid arguments. */
+size_t moe_workspace_bytes(int max_tokens, int n_experts, int top_k, int hidden, int inter);
+
+/* Zero the workspace's control words (status, counters).  Call once after
+ * allocating a workspace, before its first use. */
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Read and clear the device status word of a workspace (synchronises the
+ * stream).  *device_status receives MOE_OK or MOE_ERR_TIMEOUT. */
+moe_status moe_get_device_status(void* ws, size_t ws_bytes, int* device_status,
+                                 cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Routing [803-gate], [1329].
+ *
+ * moe_route computes, for each token t of x [T, hidden]:
+ *   l[t, e] = sum_h W_r[e, h] * x[t, h] + logit_bias[e]      (fp32)
+ *   slots 0..k-1 = the k experts ordered by (logit desc, id asc); NaN ranks
+ *                  below every number, NaNs among themselves by id
+ *   w[t, j] = exp(l_j - l_0) / sum_i exp(l_i - l_0)          (fp32)
+ *   shared_gate_w[t] = 1 / (1 + exp(-sum_h g[h] x[t, h]))    (if shared_gate)
+ * and buckets the assignments a = t*k + j by expert: bucket_offsets [E+1]
+ * (exclusive prefix sum of the per-expert counts) and bucket_perm [T*k] (the
+ * assignment ids sorted by expert, ascending a within an expert).
+ *   router       [E, hidden] in F32, BF16 or AFFINE8_G64
+ *   logit_bias   nullable [E] fp32 per-expert logit offset
+ *   shared_gate  nullable [1, hidden] in F32, BF16 or AFFINE8_G64
+ *   act          MOE_FMT_BF16 or MOE_FMT_F16 (type of x)
+ *   top_k        1..8, <= E;  E <= 256
+ *   logits       nullable [T, E] fp32 output
+ *   topk_idx [T, k] int32, topk_w [T, k] fp32, shared_gate_w nullable [T]
+ */
+moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
+                     const moe_qmatrix* shared_gate, const void* x, int act, int n_tokens,
+                     int top_k, float* logits, int32_t* topk_idx, float* topk_w,
+                     float* shared_gate_w, int32_t* bucket_offsets, int32_t* bucket_perm,
+                     void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Top-k + weights from given fp32 logits [T, E] (same rules as moe_route). */
+moe_status moe_topk_softmax(const float* logits, int n_tokens, int n_experts, int top_k,
+                            int32_t* topk_idx, float* topk_w, cudaStream_t stream);
+
+/* Bucketing alone: counting sort of topk_idx [T, k] by expert (see moe_route). */
+moe_status moe_bucket(const int32_t* topk_idx, int n_tokens, int top_k, int n_experts,
+                      int32_t* bucket_offsets, int32_t* bucket_perm, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Experts [803-gate]: for an expert with gate Wg, up Wu (rows of w13) and down
+ * Wd (w2):  h = silu(Wg x) * (Wu x),  y = Wd h  (fp32 accumulation).
+ *
+ * moe_expert_mlp runs expert `expert` of `bank` on all n_tokens rows of x:
+ *   h_out nullable [T, inter] fp32, y_out [T, hidden] fp32.
+ * moe_shared_expert is the same for expert 0 of a one-expert bank:
+ *   y_shared [T, hidden] fp32.
+ * Formats: AFFINE4_G64, AFFINE3_G64 (hidden and inter multiples of 128),
+ * W4A16_SYM_G128 (multiples of 256); inter and hidden multiples of 16.
+ */
+moe_status moe_expert_mlp(const moe_expert_bank* bank, int expert, const void* x, int act,
+                          int n_tokens, float* h_out, float* y_out, void* ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
+moe_status moe_shared_expert(const moe_expert_bank* shared, const void* x, int act,
+                             int n_tokens, float* y_shared, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/* The routed experts and the combine [803-gate]:
+ *   out[t, :] = round( sum_{j<k} w[t, j] * y_{t,j} + s_t * y_shared[t, :] )
+ * an fp32 fma chain in slot order with the shared slot last, rounded once to
+ * the activation type.  y_shared/shared_gate_w nullable (no shared slot when
+ * y_shared is NULL; weight 1 when only shared_gate_w is NULL).
+ * Routing inputs are moe_route's outputs (or any valid equivalent).
+ * Every token's output row depends only on that token's inputs: a row is
+ * bit-identical whatever the other rows of the call ([547-win]).       */
+moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, int act,
+                               int n_tokens, int top_k, const int32_t* topk_idx,
+                               const float* topk_w, const int32_t* bucket_offsets,
+                               const int32_t* bucket_perm, const float* y_shared,
+                               const float* shared_gate_w, void* out, int flags, void* ws,
+                               size_t ws_bytes, cudaStream_t stream);
+
+/* The whole layer in one call: route, shared expert, routed experts, combine.
+ * shared (nullable) is a one-expert bank; shared_gate nullable.
+ * topk_idx/topk_w nullable outputs [T, k]. */
+moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
+                             const moe_qmatrix* shared_gate, const moe_expert_bank* experts,
+                             const moe_expert_bank* shared, const void* x, int act,
+                             int n_tokens, int top_k, void* out, int32_t* topk_idx,
+                             float* topk_w, int flags, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Pack / unpack / dequantise, one pair per quantised format [803-run],
+ * [w4a16].  codes are [rows, cols] bytes: unsigned 0..2^bits-1 for affine,
+ * signed -8..7 (int8) for W4A16.  packed is [rows, cols*bits/32] uint32.
+ * cols must be a multiple of 32.  A code out of range sets the packed word
+ * to the low bits of the code (no error is reported on the device).     */
+moe_status moe_pack_affine8_g64(const uint8_t* codes, int rows, int cols, uint32_t* packed,
+                                cudaStream_t stream);
+moe_status moe_unpack_affine8_g64(const uint32_t* packed, int rows, int cols, uint8_t* codes,
+                                  cudaStream_t stream);
+moe_status moe_pack_affine4_g64(const uint8_t* codes, int rows, int cols, uint32_t* packed,
+                                cudaStream_t stream);
+moe_status moe_unpack_affine4_g64(const uint32_t* packed, int rows, int cols, uint8_t* codes,
+                                  cudaStream_t stream);
+moe_status moe_pack_affine3_g64(const uint8_t* codes, int rows, int cols, uint32_t* packed,
+                                cudaStream_t stream);
+moe_status moe_unpack_affine3_g64(const uint32_t* packed, int rows, int cols, uint8_t* codes,
+                                  cudaStream_t stream);
+moe_status moe_pack_w4a16_g128(const int8_t* codes, int rows, int cols, uint32_t* packed,
+                               cudaStream_t stream);
+moe_status moe_unpack_w4a16_g128(const uint32_t* packed, int rows, int cols, int8_t* codes,
+                                 cudaStream_t stream);
+
+/* Dequantise any matrix to fp32: w = fmaf(scale, q, bias) for affine (the
+ * exact value scale*q + bias rounded once to fp32) or scale * q for W4A16
+ * (exact); F32/BF16/F16 values are widened.  w is [rows, cols] fp32.    */
+moe_status moe_dequant(const moe_qmatrix* m, float* w, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,349 @@
+"""GPU parity of the CUDA path against the fp64 CPU oracle (calls go through the C ABI).
+
+Exact: packed bytes, unpacked codes, dequantised weights (fp32 rounding of the
+exact value), top-k indices (given the GPU's own fp32 logits), bucket layouts,
+3-bit vs widened 4-bit outputs, batch invariance.  Within tolerance
+(|gpu - oracle| <= 1e-2 rms(oracle) + 1e-3): logits, routing weights, expert
+projections, layer outputs.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+from bit_affine_quantized_fp32_gb300 import synth
+from oracle import oracle as O
+
+from . import _harness as Hn
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["affine8_g64", "affine4_g64", "affine3_g64", "w4a16_g128"]
+
+
+@pytest.fixture(scope="module")
+def capi():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_affine_quantized_fp32_gb300 import build
+    build.build()
+    from bit_affine_quantized_fp32_gb300 import capi as C
+    return C
+
+
+# --------------------------------------------------------------------------
+# formats
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(1, 128), (7, 256), (33, 2048), (512, 640)])
+def test_pack_unpack_bitexact(capi, fmt, shape):
+    rng = np.random.default_rng(100 + shape[0])
+    codes = synth.gen_codes(rng, fmt, *shape)
+    gpu = Hn.gpu_pack(fmt, codes)
+    ref = O.pack(fmt, codes)
+    assert np.array_equal(gpu.cpu().numpy().view(np.uint32), ref)
+    torch = Hn.torch()
+    out = torch.empty(shape, dtype=torch.int8 if fmt == "w4a16_g128" else torch.uint8,
+                      device="cuda")
+    capi.moe_unpack(fmt, gpu, shape[0], shape[1], out)
+    assert np.array_equal(out.cpu().numpy().astype(np.int32), codes)
+
+
+@pytest.mark.parametrize("fmt", FMTS + ["f32", "bf16"])
+def test_dequant_bitexact(capi, fmt):
+    rng = np.random.default_rng(7)
+    rows, cols = 24, 512
+    m = synth.gen_qmatrix(rng, fmt, rows, cols)
+    gm = Hn.gpu_matrix(m)
+    torch = Hn.torch()
+    w = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+    capi.moe_dequant(gm, w)
+    om = Hn.oracle_matrix(m)
+    ref = O.dequant(fmt, om["q"], om.get("s"), om.get("b"), rows, cols).astype(np.float32)
+    assert np.array_equal(w.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_special_scales(capi):
+    # zero, subnormal, negative and maximal fp16 scales/biases
+    fmt = "affine4_g64"
+    rows, cols = 8, 128
+    codes = np.tile(np.arange(16, dtype=np.int32), (rows, cols // 16))
+    special = np.array([0x0000, 0x8000, 0x0001, 0x03FF, 0x7BFF, 0xFBFF, 0x3C00, 0xB555], np.uint16)
+    s = np.stack([special, special[::-1]], axis=1)
+    b = np.stack([special[::-1], special], axis=1)
+    m = synth.QMatrix(fmt, rows, cols, codes=codes, scales=s, biases=b)
+    gm = Hn.gpu_matrix(m)
+    torch = Hn.torch()
+    w = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+    capi.moe_dequant(gm, w)
+    om = Hn.oracle_matrix(m)
+    with np.errstate(over="ignore", invalid="ignore"):
+        ref = O.dequant(fmt, om["q"], s, b, rows, cols).astype(np.float32)
+    got = w.cpu().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok].view(np.uint32), ref[ok].view(np.uint32))
+
+
+# --------------------------------------------------------------------------
+# routing
+
+def _route_case(T, E, k, H, rfmt, gfmt, zipf, seed):
+    L = synth.gen_layer(T=T, E=E, k=k, H=H, I=128, expert_fmt="affine4_g64", router_fmt=rfmt,
+                        shared_fmt="affine4_g64" if gfmt else None, gate_fmt=gfmt, zipf=zipf,
+                        seed=seed)
+    return L
+
+
+@pytest.mark.parametrize("T,E,k,H,rfmt,gfmt,zipf", [
+    (1, 256, 8, 2048, "f32", None, False),
+    (8, 256, 8, 2048, "f32", "affine8_g64", True),
+    (4, 256, 8, 2048, "affine8_g64", "affine8_g64", False),
+    (32, 256, 8, 2048, "f32", "bf16", False),
+    (37, 16, 4, 384, "bf16", "bf16", True),
+    (200, 64, 8, 256, "f32", None, True),
+])
+def test_route_parity(capi, T, E, k, H, rfmt, gfmt, zipf):
+    L = _route_case(T, E, k, H, rfmt, gfmt, zipf, seed=T + E)
+    g = Hn.GpuLayer(L)
+    r = g.route()
+    lg = r["logits"].cpu().numpy().astype(np.float64)
+    x = O.act_to_double(L.act, L.x)
+    ref = O.router_logits(Hn.oracle_matrix(L.router), x, L.logit_bias)
+    # fp32 dot product of H terms: error bound ~ H * 2^-24 * sum |w x|
+    W = np.abs(O.dequant(rfmt, Hn.oracle_matrix(L.router)["q"], Hn.oracle_matrix(L.router).get("s"),
+                         Hn.oracle_matrix(L.router).get("b"), E, H))
+    bound = H * 2.0 ** -24 * (np.abs(x) @ W.T) + 1e-6
+    assert np.all(np.abs(lg - ref) <= bound)
+    # top-k on the GPU's own fp32 logits: indices exact, weights close
+    idx_ref, w_ref = O.topk(lg, k)
+    idx = r["idx"].cpu().numpy()
+    assert np.array_equal(idx, idx_ref)
+    assert np.allclose(r["w"].cpu().numpy(), w_ref, rtol=2e-6, atol=1e-7)
+    # against fp64 logits: equal except at near ties (within the bound)
+    idx64, _ = O.topk(ref, k)
+    for t in np.nonzero(np.any(idx64 != idx, axis=1))[0]:
+        srt = np.sort(ref[t])[::-1]
+        gaps = np.abs(np.diff(srt[: k + 1]))
+        assert gaps.min() <= 2 * bound[t].max(), f"token {t}: routing differs without a near tie"
+    # shared gate
+    if gfmt:
+        _, sg_ref = O.shared_gate(Hn.oracle_matrix(L.gate), x)
+        assert np.allclose(r["sg"].cpu().numpy(), sg_ref, rtol=1e-5, atol=1e-6)
+    # bucketing: exact against the oracle's counting sort of the GPU's picks
+    counts, offs, perm, active = O.bucket(idx, E)
+    assert np.array_equal(r["offsets"].cpu().numpy(), offs)
+    assert np.array_equal(r["perm"].cpu().numpy(), perm)
+
+
+def test_topk_edge_rows(capi):
+    torch = Hn.torch()
+    E, k = 256, 8
+    rows = []
+    rows.append(np.zeros(E))                             # flat row
+    r = np.zeros(E); r[[200, 3, 77]] = 5.0; rows.append(r)  # ties -> lower id first
+    rows.append(np.full(E, np.nan))                      # all NaN -> ids 0..7
+    r = np.arange(E, dtype=np.float64); r[255] = np.nan; r[254] = -np.inf; rows.append(r)
+    r = np.full(E, -np.inf); r[9] = 1.0; rows.append(r)
+    r = -np.arange(E, dtype=np.float64); r[[0, 1]] = np.nan; rows.append(r)
+    rng = np.random.default_rng(3)
+    rows.append(rng.integers(-2, 3, E).astype(np.float64))  # many ties
+    lg = np.stack(rows).astype(np.float32)
+    T = lg.shape[0]
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    capi.moe_topk_softmax(Hn.dev(lg), k, idx, w)
+    idx_ref, w_ref = O.topk(lg.astype(np.float64), k)
+    assert np.array_equal(idx.cpu().numpy(), idx_ref)
+    wg = w.cpu().numpy()
+    assert np.array_equal(np.isnan(wg), np.isnan(w_ref))
+    ok = ~np.isnan(w_ref)
+    assert np.allclose(wg[ok], w_ref[ok], rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("T,k,E", [(0, 8, 16), (1, 8, 256), (32, 8, 256), (512, 8, 256),
+                                   (4096, 8, 256), (3, 1, 1), (100, 3, 5)])
+def test_bucket_bitexact(capi, T, k, E):
+    torch = Hn.torch()
+    rng = np.random.default_rng(T + k + E)
+    if T:
+        p = np.exp(-1.1 * np.log(np.arange(1, E + 1)))
+        idx = np.stack([rng.choice(E, size=k, replace=False, p=p / p.sum()) for _ in range(T)])
+    else:
+        idx = np.zeros((0, k), np.int64)
+    idx = idx.astype(np.int32)
+    offs = torch.full((E + 1,), -1, dtype=torch.int32, device="cuda")
+    perm = torch.full((max(T * k, 1),), -1, dtype=torch.int32, device="cuda")
+    capi.moe_bucket(Hn.dev(idx) if T else torch.zeros((0, k), dtype=torch.int32, device="cuda"),
+                    E, offs, perm)
+    _, offs_ref, perm_ref, _ = O.bucket(idx, E)
+    assert np.array_equal(offs.cpu().numpy(), offs_ref)
+    assert np.array_equal(perm.cpu().numpy()[: T * k], perm_ref)
+
+
+# --------------------------------------------------------------------------
+# experts
+
+@pytest.mark.parametrize("fmt,act,T,H,I", [
+    ("affine4_g64", "bf16", 1, 2048, 512),
+    ("affine4_g64", "bf16", 13, 256, 128),
+    ("affine3_g64", "bf16", 5, 2048, 512),
+    ("affine3_g64", "bf16", 40, 384, 256),
+    ("w4a16_g128", "f16", 32, 2048, 512),
+    ("w4a16_g128", "bf16", 3, 512, 256),
+    ("affine4_g64", "f16", 9, 512, 128),
+])
+def test_expert_mlp_per_projection(capi, fmt, act, T, H, I):
+    torch = Hn.torch()
+    rng = np.random.default_rng(T * 7 + H)
+    bank = synth.gen_bank(rng, fmt, 2, I, H)
+    x = synth.gen_x(rng, T, H, act)
+    gb = Hn.gpu_bank(bank)
+    ws = Hn.workspace(T, 2, 1, H, I)
+    h = torch.empty((T, I), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    capi.moe_expert_mlp(gb, 1, Hn.bits16(x, act), h, y, ws)
+    xd = O.act_to_double(act, x)
+    ob = Hn.oracle_bank(bank)
+    h_ref, y_ref = O.expert_mlp(fmt, I, H, Hn.oracle_expert(ob, 1), xd)
+    hg = h.cpu().numpy().astype(np.float64)
+    Hn.assert_layer_close(hg, h_ref, "h (gate/up projection)")
+    # gate/up sums are exact-product fp32 sums: far inside the tolerance
+    assert Hn.projection_errors(hg, h_ref)["aggregate_rel"] < 1e-5
+    # down alone, on the GPU's own h
+    y_down = O.down(fmt, H, I, ob["w2"][1], ob["s2"][1], ob.get("b2", [None, None])[1], hg)
+    yg = y.cpu().numpy().astype(np.float64)
+    Hn.assert_layer_close(yg, y_down, "y (down projection)")
+    assert Hn.projection_errors(yg, y_down)["aggregate_rel"] < 1e-4
+    Hn.assert_layer_close(yg, y_ref, "y (expert)")
+
+
+# --------------------------------------------------------------------------
+# the layer
+
+SMALL = [
+    # (name-like, overrides)
+    dict(T=1, E=16, k=8, H=256, I=128, expert_fmt="affine4_g64", seed=1),
+    dict(T=8, E=32, k=8, H=512, I=128, expert_fmt="affine4_g64", shared_fmt="affine4_g64",
+         gate_fmt="affine8_g64", zipf=True, seed=2),
+    dict(T=4, E=16, k=8, H=512, I=256, expert_fmt="affine3_g64", router_fmt="affine8_g64",
+         shared_fmt="affine4_g64", gate_fmt="affine8_g64", seed=3),
+    dict(T=32, E=64, k=8, H=512, I=256, expert_fmt="w4a16_g128", shared_fmt="w4a16_g128",
+         gate_fmt="bf16", act="f16", seed=4),
+    dict(T=19, E=12, k=3, H=384, I=128, expert_fmt="affine4_g64", shared_fmt="affine3_g64",
+         gate_fmt="f32", seed=5),
+    dict(T=70, E=16, k=4, H=256, I=128, expert_fmt="affine4_g64", shared_fmt="affine4_g64",
+         gate_fmt="affine8_g64", zipf=True, seed=6),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: f"T{c['T']}_{c['expert_fmt']}")
+def test_layer_small(capi, cfg):
+    L = synth.gen_layer(**cfg)
+    g = Hn.GpuLayer(L)
+    out, idx, w = g.forward()
+    idx = idx.cpu().numpy()
+    ref = Hn.oracle_layer(L, idx_override=idx)
+    Hn.assert_layer_close(Hn.to_np(out), ref["out"])
+
+
+@pytest.mark.parametrize("name", ["decode1_affine4", "decode8_affine4_shared_zipf",
+                                  "decode4_affine3", "decode32_w4a16"])
+def test_layer_full_size(capi, name):
+    """Every output of the workload at its full size (E=256, hidden 2048,
+    inter 512), from the seeded synthetic inputs, against the oracle."""
+    L = synth.workload(name)
+    g = Hn.GpuLayer(L)
+    out, idx, w = g.forward()
+    idx = idx.cpu().numpy()
+    ref = Hn.oracle_layer(L, idx_override=idx)
+    own = ref["idx"]
+    Hn.assert_layer_close(Hn.to_np(out), ref["out"])
+    # routing matched the oracle's own fp64 routing except at near ties
+    assert np.mean(np.all(own == idx, axis=1)) >= 0.9
+
+
+def test_batch_invariance(capi):
+    """Row r of a T-token call is bit-identical to the same token alone, in
+    any batch composition and order."""
+    L = synth.gen_layer(T=32, E=64, k=8, H=512, I=256, expert_fmt="affine4_g64",
+                        shared_fmt="affine4_g64", gate_fmt="affine8_g64", zipf=True, seed=21)
+    g = Hn.GpuLayer(L, max_tokens=32)
+    full, _, _ = g.forward()
+    full = full.cpu()
+    torch = Hn.torch()
+    for t in [0, 5, 31]:
+        one, _, _ = g.forward(g.x[t:t + 1])
+        assert torch.equal(one.cpu()[0], full[t])
+    for lo, hi in [(0, 4), (8, 16), (3, 30)]:
+        part, _, _ = g.forward(g.x[lo:hi].contiguous())
+        assert torch.equal(part.cpu(), full[lo:hi])
+    p = torch.randperm(32, generator=torch.Generator().manual_seed(0))
+    perm_out, _, _ = g.forward(g.x[p.cuda()].contiguous())
+    assert torch.equal(perm_out.cpu(), full[p])
+
+
+def test_3bit_widened_to_4bit_bitexact(capi):
+    """The same 3-bit codes stored as 4-bit words give bit-identical outputs."""
+    L3 = synth.gen_layer(T=6, E=16, k=8, H=512, I=256, expert_fmt="affine3_g64",
+                         shared_fmt="affine3_g64", gate_fmt="affine8_g64", seed=22)
+    g3 = Hn.GpuLayer(L3)
+    out3, _, _ = g3.forward()
+
+    def widen(b):
+        nb = synth.ExpertBank("affine4_g64", b.E, b.I, b.H)
+        nb.w13 = [synth.QMatrix("affine4_g64", m.rows, m.cols, codes=m.codes, scales=m.scales,
+                                biases=m.biases) for m in b.w13]
+        nb.w2 = [synth.QMatrix("affine4_g64", m.rows, m.cols, codes=m.codes, scales=m.scales,
+                               biases=m.biases) for m in b.w2]
+        return nb
+
+    L3.experts = widen(L3.experts)
+    L3.shared = widen(L3.shared)
+    g4 = Hn.GpuLayer(L3)
+    out4, _, _ = g4.forward()
+    assert Hn.torch().equal(out3, out4)
+
+
+def test_zero_tokens_and_zero_input(capi):
+    L = synth.gen_layer(T=3, E=8, k=2, H=256, I=128, expert_fmt="affine4_g64",
+                        shared_fmt="affine4_g64", gate_fmt="affine8_g64", seed=23)
+    g = Hn.GpuLayer(L)
+    torch = Hn.torch()
+    out, _, _ = g.forward(g.x[:0])
+    assert out.shape == (0, 256)
+    z = torch.zeros_like(g.x)
+    out, _, _ = g.forward(z)
+    assert torch.count_nonzero(out.float()) == 0
+
+
+def test_decode_path_large_T(capi):
+    """The grouped-GEMV path at a prefill-sized T (more than 4 n-tiles per
+    expert) on sampled rows."""
+    L = synth.gen_layer(T=300, E=16, k=4, H=256, I=128, expert_fmt="affine4_g64",
+                        shared_fmt="affine4_g64", gate_fmt="affine8_g64", zipf=True, seed=24)
+    g = Hn.GpuLayer(L)
+    out, idx, _ = g.forward(flags=1)
+    ref = Hn.oracle_layer(L, idx_override=idx.cpu().numpy())
+    Hn.assert_layer_close(Hn.to_np(out), ref["out"])
+
+
+def test_validation_errors(capi):
+    torch = Hn.torch()
+    L = synth.gen_layer(T=2, E=8, k=2, H=256, I=128, expert_fmt="affine4_g64", seed=25)
+    g = Hn.GpuLayer(L)
+    out = torch.empty((2, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(capi.MoeError) as e:
+        capi.moe_layer_forward(g.router, None, None, g.experts, None, g.x, 9, out, ws=g.ws)
+    assert e.value.status == 1
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(capi.MoeError) as e:
+        capi.moe_layer_forward(g.router, None, None, g.experts, None, g.x, 2, out, ws=small)
+    assert e.value.status == 3
+    bad = capi.ExpertBank("affine8_g64", 8, 128, 256, *g.experts.tensors)
+    with pytest.raises(capi.MoeError) as e:
+        capi.moe_layer_forward(g.router, None, None, bad, None, g.x, 2, out, ws=g.ws)
+    assert e.value.status == 2 and "AFFINE8_G64" in str(e.value)
+    assert capi.moe_get_device_status(g.ws) == 0
