@@ -181,13 +181,13 @@ class Bank:
         self.bias = synth.device_zipf_bias(E, seed + 1, device) if cfg["zipf"] else None
         ex = synth.device_bank(cfg["expert_fmt"], E, I, H, seed + 2, device)
         self.experts = capi.ExpertBank(cfg["expert_fmt"], E, I, H, ex["w13"], ex["s13"], ex["b13"],
-                                       ex["w2"], ex["s2"], ex["b2"])
+                                       ex["w2"], ex["s2"], ex["b2"]).tiled()
         self.raw = {"router": r, "experts": ex}
         self.shared = self.gate = None
         if cfg["shared_fmt"]:
             sh = synth.device_bank(cfg["shared_fmt"], 1, I, H, seed + 3, device)
             self.shared = capi.ExpertBank(cfg["shared_fmt"], 1, I, H, sh["w13"], sh["s13"],
-                                          sh["b13"], sh["w2"], sh["s2"], sh["b2"])
+                                          sh["b13"], sh["w2"], sh["s2"], sh["b2"]).tiled()
             self.raw["shared"] = sh
         if cfg["gate_fmt"]:
             g = synth.device_matrix(cfg["gate_fmt"], 1, H, seed + 4, device)
@@ -340,7 +340,8 @@ def run_gpu(args, ws_world, rank, local):
     peak = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
-    launches_per_step = 3 + (4 if cfg["shared_fmt"] else 0) + 6
+    # one persistent launch per layer call for decode batches (<= 32 tokens)
+    launches_per_step = 1 if T <= 32 else 3 + (4 if cfg["shared_fmt"] else 0) + 6
     line = {
         "metric": "MoE-layer tokens/s (decode batch %d, %s)" % (T, cfg["expert_fmt"]),
         "value": round(value, 1),
@@ -364,7 +365,8 @@ def run_gpu(args, ws_world, rank, local):
                    "experts_touched_mean": round(float(np.mean(U)), 2)},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / peak, 4), "traffic": None,
-                     "kernel": "whole step (all launches of one layer call)",
+                     "kernel": ("k_decode: the whole layer in one persistent launch" if T <= 32
+                                else "whole step (all launches of one layer call)"),
                      "peak_source": peak_src,
                      "algorithmic_bytes_per_step": round(float(np.mean(step_bytes)))},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",

@@ -18,6 +18,7 @@ LIB_PATH = Path(__file__).resolve().parent / "libmoe_gb300.so"
 FMT = {"f32": 0, "bf16": 1, "f16": 2, "affine8_g64": 3, "affine4_g64": 4,
        "affine3_g64": 5, "w4a16_g128": 6}
 MOE_FLAG_FORCE_DECODE = 1
+MOE_FLAG_UNFUSED = 2
 MOE_DECODE_MAX_TOKENS = 32
 
 EXPORTS = [
@@ -26,8 +27,11 @@ EXPORTS = [
     "moe_shared_expert", "moe_experts_forward", "moe_layer_forward",
     "moe_pack_affine8_g64", "moe_unpack_affine8_g64", "moe_pack_affine4_g64",
     "moe_unpack_affine4_g64", "moe_pack_affine3_g64", "moe_unpack_affine3_g64",
-    "moe_pack_w4a16_g128", "moe_unpack_w4a16_g128", "moe_dequant",
+    "moe_pack_w4a16_g128", "moe_unpack_w4a16_g128", "moe_tiled_bytes", "moe_repack_bank",
+    "moe_unrepack_bank", "moe_dequant",
 ]
+LAYOUT_CANONICAL = 0
+LAYOUT_TILED = 1
 
 
 class MoeError(RuntimeError):
@@ -43,7 +47,7 @@ class QMatrixS(ctypes.Structure):
 
 class ExpertBankS(ctypes.Structure):
     _fields_ = [("fmt", c_int32), ("n_experts", c_int32), ("inter", c_int32), ("hidden", c_int32),
-                ("w13", c_void_p), ("s13", c_void_p), ("b13", c_void_p),
+                ("layout", c_int32), ("reserved", c_int32), ("w13", c_void_p), ("s13", c_void_p), ("b13", c_void_p),
                 ("w2", c_void_p), ("s2", c_void_p), ("b2", c_void_p)]
 
 
@@ -72,9 +76,14 @@ def _load():
     for n in ("affine8_g64", "affine4_g64", "affine3_g64", "w4a16_g128"):
         getattr(L, f"moe_pack_{n}").argtypes = [P, c_int, c_int, P, P]
         getattr(L, f"moe_unpack_{n}").argtypes = [P, c_int, c_int, P, P]
+    L.moe_tiled_bytes.restype = c_size_t
+    L.moe_tiled_bytes.argtypes = [c_int] * 5
+    L.moe_repack_bank.argtypes = [P, P, P, P]
+    L.moe_unrepack_bank.argtypes = [P] * 8
     L.moe_dequant.argtypes = [P, P, P]
     for name in EXPORTS:
-        if name not in ("moe_status_string", "moe_last_error", "moe_workspace_bytes"):
+        if name not in ("moe_status_string", "moe_last_error", "moe_workspace_bytes",
+                        "moe_tiled_bytes"):
             getattr(L, name).restype = c_int
     return L
 
@@ -120,17 +129,32 @@ class QMatrix:
 
 
 class ExpertBank:
-    """E experts: w13 [E, 2I, *] (gate rows then up rows), w2 [E, H, *] plus scales/biases."""
+    """E experts.  CANONICAL: w13 [E, 2I, *] (gate rows then up rows), w2 [E, H, *]
+    packed words plus fp16 scales/biases.  TILED: w13 and w2 are the two
+    kernel-tiled byte buffers (moe_repack_bank), scales/biases None."""
 
     def __init__(self, fmt: str, n_experts: int, inter: int, hidden: int, w13, s13, b13, w2, s2,
-                 b2):
+                 b2, layout: int = LAYOUT_CANONICAL):
         self.fmt, self.n_experts, self.inter, self.hidden = fmt, n_experts, inter, hidden
+        self.layout = layout
         self.tensors = (w13, s13, b13, w2, s2, b2)
-        self.struct = ExpertBankS(FMT[fmt], n_experts, inter, hidden, _ptr(w13), _ptr(s13),
-                                  _ptr(b13), _ptr(w2), _ptr(s2), _ptr(b2))
+        self.struct = ExpertBankS(FMT[fmt], n_experts, inter, hidden, layout, 0, _ptr(w13),
+                                  _ptr(s13), _ptr(b13), _ptr(w2), _ptr(s2), _ptr(b2))
 
     def ref(self):
         return ctypes.byref(self.struct)
+
+    def tiled(self, stream=None) -> "ExpertBank":
+        """The TILED copy of this CANONICAL bank (device buffers from torch)."""
+        import torch
+        dev = self.tensors[0].device
+        b13 = moe_tiled_bytes(self.fmt, self.n_experts, self.inter, self.hidden, 0)
+        b2 = moe_tiled_bytes(self.fmt, self.n_experts, self.inter, self.hidden, 1)
+        t13 = torch.empty(b13, dtype=torch.uint8, device=dev)
+        t2 = torch.empty(b2, dtype=torch.uint8, device=dev)
+        moe_repack_bank(self, t13, t2, stream)
+        return ExpertBank(self.fmt, self.n_experts, self.inter, self.hidden, t13, None, None, t2,
+                          None, None, layout=LAYOUT_TILED)
 
 
 def _ref(o):
@@ -211,6 +235,23 @@ def moe_pack(fmt: str, codes, packed, stream=None):
 def moe_unpack(fmt: str, packed, rows: int, cols: int, codes, stream=None):
     _check(getattr(lib, f"moe_unpack_{fmt}")(_ptr(packed), rows, cols, _ptr(codes),
                                              _stream(stream)))
+
+
+def moe_tiled_bytes(fmt: str, n_experts: int, inter: int, hidden: int, which: int) -> int:
+    n = lib.moe_tiled_bytes(FMT[fmt], n_experts, inter, hidden, which)
+    if n == 0:
+        raise MoeError(1, lib.moe_last_error().decode())
+    return n
+
+
+def moe_repack_bank(canonical: ExpertBank, w13_tiled, w2_tiled, stream=None):
+    _check(lib.moe_repack_bank(canonical.ref(), _ptr(w13_tiled), _ptr(w2_tiled),
+                               _stream(stream)))
+
+
+def moe_unrepack_bank(tiled: ExpertBank, w13, s13, b13, w2, s2, b2, stream=None):
+    _check(lib.moe_unrepack_bank(tiled.ref(), _ptr(w13), _ptr(s13), _ptr(b13), _ptr(w2),
+                                 _ptr(s2), _ptr(b2), _stream(stream)))
 
 
 def moe_dequant(m: QMatrix, w, stream=None):

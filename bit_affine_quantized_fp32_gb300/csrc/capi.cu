@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "decode.h"
 
 namespace moe {
 int router_ks(int H);
@@ -73,6 +74,7 @@ int fmt_group(int f) { return f == MOE_FMT_W4A16_SYM_G128 ? 128 : 64; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
 
 int sm_count() {
   static int cache[64] = {0};
@@ -124,7 +126,8 @@ moe_status check_hidden(int H) {
   return MOE_OK;
 }
 
-moe_status check_bank(const moe_expert_bank* b, const char* what) {
+// Format and shape of a bank (either layout).
+moe_status check_bank_shape(const moe_expert_bank* b, const char* what) {
   if (!b) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", what);
   const int f = b->fmt;
   if (f != MOE_FMT_AFFINE4_G64 && f != MOE_FMT_AFFINE3_G64 && f != MOE_FMT_W4A16_SYM_G128)
@@ -139,42 +142,45 @@ moe_status check_bank(const moe_expert_bank* b, const char* what) {
   if (H <= 0 || H % q != 0 || I <= 0 || I % q != 0)
     return fail(MOE_ERR_INVALID_ARG, "%s: hidden=%d and inter=%d must be multiples of %d for %s",
                 what, H, I, q, fmt_name(f));
-  if (I > 1024) return fail(MOE_ERR_INVALID_ARG, "%s: inter=%d > 1024 unsupported", what, I);
+  if (I > 512) return fail(MOE_ERR_INVALID_ARG, "%s: inter=%d > 512 unsupported", what, I);
   if (H > 8192) return fail(MOE_ERR_INVALID_ARG, "%s: hidden=%d > 8192 unsupported", what, H);
-  if (!b->w13 || !b->s13 || !b->w2 || !b->s2)
-    return fail(MOE_ERR_INVALID_ARG, "%s: weight or scale pointer is NULL", what);
-  if (f != MOE_FMT_W4A16_SYM_G128 && (!b->b13 || !b->b2))
-    return fail(MOE_ERR_INVALID_ARG, "%s: affine format needs biases", what);
-  if (!aligned16(b->w13) || !aligned16(b->w2) || !aligned16(b->s13) || !aligned16(b->s2) ||
-      (b->b13 && !aligned16(b->b13)) || (b->b2 && !aligned16(b->b2)))
-    return fail(MOE_ERR_MISALIGNED, "%s: weight/scale/bias pointers must be 16-byte aligned", what);
   return MOE_OK;
 }
 
-int sb_granule(int bytes_row, int bytes_chunk) {
-  for (int g = 16; g >= 4; g >>= 1)
-    if (bytes_row % g == 0 && bytes_chunk % g == 0) return g;
-  return 0;
+// A bank the expert kernels read: TILED, two 16-byte aligned buffers.
+moe_status check_bank(const moe_expert_bank* b, const char* what) {
+  if (moe_status st = check_bank_shape(b, what)) return st;
+  if (b->layout != MOE_LAYOUT_TILED)
+    return fail(MOE_ERR_INVALID_ARG,
+                "%s: layout %d; the expert kernels read TILED banks (moe_repack_bank)", what,
+                b->layout);
+  if (!b->w13 || !b->w2) return fail(MOE_ERR_INVALID_ARG, "%s: tiled buffer is NULL", what);
+  if (!aligned16(b->w13) || !aligned16(b->w2))
+    return fail(MOE_ERR_MISALIGNED, "%s: tiled buffers must be 16-byte aligned", what);
+  return MOE_OK;
 }
 
-// GEMV job for gate/up (w13) or down (w2) of a bank.
-GemvJob bank_job(const moe_expert_bank* b, bool down) {
-  GemvJob J{};
-  const int f = b->fmt, H = b->hidden, I = b->inter;
-  const int G = fmt_group(f), bits = fmt_bits(f);
-  J.fmt = f;
-  J.rows = down ? H : 2 * I;
-  J.K = down ? I : H;
-  J.CK = down ? I : gu_chunk(H);
-  J.row_bytes = J.K * bits / 8;
-  J.sb_cols = J.K / G;
-  J.sb_gran = sb_granule(J.sb_cols * 2, (J.CK / G) * 2);
-  J.w = static_cast<const uint8_t*>(down ? b->w2 : b->w13);
-  J.s = static_cast<const uint16_t*>(down ? b->s2 : b->s13);
-  J.b = f == MOE_FMT_W4A16_SYM_G128 ? nullptr : static_cast<const uint16_t*>(down ? b->b2 : b->b13);
-  J.w_estride = (long long)J.rows * J.row_bytes;
-  J.sb_estride = (long long)J.rows * J.sb_cols;
-  return J;
+// A CANONICAL bank: words 4-byte aligned, scales/biases 2-byte aligned.
+moe_status check_canonical(const moe_expert_bank* b, const char* what) {
+  if (moe_status st = check_bank_shape(b, what)) return st;
+  if (b->layout != MOE_LAYOUT_CANONICAL)
+    return fail(MOE_ERR_INVALID_ARG, "%s: layout %d, expected CANONICAL", what, b->layout);
+  if (!b->w13 || !b->s13 || !b->w2 || !b->s2)
+    return fail(MOE_ERR_INVALID_ARG, "%s: weight or scale pointer is NULL", what);
+  if (b->fmt != MOE_FMT_W4A16_SYM_G128 && (!b->b13 || !b->b2))
+    return fail(MOE_ERR_INVALID_ARG, "%s: affine format needs biases", what);
+  if (!aligned4(b->w13) || !aligned4(b->w2) || !aligned2(b->s13) || !aligned2(b->s2) ||
+      (b->b13 && !aligned2(b->b13)) || (b->b2 && !aligned2(b->b2)))
+    return fail(MOE_ERR_MISALIGNED, "%s: words need 4-byte, scales/biases 2-byte alignment", what);
+  return MOE_OK;
+}
+
+// Geometry of w13 (gate/up) and w2 (down) of a TILED bank.
+MatGeo geo13(const moe_expert_bank* b) {
+  return MatGeo{tile_geo(b->fmt, b->inter, b->hidden, 0), static_cast<const uint8_t*>(b->w13)};
+}
+MatGeo geo2(const moe_expert_bank* b) {
+  return MatGeo{tile_geo(b->fmt, b->inter, b->hidden, 1), static_cast<const uint8_t*>(b->w2)};
 }
 
 char* wsp(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
@@ -188,41 +194,39 @@ moe_status check_ws(void* ws, size_t ws_bytes, size_t need) {
 }
 
 // One expert (a fixed slot holding every token) over the T rows of x, with
-// the given workspace layout: x prep -> gate/up GEMV -> SwiGLU -> down GEMV.
+// the given workspace layout: x prep -> gate/up units -> SwiGLU -> down units.
 moe_status run_expert_mlp(const moe_expert_bank* bank, int expert, const void* x, bool f16,
                           int T, float* h_out, float* y_out, void* ws, const WsLayout& L,
                           cudaStream_t stream) {
   const int sms = sm_count();
   const int H = bank->hidden, I = bank->inter;
-  MOE_CUDA(launch_xprep(static_cast<const uint16_t*>(x), T, H, f16,
-                        reinterpret_cast<uint16_t*>(wsp(ws, L.xperm)),
-                        reinterpret_cast<float*>(wsp(ws, L.xsum)), stream),
-           "x prep");
-  GemvJob J = bank_job(bank, false);
-  J.fixed_expert = expert;
-  J.fixed_cnt = T;
-  J.B = reinterpret_cast<const uint16_t*>(wsp(ws, L.xperm));
-  J.Bsum = reinterpret_cast<const float*>(wsp(ws, L.xsum));
-  J.out = reinterpret_cast<float*>(wsp(ws, L.sh_part));
-  J.P = T;
-  J.max_units = (J.rows / 16) * (J.K / J.CK);
-  MOE_CUDA(launch_gemv(J, f16, false, sms, stream), "gate/up kernel");
-  const int nch = H / J.CK;
-  MOE_CUDA(launch_hprep(reinterpret_cast<const float*>(wsp(ws, L.sh_part)), nch, T, I,
-                        reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh)),
-                        reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl)),
-                        reinterpret_cast<float*>(wsp(ws, L.sh_hsum)), h_out, stream),
-           "swiglu kernel");
-  GemvJob D = bank_job(bank, true);
-  D.fixed_expert = expert;
-  D.fixed_cnt = T;
-  D.B = reinterpret_cast<const uint16_t*>(wsp(ws, L.sh_hh));
-  D.Blo = reinterpret_cast<const uint16_t*>(wsp(ws, L.sh_hl));
-  D.Bsum = reinterpret_cast<const float*>(wsp(ws, L.sh_hsum));
-  D.out = y_out;
-  D.P = T;
-  D.max_units = D.rows / 16;
-  MOE_CUDA(launch_gemv(D, false, true, sms, stream), "down kernel");
+  uint16_t* xperm = reinterpret_cast<uint16_t*>(wsp(ws, L.xperm));
+  float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
+  MOE_CUDA(launch_xprep(static_cast<const uint16_t*>(x), T, H, f16, xperm, xsum, stream), "x prep");
+  const int nss = (T + kMaxTok - 1) / kMaxTok;
+  UnitJob J{};
+  J.g = geo13(bank);
+  J.down = 0;
+  J.inter = I;
+  J.ss = SubSlots{nullptr, nullptr, nullptr, nullptr, expert, T};
+  J.op = OperandSrc{xperm, nullptr, xsum, nullptr};
+  J.hh = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh));
+  J.hl = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl));
+  J.hsum = reinterpret_cast<float*>(wsp(ws, L.sh_hsum));
+  J.hout = h_out;
+  J.status = static_cast<int*>(ws);
+  J.max_units = nss * (I / 64);
+  MOE_CUDA(launch_units(J, f16, sms, stream), "gate/up kernel");
+  UnitJob D{};
+  D.g = geo2(bank);
+  D.down = 1;
+  D.inter = I;
+  D.ss = J.ss;
+  D.op = OperandSrc{J.hh, J.hl, J.hsum, nullptr};
+  D.sink = Sink{y_out, nullptr, H};
+  D.status = static_cast<int*>(ws);
+  D.max_units = nss * (H / kUnitRows);
+  MOE_CUDA(launch_units(D, false, sms, stream), "down kernel");
   return MOE_OK;
 }
 
@@ -252,15 +256,15 @@ size_t moe_workspace_bytes(int max_tokens, int n_experts, int top_k, int hidden,
 }
 
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
-  moe_status s = check_ws(ws, ws_bytes, 256);
+  moe_status s = check_ws(ws, ws_bytes, kCtlBytes);
   if (s) return s;
-  MOE_CUDA(cudaMemsetAsync(ws, 0, 256, stream), "workspace init");
+  MOE_CUDA(cudaMemsetAsync(ws, 0, kCtlBytes, stream), "workspace init");
   return ok();
 }
 
 moe_status moe_get_device_status(void* ws, size_t ws_bytes, int* device_status,
                                  cudaStream_t stream) {
-  moe_status s = check_ws(ws, ws_bytes, 256);
+  moe_status s = check_ws(ws, ws_bytes, kCtlBytes);
   if (s) return s;
   if (!device_status) return fail(MOE_ERR_INVALID_ARG, "device_status is NULL");
   int v = 0;
@@ -406,48 +410,51 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
                         reinterpret_cast<uint16_t*>(wsp(ws, L.xperm)),
                         reinterpret_cast<float*>(wsp(ws, L.xsum)), stream),
            "x prep");
-  int* nslots = reinterpret_cast<int*>(wsp(ws, L.nslots));
-  int* se = reinterpret_cast<int*>(wsp(ws, L.slot_e));
-  int* so = reinterpret_cast<int*>(wsp(ws, L.slot_off));
-  int* sc = reinterpret_cast<int*>(wsp(ws, L.slot_cnt));
+  int* nss = reinterpret_cast<int*>(wsp(ws, L.nss));
+  int* se = reinterpret_cast<int*>(wsp(ws, L.ss_e));
+  int* so = reinterpret_cast<int*>(wsp(ws, L.ss_off));
+  int* sc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
   int* blist = reinterpret_cast<int*>(wsp(ws, L.blist));
-  MOE_CUDA(launch_slots(bucket_offsets, bucket_perm, T, top_k, E, nslots, se, so, sc, blist, stream),
-           "slot kernel");
-  const int max_slots = E < P ? E : P;
-  GemvJob J = bank_job(experts, false);
-  J.n_slots = nslots;
-  J.slot_expert = se;
-  J.slot_off = so;
-  J.slot_cnt = sc;
-  J.b_row = blist;
-  J.B = reinterpret_cast<const uint16_t*>(wsp(ws, L.xperm));
-  J.Bsum = reinterpret_cast<const float*>(wsp(ws, L.xsum));
-  J.out = reinterpret_cast<float*>(wsp(ws, L.part));
-  J.P = P;
-  J.max_units = max_slots * (J.rows / 16) * (J.K / J.CK);
-  MOE_CUDA(launch_gemv(J, f16, false, sms, stream), "gate/up kernel");
-  const int nch = H / J.CK;
-  MOE_CUDA(launch_hprep(reinterpret_cast<const float*>(wsp(ws, L.part)), nch, P, I,
-                        reinterpret_cast<uint16_t*>(wsp(ws, L.hh)),
-                        reinterpret_cast<uint16_t*>(wsp(ws, L.hl)),
-                        reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr, stream),
-           "swiglu kernel");
-  GemvJob D = bank_job(experts, true);
-  D.n_slots = nslots;
-  D.slot_expert = se;
-  D.slot_off = so;
-  D.slot_cnt = sc;
-  D.B = reinterpret_cast<const uint16_t*>(wsp(ws, L.hh));
-  D.Blo = reinterpret_cast<const uint16_t*>(wsp(ws, L.hl));
-  D.Bsum = reinterpret_cast<const float*>(wsp(ws, L.hsum));
-  D.out = reinterpret_cast<float*>(wsp(ws, L.y));
-  D.out_idx = bucket_perm;
-  D.P = P;
-  D.max_units = max_slots * (D.rows / 16);
-  MOE_CUDA(launch_gemv(D, false, true, sms, stream), "down kernel");
-  MOE_CUDA(launch_combine(reinterpret_cast<const float*>(wsp(ws, L.y)), topk_w, top_k, y_shared,
-                          shared_gate_w, T, H, f16, static_cast<uint16_t*>(out), stream),
-           "combine kernel");
+  MOE_CUDA(launch_subslots(bucket_offsets, bucket_perm, T, top_k, E, nss, se, so, sc, blist,
+                           stream),
+           "sub-slot kernel");
+  const int max_ss = int(max_subslots(T, E, top_k));
+  uint16_t* xperm = reinterpret_cast<uint16_t*>(wsp(ws, L.xperm));
+  float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
+  UnitJob J{};
+  J.g = geo13(experts);
+  J.down = 0;
+  J.inter = I;
+  J.ss = SubSlots{nss, se, so, sc, 0, 0};
+  J.op = OperandSrc{xperm, nullptr, xsum, blist};
+  J.hh = reinterpret_cast<uint16_t*>(wsp(ws, L.hh));
+  J.hl = reinterpret_cast<uint16_t*>(wsp(ws, L.hl));
+  J.hsum = reinterpret_cast<float*>(wsp(ws, L.hsum));
+  J.status = static_cast<int*>(ws);
+  J.max_units = max_ss * (I / 64);
+  MOE_CUDA(launch_units(J, f16, sms, stream), "gate/up kernel");
+  UnitJob D{};
+  D.g = geo2(experts);
+  D.down = 1;
+  D.inter = I;
+  D.ss = J.ss;
+  D.op = OperandSrc{J.hh, J.hl, J.hsum, nullptr};
+  D.sink = Sink{reinterpret_cast<float*>(wsp(ws, L.y)), bucket_perm, H};
+  D.status = static_cast<int*>(ws);
+  D.max_units = max_ss * (H / kUnitRows);
+  MOE_CUDA(launch_units(D, false, sms, stream), "down kernel");
+  CombineArgs C{};
+  C.y = reinterpret_cast<const float*>(wsp(ws, L.y));
+  C.w = topk_w;
+  C.ysh = y_shared;
+  C.sg = shared_gate_w;
+  C.out = static_cast<uint16_t*>(out);
+  C.nchd = 1;
+  C.T = T;
+  C.k = top_k;
+  C.H = H;
+  C.f16 = f16;
+  MOE_CUDA(launch_combine(C, stream), "combine kernel");
   return ok();
 }
 
@@ -473,6 +480,79 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
   const WsLayout L = ws_layout(T, E, top_k, H, I);
   if ((s = check_ws(ws, ws_bytes, L.total))) return s;
   if (T == 0) return ok();
+  if (flags & ~(MOE_FLAG_FORCE_DECODE | MOE_FLAG_UNFUSED))
+    return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if (!(flags & MOE_FLAG_UNFUSED) && T <= MOE_DECODE_MAX_TOKENS) {
+    // validate what moe_route / moe_experts_forward would, then one launch
+    if ((s = check_hidden(H))) return s;
+    if ((s = check_router_matrix(router, "router", E, H))) return s;
+    if (shared_gate && (s = check_router_matrix(shared_gate, "shared_gate", 1, H))) return s;
+    if ((s = check_act(act))) return s;
+    if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x/out is NULL");
+    if (!aligned16(x) || !aligned16(out))
+      return fail(MOE_ERR_MISALIGNED, "x/out must be 16-byte aligned");
+    const bool f16 = act == MOE_FMT_F16;
+    DecodeArgs A{};
+    A.R.fmt = router->fmt;
+    A.R.q = router->qweight;
+    A.R.s = static_cast<const uint16_t*>(router->scales);
+    A.R.b = static_cast<const uint16_t*>(router->biases);
+    if (shared_gate) {
+      A.R.gfmt = shared_gate->fmt;
+      A.R.gq = shared_gate->qweight;
+      A.R.gs = static_cast<const uint16_t*>(shared_gate->scales);
+      A.R.gb = static_cast<const uint16_t*>(shared_gate->biases);
+    }
+    A.R.bias = logit_bias;
+    A.R.x = static_cast<const uint16_t*>(x);
+    A.R.f16 = f16;
+    A.R.T = T;
+    A.R.E = E;
+    A.R.H = H;
+    A.R.logits = reinterpret_cast<float*>(wsp(ws, L.logits));
+    A.R.gate_logit = reinterpret_cast<float*>(wsp(ws, L.gate_logit));
+    A.k = top_k;
+    A.inter = I;
+    A.f16 = f16;
+    A.has_shared = shared ? 1 : 0;
+    A.KS = router_ks(H);
+    A.NR = router_blocks(E, shared_gate != nullptr, H);
+    A.XB = (T * (H / 64) + kUnitWarps - 1) / kUnitWarps;
+    A.g13 = geo13(experts);
+    A.g2 = geo2(experts);
+    A.g13s = shared ? geo13(shared) : A.g13;
+    A.g2s = shared ? geo2(shared) : A.g2;
+    A.xperm = reinterpret_cast<uint16_t*>(wsp(ws, L.xperm));
+    A.xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
+    A.idx = reinterpret_cast<int32_t*>(wsp(ws, L.idx));
+    A.w = reinterpret_cast<float*>(wsp(ws, L.w));
+    A.sgw = shared_gate ? reinterpret_cast<float*>(wsp(ws, L.sgw)) : nullptr;
+    A.offsets = reinterpret_cast<int32_t*>(wsp(ws, L.offsets));
+    A.perm = reinterpret_cast<int32_t*>(wsp(ws, L.perm));
+    A.nss = reinterpret_cast<int*>(wsp(ws, L.nss));
+    A.se = reinterpret_cast<int*>(wsp(ws, L.ss_e));
+    A.so = reinterpret_cast<int*>(wsp(ws, L.ss_off));
+    A.sc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
+    A.rows = reinterpret_cast<int*>(wsp(ws, L.ss_rows));
+    A.blist = reinterpret_cast<int*>(wsp(ws, L.blist));
+    A.hh = reinterpret_cast<uint16_t*>(wsp(ws, L.hh));
+    A.hl = reinterpret_cast<uint16_t*>(wsp(ws, L.hl));
+    A.hsum = reinterpret_cast<float*>(wsp(ws, L.hsum));
+    A.y = reinterpret_cast<float*>(wsp(ws, L.y));
+    A.sh_hh = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh));
+    A.sh_hl = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl));
+    A.sh_hsum = reinterpret_cast<float*>(wsp(ws, L.sh_hsum));
+    A.ysh = reinterpret_cast<float*>(wsp(ws, L.ysh));
+    A.user_idx = topk_idx;
+    A.user_w = topk_w;
+    A.out = static_cast<uint16_t*>(out);
+    A.ctrl = static_cast<int*>(ws);
+    if (decode_smem_bytes(A) > kUnitSmemMax)
+      return fail(MOE_ERR_INVALID_ARG, "shape needs %d bytes of shared memory per CTA",
+                  decode_smem_bytes(A));
+    MOE_CUDA(launch_decode(A, sm_count(), stream), "fused decode kernel");
+    return ok();
+  }
   int32_t* idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(wsp(ws, L.idx));
   float* w = topk_w ? topk_w : reinterpret_cast<float*>(wsp(ws, L.w));
   float* sgw = reinterpret_cast<float*>(wsp(ws, L.sgw));
@@ -488,8 +568,8 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
     if (s) return s;
   }
   return moe_experts_forward(experts, x, act, T, top_k, idx, w, offs, perm, ysh,
-                             shared && shared_gate ? sgw : nullptr, out, flags, ws, ws_bytes,
-                             stream);
+                             shared && shared_gate ? sgw : nullptr, out,
+                             flags & MOE_FLAG_FORCE_DECODE, ws, ws_bytes, stream);
 }
 
 #define MOE_PACK_PAIR(NAME, FMT, CT)                                                           \
@@ -523,6 +603,60 @@ MOE_PACK_PAIR(affine8_g64, MOE_FMT_AFFINE8_G64, uint8_t)
 MOE_PACK_PAIR(affine4_g64, MOE_FMT_AFFINE4_G64, uint8_t)
 MOE_PACK_PAIR(affine3_g64, MOE_FMT_AFFINE3_G64, uint8_t)
 MOE_PACK_PAIR(w4a16_g128, MOE_FMT_W4A16_SYM_G128, int8_t)
+
+size_t moe_tiled_bytes(int fmt, int n_experts, int inter, int hidden, int which) {
+  moe_expert_bank b{};
+  b.fmt = fmt;
+  b.n_experts = n_experts;
+  b.inter = inter;
+  b.hidden = hidden;
+  if (check_bank_shape(&b, "tiled_bytes") || (which != 0 && which != 1)) return 0;
+  return size_t(tile_geo(fmt, inter, hidden, which).expert_bytes) * size_t(n_experts);
+}
+
+moe_status moe_repack_bank(const moe_expert_bank* canonical, void* w13_tiled, void* w2_tiled,
+                           cudaStream_t stream) {
+  if (moe_status st = check_canonical(canonical, "repack: canonical bank")) return st;
+  if (!w13_tiled || !w2_tiled) return fail(MOE_ERR_INVALID_ARG, "repack: tiled buffer is NULL");
+  if (!aligned16(w13_tiled) || !aligned16(w2_tiled))
+    return fail(MOE_ERR_MISALIGNED, "repack: tiled buffers must be 16-byte aligned");
+  const moe_expert_bank& b = *canonical;
+  const bool aff = b.fmt != MOE_FMT_W4A16_SYM_G128;
+  MOE_CUDA(launch_repack(tile_geo(b.fmt, b.inter, b.hidden, 0), b.n_experts,
+                         static_cast<const uint32_t*>(b.w13), static_cast<const uint16_t*>(b.s13),
+                         aff ? static_cast<const uint16_t*>(b.b13) : nullptr,
+                         static_cast<uint8_t*>(w13_tiled), stream),
+           "repack w13");
+  MOE_CUDA(launch_repack(tile_geo(b.fmt, b.inter, b.hidden, 1), b.n_experts,
+                         static_cast<const uint32_t*>(b.w2), static_cast<const uint16_t*>(b.s2),
+                         aff ? static_cast<const uint16_t*>(b.b2) : nullptr,
+                         static_cast<uint8_t*>(w2_tiled), stream),
+           "repack w2");
+  return ok();
+}
+
+moe_status moe_unrepack_bank(const moe_expert_bank* tiled, void* w13, void* s13, void* b13,
+                             void* w2, void* s2, void* b2, cudaStream_t stream) {
+  if (moe_status st = check_bank(tiled, "unrepack: tiled bank")) return st;
+  const bool aff = tiled->fmt != MOE_FMT_W4A16_SYM_G128;
+  if (!w13 || !s13 || !w2 || !s2 || (aff && (!b13 || !b2)))
+    return fail(MOE_ERR_INVALID_ARG, "unrepack: output pointer is NULL");
+  if (!aligned4(w13) || !aligned4(w2) || !aligned2(s13) || !aligned2(s2) ||
+      (aff && (!aligned2(b13) || !aligned2(b2))))
+    return fail(MOE_ERR_MISALIGNED, "unrepack: words need 4-byte, scales 2-byte alignment");
+  const moe_expert_bank& b = *tiled;
+  MOE_CUDA(launch_unrepack(tile_geo(b.fmt, b.inter, b.hidden, 0), b.n_experts,
+                           static_cast<const uint8_t*>(b.w13), static_cast<uint32_t*>(w13),
+                           static_cast<uint16_t*>(s13), aff ? static_cast<uint16_t*>(b13) : nullptr,
+                           stream),
+           "unrepack w13");
+  MOE_CUDA(launch_unrepack(tile_geo(b.fmt, b.inter, b.hidden, 1), b.n_experts,
+                           static_cast<const uint8_t*>(b.w2), static_cast<uint32_t*>(w2),
+                           static_cast<uint16_t*>(s2), aff ? static_cast<uint16_t*>(b2) : nullptr,
+                           stream),
+           "unrepack w2");
+  return ok();
+}
 
 moe_status moe_dequant(const moe_qmatrix* m, float* w, cudaStream_t stream) {
   if (!m || !w) return fail(MOE_ERR_INVALID_ARG, "dequant: NULL argument");

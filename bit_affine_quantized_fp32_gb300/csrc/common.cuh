@@ -17,7 +17,7 @@ constexpr int kWarp = 32;
 // on the call's shape, so any workspace of moe_workspace_bytes(max_tokens, ...)
 // bytes serves every call with n_tokens <= max_tokens.
 struct WsLayout {
-  size_t ctrl;        // int32[64]: [0] device status word
+  size_t ctrl;        // int32 control words ([0] device status), 16 KiB
   size_t logits;      // f32 [T][E]
   size_t gate_logit;  // f32 [T]
   size_t xperm;       // u16 [T][H]   activations, k-permuted inside 8-blocks
@@ -27,17 +27,16 @@ struct WsLayout {
   size_t sgw;         // f32 [T]
   size_t offsets;     // i32 [E+1]
   size_t perm;        // i32 [T*k]
-  size_t nslots;      // i32 [1]
-  size_t slot_e;      // i32 [E]
-  size_t slot_off;    // i32 [E]
-  size_t slot_cnt;    // i32 [E]
+  size_t nss;         // i32 [1]   number of sub-slots
+  size_t ss_e;        // i32 [maxss] expert of each sub-slot
+  size_t ss_off;      // i32 [maxss] first bucket position
+  size_t ss_cnt;      // i32 [maxss] tokens (1..8)
+  size_t ss_rows;     // i32 [maxss][8] token of each sub-slot position
   size_t blist;       // i32 [T*k]  bucket position -> token
-  size_t part;        // f32 [nch][T*k][2I] gate/up partial sums per k-chunk
   size_t hh;          // u16 [T*k][I] bf16 high part of h (k-permuted)
   size_t hl;          // u16 [T*k][I] bf16 low part of h
   size_t hsum;        // f32 [T*k][I/64]
   size_t y;           // f32 [T*k][H] per-assignment expert outputs
-  size_t sh_part;     // f32 [nch][T][2I]
   size_t sh_hh;       // u16 [T][I]
   size_t sh_hl;       // u16 [T][I]
   size_t sh_hsum;     // f32 [T][I/64]
@@ -53,6 +52,12 @@ inline int gu_chunk(int H) {
   return 128;
 }
 
+// Upper bound of the number of sub-slots (runs of <= 8 tokens of one expert).
+inline long max_subslots(long T, long E, long k) {
+  const long P = T * k;
+  return (E < P ? E : P) + (P + 7) / 8 + 1;
+}
+
 inline WsLayout ws_layout(long T, long E, long k, long H, long I) {
   WsLayout L{};
   size_t o = 0;
@@ -62,8 +67,8 @@ inline WsLayout ws_layout(long T, long E, long k, long H, long I) {
     return at;
   };
   const long P = T * k;
-  const long nch = H / gu_chunk((int)H);
-  L.ctrl = take(256);
+  const long mss = max_subslots(T, E, k);
+  L.ctrl = take(16384);
   L.logits = take(4 * T * E);
   L.gate_logit = take(4 * T);
   L.xperm = take(2 * T * H);
@@ -73,17 +78,16 @@ inline WsLayout ws_layout(long T, long E, long k, long H, long I) {
   L.sgw = take(4 * T);
   L.offsets = take(4 * (E + 1));
   L.perm = take(4 * P);
-  L.nslots = take(4);
-  L.slot_e = take(4 * E);
-  L.slot_off = take(4 * E);
-  L.slot_cnt = take(4 * E);
+  L.nss = take(4);
+  L.ss_e = take(4 * mss);
+  L.ss_off = take(4 * mss);
+  L.ss_cnt = take(4 * mss);
+  L.ss_rows = take(4 * 8 * mss);
   L.blist = take(4 * P);
-  L.part = take(4 * nch * P * 2 * I);
   L.hh = take(2 * P * I);
   L.hl = take(2 * P * I);
   L.hsum = take(4 * P * (I / 64));
   L.y = take(4 * P * H);
-  L.sh_part = take(4 * nch * T * 2 * I);
   L.sh_hh = take(2 * T * I);
   L.sh_hl = take(2 * T * I);
   L.sh_hsum = take(4 * T * (I / 64));
@@ -137,15 +141,15 @@ template <bool F16>
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t a0, const uint32_t a1,
                                          const uint32_t a2, const uint32_t a3, const uint32_t b0,
                                          const uint32_t b1) {
+  // not volatile: a pure register operation, so the compiler may interleave
+  // independent MMAs and hide their latency
   if constexpr (F16) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -202,6 +206,48 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------
+// TMA bulk copies (cp.async.bulk) completing on a shared-memory mbarrier.
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+// make mbarrier inits and earlier generic shared-memory writes visible to the
+// async proxy (the TMA engine)
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for phase `parity` of a stage barrier (each try_wait suspends
+// for a hardware-defined interval); false after the limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+  for (int i = 0; i < (1 << 22); ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
 }
 
 }  // namespace moe

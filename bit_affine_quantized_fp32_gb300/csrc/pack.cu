@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tiled.cuh"
 
 namespace moe {
 
@@ -106,7 +107,207 @@ __global__ void k_dequant(int fmt, const void* __restrict__ q, const uint16_t* _
   }
 }
 
+// ---- kernel-tiled layout (geometry in tiled.cuh) --------------------------
+
+// Where code (row r, column k) of expert e sits in a tiled buffer.
+struct TiledPos {
+  long long block;  // byte offset of its (w, G) code block
+  int lane;         // fragment lane g*4 + t
+  int widx;         // word W0..W3 of that lane
+  int nib;          // code index inside the word
+};
+
+__device__ __forceinline__ void tiled_rowpos(const TileGeo& g, int r, int& blk, int& w, int& sub) {
+  if (g.down) {
+    blk = r / 128;
+    w = (r % 128) / 16;
+  } else if (r < g.inter) {
+    blk = r / 64;
+    w = (r % 64) / 16;
+  } else {
+    blk = (r - g.inter) / 64;
+    w = 4 + ((r - g.inter) % 64) / 16;
+  }
+  sub = r % 16;
+}
+
+__device__ __forceinline__ long long tiled_item(const TileGeo& g, int e, int blk, int c) {
+  return (long long)e * g.expert_bytes + (long long)(blk * g.nch + c) * g.item_bytes;
+}
+
+__device__ __forceinline__ TiledPos tiled_pos(const TileGeo& g, int e, int r, int k) {
+  int blk, w, sub;
+  tiled_rowpos(g, r, blk, w, sub);
+  const int c = k / g.CK, kk = k % g.CK;
+  const int G = kk / 64, t = (kk % 64) / 16, half = (kk % 16) / 8;
+  TiledPos p;
+  p.block = tiled_item(g, e, blk, c) +
+            (long long)(w * g.ng + G) * (g.fmt == MOE_FMT_AFFINE3_G64 ? 384 : 512);
+  p.lane = (sub & 7) * 4 + t;
+  p.widx = (sub >> 3) * 2 + half;
+  p.nib = k % 8;
+  return p;
+}
+
+// one thread per (expert, item, tile w, group G, lane): the lane's four words
+__global__ void k_repack_codes(TileGeo g, int E, const uint32_t* __restrict__ wc,
+                               uint8_t* __restrict__ out) {
+  const long long n = (long long)E * g.nblk * g.nch * 8 * g.ng * 32;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  long long q = i;
+  const int lane = int(q % 32); q /= 32;
+  const int G = int(q % g.ng); q /= g.ng;
+  const int w = int(q % 8); q /= 8;
+  const int c = int(q % g.nch); q /= g.nch;
+  const int blk = int(q % g.nblk); q /= g.nblk;
+  const int e = int(q);
+  const int gq = lane >> 2, t = lane & 3;
+  const int r0 = tiled_row(g, blk, w) + gq;
+  const int k0 = c * g.CK + 64 * G + 16 * t;
+  const long wpr = long(g.K) * fmt_bits(g.fmt) / 32;
+  uint32_t W[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = r0 + (j >> 1) * 8;
+    const uint32_t* row = wc + ((long long)e * g.rows + r) * wpr;
+    const int ks = k0 + 8 * (j & 1);
+    uint32_t v = 0;
+    for (int q2 = 0; q2 < 8; ++q2) v |= get_code(g.fmt, row, ks + q2) << (4 * q2);
+    W[j] = v;
+  }
+  uint8_t* blkp = out + tiled_item(g, e, blk, c);
+  if (g.fmt == MOE_FMT_AFFINE3_G64) {
+    uint32_t* pl = reinterpret_cast<uint32_t*>(blkp + (long long)(w * g.ng + G) * 384) + lane;
+    pl[0] = planes_l(W[0], W[1]);
+    pl[32] = planes_l(W[2], W[3]);
+    pl[64] = planes_h(W[0], W[1], W[2], W[3]);
+  } else {
+    *reinterpret_cast<uint4*>(blkp + (long long)(w * g.ng + G) * 512 + lane * 16) =
+        make_uint4(W[0], W[1], W[2], W[3]);
+  }
+}
+
+// Scale-group size of a format and the number of its groups in one item.
+__host__ __device__ inline int tiled_gsz(const TileGeo& g) {
+  return g.fmt == MOE_FMT_W4A16_SYM_G128 ? 128 : 64;
+}
+
+// one thread per (expert, item, tile w, scale group G', fragment row g)
+__global__ void k_repack_scales(TileGeo g, int E, const uint16_t* __restrict__ s,
+                                const uint16_t* __restrict__ b, uint8_t* __restrict__ out) {
+  const int gsz = tiled_gsz(g);
+  const int nsg = g.CK / gsz;
+  const long long n = (long long)E * g.nblk * g.nch * 8 * nsg * 8;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  long long q = i;
+  const int gq = int(q % 8); q /= 8;
+  const int G = int(q % nsg); q /= nsg;
+  const int w = int(q % 8); q /= 8;
+  const int c = int(q % g.nch); q /= g.nch;
+  const int blk = int(q % g.nblk); q /= g.nblk;
+  const int e = int(q);
+  const int r0 = tiled_row(g, blk, w) + gq;
+  const int gpr = g.K / gsz;
+  const long long i0 = ((long long)e * g.rows + r0) * gpr + c * nsg + G;
+  const long long i1 = i0 + 8LL * gpr;
+  uint8_t* sc = out + tiled_item(g, e, blk, c) + g.code_bytes;
+  if (g.fmt == MOE_FMT_W4A16_SYM_G128) {
+    *reinterpret_cast<uint32_t*>(sc + ((w * nsg + G) * 8 + gq) * 4) =
+        uint32_t(s[i0]) | (uint32_t(s[i1]) << 16);
+  } else {
+    *reinterpret_cast<uint2*>(sc + ((w * nsg + G) * 8 + gq) * 8) =
+        make_uint2(uint32_t(s[i0]) | (uint32_t(b[i0]) << 16),
+                   uint32_t(s[i1]) | (uint32_t(b[i1]) << 16));
+  }
+}
+
+__device__ __forceinline__ uint32_t tiled_code(const TileGeo& g, const uint8_t* tl, int e, int r,
+                                               int k) {
+  const TiledPos p = tiled_pos(g, e, r, k);
+  uint32_t W;
+  if (g.fmt == MOE_FMT_AFFINE3_G64) {
+    const uint32_t* pl = reinterpret_cast<const uint32_t*>(tl + p.block) + p.lane;
+    uint32_t w0, w1, w2, w3;
+    planes_to_words(pl[0], pl[32], pl[64], w0, w1, w2, w3);
+    W = p.widx == 0 ? w0 : p.widx == 1 ? w1 : p.widx == 2 ? w2 : w3;
+  } else {
+    W = reinterpret_cast<const uint32_t*>(tl + p.block + p.lane * 16)[p.widx];
+  }
+  return (W >> (4 * p.nib)) & 15u;
+}
+
+// one thread per canonical packed word
+__global__ void k_unrepack_codes(TileGeo g, int E, const uint8_t* __restrict__ tl,
+                                 uint32_t* __restrict__ wc) {
+  const int bits = fmt_bits(g.fmt);
+  const long wpr = long(g.K) * bits / 32;
+  const long long n = (long long)E * g.rows * wpr;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const long long er = i / wpr;
+  const int j = int(i - er * wpr);
+  const int e = int(er / g.rows), r = int(er % g.rows);
+  uint32_t v = 0;
+  if (g.fmt == MOE_FMT_AFFINE3_G64) {
+    for (int b = 0; b < 32; ++b) {
+      const long s = long(j) * 32 + b;
+      v |= ((tiled_code(g, tl, e, r, int(s / 3)) >> (s % 3)) & 1u) << b;
+    }
+  } else {
+    for (int q = 0; q < 8; ++q) v |= tiled_code(g, tl, e, r, 8 * j + q) << (4 * q);
+  }
+  wc[i] = v;
+}
+
+// one thread per canonical scale (and bias) entry
+__global__ void k_unrepack_scales(TileGeo g, int E, const uint8_t* __restrict__ tl,
+                                  uint16_t* __restrict__ s, uint16_t* __restrict__ b) {
+  const int gsz = tiled_gsz(g);
+  const int gpr = g.K / gsz, nsg = g.CK / gsz;
+  const long long n = (long long)E * g.rows * gpr;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const long long er = i / gpr;
+  const int gi = int(i - er * gpr);
+  const int e = int(er / g.rows), r = int(er % g.rows);
+  int blk, w, sub;
+  tiled_rowpos(g, r, blk, w, sub);
+  const int c = gi / nsg, G = gi % nsg, gq = sub & 7, hi = sub >> 3;
+  const uint8_t* sc = tl + tiled_item(g, e, blk, c) + g.code_bytes;
+  if (g.fmt == MOE_FMT_W4A16_SYM_G128) {
+    s[i] = reinterpret_cast<const uint16_t*>(sc + ((w * nsg + G) * 8 + gq) * 4)[hi];
+  } else {
+    const uint16_t* ent = reinterpret_cast<const uint16_t*>(sc + ((w * nsg + G) * 8 + gq) * 8);
+    s[i] = ent[2 * hi];
+    b[i] = ent[2 * hi + 1];
+  }
+}
+
+unsigned blocks_for(long long n) { return unsigned((n + 255) / 256); }
+
 }  // namespace
+
+cudaError_t launch_repack(const TileGeo& g, int E, const uint32_t* wc, const uint16_t* s,
+                          const uint16_t* b, uint8_t* tiled, cudaStream_t st) {
+  const long long nc = (long long)E * g.nblk * g.nch * 8 * g.ng * 32;
+  const long long ns = (long long)E * g.nblk * g.nch * 8 * (g.CK / tiled_gsz(g)) * 8;
+  if (nc == 0) return cudaSuccess;
+  k_repack_codes<<<blocks_for(nc), 256, 0, st>>>(g, E, wc, tiled);
+  k_repack_scales<<<blocks_for(ns), 256, 0, st>>>(g, E, s, b, tiled);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unrepack(const TileGeo& g, int E, const uint8_t* tiled, uint32_t* wc,
+                            uint16_t* s, uint16_t* b, cudaStream_t st) {
+  const long long nc = (long long)E * g.rows * (long long)g.K * fmt_bits(g.fmt) / 32;
+  const long long ns = (long long)E * g.rows * (g.K / tiled_gsz(g));
+  if (nc == 0) return cudaSuccess;
+  k_unrepack_codes<<<blocks_for(nc), 256, 0, st>>>(g, E, tiled, wc);
+  k_unrepack_scales<<<blocks_for(ns), 256, 0, st>>>(g, E, tiled, s, b);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pack(int fmt, const uint8_t* codes, int rows, int cols, uint32_t* packed,
                         cudaStream_t st) {

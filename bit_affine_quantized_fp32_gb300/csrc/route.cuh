@@ -1,0 +1,423 @@
+// route.cuh -- routing as CTA/warp-level device functions: router logits,
+// top-k with routing weights, bucketing, active-expert slots.  Used by the
+// standalone routing kernels and by the fused decode kernel.
+//
+// Source: "qwen3_5_moe on native CUDA with 3-bit routed experts ... #803",
+// comment "Progress on the 4-bit gate": fp32 logits over the experts and the
+// shared expert's gate row, top-k by logit with ties to the lower id, weights
+// exp(l - l_top) over the k (normalised over the k here), the shared expert
+// weighted by sigmoid(gate).  Bucketing (a stable counting sort of the
+// assignments by expert) feeds the grouped experts of "Sage-A1.5 ... on the
+// XPU backend #1329" (Proposal: grouped MoE).
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kRouterTT = 64;  // tokens per pass of a router block
+
+// Four consecutive weights of row r at column k (k % 4 == 0) as fp32.
+__device__ __forceinline__ void router_load_w4(int fmt, const void* q, const uint16_t* s,
+                                               const uint16_t* b, int r, int H, int k,
+                                               float (&w)[4]) {
+  if (fmt == MOE_FMT_F32) {
+    const float4 v =
+        *reinterpret_cast<const float4*>(static_cast<const float*>(q) + size_t(r) * H + k);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if (fmt == MOE_FMT_BF16 || fmt == MOE_FMT_F16) {
+    const uint2 v =
+        *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(q) + size_t(r) * H + k);
+    const bool f16 = fmt == MOE_FMT_F16;
+    w[0] = act_to_float(uint16_t(v.x & 0xFFFF), f16);
+    w[1] = act_to_float(uint16_t(v.x >> 16), f16);
+    w[2] = act_to_float(uint16_t(v.y & 0xFFFF), f16);
+    w[3] = act_to_float(uint16_t(v.y >> 16), f16);
+  } else {  // MOE_FMT_AFFINE8_G64: w = scale * q + bias
+    const uint32_t word = static_cast<const uint32_t*>(q)[size_t(r) * (H / 4) + k / 4];
+    const size_t gi = size_t(r) * (H / 64) + k / 64;
+    const float sc = half_bits_to_float(s[gi]);
+    const float bi = half_bits_to_float(b[gi]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = fmaf(sc, float((word >> (8 * j)) & 0xFFu), bi);
+  }
+}
+
+// Router block rb (8 warps): rows [rb*RPB, rb*RPB + RPB) of the router plus
+// the shared-gate row (row E), RPB = 8 / KS; warp (row, q) holds the 4*NI
+// weights of its k-split q in registers and runs over the tokens; the KS
+// partial sums of a row are added in a fixed order.  xs points at the x rows
+// of tokens t0 .. t0+tn-1 (row stride H; global or shared memory), tn <=
+// kRouterTT.  `part` is 8 x kRouterTT floats of shared memory.  Needs
+// blockDim.x == 256.  A token's logit does not depend on the other tokens.
+template <int NI>
+__device__ __forceinline__ void router_block(const RouterJob& J, int KS, int rb, float* part,
+                                             const uint16_t* xs, int t0, int tn) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int RPB = 8 / KS;
+  const int rl = wid / KS, q = wid - rl * KS;
+  const int row = rb * RPB + rl;
+  const int nrows = J.E + (J.gq ? 1 : 0);
+  const bool active = row < nrows;
+  const int kq = q * (J.H / KS);
+  float w[NI][4];
+  if (active) {
+    const bool gate = row >= J.E;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int k = kq + 128 * i + 4 * lane;
+      if (gate)
+        router_load_w4(J.gfmt, J.gq, J.gs, J.gb, 0, J.H, k, w[i]);
+      else
+        router_load_w4(J.fmt, J.q, J.s, J.b, row, J.H, k, w[i]);
+    }
+  }
+  for (int tl = 0; tl < tn; tl += 4) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (active) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (tl + u < tn) {
+          const uint16_t* xr = xs + size_t(tl + u) * J.H;
+#pragma unroll
+          for (int i = 0; i < NI; ++i) {
+            const uint2 v = *reinterpret_cast<const uint2*>(xr + kq + 128 * i + 4 * lane);
+            acc[u] = fmaf(w[i][0], act_to_float(uint16_t(v.x & 0xFFFF), J.f16), acc[u]);
+            acc[u] = fmaf(w[i][1], act_to_float(uint16_t(v.x >> 16), J.f16), acc[u]);
+            acc[u] = fmaf(w[i][2], act_to_float(uint16_t(v.y & 0xFFFF), J.f16), acc[u]);
+            acc[u] = fmaf(w[i][3], act_to_float(uint16_t(v.y >> 16), J.f16), acc[u]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+      if (lane == 0 && tl + u < tn) part[wid * kRouterTT + tl + u] = acc[u];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < RPB * tn; i += blockDim.x) {
+    const int r2 = i / tn, tl = i - r2 * tn;
+    const int row2 = rb * RPB + r2;
+    if (row2 >= nrows) continue;
+    float s = 0.f;
+    for (int qq = 0; qq < KS; ++qq) s += part[(r2 * KS + qq) * kRouterTT + tl];
+    if (row2 < J.E) {
+      if (J.bias) s += J.bias[row2];
+      J.logits[size_t(t0 + tl) * J.E + row2] = s;
+    } else {
+      J.gate_logit[t0 + tl] = s;
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void router_block_any(const RouterJob& J, int KS, int rb, float* part,
+                                                 const uint16_t* xs, int t0, int tn) {
+  const int NI = J.H / (KS * 128);
+  if (NI == 1)
+    router_block<1>(J, KS, rb, part, xs, t0, tn);
+  else if (NI == 2)
+    router_block<2>(J, KS, rb, part, xs, t0, tn);
+  else if (NI == 3)
+    router_block<3>(J, KS, rb, part, xs, t0, tn);
+  else
+    router_block<4>(J, KS, rb, part, xs, t0, tn);
+}
+
+// Ranking key of (logit v, expert id): a larger key ranks first.  The high
+// word is an order-preserving image of the float (-0 folded onto +0, so equal
+// logits tie), 0 for NaN; the low word is 256 - id, so equal logits go to the
+// lower id and every real key is >= 1 (0 marks "no expert").
+__device__ __forceinline__ unsigned long long rank_key(float v, int id) {
+  unsigned u = __float_as_uint(v == 0.f ? 0.f : v);
+  unsigned hi = (v != v) ? 0u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+  return ((unsigned long long)hi << 32) | unsigned(256 - id);
+}
+
+__device__ __forceinline__ float key_value(unsigned hi) {
+  if (hi == 0u) return __uint_as_float(0x7fc00000u);
+  return __uint_as_float((hi & 0x80000000u) ? (hi & 0x7fffffffu) : ~hi);
+}
+
+// Top-k + weights of token t by one warp: each lane sorts the keys of experts
+// lane, lane+32, ... (8 at most) once; each of the k rounds takes the warp
+// maximum of the lanes' heads (two redux.max) and the winning lane pops its
+// head.  Then w_j = exp(l_j - l_0) / sum.  Logits are read through L2 (they
+// may come from other CTAs of this kernel).
+__device__ __forceinline__ void topk_warp(const float* logits, const float* gate_logit, int t,
+                                          int E, int k, int32_t* idx, float* w, float* sg,
+                                          int32_t* idx2, float* w2, int* idx_smem = nullptr) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = e < E ? rank_key(__ldcg(logits + size_t(t) * E + e), e) : 0ull;
+  }
+  // sorting network (descending), 19 compare-exchanges
+#define MOE_CX(a, b)                                  \
+  {                                                   \
+    const unsigned long long x_ = key[a], y_ = key[b]; \
+    key[a] = x_ > y_ ? x_ : y_;                       \
+    key[b] = x_ > y_ ? y_ : x_;                       \
+  }
+  MOE_CX(0, 1) MOE_CX(2, 3) MOE_CX(4, 5) MOE_CX(6, 7)
+  MOE_CX(0, 2) MOE_CX(1, 3) MOE_CX(4, 6) MOE_CX(5, 7)
+  MOE_CX(1, 2) MOE_CX(5, 6) MOE_CX(0, 4) MOE_CX(3, 7)
+  MOE_CX(1, 5) MOE_CX(2, 6)
+  MOE_CX(1, 4) MOE_CX(3, 6)
+  MOE_CX(2, 4) MOE_CX(3, 5)
+  MOE_CX(3, 4)
+#undef MOE_CX
+  int sel_e[8];
+  float sel_v[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    sel_e[r] = 0;
+    sel_v[r] = 0.f;
+    if (r < k) {
+      const unsigned hi = unsigned(key[0] >> 32), lo = unsigned(key[0]);
+      const unsigned mh = __reduce_max_sync(0xffffffffu, hi);
+      const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
+      if (hi == mh && lo == ml) {
+#pragma unroll
+        for (int i = 0; i < 7; ++i) key[i] = key[i + 1];
+        key[7] = 0ull;
+      }
+      sel_e[r] = 256 - int(ml);
+      sel_v[r] = key_value(mh);
+    }
+  }
+  if (lane == 0) {
+    const float top = sel_v[0];
+    float ex[8];
+    float den = 0.f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      ex[r] = r < k ? expf(sel_v[r] - top) : 0.f;
+      if (r < k) den += ex[r];
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (r < k) {
+        const float wr = ex[r] / den;
+        idx[size_t(t) * k + r] = sel_e[r];
+        w[size_t(t) * k + r] = wr;
+        if (idx2) idx2[size_t(t) * k + r] = sel_e[r];
+        if (w2) w2[size_t(t) * k + r] = wr;
+        if (idx_smem) idx_smem[t * k + r] = sel_e[r];
+      }
+    }
+    if (gate_logit && sg) sg[t] = 1.f / (1.f + expf(-__ldcg(gate_logit + t)));
+  }
+}
+
+// Shared memory of bucket_cta for NW warps.
+struct BucketSmem {
+  int cnt[256];
+  int cur[256];
+  int wsum[32];
+  int wc[32][256];
+};
+
+// Stable counting sort of the N assignment ids by expert (one CTA of NW
+// warps): histogram, exclusive prefix sum over <= 256 experts, then chunks of
+// 32*NW assignments in order, ranked inside a chunk with warp match + per-warp
+// counts.  Ids outside 0..E-1 are skipped.
+__device__ __forceinline__ void bucket_cta(const int32_t* idx, int N, int E, int32_t* offsets,
+                                           int32_t* perm, BucketSmem& S) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int NT = blockDim.x, NW = NT >> 5;
+  for (int i = tid; i < 256; i += NT) S.cnt[i] = 0;
+  __syncthreads();
+  for (int a = tid; a < N; a += NT) {
+    const int e = __ldcg(idx + a);
+    if (e >= 0 && e < E) atomicAdd(&S.cnt[e], 1);
+  }
+  __syncthreads();
+  // exclusive scan of cnt[0..255] by the first 8 warps
+  int incl = 0;
+  if (tid < 256) {
+    incl = tid < E ? S.cnt[tid] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) S.wsum[wid] = incl;
+  }
+  __syncthreads();
+  if (tid < 256) {
+    int pre = 0;
+    for (int i = 0; i < wid; ++i) pre += S.wsum[i];
+    incl += pre;
+    const int c = tid < E ? S.cnt[tid] : 0;
+    S.cur[tid] = incl - c;
+    if (tid < E) offsets[tid + 1] = incl;
+    if (tid == 0) offsets[0] = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < N; base += NT) {
+    for (int i = lane; i < 256; i += 32) S.wc[wid][i] = 0;
+    __syncwarp();
+    const int a = base + tid;
+    int e = a < N ? __ldcg(idx + a) : -1;
+    if (e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const bool leader = (__ffs(peers) - 1) == lane;
+    if (e >= 0 && leader) S.wc[wid][e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int pre = 0;
+      for (int i = 0; i < wid; ++i) pre += S.wc[i][e];
+      perm[S.cur[e] + pre + rank] = a;
+    }
+    __syncthreads();
+    for (int x = tid; x < E; x += NT) {
+      int tot = 0;
+      for (int i = 0; i < NW; ++i) tot += S.wc[i][x];
+      S.cur[x] += tot;
+    }
+    __syncthreads();
+  }
+}
+
+// Sub-slots from the bucket offsets: every active expert (ascending id) is
+// cut into runs of at most 8 bucket positions; also the token of every bucket
+// position.  Needs blockDim.x >= 256 (the first 256 threads scan).
+__device__ __forceinline__ void subslots_cta(const int32_t* offsets, const int32_t* perm, int P,
+                                             int k, int E, int* nss, int* se, int* so, int* sc,
+                                             int* blist, int* wcount /* 8 ints of smem */) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int c = 0, off = 0, nsub = 0, incl = 0;
+  if (tid < 256) {
+    if (tid < E) {
+      off = __ldcg(offsets + tid);
+      c = __ldcg(offsets + tid + 1) - off;
+    }
+    nsub = (c + 7) >> 3;
+    incl = nsub;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wcount[wid] = incl;
+  }
+  __syncthreads();
+  if (tid < 256) {
+    int pre = 0;
+    for (int i = 0; i < wid; ++i) pre += wcount[i];
+    const int base = pre + incl - nsub;
+    for (int i = 0; i < nsub; ++i) {
+      se[base + i] = tid;
+      so[base + i] = off + 8 * i;
+      sc[base + i] = min(8, c - 8 * i);
+    }
+    if (tid == 0) {
+      int tot = 0;
+      for (int i = 0; i < 8; ++i) tot += wcount[i];
+      *nss = tot;
+    }
+  }
+  for (int p = tid; p < P; p += blockDim.x) blist[p] = __ldcg(perm + p) / k;
+  __syncthreads();
+}
+
+// Routing of a decode batch (T*k <= 256 assignments) by one CTA of 256
+// threads, with every intermediate in shared memory: top-k + weights (also
+// stored to idx/w/sg and the optional user outputs), the bucket offsets and
+// permutation (the stable counting sort of bucket_cta), and the sub-slot
+// table of subslots_cta plus the token of each sub-slot position (rows,
+// 8 per sub-slot).  Same definitions as the global kernels, same results.
+struct SmallRouteSmem {
+  int idx[256];
+  int cnt[256];
+  int off[256];
+  int sbase[256];
+  int perm[256];
+  int wc[8][256];
+  int wsum[8];
+  int wsub[8];
+};
+
+__device__ __forceinline__ void route_small_cta(const float* logits, const float* gate_logit,
+                                                int T, int E, int k, int32_t* idx_g, float* w_g,
+                                                float* sg, int32_t* user_idx, float* user_w,
+                                                int32_t* offsets_g, int32_t* perm_g, int* nss_g,
+                                                int* se_g, int* so_g, int* sc_g, int* rows_g,
+                                                SmallRouteSmem& S) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int N = T * k;
+  S.cnt[tid] = 0;
+  for (int i = lane; i < 256; i += 32) S.wc[wid][i] = 0;
+  for (int t = wid; t < T; t += 8)
+    topk_warp(logits, gate_logit, t, E, k, idx_g, w_g, sg, user_idx, user_w, S.idx);
+  __syncthreads();
+  const int e_a = tid < N ? S.idx[tid] : -1;
+  if (e_a >= 0) atomicAdd(&S.cnt[e_a], 1);
+  __syncthreads();
+  // exclusive scans of the counts and of the sub-slot counts over experts
+  const int c = tid < E ? S.cnt[tid] : 0;
+  const int ns = (c + 7) >> 3;
+  int ic = c, isub = ns;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y1 = __shfl_up_sync(0xffffffffu, ic, o);
+    const int y2 = __shfl_up_sync(0xffffffffu, isub, o);
+    if (lane >= o) {
+      ic += y1;
+      isub += y2;
+    }
+  }
+  if (lane == 31) {
+    S.wsum[wid] = ic;
+    S.wsub[wid] = isub;
+  }
+  __syncthreads();
+  int pc = 0, ps = 0;
+  for (int i = 0; i < wid; ++i) {
+    pc += S.wsum[i];
+    ps += S.wsub[i];
+  }
+  S.off[tid] = pc + ic - c;
+  S.sbase[tid] = ps + isub - ns;
+  if (tid < E) offsets_g[tid + 1] = pc + ic;
+  if (tid == 0) {
+    offsets_g[0] = 0;
+    int tot = 0;
+    for (int i = 0; i < 8; ++i) tot += S.wsub[i];
+    *nss_g = tot;
+  }
+  // stable scatter: rank among the same expert's assignments, in id order
+  const unsigned peers = __match_any_sync(0xffffffffu, e_a);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (e_a >= 0 && (__ffs(peers) - 1) == lane) S.wc[wid][e_a] = __popc(peers);
+  __syncthreads();
+  if (e_a >= 0) {
+    int pre = 0;
+    for (int i = 0; i < wid; ++i) pre += S.wc[i][e_a];
+    const int pos = S.off[e_a] + pre + rank;
+    S.perm[pos] = tid;
+    perm_g[pos] = tid;
+  }
+  __syncthreads();
+  // sub-slot table: expert tid's runs of at most 8 positions
+  for (int i = 0; i < ns; ++i) {
+    const int ss = S.sbase[tid] + i;
+    const int o = S.off[tid] + 8 * i;
+    const int ci = min(8, c - 8 * i);
+    se_g[ss] = tid;
+    so_g[ss] = o;
+    sc_g[ss] = ci;
+    for (int n = 0; n < 8; ++n) rows_g[ss * 8 + n] = n < ci ? S.perm[o + n] / k : 0;
+  }
+  __syncthreads();
+}
+
+}  // namespace moe

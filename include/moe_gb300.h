@@ -93,15 +93,28 @@ typedef struct moe_qmatrix {
   const void* biases;
 } moe_qmatrix;
 
-/* n_experts experts in one quantised format, stacked contiguously:
+/* Storage layouts of an expert bank. */
+typedef enum moe_layout {
+  MOE_LAYOUT_CANONICAL = 0, /* the format's own row-major words + scale tables */
+  MOE_LAYOUT_TILED = 1      /* kernel-tiled (moe_repack_bank), read by the expert kernels */
+} moe_layout;
+
+/* n_experts experts in one quantised format.
+ * CANONICAL layout, stacked contiguously:
  *   w13 [E][2*inter][hidden] : gate rows 0..inter-1, then up rows
  *   w2  [E][hidden][inter]   : down projection
- * with s13/b13 and s2/b2 their fp16 scales/biases ([E][rows][cols/G]).  */
+ * with s13/b13 and s2/b2 their fp16 scales/biases ([E][rows][cols/G]).
+ * TILED layout (produced by moe_repack_bank): w13 and w2 each point at one
+ * buffer of moe_tiled_bytes() bytes holding codes, scales and biases cut
+ * into per-(expert, 128-row block, k-chunk) blocks in MMA fragment order;
+ * s13/b13/s2/b2 are NULL.  The expert kernels read TILED banks only.  */
 typedef struct moe_expert_bank {
   int32_t fmt;
   int32_t n_experts;
   int32_t inter;
   int32_t hidden;
+  int32_t layout;   /* moe_layout */
+  int32_t reserved;
   const void* w13;
   const void* s13;
   const void* b13;
@@ -112,6 +125,8 @@ typedef struct moe_expert_bank {
 
 /* flags of moe_experts_forward / moe_layer_forward */
 #define MOE_FLAG_FORCE_DECODE 1   /* use the decode (grouped GEMV) kernels at any T */
+#define MOE_FLAG_UNFUSED 2        /* moe_layer_forward: one launch per step instead of the
+                                     single persistent decode launch (same results) */
 
 /* Decode path is taken for n_tokens <= MOE_DECODE_MAX_TOKENS. */
 #define MOE_DECODE_MAX_TOKENS 32
@@ -127,7 +142,8 @@ const char* moe_last_error(void);
 size_t moe_workspace_bytes(int max_tokens, int n_experts, int top_k, int hidden, int inter);
 
 /* Zero the workspace's control words (status, counters).  Call once after
- * allocating a workspace, before its first use. */
+ * allocating a workspace, before its first use, and again after a call
+ * reported MOE_ERR_TIMEOUT through moe_get_device_status. */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Read and clear the device status word of a workspace (synchronises the
@@ -177,8 +193,9 @@ moe_status moe_bucket(const int32_t* topk_idx, int n_tokens, int top_k, int n_ex
  *   h_out nullable [T, inter] fp32, y_out [T, hidden] fp32.
  * moe_shared_expert is the same for expert 0 of a one-expert bank:
  *   y_shared [T, hidden] fp32.
- * Formats: AFFINE4_G64, AFFINE3_G64 (hidden and inter multiples of 128),
- * W4A16_SYM_G128 (multiples of 256); inter and hidden multiples of 16.
+ * Banks must be TILED (moe_repack_bank).  Formats: AFFINE4_G64,
+ * AFFINE3_G64 (hidden and inter multiples of 128), W4A16_SYM_G128 (multiples
+ * of 256); inter <= 512.
  */
 moe_status moe_expert_mlp(const moe_expert_bank* bank, int expert, const void* x, int act,
                           int n_tokens, float* h_out, float* y_out, void* ws, size_t ws_bytes,
@@ -205,7 +222,12 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
 
 /* The whole layer in one call: route, shared expert, routed experts, combine.
  * shared (nullable) is a one-expert bank; shared_gate nullable.
- * topk_idx/topk_w nullable outputs [T, k]. */
+ * topk_idx/topk_w nullable outputs [T, k].
+ * For n_tokens <= MOE_DECODE_MAX_TOKENS the layer runs as ONE persistent
+ * cooperative launch (one CTA per SM) whose phases synchronise through
+ * counters in the workspace; every wait is bounded and reports
+ * MOE_ERR_TIMEOUT in the workspace status word instead of hanging.  The
+ * results are bit-identical to the multi-launch path (MOE_FLAG_UNFUSED). */
 moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
                              const moe_qmatrix* shared_gate, const moe_expert_bank* experts,
                              const moe_expert_bank* shared, const void* x, int act,
@@ -235,6 +257,22 @@ moe_status moe_pack_w4a16_g128(const int8_t* codes, int rows, int cols, uint32_t
                                cudaStream_t stream);
 moe_status moe_unpack_w4a16_g128(const uint32_t* packed, int rows, int cols, int8_t* codes,
                                  cudaStream_t stream);
+
+/* Kernel-tiled expert layout.  The pages' engine likewise keeps its experts
+ * in kernel tables of its own (gate and up interleaved per group, "Progress
+ * on the 4-bit gate" comment of "qwen3_5_moe on native CUDA with 3-bit routed
+ * experts ... #803").  A TILED bank holds exactly the canonical bank's codes,
+ * scales and biases, rearranged (the 3-bit codes as bit planes, 3 bits each).
+ *   moe_tiled_bytes    bytes of the w13 (which = 0) or w2 (which = 1) buffer
+ *                      of a TILED bank; 0 on invalid arguments.
+ *   moe_repack_bank    CANONICAL bank -> the two TILED buffers (device).
+ *   moe_unrepack_bank  TILED bank -> canonical words/scales/biases
+ *                      (b13/b2 ignored for W4A16); unrepack(repack(x)) == x. */
+size_t moe_tiled_bytes(int fmt, int n_experts, int inter, int hidden, int which);
+moe_status moe_repack_bank(const moe_expert_bank* canonical, void* w13_tiled, void* w2_tiled,
+                           cudaStream_t stream);
+moe_status moe_unrepack_bank(const moe_expert_bank* tiled, void* w13, void* s13, void* b13,
+                             void* w2, void* s2, void* b2, cudaStream_t stream);
 
 /* Dequantise any matrix to fp32: w = fmaf(scale, q, bias) for affine (the
  * exact value scale*q + bias rounded once to fp32) or scale * q for W4A16

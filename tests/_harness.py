@@ -121,6 +121,11 @@ def gpu_matrix(m: synth.QMatrix):
 
 
 def gpu_bank(b: synth.ExpertBank):
+    """The bank in the TILED layout the expert kernels read."""
+    return gpu_bank_canonical(b).tiled()
+
+
+def gpu_bank_canonical(b: synth.ExpertBank):
     from bit_affine_quantized_fp32_gb300 import capi
     t = torch()
     E, I, H = b.E, b.I, b.H

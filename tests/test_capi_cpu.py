@@ -53,10 +53,10 @@ def test_workspace_bytes(capi):
     assert capi.moe_workspace_bytes(4, 256, 8, 2000, 512) == 0
 
 
-def _bank(fmt, E=8, I=128, H=256, base=1 << 20):
+def _bank(fmt, E=8, I=128, H=256, base=1 << 20, layout=1):
     S = capi_mod().ExpertBankS
     p = [base + 4096 * i for i in range(6)]
-    return S(capi_mod().FMT[fmt], E, I, H, *p)
+    return S(capi_mod().FMT[fmt], E, I, H, layout, 0, *p)
 
 
 def capi_mod():
@@ -75,7 +75,7 @@ def test_refuses_unread_width_by_name(capi):
     assert rc == 2
     assert b"AFFINE8_G64" in capi.lib.moe_last_error()
     S = capi.ExpertBankS
-    rc = _call_experts(capi, S(42, 8, 128, 256, *[1 << 20] * 6))
+    rc = _call_experts(capi, S(42, 8, 128, 256, 1, 0, *[1 << 20] * 6))
     assert rc == 2
 
 
@@ -88,8 +88,46 @@ def test_refuses_bad_shapes_and_pointers(capi):
     assert _call_experts(capi, _bank("affine4_g64"), ws=None) == 3        # no workspace
     assert _call_experts(capi, _bank("affine4_g64"), wsb=1024) == 3       # too small
     S = capi.ExpertBankS
-    nul = S(capi.FMT["affine4_g64"], 8, 128, 256, None, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20)
+    nul = S(capi.FMT["affine4_g64"], 8, 128, 256, 1, 0, None, 1 << 20, 1 << 20, 1 << 20, 1 << 20,
+            1 << 20)
     assert _call_experts(capi, nul) == 1
+    # the expert kernels read the tiled layout only
+    assert _call_experts(capi, _bank("affine4_g64", layout=0)) == 1
+    assert b"TILED" in capi.lib.moe_last_error()
+
+
+@pytest.mark.parametrize("fmt,bits,G,bias", [("affine4_g64", 4, 64, True),
+                                             ("affine3_g64", 3, 64, True),
+                                             ("w4a16_g128", 4, 128, False)])
+@pytest.mark.parametrize("E,I,H", [(256, 512, 2048), (3, 256, 768), (1, 512, 1024)])
+def test_tiled_bytes_equal_canonical_bytes(capi, fmt, bits, G, bias, E, I, H):
+    """The tiled layout only rearranges: codes at exactly `bits` bits each plus
+    one fp16 scale (and bias) per group, nothing padded."""
+    if fmt == "w4a16_g128" and (I % 256 or H % 256):
+        pytest.skip("W4A16 shapes are multiples of 256")
+    for which, rows, cols in ((0, 2 * I, H), (1, H, I)):
+        want = E * rows * (cols * bits // 8 + (cols // G) * 2 * (2 if bias else 1))
+        assert capi.lib.moe_tiled_bytes(capi.FMT[fmt], E, I, H, which) == want
+
+
+def test_tiled_bytes_refuses_bad_shapes(capi):
+    assert capi.lib.moe_tiled_bytes(capi.FMT["affine4_g64"], 8, 100, 256, 0) == 0
+    assert capi.lib.moe_tiled_bytes(capi.FMT["affine8_g64"], 8, 128, 256, 0) == 0
+    assert capi.lib.moe_tiled_bytes(capi.FMT["affine4_g64"], 8, 128, 256, 2) == 0
+
+
+def test_repack_validation(capi):
+    S = capi.ExpertBankS
+    P = 1 << 21
+    canon = _bank("affine4_g64", layout=0)
+    assert capi.lib.moe_repack_bank(ctypes.byref(canon), None, P, None) == 1
+    assert capi.lib.moe_repack_bank(ctypes.byref(canon), P + 4, P, None) == 6
+    tiled = _bank("affine4_g64", layout=1)
+    assert capi.lib.moe_repack_bank(ctypes.byref(tiled), P, P, None) == 1
+    nob = S(capi.FMT["affine4_g64"], 8, 128, 256, 0, 0, P, P, None, P, P, None)
+    assert capi.lib.moe_repack_bank(ctypes.byref(nob), P, P, None) == 1
+    assert capi.lib.moe_unrepack_bank(ctypes.byref(canon), P, P, P, P, P, P, None) == 1
+    assert capi.lib.moe_unrepack_bank(ctypes.byref(tiled), P, P, None, P, P, P, None) == 1
 
 
 def test_route_validation(capi):

@@ -51,6 +51,101 @@ def test_pack_unpack_bitexact(capi, fmt, shape):
     assert np.array_equal(out.cpu().numpy().astype(np.int32), codes)
 
 
+EXPERT_FMTS = ["affine4_g64", "affine3_g64", "w4a16_g128"]
+
+
+def _tiled_reference(fmt, mats, I, H, which):
+    """The tiled buffer of one matrix family written out in numpy from the
+    layout's definition (blocks, chunks, (w, G) code blocks, lanes, planes,
+    scale entries), independent of the repack kernel."""
+    rows, K = (H, I) if which else (2 * I, H)
+    CK = 512 if K % 512 == 0 else (256 if K % 256 == 0 else 128)
+    ng, nch = CK // 64, K // CK
+    nblk = H // 128 if which else I // 64
+    w4 = fmt == "w4a16_g128"
+    out = bytearray()
+    for m in mats:
+        codes = m.codes.astype(np.int64) + (8 if w4 else 0)          # nibble values
+        words = np.zeros((rows, K // 8), dtype=np.uint64)
+        for i in range(8):
+            words |= (codes[:, i::8].astype(np.uint64) << np.uint64(4 * i))
+        words = words.astype(np.uint32)
+        sc = m.scales.view(np.uint16) if m.scales.dtype != np.uint16 else m.scales
+        bi = None if w4 else (m.biases.view(np.uint16) if m.biases.dtype != np.uint16 else m.biases)
+        for blk in range(nblk):
+            for c in range(nch):
+                item = bytearray()
+                for w in range(8):
+                    if which:
+                        base = blk * 128 + 16 * w
+                    else:
+                        base = blk * 64 + 16 * w if w < 4 else I + blk * 64 + 16 * (w - 4)
+                    for G in range(ng):
+                        lw = np.zeros((32, 4), dtype=np.uint32)
+                        for lane in range(32):
+                            g, t = lane // 4, lane % 4
+                            k0 = c * CK + 64 * G + 16 * t
+                            for j in range(4):
+                                r = base + g + 8 * (j >> 1)
+                                lw[lane, j] = words[r, (k0 + 8 * (j & 1)) // 8]
+                        if fmt == "affine3_g64":
+                            m3 = np.uint32(0x33333333)
+                            L01 = (lw[:, 0] & m3) | ((lw[:, 1] & m3) << np.uint32(2))
+                            L23 = (lw[:, 2] & m3) | ((lw[:, 3] & m3) << np.uint32(2))
+                            Hb = (((lw[:, 0] >> np.uint32(2)) & np.uint32(0x11111111))
+                                  | ((lw[:, 1] >> np.uint32(1)) & np.uint32(0x22222222))
+                                  | (lw[:, 2] & np.uint32(0x44444444))
+                                  | ((lw[:, 3] << np.uint32(1)) & np.uint32(0x88888888)))
+                            item += np.concatenate([L01, L23, Hb]).astype("<u4").tobytes()
+                        else:
+                            item += lw.astype("<u4").tobytes()
+                gs = 128 if w4 else 64
+                nsg = CK // gs
+                for w in range(8):
+                    if which:
+                        base = blk * 128 + 16 * w
+                    else:
+                        base = blk * 64 + 16 * w if w < 4 else I + blk * 64 + 16 * (w - 4)
+                    for G in range(nsg):
+                        for g in range(8):
+                            gi = c * nsg + G
+                            r0, r1 = base + g, base + g + 8
+                            if w4:
+                                ent = [sc[r0, gi], sc[r1, gi]]
+                            else:
+                                ent = [sc[r0, gi], bi[r0, gi], sc[r1, gi], bi[r1, gi]]
+                            item += np.array(ent, dtype="<u2").tobytes()
+                out += item
+    return np.frombuffer(bytes(out), dtype=np.uint8)
+
+
+@pytest.mark.parametrize("fmt", EXPERT_FMTS)
+def test_tiled_layout_matches_definition(capi, fmt):
+    I, H = (256, 512) if fmt == "w4a16_g128" else (128, 640)   # chunks 256/512 and 128/128
+    bank = synth.gen_bank(np.random.default_rng(41), fmt, 2, I, H)
+    tb = Hn.gpu_bank(bank)
+    got13 = tb.tensors[0].cpu().numpy()
+    got2 = tb.tensors[3].cpu().numpy()
+    assert np.array_equal(got13, _tiled_reference(fmt, bank.w13, I, H, 0))
+    assert np.array_equal(got2, _tiled_reference(fmt, bank.w2, I, H, 1))
+
+
+@pytest.mark.parametrize("fmt", EXPERT_FMTS)
+@pytest.mark.parametrize("E,I,H", [(3, 256, 768), (2, 512, 2048), (1, 256, 1280)])
+def test_repack_roundtrip_bitexact(capi, fmt, E, I, H):
+    if fmt == "w4a16_g128" and (H % 256 or I % 256):
+        pytest.skip("W4A16 shapes are multiples of 256")
+    bank = synth.gen_bank(np.random.default_rng(42 + E), fmt, E, I, H)
+    canon = Hn.gpu_bank_canonical(bank)
+    tiled = canon.tiled()
+    torch = Hn.torch()
+    outs = [torch.zeros_like(t) if t is not None else None for t in canon.tensors]
+    capi.moe_unrepack_bank(tiled, *outs)
+    for a, b in zip(canon.tensors, outs):
+        if a is not None:
+            assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("fmt", FMTS + ["f32", "bf16"])
 def test_dequant_bitexact(capi, fmt):
     rng = np.random.default_rng(7)
@@ -150,6 +245,8 @@ def test_topk_edge_rows(capi):
     r = -np.arange(E, dtype=np.float64); r[[0, 1]] = np.nan; rows.append(r)
     rng = np.random.default_rng(3)
     rows.append(rng.integers(-2, 3, E).astype(np.float64))  # many ties
+    r = np.full(E, -1.0); r[5] = -0.0; r[3] = 0.0; r[200] = -0.0; rows.append(r)  # -0 == +0
+    r = np.full(E, np.inf); r[[7, 9]] = np.nan; rows.append(r)  # +inf ties
     lg = np.stack(rows).astype(np.float32)
     T = lg.shape[0]
     idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
@@ -346,4 +443,51 @@ def test_validation_errors(capi):
     with pytest.raises(capi.MoeError) as e:
         capi.moe_layer_forward(g.router, None, None, bad, None, g.x, 2, out, ws=g.ws)
     assert e.value.status == 2 and "AFFINE8_G64" in str(e.value)
+    assert capi.moe_get_device_status(g.ws) == 0
+
+
+FUSED_CASES = [
+    dict(T=1, E=256, k=8, H=2048, I=512, expert_fmt="affine4_g64", seed=31),
+    dict(T=8, E=256, k=8, H=2048, I=512, expert_fmt="affine4_g64", shared_fmt="affine4_g64",
+         gate_fmt="affine8_g64", zipf=True, seed=32),
+    dict(T=4, E=64, k=8, H=1024, I=256, expert_fmt="affine3_g64", router_fmt="affine8_g64",
+         shared_fmt="affine4_g64", gate_fmt="affine8_g64", seed=33),
+    dict(T=32, E=128, k=8, H=1024, I=512, expert_fmt="w4a16_g128", shared_fmt="w4a16_g128",
+         gate_fmt="bf16", act="f16", seed=34),
+    dict(T=13, E=12, k=3, H=384, I=128, expert_fmt="affine4_g64", shared_fmt="affine3_g64",
+         seed=35),
+]
+
+
+@pytest.mark.parametrize("cfg", FUSED_CASES, ids=lambda c: f"T{c['T']}_{c['expert_fmt']}")
+def test_fused_layer_equals_unfused_and_oracle(capi, cfg):
+    """The single persistent launch gives the same bits as the launch-per-step
+    path, repeatably (its counters reset themselves), and matches the oracle."""
+    L = synth.gen_layer(**cfg)
+    g = Hn.GpuLayer(L)
+    torch = Hn.torch()
+    outs = []
+    for _ in range(3):
+        out, idx, w = g.forward()
+        outs.append((out.clone(), idx.clone(), w.clone()))
+    ref_out, ref_idx, ref_w = g.forward(flags=capi.MOE_FLAG_UNFUSED)
+    for out, idx, w in outs:
+        assert torch.equal(idx, ref_idx)
+        assert torch.equal(w, ref_w)
+        assert torch.equal(out, ref_out)
+    assert capi.moe_get_device_status(g.ws) == 0
+    ref = Hn.oracle_layer(L, idx_override=ref_idx.cpu().numpy())
+    Hn.assert_layer_close(Hn.to_np(outs[0][0]), ref["out"])
+
+
+def test_fused_alternating_shapes(capi):
+    """Fused calls of different token counts on one workspace."""
+    L = synth.gen_layer(T=32, E=64, k=8, H=512, I=256, expert_fmt="affine4_g64",
+                        shared_fmt="affine4_g64", gate_fmt="affine8_g64", zipf=True, seed=36)
+    g = Hn.GpuLayer(L, max_tokens=32)
+    torch = Hn.torch()
+    full, _, _ = g.forward()
+    for T in [1, 7, 32, 3, 16]:
+        part, _, _ = g.forward(g.x[:T].contiguous())
+        assert torch.equal(part, full[:T])
     assert capi.moe_get_device_status(g.ws) == 0
