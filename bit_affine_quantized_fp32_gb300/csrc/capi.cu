@@ -193,41 +193,69 @@ moe_status check_ws(void* ws, size_t ws_bytes, size_t need) {
   return MOE_OK;
 }
 
+// Engine configuration of one bank in slots 0 (w13) and 1 (w2), outputs to
+// the given h buffers / y.
+EngineCfg bank_cfg(const moe_expert_bank* bank, uint16_t* hh, uint16_t* hl, float* hsum,
+                   float* hout, float* y, int* status) {
+  EngineCfg C{};
+  C.geo[0] = geo13(bank);
+  C.geo[1] = geo2(bank);
+  C.geo[2] = C.geo[0];
+  C.geo[3] = C.geo[1];
+  C.tg[0] = MatTarget{hh, hl, hsum, hout, nullptr};
+  C.tg[1] = MatTarget{nullptr, nullptr, nullptr, nullptr, y};
+  C.fmt_shared = bank->fmt;
+  C.inter = bank->inter;
+  C.hidden = bank->hidden;
+  C.status = status;
+  return C;
+}
+
+// Gate/up then down units of one bank over a sub-slot list.  x rows are taken
+// by `xrows` (Direct: row = token; Gather: token of a bucket position), h is
+// kept at the unit's output rows, y written by `yrows` (Direct or Scatter).
+moe_status run_bank(const moe_expert_bank* bank, const SubSlots& ss, int max_ss, const void* x,
+                    bool f16, const float* xsum, int xrows, const int* perm, int k, uint16_t* hh,
+                    uint16_t* hl, float* hsum, float* hout, float* y, int yrows, int* status,
+                    cudaStream_t stream) {
+  const int sms = sm_count();
+  const int H = bank->hidden, I = bank->inter;
+  UnitJob J{};
+  J.C = bank_cfg(bank, hh, hl, hsum, hout, y, status);
+  J.mat = 0;
+  J.src = MatSource{static_cast<const uint16_t*>(x), nullptr, xsum, H,
+                    sums_ld(J.C.geo[0].t)};
+  J.rows = xrows;
+  J.ss = ss;
+  J.perm = perm;
+  J.k = k;
+  J.max_units = max_ss * (I / 64);
+  MOE_CUDA(launch_units(J, f16, sms, stream), "gate/up kernel");
+  UnitJob D = J;
+  D.mat = 1;
+  D.src = MatSource{hh, hl, hsum, I, sums_ld(J.C.geo[1].t)};
+  D.rows = yrows;
+  D.max_units = max_ss * (H / kUnitRows);
+  MOE_CUDA(launch_units(D, false, sms, stream), "down kernel");
+  return MOE_OK;
+}
+
 // One expert (a fixed slot holding every token) over the T rows of x, with
-// the given workspace layout: x prep -> gate/up units -> SwiGLU -> down units.
+// the given workspace layout: activation sums -> gate/up units (SwiGLU) ->
+// down units.
 moe_status run_expert_mlp(const moe_expert_bank* bank, int expert, const void* x, bool f16,
                           int T, float* h_out, float* y_out, void* ws, const WsLayout& L,
                           cudaStream_t stream) {
-  const int sms = sm_count();
-  const int H = bank->hidden, I = bank->inter;
-  uint16_t* xperm = reinterpret_cast<uint16_t*>(wsp(ws, L.xperm));
   float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
-  MOE_CUDA(launch_xprep(static_cast<const uint16_t*>(x), T, H, f16, xperm, xsum, stream), "x prep");
-  const int nss = (T + kMaxTok - 1) / kMaxTok;
-  UnitJob J{};
-  J.g = geo13(bank);
-  J.down = 0;
-  J.inter = I;
-  J.ss = SubSlots{nullptr, nullptr, nullptr, nullptr, expert, T};
-  J.op = OperandSrc{xperm, nullptr, xsum, nullptr};
-  J.hh = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh));
-  J.hl = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl));
-  J.hsum = reinterpret_cast<float*>(wsp(ws, L.sh_hsum));
-  J.hout = h_out;
-  J.status = static_cast<int*>(ws);
-  J.max_units = nss * (I / 64);
-  MOE_CUDA(launch_units(J, f16, sms, stream), "gate/up kernel");
-  UnitJob D{};
-  D.g = geo2(bank);
-  D.down = 1;
-  D.inter = I;
-  D.ss = J.ss;
-  D.op = OperandSrc{J.hh, J.hl, J.hsum, nullptr};
-  D.sink = Sink{y_out, nullptr, H};
-  D.status = static_cast<int*>(ws);
-  D.max_units = nss * (H / kUnitRows);
-  MOE_CUDA(launch_units(D, false, sms, stream), "down kernel");
-  return MOE_OK;
+  MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, bank->hidden, f16, geo13(bank).t, xsum,
+                       stream),
+           "activation sums");
+  const SubSlots ss{nullptr, nullptr, nullptr, nullptr, expert, T};
+  return run_bank(bank, ss, (T + kMaxTok - 1) / kMaxTok, x, f16, xsum, kRowsDirect, nullptr, 1,
+                  reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh)),
+                  reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl)),
+                  reinterpret_cast<float*>(wsp(ws, L.sh_hsum)), h_out, y_out, kRowsDirect,
+                  static_cast<int*>(ws), stream);
 }
 
 }  // namespace
@@ -326,7 +354,7 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
   if (!bucket_offsets || (T > 0 && (!topk_idx || !topk_w || !bucket_perm)))
     return fail(MOE_ERR_INVALID_ARG, "routing outputs must not be NULL");
   const WsLayout L = ws_layout(T, E, top_k, H, 128);
-  if ((s = check_ws(ws, ws_bytes, L.xperm))) return s;
+  if ((s = check_ws(ws, ws_bytes, L.part))) return s;
   float* lg = logits ? logits : reinterpret_cast<float*>(wsp(ws, L.logits));
   float* gl = reinterpret_cast<float*>(wsp(ws, L.gate_logit));
   RouterJob R{};
@@ -403,53 +431,30 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
     return fail(MOE_ERR_MISALIGNED, "x/out/y_shared must be 16-byte aligned");
   const WsLayout L = ws_layout(T, E, top_k, H, I);
   if ((s = check_ws(ws, ws_bytes, L.total))) return s;
-  const int sms = sm_count();
   const bool f16 = act == MOE_FMT_F16;
-  const int P = T * top_k;
-  MOE_CUDA(launch_xprep(static_cast<const uint16_t*>(x), T, H, f16,
-                        reinterpret_cast<uint16_t*>(wsp(ws, L.xperm)),
-                        reinterpret_cast<float*>(wsp(ws, L.xsum)), stream),
-           "x prep");
+  float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
+  MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, f16, geo13(experts).t, xsum,
+                       stream),
+           "activation sums");
   int* nss = reinterpret_cast<int*>(wsp(ws, L.nss));
   int* se = reinterpret_cast<int*>(wsp(ws, L.ss_e));
   int* so = reinterpret_cast<int*>(wsp(ws, L.ss_off));
   int* sc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
-  int* blist = reinterpret_cast<int*>(wsp(ws, L.blist));
-  MOE_CUDA(launch_subslots(bucket_offsets, bucket_perm, T, top_k, E, nss, se, so, sc, blist,
-                           stream),
-           "sub-slot kernel");
-  const int max_ss = int(max_subslots(T, E, top_k));
-  uint16_t* xperm = reinterpret_cast<uint16_t*>(wsp(ws, L.xperm));
-  float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
-  UnitJob J{};
-  J.g = geo13(experts);
-  J.down = 0;
-  J.inter = I;
-  J.ss = SubSlots{nss, se, so, sc, 0, 0};
-  J.op = OperandSrc{xperm, nullptr, xsum, blist};
-  J.hh = reinterpret_cast<uint16_t*>(wsp(ws, L.hh));
-  J.hl = reinterpret_cast<uint16_t*>(wsp(ws, L.hl));
-  J.hsum = reinterpret_cast<float*>(wsp(ws, L.hsum));
-  J.status = static_cast<int*>(ws);
-  J.max_units = max_ss * (I / 64);
-  MOE_CUDA(launch_units(J, f16, sms, stream), "gate/up kernel");
-  UnitJob D{};
-  D.g = geo2(experts);
-  D.down = 1;
-  D.inter = I;
-  D.ss = J.ss;
-  D.op = OperandSrc{J.hh, J.hl, J.hsum, nullptr};
-  D.sink = Sink{reinterpret_cast<float*>(wsp(ws, L.y)), bucket_perm, H};
-  D.status = static_cast<int*>(ws);
-  D.max_units = max_ss * (H / kUnitRows);
-  MOE_CUDA(launch_units(D, false, sms, stream), "down kernel");
+  MOE_CUDA(launch_subslots(bucket_offsets, E, nss, se, so, sc, stream), "sub-slot kernel");
+  const SubSlots ss{nss, se, so, sc, 0, 0};
+  float* y = reinterpret_cast<float*>(wsp(ws, L.y));
+  s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
+               bucket_perm, top_k, reinterpret_cast<uint16_t*>(wsp(ws, L.hh)),
+               reinterpret_cast<uint16_t*>(wsp(ws, L.hl)),
+               reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr, y, kRowsScatter,
+               static_cast<int*>(ws), stream);
+  if (s) return s;
   CombineArgs C{};
-  C.y = reinterpret_cast<const float*>(wsp(ws, L.y));
+  C.y = y;
   C.w = topk_w;
   C.ysh = y_shared;
   C.sg = shared_gate_w;
   C.out = static_cast<uint16_t*>(out);
-  C.nchd = 1;
   C.T = T;
   C.k = top_k;
   C.H = H;
@@ -509,48 +514,43 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
     A.R.T = T;
     A.R.E = E;
     A.R.H = H;
-    A.R.logits = reinterpret_cast<float*>(wsp(ws, L.logits));
-    A.R.gate_logit = reinterpret_cast<float*>(wsp(ws, L.gate_logit));
+    int* status = static_cast<int*>(ws);
+    uint16_t* hh = reinterpret_cast<uint16_t*>(wsp(ws, L.hh));
+    uint16_t* hl = reinterpret_cast<uint16_t*>(wsp(ws, L.hl));
+    float* hsum = reinterpret_cast<float*>(wsp(ws, L.hsum));
+    uint16_t* shh = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh));
+    uint16_t* shl = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl));
+    float* shsum = reinterpret_cast<float*>(wsp(ws, L.sh_hsum));
+    float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
+    A.y = reinterpret_cast<float*>(wsp(ws, L.y));
+    A.ysh = reinterpret_cast<float*>(wsp(ws, L.ysh));
+    A.C = bank_cfg(experts, hh, hl, hsum, nullptr, A.y, status);
+    if (shared) {
+      A.C.geo[2] = geo13(shared);
+      A.C.geo[3] = geo2(shared);
+      A.C.fmt_shared = shared->fmt;
+    }
+    A.C.tg[2] = MatTarget{shh, shl, shsum, nullptr, nullptr};
+    A.C.tg[3] = MatTarget{nullptr, nullptr, nullptr, nullptr, A.ysh};
+    const int ldx = sums_ld(A.C.geo[0].t), ldh = sums_ld(A.C.geo[1].t);
+    A.src[0] = MatSource{A.R.x, nullptr, xsum, H, ldx};
+    A.src[1] = MatSource{hh, hl, hsum, I, ldh};
+    A.src[2] = A.src[0];
+    A.src[3] = MatSource{shh, shl, shsum, I, ldh};
     A.k = top_k;
-    A.inter = I;
-    A.f16 = f16;
     A.has_shared = shared ? 1 : 0;
     A.KS = router_ks(H);
-    A.NR = router_blocks(E, shared_gate != nullptr, H);
-    A.XB = (T * (H / 64) + kUnitWarps - 1) / kUnitWarps;
-    A.g13 = geo13(experts);
-    A.g2 = geo2(experts);
-    A.g13s = shared ? geo13(shared) : A.g13;
-    A.g2s = shared ? geo2(shared) : A.g2;
-    A.xperm = reinterpret_cast<uint16_t*>(wsp(ws, L.xperm));
-    A.xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
-    A.idx = reinterpret_cast<int32_t*>(wsp(ws, L.idx));
-    A.w = reinterpret_cast<float*>(wsp(ws, L.w));
-    A.sgw = shared_gate ? reinterpret_cast<float*>(wsp(ws, L.sgw)) : nullptr;
-    A.offsets = reinterpret_cast<int32_t*>(wsp(ws, L.offsets));
-    A.perm = reinterpret_cast<int32_t*>(wsp(ws, L.perm));
-    A.nss = reinterpret_cast<int*>(wsp(ws, L.nss));
-    A.se = reinterpret_cast<int*>(wsp(ws, L.ss_e));
-    A.so = reinterpret_cast<int*>(wsp(ws, L.ss_off));
-    A.sc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
-    A.rows = reinterpret_cast<int*>(wsp(ws, L.ss_rows));
-    A.blist = reinterpret_cast<int*>(wsp(ws, L.blist));
-    A.hh = reinterpret_cast<uint16_t*>(wsp(ws, L.hh));
-    A.hl = reinterpret_cast<uint16_t*>(wsp(ws, L.hl));
-    A.hsum = reinterpret_cast<float*>(wsp(ws, L.hsum));
-    A.y = reinterpret_cast<float*>(wsp(ws, L.y));
-    A.sh_hh = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh));
-    A.sh_hl = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl));
-    A.sh_hsum = reinterpret_cast<float*>(wsp(ws, L.sh_hsum));
-    A.ysh = reinterpret_cast<float*>(wsp(ws, L.ysh));
+    A.part = reinterpret_cast<float*>(wsp(ws, L.part));
     A.user_idx = topk_idx;
     A.user_w = topk_w;
     A.out = static_cast<uint16_t*>(out);
-    A.ctrl = static_cast<int*>(ws);
-    if (decode_smem_bytes(A) > kUnitSmemMax)
-      return fail(MOE_ERR_INVALID_ARG, "shape needs %d bytes of shared memory per CTA",
-                  decode_smem_bytes(A));
-    MOE_CUDA(launch_decode(A, sm_count(), stream), "fused decode kernel");
+    A.ctrl = status;
+    int S = 0, SB = 0, smem = 0;
+    decode_smem(A, &S, &SB, &smem);
+    if (S < 2)
+      return fail(MOE_ERR_INVALID_ARG, "shape needs %d-byte stages; two do not fit in shared memory",
+                  SB);
+    MOE_CUDA(launch_decode(A, experts->fmt, sm_count(), stream), "fused decode kernel");
     return ok();
   }
   int32_t* idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(wsp(ws, L.idx));

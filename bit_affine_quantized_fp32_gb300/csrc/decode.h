@@ -9,51 +9,31 @@ namespace moe {
 // start at zero (moe_workspace_init); the last CTA of every fused call zeroes
 // them again, except the exit counter, which only ever grows.
 constexpr int kCtlStatus = 0;
-constexpr int kCtlRouterDone = 32;    // router blocks finished
-constexpr int kCtlXprepDone = 33;     // x-preparation blocks finished
-constexpr int kCtlRoutingReady = 34;  // 1 once routing and sub-slots are written
-constexpr int kCtlExit = 35;          // CTAs finished (monotonic)
-constexpr int kMaxSubFused = 296;     // routed sub-slots of a fused call (T <= 32)
-constexpr int kCtlReady = 64;         // [320]: 64-row h groups done per sub-slot
-constexpr int kSharedReady = kCtlReady + kMaxSubFused;  // shared-expert sub-slots
-constexpr int kCtlRb = kCtlReady + 320;                 // [64]: down units done per block
+constexpr int kCtlPhase0 = 32;       // router and activation-sum tasks finished
+constexpr int kCtlExit = 35;         // CTAs finished (monotonic)
+constexpr int kCtlReady = 64;        // [296]: 64-row h groups done per routed sub-slot
+constexpr int kSharedReady = kCtlReady + 296;  // [24]: same for the shared sub-slots
+constexpr int kCtlRb = kCtlReady + 320;        // [64]: down units done per 128-row block
 constexpr int kCtlEnd = kCtlRb + 64;
 constexpr int kCtlBytes = 16384;
 static_assert(kCtlEnd * 4 <= kCtlBytes, "control region too small");
 
 struct DecodeArgs {
-  RouterJob R;                 // router, shared gate, x, T, E, H, logits, gate logits
-  int k, inter, f16, has_shared;
-  int KS, NR, XB;              // router k-splits, router blocks, x-prep blocks
-  MatGeo g13, g2, g13s, g2s;   // routed and shared matrices
-  uint16_t* xperm;
-  float* xsum;
-  int32_t* idx;
-  float* w;
-  float* sgw;                  // nullptr without a shared gate
-  int32_t* offsets;
-  int32_t* perm;
-  int* nss;
-  int* se;
-  int* so;
-  int* sc;
-  int* rows;                   // [sub-slot][8] token ids
-  int* blist;
-  uint16_t* hh;
-  uint16_t* hl;
-  float* hsum;
-  float* y;
-  uint16_t* sh_hh;
-  uint16_t* sh_hl;
-  float* sh_hsum;
-  float* ysh;
-  int32_t* user_idx;           // nullable outputs
+  RouterJob R;          // router, shared gate, bias, x, T, E, H, f16
+  EngineCfg C;          // geo/targets: 0 routed w13, 1 routed w2, 2 shared w13, 3 shared w2
+  MatSource src[4];     // operands of the four matrix slots
+  int k, has_shared, KS;
+  float* part;          // router partial sums [KS][T][E1]
+  float* y;             // [T*k][H] per-assignment expert outputs
+  float* ysh;           // [T][H] shared-expert outputs
+  int32_t* user_idx;    // nullable outputs [T][k]
   float* user_w;
-  uint16_t* out;
+  uint16_t* out;        // [T][H]
   int* ctrl;
 };
 
-int decode_smem_bytes(const DecodeArgs& A);
-cudaError_t launch_decode(const DecodeArgs& A, int sms, cudaStream_t st);
+// Stage count, stage bytes and total dynamic shared memory of a launch.
+void decode_smem(const DecodeArgs& A, int* S, int* SB, int* bytes);
+cudaError_t launch_decode(const DecodeArgs& A, int fmt, int sms, cudaStream_t st);
 
 }  // namespace moe

@@ -4,32 +4,52 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "units.cuh"
+#include "engine.cuh"
 
 namespace moe {
 
-constexpr int kUnitSmemMax = 220 * 1024;
+// Sub-slot list of a standalone job: sub-slot ss holds tokens [off, off + cnt)
+// of expert e, in bucket positions (a table written by k_subslots) -- or, for
+// a fixed expert over T tokens, sub-slot ss is tokens [8 ss, min(T, 8 ss + 8)).
+struct SubSlots {
+  const int* n;  // device count (nullptr: fixed expert)
+  const int* e;
+  const int* off;
+  const int* cnt;
+  int fixed_e;
+  int fixed_T;
+};
 
-// A launch of units of one matrix family over sub-slots.
+// A standalone launch of units of one matrix family (slot `mat`, 0 = w13 or
+// 1 = w2 of the bank in C.geo[0..1]) over a sub-slot list.
 struct UnitJob {
-  MatGeo g;
-  int down;                 // 0: gate/up units (SwiGLU epilogue), 1: down units
-  int inter;                // I
+  EngineCfg C;
+  MatSource src;       // operand rows of `mat`
+  int mat;
+  int rows;            // kRowsDirect / kRowsGather / kRowsScatter
   SubSlots ss;
-  OperandSrc op;
-  Sink sink;                // down units: y rows
-  uint16_t* hh;             // gate/up units: h outputs (k-permuted bf16 hi / lo)
-  uint16_t* hl;
-  float* hsum;
-  float* hout;              // nullable fp32 h [rows][I]
-  int max_units;            // host upper bound (grid sizing)
-  int* status;              // workspace status word (bounded-wait timeouts)
+  const int* perm;     // bucket position -> assignment id (Gather / Scatter)
+  int k;
+  int max_units;       // host upper bound (grid sizing)
 };
 
 cudaError_t launch_units(const UnitJob& J, bool f16a, int sms, cudaStream_t st);
-cudaError_t launch_xprep(const uint16_t* x, int T, int H, bool f16, uint16_t* xperm, float* xsum,
-                         cudaStream_t st);
+cudaError_t launch_xsum(const uint16_t* x, int T, int H, bool f16, const TileGeo& g13,
+                        float* xsum, cudaStream_t st);
+
+struct CombineArgs {
+  const float* y;    // [T*k][H]
+  const float* w;    // [T][k]
+  const float* ysh;  // [T][H] or nullptr
+  const float* sg;   // [T] or nullptr (weight 1)
+  uint16_t* out;     // [T][H]
+  int T, k, H, f16;
+};
 cudaError_t launch_combine(const CombineArgs& A, cudaStream_t st);
+
+// Dynamic shared memory of an engine kernel: stage count and stage bytes for
+// the given matrices (at most kMaxStages stages within the budget).
+void engine_stages(const TileGeo* geos, int n, int static_bytes, int* S, int* SB);
 
 // routing
 struct RouterJob {
@@ -55,8 +75,8 @@ cudaError_t launch_topk(const float* logits, const float* gate_logit, int T, int
                         int32_t* idx, float* w, float* sg, cudaStream_t st);
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets,
                           int32_t* perm, cudaStream_t st);
-cudaError_t launch_subslots(const int32_t* offsets, const int32_t* perm, int T, int k, int E,
-                            int* nss, int* se, int* so, int* sc, int* blist, cudaStream_t st);
+cudaError_t launch_subslots(const int32_t* offsets, int E, int* nss, int* se, int* so, int* sc,
+                            cudaStream_t st);
 
 // formats
 cudaError_t launch_pack(int fmt, const uint8_t* codes, int rows, int cols, uint32_t* packed,

@@ -145,7 +145,7 @@ __device__ __forceinline__ TiledPos tiled_pos(const TileGeo& g, int e, int r, in
             (long long)(w * g.ng + G) * (g.fmt == MOE_FMT_AFFINE3_G64 ? 384 : 512);
   p.lane = (sub & 7) * 4 + t;
   p.widx = (sub >> 3) * 2 + half;
-  p.nib = k % 8;
+  p.nib = tiled_nib(k % 8);
   return p;
 }
 
@@ -173,7 +173,7 @@ __global__ void k_repack_codes(TileGeo g, int E, const uint32_t* __restrict__ wc
     const uint32_t* row = wc + ((long long)e * g.rows + r) * wpr;
     const int ks = k0 + 8 * (j & 1);
     uint32_t v = 0;
-    for (int q2 = 0; q2 < 8; ++q2) v |= get_code(g.fmt, row, ks + q2) << (4 * q2);
+    for (int q2 = 0; q2 < 8; ++q2) v |= get_code(g.fmt, row, ks + q2) << (4 * tiled_nib(q2));
     W[j] = v;
   }
   uint8_t* blkp = out + tiled_item(g, e, blk, c);
@@ -214,10 +214,10 @@ __global__ void k_repack_scales(TileGeo g, int E, const uint16_t* __restrict__ s
   const long long i1 = i0 + 8LL * gpr;
   uint8_t* sc = out + tiled_item(g, e, blk, c) + g.code_bytes;
   if (g.fmt == MOE_FMT_W4A16_SYM_G128) {
-    *reinterpret_cast<uint32_t*>(sc + ((w * nsg + G) * 8 + gq) * 4) =
+    *reinterpret_cast<uint32_t*>(sc + ((w * 8 + gq) * nsg + G) * 4) =
         uint32_t(s[i0]) | (uint32_t(s[i1]) << 16);
   } else {
-    *reinterpret_cast<uint2*>(sc + ((w * nsg + G) * 8 + gq) * 8) =
+    *reinterpret_cast<uint2*>(sc + ((w * 8 + gq) * nsg + G) * 8) =
         make_uint2(uint32_t(s[i0]) | (uint32_t(b[i0]) << 16),
                    uint32_t(s[i1]) | (uint32_t(b[i1]) << 16));
   }
@@ -277,9 +277,9 @@ __global__ void k_unrepack_scales(TileGeo g, int E, const uint8_t* __restrict__ 
   const int c = gi / nsg, G = gi % nsg, gq = sub & 7, hi = sub >> 3;
   const uint8_t* sc = tl + tiled_item(g, e, blk, c) + g.code_bytes;
   if (g.fmt == MOE_FMT_W4A16_SYM_G128) {
-    s[i] = reinterpret_cast<const uint16_t*>(sc + ((w * nsg + G) * 8 + gq) * 4)[hi];
+    s[i] = reinterpret_cast<const uint16_t*>(sc + ((w * 8 + gq) * nsg + G) * 4)[hi];
   } else {
-    const uint16_t* ent = reinterpret_cast<const uint16_t*>(sc + ((w * nsg + G) * 8 + gq) * 8);
+    const uint16_t* ent = reinterpret_cast<const uint16_t*>(sc + ((w * 8 + gq) * nsg + G) * 8);
     s[i] = ent[2 * hi];
     b[i] = ent[2 * hi + 1];
   }

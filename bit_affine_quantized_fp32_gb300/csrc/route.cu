@@ -10,8 +10,7 @@ namespace {
 __global__ void __launch_bounds__(256) k_router(const RouterJob J, int KS) {
   __shared__ float part[8 * kRouterTT];
   for (int t0 = 0; t0 < J.T; t0 += kRouterTT)
-    router_block_any(J, KS, blockIdx.x, part, J.x + size_t(t0) * J.H, t0,
-                     min(kRouterTT, J.T - t0));
+    router_block(J, KS, blockIdx.x, part, J.x + size_t(t0) * J.H, t0, min(kRouterTT, J.T - t0));
 }
 
 __global__ void k_topk(const float* __restrict__ logits, const float* __restrict__ gate_logit,
@@ -19,7 +18,7 @@ __global__ void k_topk(const float* __restrict__ logits, const float* __restrict
                        float* __restrict__ sg) {
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
-  topk_warp(logits, gate_logit, t, E, k, idx, w, sg, nullptr, nullptr);
+  topk_warp<false>(logits, gate_logit, t, E, k, idx, w, sg, nullptr, nullptr);
 }
 
 __global__ void __launch_bounds__(1024) k_bucket(const int32_t* __restrict__ idx, int N, int E,
@@ -29,12 +28,10 @@ __global__ void __launch_bounds__(1024) k_bucket(const int32_t* __restrict__ idx
   bucket_cta(idx, N, E, offsets, perm, S);
 }
 
-__global__ void __launch_bounds__(256) k_subslots(const int32_t* __restrict__ offsets,
-                                                  const int32_t* __restrict__ perm, int P, int k,
-                                                  int E, int* nss, int* se, int* so, int* sc,
-                                                  int* blist) {
+__global__ void __launch_bounds__(256) k_subslots(const int32_t* __restrict__ offsets, int E,
+                                                  int* nss, int* se, int* so, int* sc) {
   __shared__ int wcount[8];
-  subslots_cta(offsets, perm, P, k, E, nss, se, so, sc, blist, wcount);
+  subslots_cta(offsets, E, nss, se, so, sc, wcount);
 }
 
 }  // namespace
@@ -73,9 +70,9 @@ cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offs
   return cudaGetLastError();
 }
 
-cudaError_t launch_subslots(const int32_t* offsets, const int32_t* perm, int T, int k, int E,
-                            int* nss, int* se, int* so, int* sc, int* blist, cudaStream_t st) {
-  k_subslots<<<1, 256, 0, st>>>(offsets, perm, T * k, k, E, nss, se, so, sc, blist);
+cudaError_t launch_subslots(const int32_t* offsets, int E, int* nss, int* se, int* so, int* sc,
+                            cudaStream_t st) {
+  k_subslots<<<1, 256, 0, st>>>(offsets, E, nss, se, so, sc);
   return cudaGetLastError();
 }
 

@@ -44,50 +44,40 @@ __device__ __forceinline__ void router_load_w4(int fmt, const void* q, const uin
   }
 }
 
-// Router block rb (8 warps): rows [rb*RPB, rb*RPB + RPB) of the router plus
-// the shared-gate row (row E), RPB = 8 / KS; warp (row, q) holds the 4*NI
-// weights of its k-split q in registers and runs over the tokens; the KS
-// partial sums of a row are added in a fixed order.  xs points at the x rows
-// of tokens t0 .. t0+tn-1 (row stride H; global or shared memory), tn <=
-// kRouterTT.  `part` is 8 x kRouterTT floats of shared memory.  Needs
-// blockDim.x == 256.  A token's logit does not depend on the other tokens.
+// One warp's share of the router: the dot products of router row `row` (the
+// shared-gate row when row == E) over k-split q of KS (4*NI columns per lane,
+// held in registers) with tokens 0..tn-1 of xs (row stride H; global or
+// shared memory).  Lane order and xor tree are fixed; lane 0 writes token
+// t's partial sum to out[t * ostride].
 template <int NI>
-__device__ __forceinline__ void router_block(const RouterJob& J, int KS, int rb, float* part,
-                                             const uint16_t* xs, int t0, int tn) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int RPB = 8 / KS;
-  const int rl = wid / KS, q = wid - rl * KS;
-  const int row = rb * RPB + rl;
-  const int nrows = J.E + (J.gq ? 1 : 0);
-  const bool active = row < nrows;
+__device__ __forceinline__ void router_warp(const RouterJob& J, int KS, int row, int q,
+                                            const uint16_t* xs, int tn, float* out,
+                                            int ostride) {
+  const int lane = threadIdx.x & 31;
   const int kq = q * (J.H / KS);
   float w[NI][4];
-  if (active) {
-    const bool gate = row >= J.E;
+  const bool gate = row >= J.E;
 #pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      const int k = kq + 128 * i + 4 * lane;
-      if (gate)
-        router_load_w4(J.gfmt, J.gq, J.gs, J.gb, 0, J.H, k, w[i]);
-      else
-        router_load_w4(J.fmt, J.q, J.s, J.b, row, J.H, k, w[i]);
-    }
+  for (int i = 0; i < NI; ++i) {
+    const int k = kq + 128 * i + 4 * lane;
+    if (gate)
+      router_load_w4(J.gfmt, J.gq, J.gs, J.gb, 0, J.H, k, w[i]);
+    else
+      router_load_w4(J.fmt, J.q, J.s, J.b, row, J.H, k, w[i]);
   }
   for (int tl = 0; tl < tn; tl += 4) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (active) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (tl + u < tn) {
-          const uint16_t* xr = xs + size_t(tl + u) * J.H;
+    for (int u = 0; u < 4; ++u) {
+      if (tl + u < tn) {
+        const uint16_t* xr = xs + size_t(tl + u) * J.H;
 #pragma unroll
-          for (int i = 0; i < NI; ++i) {
-            const uint2 v = *reinterpret_cast<const uint2*>(xr + kq + 128 * i + 4 * lane);
-            acc[u] = fmaf(w[i][0], act_to_float(uint16_t(v.x & 0xFFFF), J.f16), acc[u]);
-            acc[u] = fmaf(w[i][1], act_to_float(uint16_t(v.x >> 16), J.f16), acc[u]);
-            acc[u] = fmaf(w[i][2], act_to_float(uint16_t(v.y & 0xFFFF), J.f16), acc[u]);
-            acc[u] = fmaf(w[i][3], act_to_float(uint16_t(v.y >> 16), J.f16), acc[u]);
-          }
+        for (int i = 0; i < NI; ++i) {
+          const uint2 v = *reinterpret_cast<const uint2*>(xr + kq + 128 * i + 4 * lane);
+          acc[u] = fmaf(w[i][0], act_to_float(uint16_t(v.x & 0xFFFF), J.f16), acc[u]);
+          acc[u] = fmaf(w[i][1], act_to_float(uint16_t(v.x >> 16), J.f16), acc[u]);
+          acc[u] = fmaf(w[i][2], act_to_float(uint16_t(v.y & 0xFFFF), J.f16), acc[u]);
+          acc[u] = fmaf(w[i][3], act_to_float(uint16_t(v.y >> 16), J.f16), acc[u]);
         }
       }
     }
@@ -95,37 +85,68 @@ __device__ __forceinline__ void router_block(const RouterJob& J, int KS, int rb,
     for (int u = 0; u < 4; ++u) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
-      if (lane == 0 && tl + u < tn) part[wid * kRouterTT + tl + u] = acc[u];
+      if (lane == 0 && tl + u < tn) out[size_t(tl + u) * ostride] = acc[u];
     }
   }
+}
+
+__device__ __forceinline__ void router_warp_any(const RouterJob& J, int KS, int row, int q,
+                                                const uint16_t* xs, int tn, float* out,
+                                                int ostride) {
+  const int NI_ = J.H / (KS * 128);
+  if (NI_ == 1)
+    router_warp<1>(J, KS, row, q, xs, tn, out, ostride);
+  else if (NI_ == 2)
+    router_warp<2>(J, KS, row, q, xs, tn, out, ostride);
+  else if (NI_ == 3)
+    router_warp<3>(J, KS, row, q, xs, tn, out, ostride);
+  else
+    router_warp<4>(J, KS, row, q, xs, tn, out, ostride);
+}
+
+// A logit from its KS partial sums (stride apart), added in split order, plus
+// the row's bias.
+__device__ __forceinline__ float router_finalize(const float* p, size_t stride, int KS,
+                                                 const float* bias) {
+  float s = 0.f;
+  for (int q = 0; q < KS; ++q) s += p[q * stride];
+  if (bias) s += *bias;
+  return s;
+}
+
+__device__ __forceinline__ float router_finalize_cg(const float* p, size_t stride, int KS,
+                                                    const float* bias) {
+  float s = 0.f;
+  for (int q = 0; q < KS; ++q) s += __ldcg(p + q * stride);
+  if (bias) s += *bias;
+  return s;
+}
+
+// Router block rb (8 warps): rows [rb*RPB, rb*RPB + RPB) of the router plus
+// the shared-gate row (row E), RPB = 8 / KS; warp (row, q) runs router_warp;
+// the KS partial sums of a row are finalised in split order.  Needs
+// blockDim.x == 256.  A token's logit does not depend on the other tokens.
+__device__ __forceinline__ void router_block(const RouterJob& J, int KS, int rb, float* part,
+                                             const uint16_t* xs, int t0, int tn) {
+  const int wid = threadIdx.x >> 5;
+  const int RPB = 8 / KS;
+  const int rl = wid / KS, q = wid - rl * KS;
+  const int row = rb * RPB + rl;
+  const int nrows = J.E + (J.gq ? 1 : 0);
+  if (row < nrows) router_warp_any(J, KS, row, q, xs, tn, part + wid * kRouterTT, 1);
   __syncthreads();
   for (int i = threadIdx.x; i < RPB * tn; i += blockDim.x) {
     const int r2 = i / tn, tl = i - r2 * tn;
     const int row2 = rb * RPB + r2;
     if (row2 >= nrows) continue;
-    float s = 0.f;
-    for (int qq = 0; qq < KS; ++qq) s += part[(r2 * KS + qq) * kRouterTT + tl];
-    if (row2 < J.E) {
-      if (J.bias) s += J.bias[row2];
-      J.logits[size_t(t0 + tl) * J.E + row2] = s;
-    } else {
-      J.gate_logit[t0 + tl] = s;
-    }
+    const float* p = part + (r2 * KS) * kRouterTT + tl;
+    if (row2 < J.E)
+      J.logits[size_t(t0 + tl) * J.E + row2] =
+          router_finalize(p, kRouterTT, KS, J.bias ? J.bias + row2 : nullptr);
+    else
+      J.gate_logit[t0 + tl] = router_finalize(p, kRouterTT, KS, nullptr);
   }
   __syncthreads();
-}
-
-__device__ __forceinline__ void router_block_any(const RouterJob& J, int KS, int rb, float* part,
-                                                 const uint16_t* xs, int t0, int tn) {
-  const int NI = J.H / (KS * 128);
-  if (NI == 1)
-    router_block<1>(J, KS, rb, part, xs, t0, tn);
-  else if (NI == 2)
-    router_block<2>(J, KS, rb, part, xs, t0, tn);
-  else if (NI == 3)
-    router_block<3>(J, KS, rb, part, xs, t0, tn);
-  else
-    router_block<4>(J, KS, rb, part, xs, t0, tn);
 }
 
 // Ranking key of (logit v, expert id): a larger key ranks first.  The high
@@ -146,8 +167,9 @@ __device__ __forceinline__ float key_value(unsigned hi) {
 // Top-k + weights of token t by one warp: each lane sorts the keys of experts
 // lane, lane+32, ... (8 at most) once; each of the k rounds takes the warp
 // maximum of the lanes' heads (two redux.max) and the winning lane pops its
-// head.  Then w_j = exp(l_j - l_0) / sum.  Logits are read through L2 (they
-// may come from other CTAs of this kernel).
+// head.  Then w_j = exp(l_j - l_0) / sum.  Logits come from shared memory
+// (SMEM) or through L2 (they may have been written by other CTAs).
+template <bool SMEM = false>
 __device__ __forceinline__ void topk_warp(const float* logits, const float* gate_logit, int t,
                                           int E, int k, int32_t* idx, float* w, float* sg,
                                           int32_t* idx2, float* w2, int* idx_smem = nullptr) {
@@ -156,7 +178,9 @@ __device__ __forceinline__ void topk_warp(const float* logits, const float* gate
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    key[i] = e < E ? rank_key(__ldcg(logits + size_t(t) * E + e), e) : 0ull;
+    float v = 0.f;
+    if (e < E) v = SMEM ? logits[size_t(t) * E + e] : __ldcg(logits + size_t(t) * E + e);
+    key[i] = e < E ? rank_key(v, e) : 0ull;
   }
   // sorting network (descending), 19 compare-exchanges
 #define MOE_CX(a, b)                                  \
@@ -212,7 +236,10 @@ __device__ __forceinline__ void topk_warp(const float* logits, const float* gate
         if (idx_smem) idx_smem[t * k + r] = sel_e[r];
       }
     }
-    if (gate_logit && sg) sg[t] = 1.f / (1.f + expf(-__ldcg(gate_logit + t)));
+    if (gate_logit && sg) {
+      const float gl = SMEM ? gate_logit[t] : __ldcg(gate_logit + t);
+      sg[t] = 1.f / (1.f + expf(-gl));
+    }
   }
 }
 
@@ -288,11 +315,10 @@ __device__ __forceinline__ void bucket_cta(const int32_t* idx, int N, int E, int
 }
 
 // Sub-slots from the bucket offsets: every active expert (ascending id) is
-// cut into runs of at most 8 bucket positions; also the token of every bucket
-// position.  Needs blockDim.x >= 256 (the first 256 threads scan).
-__device__ __forceinline__ void subslots_cta(const int32_t* offsets, const int32_t* perm, int P,
-                                             int k, int E, int* nss, int* se, int* so, int* sc,
-                                             int* blist, int* wcount /* 8 ints of smem */) {
+// cut into runs of at most 8 bucket positions.  Needs blockDim.x >= 256 (the
+// first 256 threads scan).
+__device__ __forceinline__ void subslots_cta(const int32_t* offsets, int E, int* nss, int* se,
+                                             int* so, int* sc, int* wcount /* 8 ints of smem */) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int c = 0, off = 0, nsub = 0, incl = 0;
   if (tid < 256) {
@@ -325,40 +351,59 @@ __device__ __forceinline__ void subslots_cta(const int32_t* offsets, const int32
       *nss = tot;
     }
   }
-  for (int p = tid; p < P; p += blockDim.x) blist[p] = __ldcg(perm + p) / k;
   __syncthreads();
 }
 
-// Routing of a decode batch (T*k <= 256 assignments) by one CTA of 256
-// threads, with every intermediate in shared memory: top-k + weights (also
-// stored to idx/w/sg and the optional user outputs), the bucket offsets and
-// permutation (the stable counting sort of bucket_cta), and the sub-slot
-// table of subslots_cta plus the token of each sub-slot position (rows,
-// 8 per sub-slot).  Same definitions as the global kernels, same results.
-struct SmallRouteSmem {
-  int idx[256];
-  int cnt[256];
+// Routing of a decode batch (T <= 32, T*k <= 256 assignments) by one CTA,
+// every result in shared memory: the logits finalised from the router's
+// partial sums, top-k + weights per token (topk_warp), the stable counting
+// sort of the assignments by expert (as bucket_cta) and the sub-slot table
+// (as subslots_cta).  Same definitions as the standalone kernels, same bits.
+constexpr int kMaxSubFused = 296;  // sub-slots of a call with T*k <= 256
+
+struct RouteTable {
+  int idx[256];                // [T*k] experts by slot
+  float w[256];                // [T*k] routing weights
+  float sg[32];                // [T] shared-gate weights
+  int perm[256];               // bucket position -> assignment id
+  int ss_e[kMaxSubFused];      // sub-slot -> expert
+  int ss_off[kMaxSubFused];    //            first bucket position
+  int ss_cnt[kMaxSubFused];    //            tokens (1..8)
+  int nss;
+  int cnt[256];                // scratch
   int off[256];
   int sbase[256];
-  int perm[256];
-  int wc[8][256];
   int wsum[8];
   int wsub[8];
 };
 
-__device__ __forceinline__ void route_small_cta(const float* logits, const float* gate_logit,
-                                                int T, int E, int k, int32_t* idx_g, float* w_g,
-                                                float* sg, int32_t* user_idx, float* user_w,
-                                                int32_t* offsets_g, int32_t* perm_g, int* nss_g,
-                                                int* se_g, int* so_g, int* sc_g, int* rows_g,
-                                                SmallRouteSmem& S) {
+// part: router partial sums [KS][T][E1] (E1 = E + 1 with a shared gate);
+// lg: T*E + T floats of shared scratch; wc: 8*256 ints of shared scratch.
+// user_idx/user_w (nullable) receive the top-k outputs.  All threads of the
+// CTA call it (blockDim.x >= 256).
+__device__ __forceinline__ void route_table_cta(const float* part, int KS, int E1,
+                                                const float* bias, bool gate, int T, int E, int k,
+                                                int32_t* user_idx, float* user_w, float* lg,
+                                                int (*wc)[256], RouteTable& S) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int N = T * k;
-  S.cnt[tid] = 0;
-  for (int i = lane; i < 256; i += 32) S.wc[wid][i] = 0;
-  for (int t = wid; t < T; t += 8)
-    topk_warp(logits, gate_logit, t, E, k, idx_g, w_g, sg, user_idx, user_w, S.idx);
+  const int NT = blockDim.x, NW = NT >> 5;
+  float* gl = lg + T * E;
+  const size_t qs = size_t(T) * E1;
+  for (int i = tid; i < T * E1; i += NT) {
+    const int t = i / E1, row = i - t * E1;
+    const float* p = part + size_t(t) * E1 + row;
+    if (row < E)
+      lg[t * E + row] = router_finalize_cg(p, qs, KS, bias ? bias + row : nullptr);
+    else
+      gl[t] = router_finalize_cg(p, qs, KS, nullptr);
+  }
+  for (int i = tid; i < 256; i += NT) S.cnt[i] = 0;
+  for (int i = tid; i < 8 * 256; i += NT) wc[i >> 8][i & 255] = 0;
   __syncthreads();
+  for (int t = wid; t < T; t += NW)
+    topk_warp<true>(lg, gate ? gl : nullptr, t, E, k, S.idx, S.w, S.sg, user_idx, user_w);
+  __syncthreads();
+  const int N = T * k;
   const int e_a = tid < N ? S.idx[tid] : -1;
   if (e_a >= 0) atomicAdd(&S.cnt[e_a], 1);
   __syncthreads();
@@ -366,56 +411,56 @@ __device__ __forceinline__ void route_small_cta(const float* logits, const float
   const int c = tid < E ? S.cnt[tid] : 0;
   const int ns = (c + 7) >> 3;
   int ic = c, isub = ns;
+  if (tid < 256) {
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y1 = __shfl_up_sync(0xffffffffu, ic, o);
-    const int y2 = __shfl_up_sync(0xffffffffu, isub, o);
-    if (lane >= o) {
-      ic += y1;
-      isub += y2;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y1 = __shfl_up_sync(0xffffffffu, ic, o);
+      const int y2 = __shfl_up_sync(0xffffffffu, isub, o);
+      if (lane >= o) {
+        ic += y1;
+        isub += y2;
+      }
+    }
+    if (lane == 31) {
+      S.wsum[wid] = ic;
+      S.wsub[wid] = isub;
     }
   }
-  if (lane == 31) {
-    S.wsum[wid] = ic;
-    S.wsub[wid] = isub;
-  }
   __syncthreads();
-  int pc = 0, ps = 0;
-  for (int i = 0; i < wid; ++i) {
-    pc += S.wsum[i];
-    ps += S.wsub[i];
-  }
-  S.off[tid] = pc + ic - c;
-  S.sbase[tid] = ps + isub - ns;
-  if (tid < E) offsets_g[tid + 1] = pc + ic;
-  if (tid == 0) {
-    offsets_g[0] = 0;
-    int tot = 0;
-    for (int i = 0; i < 8; ++i) tot += S.wsub[i];
-    *nss_g = tot;
+  if (tid < 256) {
+    int pc = 0, ps = 0;
+    for (int i = 0; i < wid; ++i) {
+      pc += S.wsum[i];
+      ps += S.wsub[i];
+    }
+    S.off[tid] = pc + ic - c;
+    S.sbase[tid] = ps + isub - ns;
+    if (tid == 0) {
+      int tot = 0;
+      for (int i = 0; i < 8; ++i) tot += S.wsub[i];
+      S.nss = tot;
+    }
   }
   // stable scatter: rank among the same expert's assignments, in id order
-  const unsigned peers = __match_any_sync(0xffffffffu, e_a);
-  const int rank = __popc(peers & ((1u << lane) - 1u));
-  if (e_a >= 0 && (__ffs(peers) - 1) == lane) S.wc[wid][e_a] = __popc(peers);
-  __syncthreads();
-  if (e_a >= 0) {
-    int pre = 0;
-    for (int i = 0; i < wid; ++i) pre += S.wc[i][e_a];
-    const int pos = S.off[e_a] + pre + rank;
-    S.perm[pos] = tid;
-    perm_g[pos] = tid;
+  unsigned peers = 0;
+  if (tid < 256) {
+    peers = __match_any_sync(0xffffffffu, e_a);
+    if (e_a >= 0 && (__ffs(peers) - 1) == lane) wc[wid][e_a] = __popc(peers);
   }
   __syncthreads();
-  // sub-slot table: expert tid's runs of at most 8 positions
-  for (int i = 0; i < ns; ++i) {
-    const int ss = S.sbase[tid] + i;
-    const int o = S.off[tid] + 8 * i;
-    const int ci = min(8, c - 8 * i);
-    se_g[ss] = tid;
-    so_g[ss] = o;
-    sc_g[ss] = ci;
-    for (int n = 0; n < 8; ++n) rows_g[ss * 8 + n] = n < ci ? S.perm[o + n] / k : 0;
+  if (tid < 256 && e_a >= 0) {
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int pre = 0;
+    for (int i = 0; i < wid; ++i) pre += wc[i][e_a];
+    S.perm[S.off[e_a] + pre + rank] = tid;
+  }
+  if (tid < E) {
+    for (int i = 0; i < ns; ++i) {
+      const int ss = S.sbase[tid] + i;
+      S.ss_e[ss] = tid;
+      S.ss_off[ss] = S.off[tid] + 8 * i;
+      S.ss_cnt[ss] = min(8, c - 8 * i);
+    }
   }
   __syncthreads();
 }

@@ -13,7 +13,10 @@
 // codes k0 = c*CK + 64G + 16t, the four 8-code words
 //   W0 = codes r0[k0, k0+8)   W1 = codes r0[k0+8, k0+16)
 //   W2 = codes r1[k0, k0+8)   W3 = codes r1[k0+8, k0+16)
-// (code i of a word at bits [4i, 4i+4), as in the 4-bit format).
+// where code j (0..7) of a word sits in nibble (j&1)*4 + j/2, i.e. the
+// nibbles hold codes [0 2 4 6 1 3 5 7]: nibbles i and i+4 are the adjacent
+// pair (2i, 2i+1), which is how an MMA register takes two k-values, so the
+// activations stay in their natural order.
 //   4-bit / W4A16: 16 bytes [W0 W1 W2 W3] per lane, (w, G) blocks of 512 B.
 //   3-bit: three 32-bit planes per (w, G) block of 384 B, plane p holding
 //     lane l's word at p*128 + 4l:
@@ -22,9 +25,12 @@
 //       H   = (W0 >> 2 & 0x11111111) | (W1 >> 1 & 0x22222222)
 //           | (W2 & 0x44444444) | (W3 << 1 & 0x88888888)        (bit 2)
 //     i.e. exactly 3 bits per code, no padding.
-// Scales of an item (fp16), entry (w, G', g):
-//   affine: [s(r0), b(r0), s(r1), b(r1)] of 64-group G' (8 bytes), G' < ng;
-//   W4A16 : [s(r0), s(r1)] of 128-group G' (4 bytes), G' < ng/2.
+// Scales of an item (fp16), one run per (w, g) so that a lane's groups are
+// contiguous:
+//   affine: entry (w, g, G) = [s(r0), b(r0), s(r1), b(r1)] of 64-group G,
+//           8 bytes at ((w*8 + g)*ng + G)*8;
+//   W4A16 : entry (w, g, G') = [s(r0), s(r1)] of 128-group G', 4 bytes at
+//           ((w*8 + g)*(ng/2) + G')*4.
 #pragma once
 
 #include "common.cuh"
@@ -68,6 +74,9 @@ __host__ __device__ inline TileGeo tile_geo(int fmt, int inter, int hidden, int 
   g.expert_bytes = (long long)g.nblk * g.nch * g.item_bytes;
   return g;
 }
+
+// Nibble of code j (0..7) inside its tiled word.
+__host__ __device__ inline int tiled_nib(int j) { return (j & 1) * 4 + (j >> 1); }
 
 // First matrix row of M-tile w of block blk.
 __host__ __device__ inline int tiled_row(const TileGeo& g, int blk, int w) {

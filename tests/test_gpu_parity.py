@@ -67,8 +67,9 @@ def _tiled_reference(fmt, mats, I, H, which):
     for m in mats:
         codes = m.codes.astype(np.int64) + (8 if w4 else 0)          # nibble values
         words = np.zeros((rows, K // 8), dtype=np.uint64)
-        for i in range(8):
-            words |= (codes[:, i::8].astype(np.uint64) << np.uint64(4 * i))
+        for i in range(8):   # code i of a word in nibble (i & 1) * 4 + i // 2
+            nib = (i & 1) * 4 + i // 2
+            words |= (codes[:, i::8].astype(np.uint64) << np.uint64(4 * nib))
         words = words.astype(np.uint32)
         sc = m.scales.view(np.uint16) if m.scales.dtype != np.uint16 else m.scales
         bi = None if w4 else (m.biases.view(np.uint16) if m.biases.dtype != np.uint16 else m.biases)
@@ -106,8 +107,8 @@ def _tiled_reference(fmt, mats, I, H, which):
                         base = blk * 128 + 16 * w
                     else:
                         base = blk * 64 + 16 * w if w < 4 else I + blk * 64 + 16 * (w - 4)
-                    for G in range(nsg):
-                        for g in range(8):
+                    for g in range(8):
+                        for G in range(nsg):
                             gi = c * nsg + G
                             r0, r1 = base + g, base + g + 8
                             if w4:
