@@ -193,18 +193,19 @@ moe_status check_ws(void* ws, size_t ws_bytes, size_t need) {
   return MOE_OK;
 }
 
-// Engine configuration of one bank in slots 0 (w13) and 1 (w2), outputs to
-// the given h buffers / y.
+// Engine configuration of one bank in slots 0 (w13) and 1 (w2) (copied to
+// 2 and 3): h to the given buffers, y as two k-half planes of yhalf elements.
 EngineCfg bank_cfg(const moe_expert_bank* bank, uint16_t* hh, uint16_t* hl, float* hsum,
-                   float* hout, float* y, int* status) {
+                   float* hout, float* y, size_t yhalf, int* status) {
   EngineCfg C{};
   C.geo[0] = geo13(bank);
   C.geo[1] = geo2(bank);
   C.geo[2] = C.geo[0];
   C.geo[3] = C.geo[1];
-  C.tg[0] = MatTarget{hh, hl, hsum, hout, nullptr};
-  C.tg[1] = MatTarget{nullptr, nullptr, nullptr, nullptr, y};
-  C.fmt_shared = bank->fmt;
+  C.tg[0] = MatTarget{hh, hl, hsum, hout, nullptr, 0};
+  C.tg[1] = MatTarget{nullptr, nullptr, nullptr, nullptr, y, yhalf};
+  C.tg[2] = C.tg[0];
+  C.tg[3] = C.tg[1];
   C.inter = bank->inter;
   C.hidden = bank->hidden;
   C.status = status;
@@ -213,18 +214,19 @@ EngineCfg bank_cfg(const moe_expert_bank* bank, uint16_t* hh, uint16_t* hl, floa
 
 // Gate/up then down units of one bank over a sub-slot list.  x rows are taken
 // by `xrows` (Direct: row = token; Gather: token of a bucket position), h is
-// kept at the unit's output rows, y written by `yrows` (Direct or Scatter).
+// kept at the unit's output rows, y written by `yrows` (Direct or Scatter) as
+// two k-half planes (y, y + yhalf).
 moe_status run_bank(const moe_expert_bank* bank, const SubSlots& ss, int max_ss, const void* x,
                     bool f16, const float* xsum, int xrows, const int* perm, int k, uint16_t* hh,
-                    uint16_t* hl, float* hsum, float* hout, float* y, int yrows, int* status,
-                    cudaStream_t stream) {
+                    uint16_t* hl, float* hsum, float* hout, float* y, size_t yhalf, int yrows,
+                    int* status, cudaStream_t stream) {
   const int sms = sm_count();
   const int H = bank->hidden, I = bank->inter;
   UnitJob J{};
-  J.C = bank_cfg(bank, hh, hl, hsum, hout, y, status);
+  J.C = bank_cfg(bank, hh, hl, hsum, hout, y, yhalf, status);
   J.mat = 0;
   J.src = MatSource{static_cast<const uint16_t*>(x), nullptr, xsum, H,
-                    sums_ld(J.C.geo[0].t)};
+                    sums_ld(J.C.geo[0].t), 0};
   J.rows = xrows;
   J.ss = ss;
   J.perm = perm;
@@ -233,7 +235,7 @@ moe_status run_bank(const moe_expert_bank* bank, const SubSlots& ss, int max_ss,
   MOE_CUDA(launch_units(J, f16, sms, stream), "gate/up kernel");
   UnitJob D = J;
   D.mat = 1;
-  D.src = MatSource{hh, hl, hsum, I, sums_ld(J.C.geo[1].t)};
+  D.src = MatSource{hh, hl, hsum, h_pitch(I), sums_ld(J.C.geo[1].t), 1};
   D.rows = yrows;
   D.max_units = max_ss * (H / kUnitRows);
   MOE_CUDA(launch_units(D, false, sms, stream), "down kernel");
@@ -242,20 +244,27 @@ moe_status run_bank(const moe_expert_bank* bank, const SubSlots& ss, int max_ss,
 
 // One expert (a fixed slot holding every token) over the T rows of x, with
 // the given workspace layout: activation sums -> gate/up units (SwiGLU) ->
-// down units.
+// down units into the two planes of the workspace's shared-expert output
+// (L.ysh); y_out (nullable) receives their sum.
 moe_status run_expert_mlp(const moe_expert_bank* bank, int expert, const void* x, bool f16,
                           int T, float* h_out, float* y_out, void* ws, const WsLayout& L,
                           cudaStream_t stream) {
+  const int H = bank->hidden;
   float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
-  MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, bank->hidden, f16, geo13(bank).t, xsum,
-                       stream),
+  MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, f16, geo13(bank).t, xsum, stream),
            "activation sums");
   const SubSlots ss{nullptr, nullptr, nullptr, nullptr, expert, T};
-  return run_bank(bank, ss, (T + kMaxTok - 1) / kMaxTok, x, f16, xsum, kRowsDirect, nullptr, 1,
-                  reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh)),
-                  reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl)),
-                  reinterpret_cast<float*>(wsp(ws, L.sh_hsum)), h_out, y_out, kRowsDirect,
-                  static_cast<int*>(ws), stream);
+  float* ysh = reinterpret_cast<float*>(wsp(ws, L.ysh));
+  const size_t half = size_t(T) * H;
+  moe_status s = run_bank(bank, ss, (T + kMaxTok - 1) / kMaxTok, x, f16, xsum, kRowsDirect,
+                          nullptr, 1, reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh)),
+                          reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl)),
+                          reinterpret_cast<float*>(wsp(ws, L.sh_hsum)), h_out, ysh, half,
+                          kRowsDirect, static_cast<int*>(ws), stream);
+  if (s) return s;
+  if (y_out)
+    MOE_CUDA(launch_add_planes(ysh, ysh + half, y_out, long(half), stream), "plane sum");
+  return MOE_OK;
 }
 
 }  // namespace
@@ -354,7 +363,7 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
   if (!bucket_offsets || (T > 0 && (!topk_idx || !topk_w || !bucket_perm)))
     return fail(MOE_ERR_INVALID_ARG, "routing outputs must not be NULL");
   const WsLayout L = ws_layout(T, E, top_k, H, 128);
-  if ((s = check_ws(ws, ws_bytes, L.part))) return s;
+  if ((s = check_ws(ws, ws_bytes, L.idx))) return s;
   float* lg = logits ? logits : reinterpret_cast<float*>(wsp(ws, L.logits));
   float* gl = reinterpret_cast<float*>(wsp(ws, L.gate_logit));
   RouterJob R{};
@@ -443,16 +452,19 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
   MOE_CUDA(launch_subslots(bucket_offsets, E, nss, se, so, sc, stream), "sub-slot kernel");
   const SubSlots ss{nss, se, so, sc, 0, 0};
   float* y = reinterpret_cast<float*>(wsp(ws, L.y));
+  const size_t yhalf = size_t(T) * top_k * H;
   s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
                bucket_perm, top_k, reinterpret_cast<uint16_t*>(wsp(ws, L.hh)),
                reinterpret_cast<uint16_t*>(wsp(ws, L.hl)),
-               reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr, y, kRowsScatter,
+               reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr, y, yhalf, kRowsScatter,
                static_cast<int*>(ws), stream);
   if (s) return s;
   CombineArgs C{};
   C.y = y;
+  C.yhalf = yhalf;
   C.w = topk_w;
   C.ysh = y_shared;
+  C.ysh2 = nullptr;
   C.sg = shared_gate_w;
   C.out = static_cast<uint16_t*>(out);
   C.T = T;
@@ -522,35 +534,38 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
     uint16_t* shl = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl));
     float* shsum = reinterpret_cast<float*>(wsp(ws, L.sh_hsum));
     float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
-    A.y = reinterpret_cast<float*>(wsp(ws, L.y));
-    A.ysh = reinterpret_cast<float*>(wsp(ws, L.ysh));
-    A.C = bank_cfg(experts, hh, hl, hsum, nullptr, A.y, status);
+    float* y = reinterpret_cast<float*>(wsp(ws, L.y));
+    float* ysh = reinterpret_cast<float*>(wsp(ws, L.ysh));
+    A.C = bank_cfg(experts, hh, hl, hsum, nullptr, y, size_t(T) * top_k * H, status);
     if (shared) {
       A.C.geo[2] = geo13(shared);
       A.C.geo[3] = geo2(shared);
-      A.C.fmt_shared = shared->fmt;
     }
-    A.C.tg[2] = MatTarget{shh, shl, shsum, nullptr, nullptr};
-    A.C.tg[3] = MatTarget{nullptr, nullptr, nullptr, nullptr, A.ysh};
+    A.C.tg[2] = MatTarget{shh, shl, shsum, nullptr, nullptr, 0};
+    A.C.tg[3] = MatTarget{nullptr, nullptr, nullptr, nullptr, ysh, size_t(T) * H};
     const int ldx = sums_ld(A.C.geo[0].t), ldh = sums_ld(A.C.geo[1].t);
-    A.src[0] = MatSource{A.R.x, nullptr, xsum, H, ldx};
-    A.src[1] = MatSource{hh, hl, hsum, I, ldh};
+    A.src[0] = MatSource{A.R.x, nullptr, xsum, H, ldx, 0};
+    A.src[1] = MatSource{hh, hl, hsum, h_pitch(I), ldh, 1};
     A.src[2] = A.src[0];
-    A.src[3] = MatSource{shh, shl, shsum, I, ldh};
+    A.src[3] = MatSource{shh, shl, shsum, h_pitch(I), ldh, 1};
     A.k = top_k;
     A.has_shared = shared ? 1 : 0;
     A.KS = router_ks(H);
-    A.part = reinterpret_cast<float*>(wsp(ws, L.part));
+    A.R.logits = reinterpret_cast<float*>(wsp(ws, L.logits));
+    A.R.gate_logit = reinterpret_cast<float*>(wsp(ws, L.gate_logit));
     A.user_idx = topk_idx;
     A.user_w = topk_w;
     A.out = static_cast<uint16_t*>(out);
     A.ctrl = status;
-    int S = 0, SB = 0, smem = 0;
-    decode_smem(A, &S, &SB, &smem);
-    if (S < 2)
-      return fail(MOE_ERR_INVALID_ARG, "shape needs %d-byte stages; two do not fit in shared memory",
-                  SB);
-    MOE_CUDA(launch_decode(A, experts->fmt, sm_count(), stream), "fused decode kernel");
+    const EnginePlan P = decode_plan(A);
+    if (P.S < 2)
+      return fail(MOE_ERR_INVALID_ARG,
+                  "shape needs %d-byte operand buffers and %d-byte stages; they do not fit in "
+                  "shared memory",
+                  P.OB, P.SB);
+    MOE_CUDA(launch_decode(A, experts->fmt, shared ? shared->fmt : experts->fmt, sm_count(),
+                           stream),
+             "fused decode kernel");
     return ok();
   }
   int32_t* idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(wsp(ws, L.idx));

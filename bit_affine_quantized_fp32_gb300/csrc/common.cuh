@@ -21,7 +21,6 @@ struct WsLayout {
   size_t ctrl;        // int32 control words ([0] device status), 16 KiB
   size_t logits;      // f32 [T][E]
   size_t gate_logit;  // f32 [T]
-  size_t part;        // f32 [8][T][E+1] router partial sums (fused path)
   size_t idx;         // i32 [T][k]
   size_t w;           // f32 [T][k]
   size_t sgw;         // f32 [T]
@@ -32,14 +31,14 @@ struct WsLayout {
   size_t ss_off;      // i32 [maxss] first bucket position
   size_t ss_cnt;      // i32 [maxss] tokens (1..8)
   size_t xsum;        // f32 [T][ldx] per-64-group sums of x
-  size_t hh;          // u16 [T*k][I] bf16 high part of h
-  size_t hl;          // u16 [T*k][I] bf16 low part of h
+  size_t hh;          // u16 [T*k][I+8] bf16 high part of h (padded pitch)
+  size_t hl;          // u16 [T*k][I+8] bf16 low part of h
   size_t hsum;        // f32 [T*k][ldh]
-  size_t y;           // f32 [T*k][H] per-assignment expert outputs
-  size_t sh_hh;       // u16 [T][I]
-  size_t sh_hl;       // u16 [T][I]
+  size_t y;           // f32 [2][T*k][H] per-assignment expert outputs (k-half planes)
+  size_t sh_hh;       // u16 [T][I+8]
+  size_t sh_hl;       // u16 [T][I+8]
   size_t sh_hsum;     // f32 [T][ldh]
-  size_t ysh;         // f32 [T][H]
+  size_t ysh;         // f32 [2][T][H]
   size_t total;
 };
 
@@ -71,7 +70,6 @@ inline WsLayout ws_layout(long T, long E, long k, long H, long I) {
   L.ctrl = take(16384);
   L.logits = take(4 * T * E);
   L.gate_logit = take(4 * T);
-  L.part = take(4 * 8 * T * (E + 1));
   L.idx = take(4 * P);
   L.w = take(4 * P);
   L.sgw = take(4 * T);
@@ -82,14 +80,14 @@ inline WsLayout ws_layout(long T, long E, long k, long H, long I) {
   L.ss_off = take(4 * mss);
   L.ss_cnt = take(4 * mss);
   L.xsum = take(4 * T * ldx);
-  L.hh = take(2 * P * I);
-  L.hl = take(2 * P * I);
+  L.hh = take(2 * P * (I + 8));   // rows at a pitch of I + 8 elements
+  L.hl = take(2 * P * (I + 8));
   L.hsum = take(4 * P * ldh);
-  L.y = take(4 * P * H);
-  L.sh_hh = take(2 * T * I);
-  L.sh_hl = take(2 * T * I);
+  L.y = take(4 * 2 * P * H);     // two k-half planes
+  L.sh_hh = take(2 * T * (I + 8));
+  L.sh_hl = take(2 * T * (I + 8));
   L.sh_hsum = take(4 * T * ldh);
-  L.ysh = take(4 * T * H);
+  L.ysh = take(4 * 2 * T * H);
   L.total = o;
   return L;
 }

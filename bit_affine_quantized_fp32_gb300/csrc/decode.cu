@@ -135,18 +135,20 @@ struct FusedSched {
   __device__ const int* perm() const { return RT->perm; }
   __device__ int topk() const { return A->k; }
   __device__ void combine(int blk) const {
-    combine_rows(A->y, RT->w, A->has_shared ? A->ysh : nullptr,
+    combine_rows(A->C.tg[1].y, A->C.tg[1].yhalf, RT->w, A->has_shared ? A->C.tg[3].y : nullptr,
+                 A->has_shared ? A->C.tg[3].y + A->C.tg[3].yhalf : nullptr,
                  A->has_shared && A->R.gq ? RT->sg : nullptr, A->out, T, A->k, A->C.hidden,
                  A->R.f16 != 0, blk, threadIdx.x, kConsumers);
   }
 };
 
-template <int FMT, bool F16A>
+template <int FMT, int FMT_SH, bool F16A>
 __global__ void __launch_bounds__(kEngineThreads, 1)
-    k_decode(const __grid_constant__ DecodeArgs A, int S, int SB) {
-  extern __shared__ __align__(128) uint8_t stages[];
+    k_decode(const __grid_constant__ DecodeArgs A, const EnginePlan P) {
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ EngineSmem E;
   __shared__ RouteTable RT;
+  __shared__ float RT_part[kConsumerWarps * 32];  // router partials [warp][T]
   __shared__ __align__(8) uint64_t xbar;
   __shared__ int last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -156,52 +158,59 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   const int T = A.R.T, H = A.R.H, NE = A.R.E;
   const bool gate = A.R.gq != nullptr;
   const int E1 = NE + (gate ? 1 : 0);
-  engine_init(E, S);
+  engine_init(E, P.S);
+  const EngineMem M{smem, smem + P.nob * P.OB, P.OB, P.nob, P.SB, P.S};
   if (tid == 0) mbar_init(&xbar, 1);
   fence_proxy_async();
   __syncthreads();
 
   // ---- phase 0: router partial sums and activation sums
-  const uint16_t* xs = A.R.x;
   const int xbytes = T * H * 2;
-  if (xbytes <= S * SB) {  // x rows into shared memory for the router tasks
-    if (tid == 0) {
-      mbar_expect_tx(&xbar, unsigned(xbytes));
-      for (int o = 0; o < xbytes; o += 65536)
-        bulk_g2s(stages + o, reinterpret_cast<const uint8_t*>(A.R.x) + o,
-                 unsigned(min(65536, xbytes - o)), &xbar);
-    }
-    mbar_wait_bounded(&xbar, 0, &E.skip, status);
-    xs = reinterpret_cast<const uint16_t*>(stages);
+  // x rows into shared memory for the router blocks of this CTA
+  const bool xsm = int(blockIdx.x) < (E1 + kConsumerWarps / A.KS - 1) / (kConsumerWarps / A.KS) &&
+                   xbytes <= P.nob * P.OB + P.S * P.SB;
+  if (xsm && tid == 0) {
+    mbar_expect_tx(&xbar, unsigned(xbytes));
+    for (int o = 0; o < xbytes; o += 65536)
+      bulk_g2s(smem + o, reinterpret_cast<const uint8_t*>(A.R.x) + o,
+               unsigned(min(65536, xbytes - o)), &xbar);
   }
-  const int n_router = E1 * A.KS;
-  const int n_tasks = n_router + T * (H >> 7);
-  int done = 0;
-  for (int i = blockIdx.x + G * warp; i < n_tasks; i += G * (kEngineThreads / 32)) {
-    if (i < n_router) {
-      const int row = i / A.KS, q = i - row * A.KS;
-      router_warp_any(A.R, A.KS, row, q, xs, T, A.part + size_t(q) * T * E1 + row, E1);
-    } else {
-      xsum_task(A.R.x, H, A.R.f16 != 0, A.C.geo[0].t, const_cast<float*>(A.src[0].Bsum),
-                i - n_router);
+  const uint16_t* xs = xsm ? reinterpret_cast<const uint16_t*>(smem) : A.R.x;
+  bool xready = !xsm;
+  auto wait_x = [&]() {
+    if (!xready) {
+      mbar_wait_bounded(&xbar, 0, &E.skip, status);
+      xready = true;
     }
+  };
+  // router blocks (all warps of a CTA, rows finalised in shared memory) first,
+  // activation-sum tasks on the CTAs after them
+  const int RPB = kConsumerWarps / A.KS;
+  const int nrb_router = (E1 + RPB - 1) / RPB;
+  const int nx = T * (H >> 7);
+  int done = 0;
+  for (int rb = blockIdx.x; rb < nrb_router; rb += G) {
+    router_rows_cta(A.R, A.KS, kConsumerWarps, rb, RT_part, xs, wait_x);
+    if (tid == 0) red_release_add(ctrl + kCtlPhase0, 1);
+  }
+  const int xb = (blockIdx.x + G - nrb_router % G) % G;
+  for (int i = xb + G * warp; i < nx; i += G * (kEngineThreads / 32)) {
+    xsum_task(A.R.x, H, A.R.f16 != 0, A.C.geo[0].t, const_cast<float*>(A.src[0].Bsum), i);
     ++done;
   }
+  wait_x();  // every thread: the copy has landed before the shared memory is reused
   __syncwarp();
-  if (lane == 0 && done) {
-    __threadfence();
-    red_release_add(ctrl + kCtlPhase0, done);
-  }
+  if (lane == 0 && done) red_release_add(ctrl + kCtlPhase0, done);
+  const int n_tasks = nrb_router + nx;
 
   // ---- routing, redundantly in every CTA
   if (tid == 0) wait_counter(ctrl + kCtlPhase0, n_tasks, &E.skip, status);
   __syncthreads();
   {
-    float* lg = reinterpret_cast<float*>(stages);
-    int(*wc)[256] = reinterpret_cast<int(*)[256]>(stages + align128i((T * NE + T) * 4));
+    int(*wc)[256] = reinterpret_cast<int(*)[256]>(smem);
     const bool first = blockIdx.x == 0;
-    route_table_cta(A.part, A.KS, E1, A.R.bias, gate, T, NE, A.k, first ? A.user_idx : nullptr,
-                    first ? A.user_w : nullptr, lg, wc, RT);
+    route_table_cta(A.R.logits, gate ? A.R.gate_logit : nullptr, T, NE, A.k,
+                    first ? A.user_idx : nullptr, first ? A.user_w : nullptr, wc, RT);
   }
   fence_proxy_async();  // routing scratch (generic writes) before TMA reuses it
   __syncthreads();
@@ -210,9 +219,11 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   {
     const FusedSched sch(&A, &RT);
     if (warp == kProducerWarp)
-      producer_run(A.C, E, stages, SB, S, sch, ctrl);
+      producer_run(A.C, E, M, sch, ctrl);
+    else if (warp == kSignalWarp)
+      signal_run(E, sch, ctrl, status);
     else
-      consumer_run<FMT, F16A>(A.C, E, stages, SB, S, sch, ctrl);
+      consumer_run<FMT, FMT_SH, F16A>(A.C, E, M, sch);
   }
 
   // ---- exit: the last CTA zeroes the counters for the next call
@@ -230,11 +241,11 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   }
 }
 
-template <int FMT, bool F16A>
+template <int FMT, int FMT_SH, bool F16A>
 cudaError_t launch_decode_t(const DecodeArgs& A, int sms, cudaStream_t st) {
-  int S = 0, SB = 0, smem = 0;
-  decode_smem(A, &S, &SB, &smem);
-  if (S < 2) return cudaErrorInvalidValue;
+  const EnginePlan P = decode_plan(A);
+  if (P.S < 2) return cudaErrorInvalidValue;
+  const int smem = P.bytes();
   // raise the dynamic shared-memory limit once per device (not a stream
   // operation, so later calls can be captured in graphs)
   static int configured[64] = {0};
@@ -243,8 +254,8 @@ cudaError_t launch_decode_t(const DecodeArgs& A, int sms, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (configured[dev] < smem) {
-    e = cudaFuncSetAttribute(k_decode<FMT, F16A>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
+    e = cudaFuncSetAttribute(k_decode<FMT, FMT_SH, F16A>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured[dev] = smem;
   }
@@ -258,32 +269,41 @@ cudaError_t launch_decode_t(const DecodeArgs& A, int sms, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode<FMT, F16A>, A, S, SB);
+  return cudaLaunchKernelEx(&cfg, k_decode<FMT, FMT_SH, F16A>, A, P);
+}
+
+template <int FMT, int FMT_SH>
+cudaError_t launch_fmt2(const DecodeArgs& A, int sms, cudaStream_t st) {
+  return A.R.f16 ? launch_decode_t<FMT, FMT_SH, true>(A, sms, st)
+                 : launch_decode_t<FMT, FMT_SH, false>(A, sms, st);
 }
 
 template <int FMT>
-cudaError_t launch_fmt(const DecodeArgs& A, int sms, cudaStream_t st) {
-  return A.R.f16 ? launch_decode_t<FMT, true>(A, sms, st)
-                 : launch_decode_t<FMT, false>(A, sms, st);
+cudaError_t launch_fmt(const DecodeArgs& A, int fmt_sh, int sms, cudaStream_t st) {
+  switch (fmt_sh) {
+    case MOE_FMT_AFFINE4_G64: return launch_fmt2<FMT, MOE_FMT_AFFINE4_G64>(A, sms, st);
+    case MOE_FMT_AFFINE3_G64: return launch_fmt2<FMT, MOE_FMT_AFFINE3_G64>(A, sms, st);
+    case MOE_FMT_W4A16_SYM_G128: return launch_fmt2<FMT, MOE_FMT_W4A16_SYM_G128>(A, sms, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
-void decode_smem(const DecodeArgs& A, int* S, int* SB, int* bytes) {
+EnginePlan decode_plan(const DecodeArgs& A) {
   const TileGeo geos[4] = {A.C.geo[0].t, A.C.geo[1].t, A.C.geo[2].t, A.C.geo[3].t};
   const int stat = int(sizeof(EngineSmem) + sizeof(RouteTable) + 64);
-  engine_stages(geos, A.has_shared ? 4 : 2, stat, S, SB);
-  // the stage area doubles as routing scratch: logits + 8 x 256 ints
-  const int scratch = align128i((A.R.T * A.R.E + A.R.T) * 4) + 8 * 256 * 4;
-  if (*S * *SB < scratch) *S = 0;
-  *bytes = *S * *SB;
+  EnginePlan P = engine_plan(geos, A.has_shared ? 4 : 2, stat);
+  // the dynamic area doubles as routing scratch (8 x 256 ints)
+  if (P.bytes() < 8 * 256 * 4) P.S = 0;
+  return P;
 }
 
-cudaError_t launch_decode(const DecodeArgs& A, int fmt, int sms, cudaStream_t st) {
+cudaError_t launch_decode(const DecodeArgs& A, int fmt, int fmt_sh, int sms, cudaStream_t st) {
   switch (fmt) {
-    case MOE_FMT_AFFINE4_G64: return launch_fmt<MOE_FMT_AFFINE4_G64>(A, sms, st);
-    case MOE_FMT_AFFINE3_G64: return launch_fmt<MOE_FMT_AFFINE3_G64>(A, sms, st);
-    case MOE_FMT_W4A16_SYM_G128: return launch_fmt<MOE_FMT_W4A16_SYM_G128>(A, sms, st);
+    case MOE_FMT_AFFINE4_G64: return launch_fmt<MOE_FMT_AFFINE4_G64>(A, fmt_sh, sms, st);
+    case MOE_FMT_AFFINE3_G64: return launch_fmt<MOE_FMT_AFFINE3_G64>(A, fmt_sh, sms, st);
+    case MOE_FMT_W4A16_SYM_G128: return launch_fmt<MOE_FMT_W4A16_SYM_G128>(A, fmt_sh, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -23,17 +23,14 @@ struct DecodeArgs {
   EngineCfg C;          // geo/targets: 0 routed w13, 1 routed w2, 2 shared w13, 3 shared w2
   MatSource src[4];     // operands of the four matrix slots
   int k, has_shared, KS;
-  float* part;          // router partial sums [KS][T][E1]
-  float* y;             // [T*k][H] per-assignment expert outputs
-  float* ysh;           // [T][H] shared-expert outputs
   int32_t* user_idx;    // nullable outputs [T][k]
   float* user_w;
   uint16_t* out;        // [T][H]
   int* ctrl;
 };
 
-// Stage count, stage bytes and total dynamic shared memory of a launch.
-void decode_smem(const DecodeArgs& A, int* S, int* SB, int* bytes);
-cudaError_t launch_decode(const DecodeArgs& A, int fmt, int sms, cudaStream_t st);
+// Dynamic shared memory of a launch (S < 2: the shape does not fit).
+EnginePlan decode_plan(const DecodeArgs& A);
+cudaError_t launch_decode(const DecodeArgs& A, int fmt, int fmt_sh, int sms, cudaStream_t st);
 
 }  // namespace moe

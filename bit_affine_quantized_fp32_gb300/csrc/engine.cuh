@@ -2,14 +2,18 @@
 // by the standalone expert kernels (units.cu) and the fused layer kernel
 // (decode.cu).
 //
-// A CTA has 17 warps: warp 16 is the producer, warps 0..15 the consumers.
+// A CTA has 18 warps: warps 0..15 are the consumers, warp 16 the producer,
+// warp 17 the signal warp (it publishes finished units to other CTAs, so the
+// consumers never wait on a gpu-scope release).
 // Work comes as "units": one sub-slot (<= 8 tokens of one expert) times one
 // 128-row block of a matrix, streamed as k-chunk "items".  An item is a
-// contiguous block of the kernel-tiled bank (codes + scales, tiled.cuh) plus
-// the operand rows (x, or h as bf16 hi + lo) and their per-64-group sums.
-//   producer: for each item, waits until its stage is free (empty barrier),
-//             writes a small descriptor into the stage, and fills the stage
-//             with TMA bulk copies that complete on the stage's full barrier;
+// contiguous block of the kernel-tiled bank (codes + scales, tiled.cuh); the
+// unit's operand rows (x, or h as bf16 hi + lo, full K) and their per-64-group
+// sums sit in one of two operand buffers for the whole unit.
+//   producer: for each item, waits until its stage is free (empty barrier)
+//             and fills it with one TMA bulk copy that completes on the
+//             stage's full barrier; once per unit it fills an operand buffer
+//             the same way (one copy per x row, or three block copies for h);
 //             it alone waits on other CTAs (operands produced in the kernel).
 //   consumers: wait for the full barrier, run the MMA pass over the item,
 //             release the stage, and after the last item of a unit reduce and
@@ -41,8 +45,10 @@ namespace moe {
 
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = 32 * kConsumerWarps;     // 512
-constexpr int kEngineThreads = kConsumers + 32;     // + the producer warp
+constexpr int kEngineThreads = kConsumers + 64;     // + producer and signal warps
 constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kSignalWarp = kConsumerWarps + 1;
+constexpr int kEpiRing = 4;
 constexpr int kUnitRows = 128;
 constexpr int kMaxTok = 8;
 constexpr int kMaxStages = 6;
@@ -67,57 +73,46 @@ __host__ __device__ inline int sums_pos(const TileGeo& t, int j) {
   return (j / t.ng) * sums_ngp(t) + j % t.ng;
 }
 
-// Item descriptor, written by the producer at the start of the stage.
-enum : int { kItemGateUp = 0, kItemDown = 1, kItemCombine = 2, kItemEnd = 3 };
+enum : int { kItemGateUp = 0, kItemDown = 1, kItemCombine = 2 };
 
-struct ItemDesc {
-  int kind;
-  int mat;     // 0 routed w13, 1 routed w2, 2 shared w13, 3 shared w2
-  int c;       // k-chunk
-  int first;   // first chunk of its unit (clear the accumulators)
-  int last;    // last chunk (epilogue)
-  int cnt;     // tokens, 1..8
-  int blk;     // 64-row group (gate/up), 128-row block (down, combine)
-  int signal;  // control word to add 1 to after the epilogue, -1 for none
-  int orow[kMaxTok];  // output row of token slot n (h row, or y row)
+// A weight stage holds one tiled item.
+__host__ __device__ inline int stage_bytes(const TileGeo& t) { return align128i(t.item_bytes); }
+
+// Operand buffer of a unit: [rows hi][rows lo (split operands)][sums], rows of
+// the full K at a pitch 16 bytes past a multiple of 128 (conflict-free
+// fragment loads), sums rows of sums_ld(t) floats.
+struct OpLayout {
+  int x, xlo, xs, bpitch, lds, bytes;
 };
 
-// Shared-memory stage: [descriptor][tiled item][operand hi][operand lo][sums]
-struct StageLayout {
-  int a, x, xlo, xs, bpitch, ngp, bytes;
-};
-
-__host__ __device__ inline StageLayout stage_layout(const TileGeo& t) {
-  StageLayout L;
-  L.bpitch = t.CK * 2 + 16;  // operand rows 16 bytes past a multiple of 128
-  L.ngp = sums_ngp(t);
-  L.a = 128;
-  L.x = L.a + align128i(t.item_bytes);
-  L.xlo = L.x + kMaxTok * L.bpitch;
-  L.xs = t.down ? L.xlo + kMaxTok * L.bpitch : L.xlo;
-  L.bytes = align128i(L.xs + kMaxTok * L.ngp * 4);
+__host__ __device__ inline OpLayout op_layout(const TileGeo& t) {
+  OpLayout L;
+  L.bpitch = t.K * 2 + 16;
+  L.lds = sums_ld(t);
+  L.x = 0;
+  L.xlo = kMaxTok * L.bpitch;
+  L.xs = t.down ? 2 * kMaxTok * L.bpitch : L.xlo;
+  L.bytes = align128i(L.xs + kMaxTok * L.lds * 4);
   return L;
-}
-
-// Bytes a stage receives for an item of `cnt` tokens.
-__host__ __device__ inline unsigned item_tx_bytes(const TileGeo& t, int cnt) {
-  const int rowb = t.CK * 2 * (t.down ? 2 : 1) + sums_ngp(t) * 4;
-  return unsigned(t.item_bytes + cnt * rowb);
 }
 
 // Where the consumers' results go, per matrix slot.
 struct MatTarget {
-  uint16_t* hh;   // gate/up: h hi part [rows][I] (bf16)
+  uint16_t* hh;   // gate/up: h hi part [rows][I + 8] (bf16, padded pitch)
   uint16_t* hl;   //          h lo part
   float* hsum;    //          padded sums of hi + lo per 64-group
-  float* hout;    //          nullable fp32 h
-  float* y;       // down:    [rows][H] fp32
+  float* hout;    //          nullable fp32 h [rows][I]
+  float* y;       // down:    [2][rows][H] fp32, one plane per k-half
+  size_t yhalf;   //          elements from the first plane to the second
 };
+
+// Row pitch (elements) of h in the workspace: 16 bytes past the row, so that a
+// run of consecutive rows copies straight into an operand buffer.
+__host__ __device__ inline int h_pitch(int I) { return I + 8; }
 
 struct EngineCfg {
   MatGeo geo[4];
   MatTarget tg[4];
-  int fmt_shared;  // format of the shared bank (slots 2, 3)
   int inter, hidden;
   int* status;     // device status word
 };
@@ -125,14 +120,40 @@ struct EngineCfg {
 // ---------------------------------------------------------------------------
 // Barrier helpers (all waits bounded).
 
-// Wait for phase `parity` of an mbarrier; on the limit, record a timeout and
-// return false.  `skip` (shared) turns every later wait into a no-op once a
-// timeout has happened, so the kernel finishes (with garbage results) quickly.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
+  return t;
+}
+
+// try_wait that lets the thread sleep (up to `hint_ns`) until the phase
+// completes instead of spinning
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, unsigned parity,
+                                                    unsigned hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second
+
+// Wait for phase `parity` of an mbarrier; after kWaitLimitNs, record a timeout
+// and return false.  `skip` (shared) turns every later wait into a no-op once
+// a timeout has happened, so the kernel finishes (with garbage results)
+// quickly.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity,
                                                   volatile int* skip, int* status) {
-  for (int i = 0; i < (1 << 22); ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63 && *skip) return false;
+  if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (*skip) return false;
+    if (global_ns() - t0 > kWaitLimitNs) break;
   }
   *skip = 1;
   atomicExch(status, int(MOE_ERR_TIMEOUT));
@@ -169,14 +190,17 @@ __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
 }
 
-// Bounded wait (one thread) until *p >= target; on the limit records a timeout
-// and sets *skip.  Returns at once when *skip is already set.
+// Bounded wait (one thread) until *p >= target; after kWaitLimitNs records a
+// timeout and sets *skip.  Returns at once when *skip is already set.
 static __device__ __noinline__ bool wait_counter(const int* p, int target, volatile int* skip,
-                                          int* status) {
+                                                 int* status) {
+  if (ld_acquire(p) >= target) return true;
+  const unsigned long long t0 = global_ns();
   unsigned ns = 32;
-  for (int i = 0; i < (1 << 21); ++i) {
+  for (;;) {
     if (ld_acquire(p) >= target) return true;
     if (*skip) return false;
+    if (global_ns() - t0 > kWaitLimitNs) break;
     __nanosleep(ns);
     if (ns < 256) ns <<= 1;
   }
@@ -213,26 +237,32 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t v) {
   return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
-// One k-chunk item for consumer warp (tile, kh): groups [kh*ng/2, (kh+1)*ng/2)
-// of M-tile `tile`, added into acc.  acc[0]: (row g, token 2t), acc[1]:
+// One k-chunk item (chunk c) for consumer warp (tile, kh): groups
+// [kh*ng/2, (kh+1)*ng/2) of M-tile `tile`, added into acc.  wst is the weight
+// stage, op the unit's operand buffer.  acc[0]: (row g, token 2t), acc[1]:
 // (g, 2t+1), acc[2]: (g+8, 2t), acc[3]: (g+8, 2t+1).  Operand columns of
-// tokens >= cnt hold whatever the stage held before; MMA columns are
+// tokens >= cnt hold whatever the buffer held before; MMA columns are
 // independent, so they only touch accumulators that are never written out.
 template <int FMT, bool F16A, bool SPLIT>
-__device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* st,
-                                             const StageLayout& L, int tile, int kh,
-                                             float (&acc)[4]) {
+__device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* wst,
+                                             const uint8_t* op, const OpLayout& L, int c,
+                                             int tile, int kh, float (&acc)[4]) {
   constexpr int CB = FMT == MOE_FMT_AFFINE3_G64 ? 384 : 512;
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, t = lane & 3;
   const int ng = tg.ng, gh = ng >> 1, G0 = kh * gh;
-  const uint8_t* codes = st + L.a + (tile * ng + G0) * CB;
-  const uint8_t* xrow = st + L.x + gq * L.bpitch + G0 * 128 + 32 * t;
-  const uint8_t* xlrow = st + L.xlo + gq * L.bpitch + G0 * 128 + 32 * t;
-  const float* xs0 = reinterpret_cast<const float*>(st + L.xs) + (2 * t) * L.ngp + G0;
-  const float* xs1 = xs0 + L.ngp;
-  const uint8_t* sc = st + L.a + tg.code_bytes;
-#pragma unroll 2
+  const uint8_t* codes = wst + (tile * ng + G0) * CB;
+  const int xo = gq * L.bpitch + c * tg.CK * 2 + G0 * 128 + 32 * t;
+  const uint8_t* xrow = op + L.x + xo;
+  const uint8_t* xlrow = op + L.xlo + xo;
+  const float* xs0 = reinterpret_cast<const float*>(op + L.xs) + (2 * t) * L.lds +
+                     c * sums_ngp(tg) + G0;
+  const float* xs1 = xs0 + L.lds;
+  const uint8_t* sc = wst + tg.code_bytes;
+  // not unrolled: one compact copy of the body keeps the consumers' loop in
+  // the per-SMSP instruction cache; the 4 consumer warps of an SMSP hide the
+  // latency of each group's chain
+#pragma unroll 1
   for (int G = 0; G < gh; ++G) {
     uint32_t w0, w1, w2, w3;
     if constexpr (FMT == MOE_FMT_AFFINE3_G64) {
@@ -306,39 +336,26 @@ __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* s
   }
 }
 
-// Format dispatch of one item (mat: 0/2 gate/up, 1/3 down).
-template <int FMT, bool F16A>
-__device__ __forceinline__ void compute_mat(const EngineCfg& C, int mat, const uint8_t* st,
-                                            int tile, int kh, float (&acc)[4]) {
+// One item of matrix slot `mat` (0/2 gate/up, 1/3 down); slots 0/1 hold
+// format FMT, slots 2/3 format FMT_SH.  With FMT_SH == FMT both share one
+// copy of the code.
+template <int FMT, int FMT_SH, bool F16A>
+__device__ __forceinline__ void compute_mat(const EngineCfg& C, int mat, const uint8_t* wst,
+                                            const uint8_t* op, int c, int tile, int kh,
+                                            float (&acc)[4]) {
   const TileGeo& tg = C.geo[mat].t;
-  const StageLayout L = stage_layout(tg);
+  const OpLayout L = op_layout(tg);
   const bool down = mat & 1;
-  if (mat < 2) {
+  if (FMT_SH == FMT || mat < 2) {
     if (down)
-      compute_item<FMT, false, true>(tg, st, L, tile, kh, acc);
+      compute_item<FMT, false, true>(tg, wst, op, L, c, tile, kh, acc);
     else
-      compute_item<FMT, F16A, false>(tg, st, L, tile, kh, acc);
-    return;
-  }
-  switch (C.fmt_shared) {
-    case MOE_FMT_AFFINE3_G64:
-      if (down)
-        compute_item<MOE_FMT_AFFINE3_G64, false, true>(tg, st, L, tile, kh, acc);
-      else
-        compute_item<MOE_FMT_AFFINE3_G64, F16A, false>(tg, st, L, tile, kh, acc);
-      break;
-    case MOE_FMT_W4A16_SYM_G128:
-      if (down)
-        compute_item<MOE_FMT_W4A16_SYM_G128, false, true>(tg, st, L, tile, kh, acc);
-      else
-        compute_item<MOE_FMT_W4A16_SYM_G128, F16A, false>(tg, st, L, tile, kh, acc);
-      break;
-    default:
-      if (down)
-        compute_item<MOE_FMT_AFFINE4_G64, false, true>(tg, st, L, tile, kh, acc);
-      else
-        compute_item<MOE_FMT_AFFINE4_G64, F16A, false>(tg, st, L, tile, kh, acc);
-      break;
+      compute_item<FMT, F16A, false>(tg, wst, op, L, c, tile, kh, acc);
+  } else {
+    if (down)
+      compute_item<FMT_SH, false, true>(tg, wst, op, L, c, tile, kh, acc);
+    else
+      compute_item<FMT_SH, F16A, false>(tg, wst, op, L, c, tile, kh, acc);
   }
 }
 
@@ -349,13 +366,16 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // Units and where their rows come from / go to.
 
-// Operand source of a matrix slot: rows of B (and Blo) of ldB elements, and
-// their padded per-64-group sums (row stride ldS floats).
+// Operand source of a matrix slot: rows of B (and Blo) at a pitch of ldB
+// elements and their padded per-64-group sums (row stride ldS floats).
+// block = 1: the rows of a unit are consecutive and ldB*2 equals the operand
+// buffer's pitch (h in the workspace), so each part is one bulk copy;
+// block = 0: one copy per row (x rows, gathered by token).
 struct MatSource {
   const uint16_t* B;
   const uint16_t* Blo;  // nullptr unless the operand is split (h)
   const float* Bsum;
-  int ldB, ldS;
+  int ldB, ldS, block;
 };
 
 enum : int {
@@ -386,8 +406,12 @@ __device__ __forceinline__ int unit_out_row(const UnitInfo& u, const int* perm, 
 
 // Engine shared memory (static part).
 struct EngineSmem {
-  uint64_t full[kMaxStages];
+  uint64_t full[kMaxStages];      // weight stages
   uint64_t empty[kMaxStages];
+  uint64_t op_full[2];            // operand buffers
+  uint64_t op_empty[2];
+  uint64_t epi_full[kEpiRing];    // unit results written (consumers -> signal warp)
+  uint64_t epi_empty[kEpiRing];   // unit published (signal warp -> consumers)
   int skip;                       // set after the first timeout
   float red[2][8][32][4];         // epilogue: accumulators by k-half, tile, lane
   float part[kConsumerWarps];     // epilogue: per-warp partial sums
@@ -399,11 +423,27 @@ __device__ __forceinline__ void engine_init(EngineSmem& E, int S) {
       mbar_init(&E.full[s], 1);
       mbar_init(&E.empty[s], kConsumerWarps);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&E.op_full[b], 1);
+      mbar_init(&E.op_empty[b], kConsumerWarps);
+    }
+    for (int b = 0; b < kEpiRing; ++b) {
+      mbar_init(&E.epi_full[b], kConsumerWarps);
+      mbar_init(&E.epi_empty[b], 1);
+    }
     E.skip = 0;
   }
 }
 
-// Stage ring position: slot and how many times it has been used.
+// Dynamic shared memory of the engine: nob operand buffers of OB bytes, then
+// S weight stages of SB bytes.
+struct EngineMem {
+  uint8_t* ops;
+  uint8_t* stages;
+  int OB, nob, SB, S;
+};
+
+// Ring position: slot and how many times it has been used.
 struct Ring {
   int slot, use, S;
   __device__ void next() {
@@ -417,89 +457,109 @@ struct Ring {
 // ---------------------------------------------------------------------------
 // Producer (warp kProducerWarp, all 32 lanes).
 
-// Fill stage `st` with item (u, c): the tiled item by four bulk copies, then
-// (after the unit's dependency, for the first chunk) the operand rows and
-// their sums, one bulk copy per row.  Completes on *full.
-__device__ __forceinline__ void produce_item(const EngineCfg& C, const MatSource& src,
-                                             const UnitInfo& u, int c, const int* perm, int k,
-                                             uint8_t* st, uint64_t* full, const int* ctrl,
-                                             volatile int* skip) {
+// Weight item (u, c) into a stage: one bulk copy.
+__device__ __forceinline__ void produce_weights(const MatGeo& g, const UnitInfo& u, int c,
+                                                uint8_t* st, uint64_t* full) {
+  if ((threadIdx.x & 31) == 0) {
+    const int bytes = g.t.item_bytes;
+    mbar_expect_tx(full, unsigned(bytes));
+    bulk_g2s(st, g.base + (size_t)u.e * g.t.expert_bytes + (size_t)(u.blk * g.t.nch + c) * bytes,
+             unsigned(bytes), full);
+  }
+}
+
+// The unit's operand rows and sums into an operand buffer, after the unit's
+// dependency (if any).  Completes on *full.
+__device__ __forceinline__ void produce_operands(const EngineCfg& C, const MatSource& src,
+                                                 const UnitInfo& u, const int* perm, int k,
+                                                 uint8_t* ob, uint64_t* full, const int* ctrl,
+                                                 volatile int* skip) {
   const int lane = threadIdx.x & 31;
   const TileGeo& tg = C.geo[u.mat].t;
-  const StageLayout L = stage_layout(tg);
-  if (lane == 0) mbar_expect_only(full, item_tx_bytes(tg, u.cnt));
-  __syncwarp();
-  const int bytes = tg.item_bytes;
-  if (lane < 4) {
-    const uint8_t* w = C.geo[u.mat].base + (size_t)u.e * tg.expert_bytes +
-                       (size_t)(u.blk * tg.nch + c) * bytes;
-    const int piece = align16i((bytes + 3) / 4);
-    const int o = lane * piece;
-    const int n = min(piece, bytes - o);
-    if (n > 0) bulk_g2s(st + L.a + o, w + o, unsigned(n), full);
-  }
-  if (u.wait_ctr >= 0 && c == 0) {
+  const OpLayout L = op_layout(tg);
+  if (u.wait_ctr >= 0) {
     if (lane == 0) wait_counter(ctrl + u.wait_ctr, u.wait_target, skip, C.status);
     __syncwarp();
     fence_proxy_async_global();
   }
-  // lanes 8..15: operand hi rows, 16..23: lo rows, 24..31: sums
-  const int part = lane >> 3, n = lane & 7;
-  if (part >= 1 && n < u.cnt) {
-    const int row = unit_op_row(u, perm, k, n);
-    if (part == 1) {
-      bulk_g2s(st + L.x + n * L.bpitch, src.B + (size_t)row * src.ldB + (size_t)c * tg.CK,
-               unsigned(tg.CK * 2), full);
-    } else if (part == 2) {
-      if (src.Blo)
-        bulk_g2s(st + L.xlo + n * L.bpitch, src.Blo + (size_t)row * src.ldB + (size_t)c * tg.CK,
-                 unsigned(tg.CK * 2), full);
-    } else {
-      bulk_g2s(st + L.xs + n * L.ngp * 4, src.Bsum + (size_t)row * src.ldS + (size_t)c * L.ngp,
-               unsigned(L.ngp * 4), full);
+  if (src.block) {
+    const unsigned rb = unsigned(u.cnt * L.bpitch), sb = unsigned(u.cnt * L.lds * 4);
+    if (lane == 0) {
+      mbar_expect_tx(full, rb * (src.Blo ? 2u : 1u) + sb);
+      bulk_g2s(ob + L.x, src.B + (size_t)u.off * src.ldB, rb, full);
+      if (src.Blo) bulk_g2s(ob + L.xlo, src.Blo + (size_t)u.off * src.ldB, rb, full);
+      bulk_g2s(ob + L.xs, src.Bsum + (size_t)u.off * src.ldS, sb, full);
     }
+  } else {
+    if (lane == 0) mbar_expect_only(full, unsigned(u.cnt * (tg.K * 2 + L.lds * 4)));
+    __syncwarp();
+    const int n = lane & 7;
+    if (n < u.cnt && lane < 16) {
+      const int row = unit_op_row(u, perm, k, n);
+      if (lane < 8)
+        bulk_g2s(ob + L.x + n * L.bpitch, src.B + (size_t)row * src.ldB, unsigned(tg.K * 2),
+                 full);
+      else
+        bulk_g2s(ob + L.xs + n * L.lds * 4, src.Bsum + (size_t)row * src.ldS,
+                 unsigned(L.lds * 4), full);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(full);
   }
-  __syncwarp();
-  if (lane == 0) mbar_arrive(full);
 }
 
-// The producer's loop over a schedule (sch.n_units(), sch.unit(j)).
+// The producer's loop over a schedule (sch.n_units(), sch.unit(j)): per unit,
+// the first weight item, then the operands, then the other items.
 template <class Sched>
-__device__ void producer_run(const EngineCfg& C, EngineSmem& E, uint8_t* stages, int SB, int S,
+__device__ void producer_run(const EngineCfg& C, EngineSmem& E, const EngineMem& M,
                              const Sched& sch, const int* ctrl) {
   const int lane = threadIdx.x & 31;
-  Ring R{0, 0, S};
-  int issued = 0;
+  Ring R{0, 0, M.S}, B{0, 0, M.nob};
   const int nu = sch.n_units();
+  auto take_stage = [&]() -> uint8_t* {
+    if (R.use > 0) {
+      if (lane == 0) mbar_wait_bounded(&E.empty[R.slot], (R.use - 1) & 1, &E.skip, C.status);
+      __syncwarp();
+    }
+    return M.stages + (size_t)R.slot * M.SB;
+  };
   for (int j = 0; j < nu; ++j) {
     const UnitInfo u = sch.unit(j);
-    const int nit = u.kind == kItemCombine ? 1 : u.nch;
-    for (int c = 0; c < nit; ++c) {
-      if (R.use > 0) {
-        if (lane == 0) mbar_wait_bounded(&E.empty[R.slot], (R.use - 1) & 1, &E.skip, C.status);
-        __syncwarp();
+    if (u.kind == kItemCombine) {
+      take_stage();
+      if (lane == 0) {
+        wait_counter(ctrl + u.wait_ctr, u.wait_target, &E.skip, C.status);
+        mbar_arrive(&E.full[R.slot]);
       }
-      uint8_t* st = stages + (size_t)R.slot * SB;
-      if (u.kind == kItemCombine) {
-        if (lane == 0) {
-          wait_counter(ctrl + u.wait_ctr, u.wait_target, &E.skip, C.status);
-          mbar_arrive(&E.full[R.slot]);
-        }
-        __syncwarp();
-      } else {
-        produce_item(C, sch.source(u.mat), u, c, sch.perm(), sch.topk(), st, &E.full[R.slot],
-                     ctrl, &E.skip);
-      }
-      ++issued;
+      __syncwarp();
+      R.next();
+      continue;
+    }
+    const MatGeo& g = C.geo[u.mat];
+    produce_weights(g, u, 0, take_stage(), &E.full[R.slot]);
+    R.next();
+    if (B.use > 0) {
+      if (lane == 0) mbar_wait_bounded(&E.op_empty[B.slot], (B.use - 1) & 1, &E.skip, C.status);
+      __syncwarp();
+    }
+    produce_operands(C, sch.source(u.mat), u, sch.perm(), sch.topk(),
+                     M.ops + (size_t)B.slot * M.OB, &E.op_full[B.slot], ctrl, &E.skip);
+    B.next();
+    for (int c = 1; c < u.nch; ++c) {
+      produce_weights(g, u, c, take_stage(), &E.full[R.slot]);
       R.next();
     }
   }
-  // wait (bounded) until every stage this warp filled has landed
+  // wait (bounded) until the last copies have landed: every stage and
+  // operand buffer's most recent fill
   if (lane == 0) {
-    Ring D{0, 0, S};
-    for (int i = 0; i < issued; ++i) {
-      if (i + S >= issued) mbar_wait_bounded(&E.full[D.slot], D.use & 1, &E.skip, C.status);
-      D.next();
+    for (int s = 0; s < M.S; ++s) {
+      const int uses = R.use + (s < R.slot ? 1 : 0);
+      if (uses > 0) mbar_wait_bounded(&E.full[s], (uses - 1) & 1, &E.skip, C.status);
+    }
+    for (int b = 0; b < M.nob; ++b) {
+      const int uses = B.use + (b < B.slot ? 1 : 0);
+      if (uses > 0) mbar_wait_bounded(&E.op_full[b], (uses - 1) & 1, &E.skip, C.status);
     }
   }
   __syncwarp();
@@ -516,7 +576,7 @@ __device__ void producer_run(const EngineCfg& C, EngineSmem& E, uint8_t* stages,
 // the two warps of the token in order).
 __device__ __forceinline__ void epilogue_gateup(const EngineCfg& C, EngineSmem& E,
                                                 const UnitInfo& u, int my_orow,
-                                                const float (&acc)[4], int* ctrl) {
+                                                const float (&acc)[4]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = warp & 7, kh = warp >> 3;
 #pragma unroll
@@ -535,10 +595,10 @@ __device__ __forceinline__ void epilogue_gateup(const EngineCfg& C, EngineSmem& 
   float s = __bfloat162float(hb) + __bfloat162float(lb);
   const int o = __shfl_sync(0xffffffffu, my_orow, n);
   if (n < u.cnt) {
-    const size_t at = (size_t)o * I + u.blk * 64 + r;
+    const size_t at = (size_t)o * h_pitch(I) + u.blk * 64 + r;
     T.hh[at] = __bfloat16_as_ushort(hb);
     T.hl[at] = __bfloat16_as_ushort(lb);
-    if (T.hout) T.hout[at] = h;
+    if (T.hout) T.hout[(size_t)o * I + u.blk * 64 + r] = h;
   }
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
@@ -550,52 +610,77 @@ __device__ __forceinline__ void epilogue_gateup(const EngineCfg& C, EngineSmem& 
     if (lane < u.cnt)
       T.hsum[(size_t)o2 * sums_ld(dg) + sums_pos(dg, u.blk)] =
           E.part[2 * lane] + E.part[2 * lane + 1];
-    __syncwarp();
-    if (lane == 0 && u.signal >= 0) {
-      __threadfence();
-      red_release_add(ctrl + u.signal, 1);
-    }
   }
 }
 
-// Output of a down unit: y[out_row(n)][128 blk + r] = k-half 0 + k-half 1.
-__device__ __forceinline__ void epilogue_down(const EngineCfg& C, EngineSmem& E,
-                                              const UnitInfo& u, int my_orow,
-                                              const float (&acc)[4], int* ctrl) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Output of a down unit: each warp writes its k-half's sums straight to its
+// plane of y (plane kh, row out_row(n), column 128 blk + 16 tile + g (+8));
+// the two planes are added (plane 0 + plane 1) where y is read.
+__device__ __forceinline__ void epilogue_down(const EngineCfg& C, const UnitInfo& u,
+                                              int my_orow, const float (&acc)[4]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tile = warp & 7, kh = warp >> 3;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) E.red[kh][tile][lane][i] = acc[i];
-  consumer_sync();
-  float* y = C.tg[u.mat].y;
+  const int g = lane >> 2, t = lane & 3;
+  const MatTarget& T = C.tg[u.mat];
+  float* y = T.y + (kh ? T.yhalf : 0) + u.blk * kUnitRows + tile * 16 + g;
   const int H = C.hidden;
-#pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    const int v = tid + kConsumers * s;
-    const int n = v >> 7, r = v & 127;
-    const int tl = r >> 4, rr = r & 15;
-    const int src = (rr & 7) * 4 + (n >> 1), idx = (rr >> 3) * 2 + (n & 1);
-    const int o = __shfl_sync(0xffffffffu, my_orow, n);
-    if (n < u.cnt)
-      y[(size_t)o * H + u.blk * kUnitRows + r] = E.red[0][tl][src][idx] + E.red[1][tl][src][idx];
+  const int o0 = __shfl_sync(0xffffffffu, my_orow, (2 * t) & 7);
+  const int o1 = __shfl_sync(0xffffffffu, my_orow, (2 * t + 1) & 7);
+  if (2 * t < u.cnt) {
+    y[(size_t)o0 * H] = acc[0];
+    y[(size_t)o0 * H + 8] = acc[2];
   }
-  consumer_sync();
-  if (tid == 0 && u.signal >= 0) {
-    __threadfence();
-    red_release_add(ctrl + u.signal, 1);
+  if (2 * t + 1 < u.cnt) {
+    y[(size_t)o1 * H] = acc[1];
+    y[(size_t)o1 * H + 8] = acc[3];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Publishing finished units.  After a unit's results are written, every
+// consumer warp arrives on epi_full[slot]; the signal warp waits for it and
+// adds 1 to the unit's control word with a release reduction (cumulative: it
+// publishes every write the signal warp has observed through the barrier),
+// then frees the slot.  Units without a control word skip all of this.
+__device__ __forceinline__ void epi_publish(EngineSmem& E, Ring& P, const UnitInfo& u,
+                                            int* status) {
+  if (u.signal < 0) return;
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (P.use > 0) mbar_wait_bounded(&E.epi_empty[P.slot], (P.use - 1) & 1, &E.skip, status);
+    mbar_arrive(&E.epi_full[P.slot]);
+  }
+  P.next();
+}
+
+template <class Sched>
+__device__ void signal_run(EngineSmem& E, const Sched& sch, int* ctrl, int* status) {
+  const int lane = threadIdx.x & 31;
+  Ring P{0, 0, kEpiRing};
+  const int nu = sch.n_units();
+  for (int j = 0; j < nu; ++j) {
+    const UnitInfo u = sch.unit(j);
+    if (u.kind == kItemCombine || u.signal < 0) continue;
+    if (lane == 0) {
+      mbar_wait_bounded(&E.epi_full[P.slot], P.use & 1, &E.skip, status);
+      red_release_add(ctrl + u.signal, 1);
+      mbar_arrive(&E.epi_empty[P.slot]);
+    }
+    __syncwarp();
+    P.next();
   }
 }
 
 // ---------------------------------------------------------------------------
 // Consumers' loop over the same schedule as the producer.  sch.combine(blk)
 // runs a combine unit (fused kernel only).
-template <int FMT, bool F16A, class Sched>
-__device__ void consumer_run(const EngineCfg& C, EngineSmem& E, const uint8_t* stages, int SB,
-                             int S, const Sched& sch, int* ctrl) {
+template <int FMT, int FMT_SH, bool F16A, class Sched>
+__device__ void consumer_run(const EngineCfg& C, EngineSmem& E, const EngineMem& M,
+                             const Sched& sch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tile = warp & 7, kh = warp >> 3;
-  Ring R{0, 0, S};
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  Ring R{0, 0, M.S}, B{0, 0, M.nob}, P{0, 0, kEpiRing};
+  float acc[4];
   const int nu = sch.n_units();
   for (int j = 0; j < nu; ++j) {
     const UnitInfo u = sch.unit(j);
@@ -608,27 +693,35 @@ __device__ void consumer_run(const EngineCfg& C, EngineSmem& E, const uint8_t* s
       continue;
     }
     const int my_orow = lane < u.cnt ? unit_out_row(u, sch.perm(), lane) : 0;
+    const uint8_t* op = M.ops + (size_t)B.slot * M.OB;
+    mbar_wait_bounded(&E.op_full[B.slot], B.use & 1, &E.skip, C.status);
     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     for (int c = 0; c < u.nch; ++c) {
       mbar_wait_bounded(&E.full[R.slot], R.use & 1, &E.skip, C.status);
-      compute_mat<FMT, F16A>(C, u.mat, stages + (size_t)R.slot * SB, tile, kh, acc);
+      compute_mat<FMT, FMT_SH, F16A>(C, u.mat, M.stages + (size_t)R.slot * M.SB, op, c, tile, kh,
+                                     acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&E.empty[R.slot]);
       R.next();
     }
+    if (lane == 0) mbar_arrive(&E.op_empty[B.slot]);
+    B.next();
     if (u.kind == kItemDown)
-      epilogue_down(C, E, u, my_orow, acc, ctrl);
+      epilogue_down(C, u, my_orow, acc);
     else
-      epilogue_gateup(C, E, u, my_orow, acc, ctrl);
+      epilogue_gateup(C, E, u, my_orow, acc);
+    epi_publish(E, P, u, C.status);
   }
 }
 
 // ---------------------------------------------------------------------------
 // Weighted combine of one 128-row block of the output, for all T tokens:
 //   out[t, h] = round( sum_j w[t, j] * y[t*k + j, h]  +  s_t * ysh[t, h] )
-// an fp32 fma chain in slot order with the shared slot last.  y and ysh are
-// read through L2 (written by other CTAs).  `nthr` threads from `tid0`.
-__device__ __forceinline__ void combine_rows(const float* y, const float* w, const float* ysh,
+// an fp32 fma chain in slot order with the shared slot last; y (and ysh when
+// ysh2 is given) come as two k-half planes, added plane 0 + plane 1 first.
+// y and ysh are read through L2 (written by other CTAs).  `nthr` threads.
+__device__ __forceinline__ void combine_rows(const float* y, size_t yhalf, const float* w,
+                                             const float* ysh, const float* ysh2,
                                              const float* sg, uint16_t* out, int T, int k, int H,
                                              bool f16, int blk, int tid, int nthr) {
   for (int v = tid; v < T * kUnitRows; v += nthr) {
@@ -636,10 +729,14 @@ __device__ __forceinline__ void combine_rows(const float* y, const float* w, con
     const int h = blk * kUnitRows + (v & 127);
     float acc = 0.f;
     for (int j = 0; j < k; ++j) {
-      const int a = t * k + j;
-      acc = fmaf(w[a], __ldcg(y + (size_t)a * H + h), acc);
+      const size_t a = (size_t)(t * k + j) * H + h;
+      acc = fmaf(w[t * k + j], __ldcg(y + a) + __ldcg(y + yhalf + a), acc);
     }
-    if (ysh) acc = fmaf(sg ? sg[t] : 1.f, __ldcg(ysh + (size_t)t * H + h), acc);
+    if (ysh) {
+      const size_t a = (size_t)t * H + h;
+      const float vs = ysh2 ? __ldcg(ysh + a) + __ldcg(ysh2 + a) : __ldcg(ysh + a);
+      acc = fmaf(sg ? sg[t] : 1.f, vs, acc);
+    }
     out[(size_t)t * H + h] = float_to_act_bits(acc, f16);
   }
 }

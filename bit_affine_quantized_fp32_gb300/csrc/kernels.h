@@ -38,18 +38,27 @@ cudaError_t launch_xsum(const uint16_t* x, int T, int H, bool f16, const TileGeo
                         float* xsum, cudaStream_t st);
 
 struct CombineArgs {
-  const float* y;    // [T*k][H]
+  const float* y;    // [2][T*k][H] k-half planes
+  size_t yhalf;      // elements to the second plane
   const float* w;    // [T][k]
   const float* ysh;  // [T][H] or nullptr
+  const float* ysh2; // second plane of ysh, or nullptr when ysh is final
   const float* sg;   // [T] or nullptr (weight 1)
   uint16_t* out;     // [T][H]
   int T, k, H, f16;
 };
 cudaError_t launch_combine(const CombineArgs& A, cudaStream_t st);
+cudaError_t launch_add_planes(const float* a, const float* b, float* dst, long n,
+                              cudaStream_t st);
 
-// Dynamic shared memory of an engine kernel: stage count and stage bytes for
-// the given matrices (at most kMaxStages stages within the budget).
-void engine_stages(const TileGeo* geos, int n, int static_bytes, int* S, int* SB);
+// Dynamic shared memory of an engine kernel for the given matrices: two
+// operand buffers when they fit (else one), then as many weight stages as fit
+// (at most kMaxStages).  S < 2 means the shape does not fit.
+struct EnginePlan {
+  int OB, nob, SB, S;
+  int bytes() const { return nob * OB + S * SB; }
+};
+EnginePlan engine_plan(const TileGeo* geos, int n, int static_bytes);
 
 // routing
 struct RouterJob {

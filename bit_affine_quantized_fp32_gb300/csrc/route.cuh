@@ -48,11 +48,16 @@ __device__ __forceinline__ void router_load_w4(int fmt, const void* q, const uin
 // shared-gate row when row == E) over k-split q of KS (4*NI columns per lane,
 // held in registers) with tokens 0..tn-1 of xs (row stride H; global or
 // shared memory).  Lane order and xor tree are fixed; lane 0 writes token
-// t's partial sum to out[t * ostride].
-template <int NI>
+// t's partial sum to out[t * ostride].  pre() runs between the weight loads
+// and the first read of xs (the fused kernel waits for its x copy there).
+struct NoPre {
+  __device__ void operator()() const {}
+};
+
+template <int NI, class Pre>
 __device__ __forceinline__ void router_warp(const RouterJob& J, int KS, int row, int q,
-                                            const uint16_t* xs, int tn, float* out,
-                                            int ostride) {
+                                            const uint16_t* xs, int tn, float* out, int ostride,
+                                            const Pre& pre) {
   const int lane = threadIdx.x & 31;
   const int kq = q * (J.H / KS);
   float w[NI][4];
@@ -65,6 +70,7 @@ __device__ __forceinline__ void router_warp(const RouterJob& J, int KS, int row,
     else
       router_load_w4(J.fmt, J.q, J.s, J.b, row, J.H, k, w[i]);
   }
+  pre();
   for (int tl = 0; tl < tn; tl += 4) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -90,18 +96,19 @@ __device__ __forceinline__ void router_warp(const RouterJob& J, int KS, int row,
   }
 }
 
+template <class Pre = NoPre>
 __device__ __forceinline__ void router_warp_any(const RouterJob& J, int KS, int row, int q,
                                                 const uint16_t* xs, int tn, float* out,
-                                                int ostride) {
+                                                int ostride, const Pre& pre = Pre()) {
   const int NI_ = J.H / (KS * 128);
   if (NI_ == 1)
-    router_warp<1>(J, KS, row, q, xs, tn, out, ostride);
+    router_warp<1>(J, KS, row, q, xs, tn, out, ostride, pre);
   else if (NI_ == 2)
-    router_warp<2>(J, KS, row, q, xs, tn, out, ostride);
+    router_warp<2>(J, KS, row, q, xs, tn, out, ostride, pre);
   else if (NI_ == 3)
-    router_warp<3>(J, KS, row, q, xs, tn, out, ostride);
+    router_warp<3>(J, KS, row, q, xs, tn, out, ostride, pre);
   else
-    router_warp<4>(J, KS, row, q, xs, tn, out, ostride);
+    router_warp<4>(J, KS, row, q, xs, tn, out, ostride, pre);
 }
 
 // A logit from its KS partial sums (stride apart), added in split order, plus
@@ -110,14 +117,6 @@ __device__ __forceinline__ float router_finalize(const float* p, size_t stride, 
                                                  const float* bias) {
   float s = 0.f;
   for (int q = 0; q < KS; ++q) s += p[q * stride];
-  if (bias) s += *bias;
-  return s;
-}
-
-__device__ __forceinline__ float router_finalize_cg(const float* p, size_t stride, int KS,
-                                                    const float* bias) {
-  float s = 0.f;
-  for (int q = 0; q < KS; ++q) s += __ldcg(p + q * stride);
   if (bias) s += *bias;
   return s;
 }
@@ -149,6 +148,36 @@ __device__ __forceinline__ void router_block(const RouterJob& J, int KS, int rb,
   __syncthreads();
 }
 
+// The fused kernel's router block rb: rows [rb*RPB, rb*RPB + RPB) with
+// RPB = NW / KS, warp (row, q) running router_warp for all T tokens into
+// part [NW][T] (shared), then every (row, token) finalised in split order
+// (router_finalize, as router_block does) into J.logits / J.gate_logit.
+// All threads of the CTA call it; it ends with a barrier.
+template <class Pre>
+__device__ __forceinline__ void router_rows_cta(const RouterJob& J, int KS, int NW, int rb,
+                                                float* part, const uint16_t* xs,
+                                                const Pre& pre) {
+  const int wid = threadIdx.x >> 5;
+  const int RPB = NW / KS;
+  const int rl = wid / KS, q = wid - rl * KS;
+  const int row = rb * RPB + rl;
+  const int nrows = J.E + (J.gq ? 1 : 0);
+  if (wid < RPB * KS && row < nrows) router_warp_any(J, KS, row, q, xs, J.T, part + wid * J.T, 1, pre);
+  __syncthreads();
+  for (int i = threadIdx.x; i < RPB * J.T; i += blockDim.x) {
+    const int r2 = i / J.T, tl = i - r2 * J.T;
+    const int row2 = rb * RPB + r2;
+    if (row2 >= nrows) continue;
+    const float* p = part + (r2 * KS) * J.T + tl;
+    if (row2 < J.E)
+      J.logits[size_t(tl) * J.E + row2] =
+          router_finalize(p, J.T, KS, J.bias ? J.bias + row2 : nullptr);
+    else
+      J.gate_logit[tl] = router_finalize(p, J.T, KS, nullptr);
+  }
+  __syncthreads();
+}
+
 // Ranking key of (logit v, expert id): a larger key ranks first.  The high
 // word is an order-preserving image of the float (-0 folded onto +0, so equal
 // logits tie), 0 for NaN; the low word is 256 - id, so equal logits go to the
@@ -164,24 +193,18 @@ __device__ __forceinline__ float key_value(unsigned hi) {
   return __uint_as_float((hi & 0x80000000u) ? (hi & 0x7fffffffu) : ~hi);
 }
 
-// Top-k + weights of token t by one warp: each lane sorts the keys of experts
-// lane, lane+32, ... (8 at most) once; each of the k rounds takes the warp
-// maximum of the lanes' heads (two redux.max) and the winning lane pops its
-// head.  Then w_j = exp(l_j - l_0) / sum.  Logits come from shared memory
-// (SMEM) or through L2 (they may have been written by other CTAs).
-template <bool SMEM = false>
-__device__ __forceinline__ void topk_warp(const float* logits, const float* gate_logit, int t,
-                                          int E, int k, int32_t* idx, float* w, float* sg,
-                                          int32_t* idx2, float* w2, int* idx_smem = nullptr) {
+// Selection of the top k of token t from each lane's keys (8 per lane, any
+// experts; see rank_key): each lane sorts its keys once; each of the k rounds
+// takes the warp maximum of the lanes' heads (redux.max on the high word, and
+// on the low word only when several lanes tie) and the winning lane pops its
+// head.  Then w_j = exp(l_j - l_0) / sum over the k, the exponentials by lanes
+// 0..k-1 in parallel and the sum in slot order.  Lanes 0..k-1 write
+// idx/w[t*k + j] (and idx2/w2 when given); lane 0 writes sg[t] from the gate
+// logit gl when has_gate.
+__device__ __forceinline__ void topk_select(unsigned long long (&key)[8], int t, int k,
+                                            int32_t* idx, float* w, float* sg, bool has_gate,
+                                            float gl, int32_t* idx2, float* w2) {
   const int lane = threadIdx.x & 31;
-  unsigned long long key[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane + 32 * i;
-    float v = 0.f;
-    if (e < E) v = SMEM ? logits[size_t(t) * E + e] : __ldcg(logits + size_t(t) * E + e);
-    key[i] = e < E ? rank_key(v, e) : 0ull;
-  }
   // sorting network (descending), 19 compare-exchanges
 #define MOE_CX(a, b)                                  \
   {                                                   \
@@ -197,50 +220,80 @@ __device__ __forceinline__ void topk_warp(const float* logits, const float* gate
   MOE_CX(2, 4) MOE_CX(3, 5)
   MOE_CX(3, 4)
 #undef MOE_CX
-  int sel_e[8];
-  float sel_v[8];
+  int my_e = 0;
+  float my_v = 0.f, top = 0.f;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
-    sel_e[r] = 0;
-    sel_v[r] = 0.f;
     if (r < k) {
       const unsigned hi = unsigned(key[0] >> 32), lo = unsigned(key[0]);
       const unsigned mh = __reduce_max_sync(0xffffffffu, hi);
-      const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
+      const unsigned tie = __ballot_sync(0xffffffffu, hi == mh);
+      const unsigned ml =
+          (tie & (tie - 1u)) ? __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u)
+                             : __shfl_sync(0xffffffffu, lo, __ffs(tie) - 1);
       if (hi == mh && lo == ml) {
 #pragma unroll
         for (int i = 0; i < 7; ++i) key[i] = key[i + 1];
         key[7] = 0ull;
       }
-      sel_e[r] = 256 - int(ml);
-      sel_v[r] = key_value(mh);
-    }
-  }
-  if (lane == 0) {
-    const float top = sel_v[0];
-    float ex[8];
-    float den = 0.f;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      ex[r] = r < k ? expf(sel_v[r] - top) : 0.f;
-      if (r < k) den += ex[r];
-    }
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      if (r < k) {
-        const float wr = ex[r] / den;
-        idx[size_t(t) * k + r] = sel_e[r];
-        w[size_t(t) * k + r] = wr;
-        if (idx2) idx2[size_t(t) * k + r] = sel_e[r];
-        if (w2) w2[size_t(t) * k + r] = wr;
-        if (idx_smem) idx_smem[t * k + r] = sel_e[r];
+      const float v = key_value(mh);
+      if (r == 0) top = v;
+      if (lane == r) {
+        my_e = 256 - int(ml);
+        my_v = v;
       }
     }
-    if (gate_logit && sg) {
-      const float gl = SMEM ? gate_logit[t] : __ldcg(gate_logit + t);
-      sg[t] = 1.f / (1.f + expf(-gl));
+  }
+  const float ex = lane < k ? expf(my_v - top) : 0.f;
+  float den = 0.f;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const float er = __shfl_sync(0xffffffffu, ex, r);
+    if (r < k) den += er;
+  }
+  if (lane < k) {
+    const float wr = ex / den;
+    idx[size_t(t) * k + lane] = my_e;
+    w[size_t(t) * k + lane] = wr;
+    if (idx2) idx2[size_t(t) * k + lane] = my_e;
+    if (w2) w2[size_t(t) * k + lane] = wr;
+  }
+  if (lane == 0 && has_gate && sg) sg[t] = 1.f / (1.f + expf(-gl));
+}
+
+// Top-k + weights of token t by one warp from fp32 logits [T][E] (E <= 256),
+// lane l taking experts 8l..8l+7, read from shared memory (SMEM) or through
+// L2 (they may have been written by other CTAs).
+template <bool SMEM = false>
+__device__ __forceinline__ void topk_warp(const float* logits, const float* gate_logit, int t,
+                                          int E, int k, int32_t* idx, float* w, float* sg,
+                                          int32_t* idx2, float* w2) {
+  const int lane = threadIdx.x & 31;
+  const float* row = logits + size_t(t) * E;
+  float v[8];
+  if ((E & 7) == 0 && 8 * lane < E && ((reinterpret_cast<uintptr_t>(row) & 15u) == 0)) {
+    const float4 a = SMEM ? *reinterpret_cast<const float4*>(row + 8 * lane)
+                          : __ldcg(reinterpret_cast<const float4*>(row + 8 * lane));
+    const float4 b = SMEM ? *reinterpret_cast<const float4*>(row + 8 * lane + 4)
+                          : __ldcg(reinterpret_cast<const float4*>(row + 8 * lane + 4));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = 8 * lane + i;
+      v[i] = e < E ? (SMEM ? row[e] : __ldcg(row + e)) : 0.f;
     }
   }
+  unsigned long long key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = 8 * lane + i;
+    key[i] = e < E ? rank_key(v[i], e) : 0ull;
+  }
+  float gl = 0.f;
+  if (gate_logit) gl = SMEM ? gate_logit[t] : __ldcg(gate_logit + t);
+  topk_select(key, t, k, idx, w, sg, gate_logit != nullptr, gl, idx2, w2);
 }
 
 // Shared memory of bucket_cta for NW warps.
@@ -355,8 +408,8 @@ __device__ __forceinline__ void subslots_cta(const int32_t* offsets, int E, int*
 }
 
 // Routing of a decode batch (T <= 32, T*k <= 256 assignments) by one CTA,
-// every result in shared memory: the logits finalised from the router's
-// partial sums, top-k + weights per token (topk_warp), the stable counting
+// every result in shared memory: top-k + weights per token (topk_warp), the
+// stable counting
 // sort of the assignments by expert (as bucket_cta) and the sub-slot table
 // (as subslots_cta).  Same definitions as the standalone kernels, same bits.
 constexpr int kMaxSubFused = 296;  // sub-slots of a call with T*k <= 256
@@ -377,31 +430,19 @@ struct RouteTable {
   int wsub[8];
 };
 
-// part: router partial sums [KS][T][E1] (E1 = E + 1 with a shared gate);
-// lg: T*E + T floats of shared scratch; wc: 8*256 ints of shared scratch.
-// user_idx/user_w (nullable) receive the top-k outputs.  All threads of the
-// CTA call it (blockDim.x >= 256).
-__device__ __forceinline__ void route_table_cta(const float* part, int KS, int E1,
-                                                const float* bias, bool gate, int T, int E, int k,
-                                                int32_t* user_idx, float* user_w, float* lg,
-                                                int (*wc)[256], RouteTable& S) {
+// logits [T][E] and gate_logit [T] (nullable) written by other CTAs; wc:
+// 8*256 ints of shared scratch.  user_idx/user_w (nullable) receive the top-k
+// outputs.  All threads of the CTA call it (blockDim.x >= 256).
+__device__ __forceinline__ void route_table_cta(const float* logits, const float* gate_logit,
+                                                int T, int E, int k, int32_t* user_idx,
+                                                float* user_w, int (*wc)[256], RouteTable& S) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int NT = blockDim.x, NW = NT >> 5;
-  float* gl = lg + T * E;
-  const size_t qs = size_t(T) * E1;
-  for (int i = tid; i < T * E1; i += NT) {
-    const int t = i / E1, row = i - t * E1;
-    const float* p = part + size_t(t) * E1 + row;
-    if (row < E)
-      lg[t * E + row] = router_finalize_cg(p, qs, KS, bias ? bias + row : nullptr);
-    else
-      gl[t] = router_finalize_cg(p, qs, KS, nullptr);
-  }
   for (int i = tid; i < 256; i += NT) S.cnt[i] = 0;
   for (int i = tid; i < 8 * 256; i += NT) wc[i >> 8][i & 255] = 0;
   __syncthreads();
   for (int t = wid; t < T; t += NW)
-    topk_warp<true>(lg, gate ? gl : nullptr, t, E, k, S.idx, S.w, S.sg, user_idx, user_w);
+    topk_warp<false>(logits, gate_logit, t, E, k, S.idx, S.w, S.sg, user_idx, user_w);
   __syncthreads();
   const int N = T * k;
   const int e_a = tid < N ? S.idx[tid] : -1;

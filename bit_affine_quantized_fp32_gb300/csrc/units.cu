@@ -61,17 +61,20 @@ struct JobSched {
 
 template <int FMT, bool F16A>
 __global__ void __launch_bounds__(kEngineThreads, 1)
-    k_units(const __grid_constant__ UnitJob J, int S, int SB) {
-  extern __shared__ __align__(128) uint8_t stages[];
+    k_units(const __grid_constant__ UnitJob J, const EnginePlan P) {
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ EngineSmem E;
-  engine_init(E, S);
+  engine_init(E, P.S);
   fence_proxy_async();
   __syncthreads();
+  const EngineMem M{smem, smem + P.nob * P.OB, P.OB, P.nob, P.SB, P.S};
   const JobSched sch(&J);
-  if ((threadIdx.x >> 5) == kProducerWarp)
-    producer_run(J.C, E, stages, SB, S, sch, nullptr);
-  else
-    consumer_run<FMT, F16A>(J.C, E, stages, SB, S, sch, nullptr);
+  const int warp = threadIdx.x >> 5;
+  if (warp == kProducerWarp)
+    producer_run(J.C, E, M, sch, nullptr);
+  else if (warp < kConsumerWarps)
+    consumer_run<FMT, FMT, F16A>(J.C, E, M, sch);
+  // the signal warp has nothing to publish in a standalone launch
 }
 
 __global__ void k_xsum(const uint16_t* __restrict__ x, int T, int H, int f16, TileGeo g13,
@@ -82,17 +85,23 @@ __global__ void k_xsum(const uint16_t* __restrict__ x, int T, int H, int f16, Ti
 }
 
 __global__ void __launch_bounds__(256) k_combine(const CombineArgs A) {
-  combine_rows(A.y, A.w, A.ysh, A.sg, A.out, A.T, A.k, A.H, A.f16 != 0, blockIdx.x, threadIdx.x,
-               blockDim.x);
+  combine_rows(A.y, A.yhalf, A.w, A.ysh, A.ysh2, A.sg, A.out, A.T, A.k, A.H, A.f16 != 0,
+               blockIdx.x, threadIdx.x, blockDim.x);
+}
+
+// dst = a + b elementwise (the two k-half planes of a down projection)
+__global__ void k_add_planes(const float* __restrict__ a, const float* __restrict__ b,
+                             float* __restrict__ dst, long n) {
+  const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = a[i] + b[i];
 }
 
 template <int FMT, bool F16A>
 cudaError_t launch_units_t(const UnitJob& J, int sms, cudaStream_t st) {
   const TileGeo geos[1] = {J.C.geo[J.mat].t};
-  int S = 0, SB = 0;
-  engine_stages(geos, 1, int(sizeof(EngineSmem)), &S, &SB);
-  if (S < 2) return cudaErrorInvalidValue;
-  const int smem = S * SB;
+  const EnginePlan P = engine_plan(geos, 1, int(sizeof(EngineSmem)));
+  if (P.S < 2) return cudaErrorInvalidValue;
+  const int smem = P.bytes();
   // raise the dynamic shared-memory limit once per device (cudaFuncSetAttribute
   // is not a stream operation, so it stays out of captured graphs afterwards)
   static int configured[64] = {0};
@@ -108,7 +117,7 @@ cudaError_t launch_units_t(const UnitJob& J, int sms, cudaStream_t st) {
   }
   const int grid = J.max_units < sms ? J.max_units : sms;
   if (grid <= 0) return cudaSuccess;
-  k_units<FMT, F16A><<<grid, kEngineThreads, smem, st>>>(J, S, SB);
+  k_units<FMT, F16A><<<grid, kEngineThreads, smem, st>>>(J, P);
   return cudaGetLastError();
 }
 
@@ -119,17 +128,23 @@ cudaError_t launch_fmt(const UnitJob& J, bool f16a, int sms, cudaStream_t st) {
 
 }  // namespace
 
-void engine_stages(const TileGeo* geos, int n, int static_bytes, int* S, int* SB) {
-  int sb = 0;
+EnginePlan engine_plan(const TileGeo* geos, int n, int static_bytes) {
+  EnginePlan P{0, 2, 0, 0};
   for (int i = 0; i < n; ++i) {
-    const int b = stage_layout(geos[i]).bytes;
-    sb = b > sb ? b : sb;
+    const int sb = stage_bytes(geos[i]), ob = op_layout(geos[i]).bytes;
+    P.SB = sb > P.SB ? sb : P.SB;
+    P.OB = ob > P.OB ? ob : P.OB;
   }
   const int avail = kEngineSmemMax - static_bytes - 1024;
-  int s = sb > 0 ? avail / sb : 0;
-  if (s > kMaxStages) s = kMaxStages;
-  *S = s;
-  *SB = sb;
+  if (P.SB <= 0) return P;
+  P.S = (avail - 2 * P.OB) / P.SB;
+  if (P.S < 2) {
+    P.nob = 1;
+    P.S = (avail - P.OB) / P.SB;
+  }
+  if (P.S > kMaxStages) P.S = kMaxStages;
+  if (P.S < 0) P.S = 0;
+  return P;
 }
 
 cudaError_t launch_units(const UnitJob& J, bool f16a, int sms, cudaStream_t st) {
@@ -148,6 +163,13 @@ cudaError_t launch_xsum(const uint16_t* x, int T, int H, bool f16, const TileGeo
   const int tasks = T * (H >> 7);
   if (tasks <= 0) return cudaSuccess;
   k_xsum<<<(tasks + 7) / 8, 256, 0, st>>>(x, T, H, f16 ? 1 : 0, g13, xsum);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_add_planes(const float* a, const float* b, float* dst, long n,
+                              cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  k_add_planes<<<unsigned((n + 255) / 256), 256, 0, st>>>(a, b, dst, n);
   return cudaGetLastError();
 }
 
