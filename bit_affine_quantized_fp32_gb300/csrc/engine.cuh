@@ -238,32 +238,32 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t v) {
 }
 
 // One k-chunk item (chunk c) for consumer warp (tile, kh): groups
-// [kh*ng/2, (kh+1)*ng/2) of M-tile `tile`, added into acc.  wst is the weight
-// stage, op the unit's operand buffer.  acc[0]: (row g, token 2t), acc[1]:
-// (g, 2t+1), acc[2]: (g+8, 2t), acc[3]: (g+8, 2t+1).  Operand columns of
-// tokens >= cnt hold whatever the buffer held before; MMA columns are
-// independent, so they only touch accumulators that are never written out.
-template <int FMT, bool F16A, bool SPLIT>
+// [kh*NG/2, (kh+1)*NG/2) of M-tile `tile`, added into acc.  NG = CK/64 is a
+// compile-time constant so the group loop unrolls completely (a rolled loop
+// costs several times the instructions).  wst is the weight stage, op the
+// unit's operand buffer.  acc[0]: (row g, token 2t), acc[1]: (g, 2t+1),
+// acc[2]: (g+8, 2t), acc[3]: (g+8, 2t+1).  Operand columns of tokens >= cnt
+// hold whatever the buffer held before; MMA columns are independent, so they
+// only touch accumulators that are never written out.
+template <int FMT, bool F16A, bool SPLIT, int NG>
 __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* wst,
                                              const uint8_t* op, const OpLayout& L, int c,
                                              int tile, int kh, float (&acc)[4]) {
   constexpr int CB = FMT == MOE_FMT_AFFINE3_G64 ? 384 : 512;
+  constexpr int GH = NG / 2;
+  constexpr int NGP = (NG + 3) & ~3;
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, t = lane & 3;
-  const int ng = tg.ng, gh = ng >> 1, G0 = kh * gh;
-  const uint8_t* codes = wst + (tile * ng + G0) * CB;
-  const int xo = gq * L.bpitch + c * tg.CK * 2 + G0 * 128 + 32 * t;
+  const int G0 = kh * GH;
+  const uint8_t* codes = wst + (tile * NG + G0) * CB;
+  const int xo = gq * L.bpitch + c * NG * 128 + G0 * 128 + 32 * t;
   const uint8_t* xrow = op + L.x + xo;
   const uint8_t* xlrow = op + L.xlo + xo;
-  const float* xs0 = reinterpret_cast<const float*>(op + L.xs) + (2 * t) * L.lds +
-                     c * sums_ngp(tg) + G0;
+  const float* xs0 = reinterpret_cast<const float*>(op + L.xs) + (2 * t) * L.lds + c * NGP + G0;
   const float* xs1 = xs0 + L.lds;
-  const uint8_t* sc = wst + tg.code_bytes;
-  // not unrolled: one compact copy of the body keeps the consumers' loop in
-  // the per-SMSP instruction cache; the 4 consumer warps of an SMSP hide the
-  // latency of each group's chain
-#pragma unroll 1
-  for (int G = 0; G < gh; ++G) {
+  const uint8_t* sc = wst + 8 * NG * CB;
+#pragma unroll
+  for (int G = 0; G < GH; ++G) {
     uint32_t w0, w1, w2, w3;
     if constexpr (FMT == MOE_FMT_AFFINE3_G64) {
       const uint32_t* pl = reinterpret_cast<const uint32_t*>(codes + G * 384) + lane;
@@ -303,7 +303,7 @@ __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* w
     float s0, s1, b0, b1;
     if constexpr (FMT == MOE_FMT_W4A16_SYM_G128) {
       const uint32_t sv = *reinterpret_cast<const uint32_t*>(
-          sc + ((tile * 8 + gq) * (ng >> 1) + ((G0 + G) >> 1)) * 4);
+          sc + ((tile * 8 + gq) * (NG / 2) + ((G0 + G) >> 1)) * 4);
       const float2 sf = half2_bits_to_float2(sv);
       s0 = sf.x;
       s1 = sf.y;
@@ -313,7 +313,7 @@ __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* w
       b1 = (F16A ? -8.f : -136.f) * s1;
     } else {
       const uint2 sv =
-          *reinterpret_cast<const uint2*>(sc + ((tile * 8 + gq) * ng + G0 + G) * 8);
+          *reinterpret_cast<const uint2*>(sc + ((tile * 8 + gq) * NG + G0 + G) * 8);
       const float2 p0 = half2_bits_to_float2(sv.x), p1 = half2_bits_to_float2(sv.y);
       s0 = p0.x;
       b0 = p0.y;
@@ -336,6 +336,19 @@ __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* w
   }
 }
 
+// Group-count dispatch (CK = 512, 256 or 128).
+template <int FMT, bool F16A, bool SPLIT>
+__device__ __forceinline__ void compute_item_any(const TileGeo& tg, const uint8_t* wst,
+                                                 const uint8_t* op, const OpLayout& L, int c,
+                                                 int tile, int kh, float (&acc)[4]) {
+  if (tg.ng == 8)
+    compute_item<FMT, F16A, SPLIT, 8>(tg, wst, op, L, c, tile, kh, acc);
+  else if (tg.ng == 4)
+    compute_item<FMT, F16A, SPLIT, 4>(tg, wst, op, L, c, tile, kh, acc);
+  else
+    compute_item<FMT, F16A, SPLIT, 2>(tg, wst, op, L, c, tile, kh, acc);
+}
+
 // One item of matrix slot `mat` (0/2 gate/up, 1/3 down); slots 0/1 hold
 // format FMT, slots 2/3 format FMT_SH.  With FMT_SH == FMT both share one
 // copy of the code.
@@ -348,14 +361,14 @@ __device__ __forceinline__ void compute_mat(const EngineCfg& C, int mat, const u
   const bool down = mat & 1;
   if (FMT_SH == FMT || mat < 2) {
     if (down)
-      compute_item<FMT, false, true>(tg, wst, op, L, c, tile, kh, acc);
+      compute_item_any<FMT, false, true>(tg, wst, op, L, c, tile, kh, acc);
     else
-      compute_item<FMT, F16A, false>(tg, wst, op, L, c, tile, kh, acc);
+      compute_item_any<FMT, F16A, false>(tg, wst, op, L, c, tile, kh, acc);
   } else {
     if (down)
-      compute_item<FMT_SH, false, true>(tg, wst, op, L, c, tile, kh, acc);
+      compute_item_any<FMT_SH, false, true>(tg, wst, op, L, c, tile, kh, acc);
     else
-      compute_item<FMT_SH, F16A, false>(tg, wst, op, L, c, tile, kh, acc);
+      compute_item_any<FMT_SH, F16A, false>(tg, wst, op, L, c, tile, kh, acc);
   }
 }
 
