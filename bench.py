@@ -92,6 +92,33 @@ BITS = {"affine8_g64": 8, "affine4_g64": 4, "affine3_g64": 3, "w4a16_g128": 4}
 GROUP = {"affine8_g64": 64, "affine4_g64": 64, "affine3_g64": 64, "w4a16_g128": 128}
 
 
+def kernel_source_hash(read=None) -> str:
+    """sha256 over the library's kernel sources and public header (file names
+    and contents, sorted), used to tell whether an ncu capture still matches."""
+    import hashlib
+    csrc = os.path.join(ROOT, "bit_affine_quantized_fp32_gb300", "csrc")
+    names = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    files = [("bit_affine_quantized_fp32_gb300/csrc/" + f) for f in names] + ["include/moe_gb300.h"]
+    h = hashlib.sha256()
+    for rel in files:
+        data = read(rel) if read else open(os.path.join(ROOT, rel), "rb").read()
+        h.update(rel.encode() + b"\0" + data + b"\0")
+    return h.hexdigest()
+
+
+def captured_traffic():
+    """DRAM bytes per launch of the fused kernel from the committed ncu
+    summary, or None when the kernel sources changed since that capture."""
+    p = os.path.join(ROOT, "profiles", "k_decode_traffic.json")
+    try:
+        rec = json.load(open(p))
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    return int(rec["dram_bytes_per_launch"])
+
+
 def matrix_bytes(fmt: str | None, rows: int, cols: int) -> int:
     if fmt is None:
         return 0
@@ -360,11 +387,12 @@ def run_gpu(args, ws_world, rank, local):
                    "router_fmt": cfg["router_fmt"], "shared_fmt": cfg["shared_fmt"],
                    "gate_fmt": cfg["gate_fmt"], "zipf": cfg["zipf"],
                    "parallelism": f"replicas{ws_world}", "weight_banks": len(banks),
-                   "l2": "inputs larger than L2 (8 rotating weight banks, %.1f GB)" % (
-                       len(banks) * (E * eb + fixed) / 1e9),
+                   "l2": "inputs larger than L2 (%d rotating weight banks, %.1f GB)" % (
+                       len(banks), len(banks) * (E * eb + fixed) / 1e9),
                    "experts_touched_mean": round(float(np.mean(U)), 2)},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gbs / peak, 4), "traffic": None,
+                     "frac": round(gbs / peak, 4),
+                     "traffic": captured_traffic() if T <= 32 else None,
                      "kernel": ("k_decode: the whole layer in one persistent launch" if T <= 32
                                 else "whole step (all launches of one layer call)"),
                      "peak_source": peak_src,
