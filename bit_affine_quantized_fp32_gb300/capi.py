@@ -23,8 +23,8 @@ MOE_DECODE_MAX_TOKENS = 32
 
 EXPORTS = [
     "moe_status_string", "moe_last_error", "moe_workspace_bytes", "moe_workspace_init",
-    "moe_get_device_status", "moe_route", "moe_topk_softmax", "moe_bucket", "moe_expert_mlp",
-    "moe_shared_expert", "moe_experts_forward", "moe_layer_forward",
+    "moe_get_device_status", "moe_route", "moe_route_static", "moe_topk_softmax", "moe_bucket",
+    "moe_expert_mlp", "moe_shared_expert", "moe_experts_forward", "moe_layer_forward",
     "moe_pack_affine8_g64", "moe_unpack_affine8_g64", "moe_pack_affine4_g64",
     "moe_unpack_affine4_g64", "moe_pack_affine3_g64", "moe_unpack_affine3_g64",
     "moe_pack_w4a16_g128", "moe_unpack_w4a16_g128", "moe_tiled_bytes", "moe_repack_bank",
@@ -65,6 +65,7 @@ def _load():
     L.moe_workspace_init.argtypes = [P, c_size_t, P]
     L.moe_get_device_status.argtypes = [P, c_size_t, P, P]
     L.moe_route.argtypes = [P, P, P, P, c_int, c_int, c_int, P, P, P, P, P, P, P, c_size_t, P]
+    L.moe_route_static.argtypes = [P, P, P, P, c_int, c_int, c_int, P, P, P, P, P, P]
     L.moe_topk_softmax.argtypes = [P, c_int, c_int, c_int, P, P, P]
     L.moe_bucket.argtypes = [P, c_int, c_int, c_int, P, P, P]
     L.moe_expert_mlp.argtypes = [P, c_int, P, c_int, c_int, P, P, P, c_size_t, P]
@@ -183,6 +184,14 @@ def moe_route(router: QMatrix, logit_bias, shared_gate: QMatrix | None, x, top_k
                          x.shape[0], top_k, _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
                          _ptr(shared_gate_w), _ptr(bucket_offsets), _ptr(bucket_perm), _ptr(ws),
                          ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_route_static(router: QMatrix, logit_bias, shared_gate: QMatrix | None, x, top_k: int,
+                     topk_idx, topk_w, shared_gate_w, bucket_offsets, bucket_perm, stream=None):
+    _check(lib.moe_route_static(router.ref(), _ptr(logit_bias), _ref(shared_gate), _ptr(x),
+                                act_code(x), x.shape[0], top_k, _ptr(topk_idx), _ptr(topk_w),
+                                _ptr(shared_gate_w), _ptr(bucket_offsets), _ptr(bucket_perm),
+                                _stream(stream)))
 
 
 def moe_topk_softmax(logits, top_k: int, topk_idx, topk_w, stream=None):

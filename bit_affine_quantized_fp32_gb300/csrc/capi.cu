@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -670,6 +671,104 @@ moe_status moe_unrepack_bank(const moe_expert_bank* tiled, void* w13, void* s13,
                            static_cast<uint16_t*>(s2), aff ? static_cast<uint16_t*>(b2) : nullptr,
                            stream),
            "unrepack w2");
+  return ok();
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Routing without a caller workspace (moe_route_static).  Some callers cannot
+// hand the library memory: a caller that owns no device allocator of its own
+// (a plain C host application driving the layer through this ABI), or one that
+// must not allocate once its serving loop runs (cudaMalloc synchronises the
+// device and may fail under memory pressure).  For them the router's one
+// scratch buffer -- the fp32 logits and shared-gate logits between the router
+// kernel and the top-k kernel -- lives in this file-scope device array.
+// Nothing in it has to start at zero: every element a call reads was written
+// earlier in the same call.  There is one array per device, so calls that
+// overlap in time on one device (two streams, two host threads) race on it.
+namespace {
+
+constexpr int kStaticRouteMaxLogits = 32 * 256;  // T * E of at most 32 tokens x 256 experts
+constexpr int kStaticRouteMaxTokens = 32;        // shared-gate logits
+__device__ __align__(256) float g_static_route_scratch[kStaticRouteMaxLogits +
+                                                       kStaticRouteMaxTokens];
+
+// The array's device address, looked up once per device with that device
+// current.  The first call on a device does this set-up (a synchronous
+// runtime query), so it should run before any stream capture.
+moe_status static_route_scratch(float** out) {
+  static std::mutex mu;
+  static float* addr[64] = {nullptr};
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(MOE_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    MOE_CUDA(cudaGetSymbolAddress(&p, g_static_route_scratch), "cudaGetSymbolAddress");
+    addr[dev] = static_cast<float*>(p);
+  }
+  *out = addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_route_static(const moe_qmatrix* router, const float* logit_bias,
+                            const moe_qmatrix* shared_gate, const void* x, int act,
+                            int n_tokens, int top_k, int32_t* topk_idx, float* topk_w,
+                            float* shared_gate_w, int32_t* bucket_offsets, int32_t* bucket_perm,
+                            cudaStream_t stream) {
+  moe_status s;
+  if (!router) return fail(MOE_ERR_INVALID_ARG, "router is NULL");
+  const int E = router->rows, H = router->cols, T = n_tokens;
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "n_tokens=%d < 0", T);
+  if (E < 1 || E > 256) return fail(MOE_ERR_INVALID_ARG, "router rows (experts)=%d not in 1..256", E);
+  if (top_k < 1 || top_k > 8 || top_k > E)
+    return fail(MOE_ERR_INVALID_ARG, "top_k=%d not in 1..min(8, experts)", top_k);
+  if (T > kStaticRouteMaxTokens || long(T) * E > kStaticRouteMaxLogits)
+    return fail(MOE_ERR_WORKSPACE,
+                "moe_route_static: n_tokens=%d x experts=%d exceeds its static scratch of %d "
+                "logits (at most %d tokens); use moe_route with a workspace",
+                T, E, kStaticRouteMaxLogits, kStaticRouteMaxTokens);
+  if ((s = check_hidden(H))) return s;
+  if ((s = check_router_matrix(router, "router", E, H))) return s;
+  if (shared_gate && (s = check_router_matrix(shared_gate, "shared_gate", 1, H))) return s;
+  if ((s = check_act(act))) return s;
+  if (T > 0 && !x) return fail(MOE_ERR_INVALID_ARG, "x is NULL");
+  if (x && !aligned16(x)) return fail(MOE_ERR_MISALIGNED, "x not 16-byte aligned");
+  if (!bucket_offsets || (T > 0 && (!topk_idx || !topk_w || !bucket_perm)))
+    return fail(MOE_ERR_INVALID_ARG, "routing outputs must not be NULL");
+  float* scratch = nullptr;
+  if ((s = static_route_scratch(&scratch))) return s;
+  RouterJob R{};
+  R.fmt = router->fmt;
+  R.q = router->qweight;
+  R.s = static_cast<const uint16_t*>(router->scales);
+  R.b = static_cast<const uint16_t*>(router->biases);
+  if (shared_gate) {
+    R.gfmt = shared_gate->fmt;
+    R.gq = shared_gate->qweight;
+    R.gs = static_cast<const uint16_t*>(shared_gate->scales);
+    R.gb = static_cast<const uint16_t*>(shared_gate->biases);
+  }
+  R.bias = logit_bias;
+  R.x = static_cast<const uint16_t*>(x);
+  R.f16 = act == MOE_FMT_F16;
+  R.T = T;
+  R.E = E;
+  R.H = H;
+  R.logits = scratch;
+  R.gate_logit = scratch + kStaticRouteMaxLogits;
+  MOE_CUDA(launch_router(R, stream), "router kernel");
+  MOE_CUDA(launch_topk(R.logits, shared_gate ? R.gate_logit : nullptr, T, E, top_k, topk_idx,
+                       topk_w, shared_gate ? shared_gate_w : nullptr, stream),
+           "top-k kernel");
+  MOE_CUDA(launch_bucket(topk_idx, T, top_k, E, bucket_offsets, bucket_perm, stream),
+           "bucket kernel");
   return ok();
 }
 

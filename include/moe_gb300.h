@@ -177,6 +177,24 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
                      float* shared_gate_w, int32_t* bucket_offsets, int32_t* bucket_perm,
                      void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* moe_route without a workspace, for callers that cannot hand the library
+ * memory (no device allocator of their own, or no allocation allowed once
+ * serving).  The pages have no counterpart to this entry point: it is
+ * moe_route (same kernels, same results) with its one scratch buffer -- the
+ * fp32 logits between the router and top-k kernels -- in a static device
+ * array of 32 * 256 + 32 floats per device; no logits output.
+ *   Limits: n_tokens <= 32 and n_tokens * experts <= 8192, else
+ *           MOE_ERR_WORKSPACE before anything is launched.
+ *   The first call on a device looks the array's address up (a synchronous
+ *   runtime query), so make it before any stream capture.
+ *   Nothing in the array needs to start at zero.  Calls that overlap in time
+ *   on one device (other streams, other host threads) race on the array. */
+moe_status moe_route_static(const moe_qmatrix* router, const float* logit_bias,
+                            const moe_qmatrix* shared_gate, const void* x, int act,
+                            int n_tokens, int top_k, int32_t* topk_idx, float* topk_w,
+                            float* shared_gate_w, int32_t* bucket_offsets, int32_t* bucket_perm,
+                            cudaStream_t stream);
+
 /* Top-k + weights from given fp32 logits [T, E] (same rules as moe_route). */
 moe_status moe_topk_softmax(const float* logits, int n_tokens, int n_experts, int top_k,
                             int32_t* topk_idx, float* topk_w, cudaStream_t stream);

@@ -150,3 +150,18 @@ def test_route_validation(capi):
 def test_pack_validation(capi):
     assert capi.lib.moe_pack_affine4_g64(1 << 20, 4, 33, 1 << 21, None) == 1
     assert capi.lib.moe_pack_affine3_g64(None, 4, 64, 1 << 21, None) == 1
+
+
+def test_route_static_limits(capi):
+    """moe_route_static refuses shapes beyond its static scratch before any
+    launch (no device needed)."""
+    Q = capi.QMatrixS
+    P = 1 << 21
+    r = Q(capi.FMT["f32"], 256, 2048, 0, P, None, None)
+    rc = capi.lib.moe_route_static(ctypes.byref(r), None, None, P, 1, 33, 8, P, P, None, P, P,
+                                   None)
+    assert rc == 3 and b"static scratch" in capi.lib.moe_last_error()
+    r = Q(capi.FMT["f32"], 256, 2048, 0, P, None, None)
+    rc = capi.lib.moe_route_static(ctypes.byref(r), None, None, P, 1, 32, 8, None, P, None, P,
+                                   P, None)
+    assert rc == 1   # NULL topk_idx, caught before the scratch is looked up
