@@ -210,6 +210,8 @@ EngineCfg bank_cfg(const moe_expert_bank* bank, uint16_t* hh, uint16_t* hl, floa
   C.inter = bank->inter;
   C.hidden = bank->hidden;
   C.status = status;
+  C.magic_bf16 = 0x43004300u;
+  C.magic_f16 = 0x64006400u;
   return C;
 }
 

@@ -115,6 +115,8 @@ struct EngineCfg {
   MatTarget tg[4];
   int inter, hidden;
   int* status;     // device status word
+  uint32_t magic_bf16;  // 0x43004300, see code_pair (held in the parameter space
+  uint32_t magic_f16;   // 0x64006400  so the compiler keeps it out of immediates)
 };
 
 // ---------------------------------------------------------------------------
@@ -216,20 +218,24 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // Consumer arithmetic.
 
-// Two codes (bits [0,4) and [16,20) of v) -> two 16-bit floats.  bf16: the
-// code is ORed into the mantissa of 128.0 (0x4300), giving exactly 128 + q;
-// the 128 is taken out in the fold (bias' = bias - 128 scale).  fp16: 1024 + q
-// (0x6400) minus 1024, exact, so the operand is q itself.
+// Two codes (bits [0,4) and [16,20) of v) -> two 16-bit floats: one lop3
+// (v & 0x000F000F) | magic.  bf16: magic 0x43004300 (128.0) gives exactly
+// 128 + q; the 128 is taken out in the fold (bias' = bias - 128 scale).
+// fp16: magic 0x64006400 (1024.0) gives 1024 + q, minus 1024 exactly.  The
+// magic comes in a register (a kernel parameter): with both constants as
+// immediates the compiler emits two instructions, and the code conversion is
+// what bounds the consumers (integer ALU pipe).
 template <bool F16>
-__device__ __forceinline__ uint32_t code_pair(uint32_t v) {
+__device__ __forceinline__ uint32_t code_pair(uint32_t v, uint32_t magic) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;\n" : "=r"(r) : "r"(v), "r"(magic));
   if constexpr (F16) {
-    uint32_t r = (v & 0x000F000Fu) | 0x64006400u;
     __half2 h = *reinterpret_cast<__half2*>(&r);
     const __half2 off = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
     h = __hsub2(h, off);
     return *reinterpret_cast<uint32_t*>(&h);
   } else {
-    return (v & 0x000F000Fu) | 0x43004300u;
+    return r;
   }
 }
 
@@ -248,7 +254,7 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t v) {
 template <int FMT, bool F16A, bool SPLIT, int NG>
 __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* wst,
                                              const uint8_t* op, const OpLayout& L, int c,
-                                             int tile, int kh, float (&acc)[4]) {
+                                             int tile, int kh, uint32_t mg, float (&acc)[4]) {
   constexpr int CB = FMT == MOE_FMT_AFFINE3_G64 ? 384 : 512;
   constexpr int GH = NG / 2;
   constexpr int NGP = (NG + 3) & ~3;
@@ -279,14 +285,14 @@ __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* w
     const uint4 xb = *reinterpret_cast<const uint4*>(xrow + G * 128 + 16);
     // k-step m takes code pairs (4m, 4m+1) and (4m+2, 4m+3) of the lane's 16
     // codes: nibbles (m&1)*2 and (m&1)*2+1 of word W0/W1 (row g), W2/W3 (g+8)
-    const uint32_t A00 = code_pair<F16A>(w0), A01 = code_pair<F16A>(w2);
-    const uint32_t A02 = code_pair<F16A>(w0 >> 4), A03 = code_pair<F16A>(w2 >> 4);
-    const uint32_t A10 = code_pair<F16A>(w0 >> 8), A11 = code_pair<F16A>(w2 >> 8);
-    const uint32_t A12 = code_pair<F16A>(w0 >> 12), A13 = code_pair<F16A>(w2 >> 12);
-    const uint32_t A20 = code_pair<F16A>(w1), A21 = code_pair<F16A>(w3);
-    const uint32_t A22 = code_pair<F16A>(w1 >> 4), A23 = code_pair<F16A>(w3 >> 4);
-    const uint32_t A30 = code_pair<F16A>(w1 >> 8), A31 = code_pair<F16A>(w3 >> 8);
-    const uint32_t A32 = code_pair<F16A>(w1 >> 12), A33 = code_pair<F16A>(w3 >> 12);
+    const uint32_t A00 = code_pair<F16A>(w0, mg), A01 = code_pair<F16A>(w2, mg);
+    const uint32_t A02 = code_pair<F16A>(w0 >> 4, mg), A03 = code_pair<F16A>(w2 >> 4, mg);
+    const uint32_t A10 = code_pair<F16A>(w0 >> 8, mg), A11 = code_pair<F16A>(w2 >> 8, mg);
+    const uint32_t A12 = code_pair<F16A>(w0 >> 12, mg), A13 = code_pair<F16A>(w2 >> 12, mg);
+    const uint32_t A20 = code_pair<F16A>(w1, mg), A21 = code_pair<F16A>(w3, mg);
+    const uint32_t A22 = code_pair<F16A>(w1 >> 4, mg), A23 = code_pair<F16A>(w3 >> 4, mg);
+    const uint32_t A30 = code_pair<F16A>(w1 >> 8, mg), A31 = code_pair<F16A>(w3 >> 8, mg);
+    const uint32_t A32 = code_pair<F16A>(w1 >> 12, mg), A33 = code_pair<F16A>(w3 >> 12, mg);
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     mma16816<F16A>(d, A00, A01, A02, A03, xa.x, xa.y);
     mma16816<F16A>(d, A10, A11, A12, A13, xa.z, xa.w);
@@ -340,13 +346,14 @@ __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* w
 template <int FMT, bool F16A, bool SPLIT>
 __device__ __forceinline__ void compute_item_any(const TileGeo& tg, const uint8_t* wst,
                                                  const uint8_t* op, const OpLayout& L, int c,
-                                                 int tile, int kh, float (&acc)[4]) {
+                                                 int tile, int kh, uint32_t mg,
+                                                 float (&acc)[4]) {
   if (tg.ng == 8)
-    compute_item<FMT, F16A, SPLIT, 8>(tg, wst, op, L, c, tile, kh, acc);
+    compute_item<FMT, F16A, SPLIT, 8>(tg, wst, op, L, c, tile, kh, mg, acc);
   else if (tg.ng == 4)
-    compute_item<FMT, F16A, SPLIT, 4>(tg, wst, op, L, c, tile, kh, acc);
+    compute_item<FMT, F16A, SPLIT, 4>(tg, wst, op, L, c, tile, kh, mg, acc);
   else
-    compute_item<FMT, F16A, SPLIT, 2>(tg, wst, op, L, c, tile, kh, acc);
+    compute_item<FMT, F16A, SPLIT, 2>(tg, wst, op, L, c, tile, kh, mg, acc);
 }
 
 // One item of matrix slot `mat` (0/2 gate/up, 1/3 down); slots 0/1 hold
@@ -359,16 +366,18 @@ __device__ __forceinline__ void compute_mat(const EngineCfg& C, int mat, const u
   const TileGeo& tg = C.geo[mat].t;
   const OpLayout L = op_layout(tg);
   const bool down = mat & 1;
+  // the down operand (h) is bf16 whatever the activation type
+  const uint32_t mg = (F16A && !down) ? C.magic_f16 : C.magic_bf16;
   if (FMT_SH == FMT || mat < 2) {
     if (down)
-      compute_item_any<FMT, false, true>(tg, wst, op, L, c, tile, kh, acc);
+      compute_item_any<FMT, false, true>(tg, wst, op, L, c, tile, kh, mg, acc);
     else
-      compute_item_any<FMT, F16A, false>(tg, wst, op, L, c, tile, kh, acc);
+      compute_item_any<FMT, F16A, false>(tg, wst, op, L, c, tile, kh, mg, acc);
   } else {
     if (down)
-      compute_item_any<FMT_SH, false, true>(tg, wst, op, L, c, tile, kh, acc);
+      compute_item_any<FMT_SH, false, true>(tg, wst, op, L, c, tile, kh, mg, acc);
     else
-      compute_item_any<FMT_SH, F16A, false>(tg, wst, op, L, c, tile, kh, acc);
+      compute_item_any<FMT_SH, F16A, false>(tg, wst, op, L, c, tile, kh, mg, acc);
   }
 }
 
