@@ -1,17 +1,16 @@
 // decode.cu -- the whole decode layer in one persistent launch.
 //
-// One CTA per SM, co-resident (cooperative launch), 17 warps each.
+// One CTA per SM, co-resident (cooperative launch), 18 warps each.
 //   phase 0  router tasks (one router row x one k-split, partial sums for all
 //            tokens) and activation-sum tasks, spread over every warp of the
 //            grid; each finished task adds 1 to a workspace counter;
 //   routing  every CTA waits for the counter, then builds the whole routing
 //            table itself in shared memory (logits from the partial sums,
 //            top-k, bucketing, sub-slots): no second grid-wide round trip;
-//   phase 1  units in one global order -- shared-expert gate/up, routed
-//            gate/up, shared down, routed down, combine blocks -- unit u going
-//            to CTA (u + 1) mod G, run by the item engine (engine.cuh): the
-//            producer warp streams items through TMA stages, 16 consumer warps
-//            compute.
+//   phase 1  gate/up units, then down units, then combine blocks, balanced
+//            over the CTAs in closed form (FusedSched), run by the item engine
+//            (engine.cuh): the producer warp streams items through TMA stages,
+//            16 consumer warps compute, a signal warp publishes results.
 // Producers of data never wait: a finished gate/up or down unit adds 1 to a
 // counter with a release reduction.  Only the producer warp polls, just
 // before it copies operands that other CTAs write (h rows, y rows for the
@@ -37,12 +36,23 @@ namespace moe {
 
 namespace {
 
-// The units of one CTA in the global order, resolved from the CTA's own
-// routing table.
+// The units of one CTA, resolved from the CTA's own routing table.  Work is
+// balanced in closed form (every CTA computes the same assignment):
+//   gate/up units ("big", c1 items each; shared expert first, then routed in
+//   sub-slot order) go round-robin: big unit b to CTA b mod G;
+//   down units ("small", c2 items each; shared first, then routed in sub-slot
+//   order, so early indices depend on early gate/up units) first fill the
+//   CTAs that got one big unit fewer, q = ceil(c1/c2) each, spread
+//   round-robin over them, then the rest go round-robin over all CTAs;
+//   combine blocks go to CTAs G-1, G-2, ... (those with the least work).
+// A CTA runs its big units, then its small units, then its combine blocks:
+// big units never wait, small units wait only on big units, combine blocks
+// only on small units, so every wait is on work that is already queued ahead.
 struct FusedSched {
   const DecodeArgs* A;
   const RouteTable* RT;
-  int T, ngr, nrb, nss_sh, nss, nA, nB, nC, nD, total, u0, nu;
+  int T, ngr, nrb, nss_sh, nss, nA, nB, nC, nD;
+  int G, c, NB, NS, r, q, atot, nb, qa, qb, ne;
 
   __device__ FusedSched(const DecodeArgs* a, const RouteTable* rt) : A(a), RT(rt) {
     T = A->R.T;
@@ -54,82 +64,99 @@ struct FusedSched {
     nB = nss * ngr;
     nC = nss_sh * nrb;
     nD = nss * nrb;
-    total = nA + nB + nC + nD + nrb;
-    const int G = gridDim.x;
-    u0 = (blockIdx.x + G - 1) % G;
-    nu = total > u0 ? (total - u0 + G - 1) / G : 0;
+    G = gridDim.x;
+    c = blockIdx.x;
+    NB = nA + nB;
+    NS = nC + nD;
+    const int c1 = A->C.geo[0].t.nch, c2 = A->C.geo[1].t.nch;
+    r = NB % G;
+    q = r ? (c1 + c2 - 1) / c2 : 0;
+    atot = min(NS, (G - r) * q);
+    nb = NB / G + (c < r ? 1 : 0);
+    // phase-A small units of CTA c: i = k*(G-r) + (c-r), k < q, i < atot
+    qa = 0;
+    if (c >= r && q > 0 && c - r < atot) qa = min(q, (atot - (c - r) + (G - r) - 1) / (G - r));
+    // phase-B small units: i = atot + m*G + c < NS
+    qb = NS - atot > c ? (NS - atot - c + G - 1) / G : 0;
+    // combine block e on CTA G-1 - (e mod G)
+    const int cc = G - 1 - c;
+    ne = nrb > cc ? (nrb - cc + G - 1) / G : 0;
   }
-  __device__ int n_units() const { return nu; }
+  __device__ int n_units() const { return nb + qa + qb + ne; }
   __device__ UnitInfo unit(int j) const {
-    int v = u0 + j * gridDim.x;
-    UnitInfo r{};
-    r.wait_ctr = -1;
+    UnitInfo r_{};
+    r_.wait_ctr = -1;
+    if (j < nb) return big(c + j * G);
+    j -= nb;
+    if (j < qa) return small(j * (G - r) + (c - r));
+    j -= qa;
+    if (j < qb) return small(atot + j * G + c);
+    j -= qb;
+    const int e = (G - 1 - c) + j * G;
+    r_.kind = kItemCombine;
+    r_.blk = e;
+    r_.signal = -1;
+    r_.wait_ctr = kCtlRb + e;
+    r_.wait_target = nss + nss_sh;
+    return r_;
+  }
+  __device__ UnitInfo big(int v) const {
+    UnitInfo r_{};
+    r_.wait_ctr = -1;
+    r_.kind = kItemGateUp;
     if (v < nA) {
       const int ss = v / ngr;
-      r.kind = kItemGateUp;
-      r.mat = 2;
-      r.e = 0;
-      r.blk = v - ss * ngr;
-      r.off = kMaxTok * ss;
-      r.cnt = min(kMaxTok, T - kMaxTok * ss);
-      r.nch = A->C.geo[2].t.nch;
-      r.rows = kRowsDirect;
-      r.signal = kSharedReady + ss;
-      return r;
+      r_.mat = 2;
+      r_.e = 0;
+      r_.blk = v - ss * ngr;
+      r_.off = kMaxTok * ss;
+      r_.cnt = min(kMaxTok, T - kMaxTok * ss);
+      r_.nch = A->C.geo[2].t.nch;
+      r_.rows = kRowsDirect;
+      r_.signal = kSharedReady + ss;
+      return r_;
     }
     v -= nA;
-    if (v < nB) {
-      const int ss = v / ngr;
-      r.kind = kItemGateUp;
-      r.mat = 0;
-      r.e = RT->ss_e[ss];
-      r.blk = v - ss * ngr;
-      r.off = RT->ss_off[ss];
-      r.cnt = RT->ss_cnt[ss];
-      r.nch = A->C.geo[0].t.nch;
-      r.rows = kRowsGather;
-      r.signal = kCtlReady + ss;
-      return r;
-    }
-    v -= nB;
+    const int ss = v / ngr;
+    r_.mat = 0;
+    r_.e = RT->ss_e[ss];
+    r_.blk = v - ss * ngr;
+    r_.off = RT->ss_off[ss];
+    r_.cnt = RT->ss_cnt[ss];
+    r_.nch = A->C.geo[0].t.nch;
+    r_.rows = kRowsGather;
+    r_.signal = kCtlReady + ss;
+    return r_;
+  }
+  __device__ UnitInfo small(int v) const {
+    UnitInfo r_{};
+    r_.kind = kItemDown;
+    r_.wait_target = ngr;
     if (v < nC) {
       const int ss = v / nrb;
-      r.kind = kItemDown;
-      r.mat = 3;
-      r.e = 0;
-      r.blk = v - ss * nrb;
-      r.off = kMaxTok * ss;
-      r.cnt = min(kMaxTok, T - kMaxTok * ss);
-      r.nch = A->C.geo[3].t.nch;
-      r.rows = kRowsDirect;
-      r.signal = kCtlRb + r.blk;
-      r.wait_ctr = kSharedReady + ss;
-      r.wait_target = ngr;
-      return r;
+      r_.mat = 3;
+      r_.e = 0;
+      r_.blk = v - ss * nrb;
+      r_.off = kMaxTok * ss;
+      r_.cnt = min(kMaxTok, T - kMaxTok * ss);
+      r_.nch = A->C.geo[3].t.nch;
+      r_.rows = kRowsDirect;
+      r_.signal = kCtlRb + r_.blk;
+      r_.wait_ctr = kSharedReady + ss;
+      return r_;
     }
     v -= nC;
-    if (v < nD) {
-      const int ss = v / nrb;
-      r.kind = kItemDown;
-      r.mat = 1;
-      r.e = RT->ss_e[ss];
-      r.blk = v - ss * nrb;
-      r.off = RT->ss_off[ss];
-      r.cnt = RT->ss_cnt[ss];
-      r.nch = A->C.geo[1].t.nch;
-      r.rows = kRowsScatter;
-      r.signal = kCtlRb + r.blk;
-      r.wait_ctr = kCtlReady + ss;
-      r.wait_target = ngr;
-      return r;
-    }
-    v -= nD;
-    r.kind = kItemCombine;
-    r.blk = v;
-    r.signal = -1;
-    r.wait_ctr = kCtlRb + v;
-    r.wait_target = nss + nss_sh;
-    return r;
+    const int ss = v / nrb;
+    r_.mat = 1;
+    r_.e = RT->ss_e[ss];
+    r_.blk = v - ss * nrb;
+    r_.off = RT->ss_off[ss];
+    r_.cnt = RT->ss_cnt[ss];
+    r_.nch = A->C.geo[1].t.nch;
+    r_.rows = kRowsScatter;
+    r_.signal = kCtlRb + r_.blk;
+    r_.wait_ctr = kCtlReady + ss;
+    return r_;
   }
   __device__ const MatSource& source(int mat) const { return A->src[mat]; }
   __device__ const int* perm() const { return RT->perm; }
@@ -149,7 +176,6 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   __shared__ EngineSmem E;
   __shared__ RouteTable RT;
   __shared__ float RT_part[kConsumerWarps * 32];  // router partials [warp][T]
-  __shared__ __align__(8) uint64_t xbar;
   __shared__ int last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x;
@@ -160,45 +186,34 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   const int E1 = NE + (gate ? 1 : 0);
   engine_init(E, P.S);
   const EngineMem M{smem, smem + P.nob * P.OB, P.OB, P.nob, P.SB, P.S};
-  if (tid == 0) mbar_init(&xbar, 1);
   fence_proxy_async();
   __syncthreads();
 
-  // ---- phase 0: router partial sums and activation sums
-  const int xbytes = T * H * 2;
-  // x rows into shared memory for the router blocks of this CTA
-  const bool xsm = int(blockIdx.x) < (E1 + kConsumerWarps / A.KS - 1) / (kConsumerWarps / A.KS) &&
-                   xbytes <= P.nob * P.OB + P.S * P.SB;
-  if (xsm && tid == 0) {
-    mbar_expect_tx(&xbar, unsigned(xbytes));
-    for (int o = 0; o < xbytes; o += 65536)
-      bulk_g2s(smem + o, reinterpret_cast<const uint8_t*>(A.R.x) + o,
-               unsigned(min(65536, xbytes - o)), &xbar);
-  }
-  const uint16_t* xs = xsm ? reinterpret_cast<const uint16_t*>(smem) : A.R.x;
-  bool xready = !xsm;
-  auto wait_x = [&]() {
-    if (!xready) {
-      mbar_wait_bounded(&xbar, 0, &E.skip, status);
-      xready = true;
-    }
-  };
-  // router blocks (all warps of a CTA, rows finalised in shared memory) first,
-  // activation-sum tasks on the CTAs after them
-  const int RPB = kConsumerWarps / A.KS;
+  // ---- phase 0: router rows and activation sums
+  // Router blocks of RPB rows x KS k-splits (one warp each, rows finalised in
+  // shared memory), as few rows per CTA as the grid allows so that each SM
+  // streams little of the router; x is read through L2 together with the
+  // weights.  Activation-sum tasks go to the CTAs without router rows.
+  const int KS = A.KS;
+  const int RPB = max(1, min(kConsumerWarps / KS, (E1 + G - 1) / G));
   const int nrb_router = (E1 + RPB - 1) / RPB;
   const int nx = T * (H >> 7);
   int done = 0;
   for (int rb = blockIdx.x; rb < nrb_router; rb += G) {
-    router_rows_cta(A.R, A.KS, kConsumerWarps, rb, RT_part, xs, wait_x);
+    router_rows_cta(A.R, KS, RPB * KS, rb, RT_part, A.R.x, NoPre());
     if (tid == 0) red_release_add(ctrl + kCtlPhase0, 1);
   }
-  const int xb = (blockIdx.x + G - nrb_router % G) % G;
-  for (int i = xb + G * warp; i < nx; i += G * (kEngineThreads / 32)) {
-    xsum_task(A.R.x, H, A.R.f16 != 0, A.C.geo[0].t, const_cast<float*>(A.src[0].Bsum), i);
-    ++done;
+  {
+    const int free_ctas = nrb_router < G ? G - nrb_router : G;
+    const int first = nrb_router < G ? nrb_router : 0;
+    const int me = int(blockIdx.x) - first;
+    if (me >= 0) {
+      for (int i = me + free_ctas * warp; i < nx; i += free_ctas * (kEngineThreads / 32)) {
+        xsum_task(A.R.x, H, A.R.f16 != 0, A.C.geo[0].t, const_cast<float*>(A.src[0].Bsum), i);
+        ++done;
+      }
+    }
   }
-  wait_x();  // every thread: the copy has landed before the shared memory is reused
   __syncwarp();
   if (lane == 0 && done) red_release_add(ctrl + kCtlPhase0, done);
   const int n_tasks = nrb_router + nx;

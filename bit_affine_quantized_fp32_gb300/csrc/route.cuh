@@ -71,10 +71,12 @@ __device__ __forceinline__ void router_warp(const RouterJob& J, int KS, int row,
       router_load_w4(J.fmt, J.q, J.s, J.b, row, J.H, k, w[i]);
   }
   pre();
-  for (int tl = 0; tl < tn; tl += 4) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // 8 tokens per pass: every x load of a pass is issued before its sums
+  for (int tl = 0; tl < tn; tl += 8) {
+    float acc[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
+      acc[u] = 0.f;
       if (tl + u < tn) {
         const uint16_t* xr = xs + size_t(tl + u) * J.H;
 #pragma unroll
@@ -88,7 +90,7 @@ __device__ __forceinline__ void router_warp(const RouterJob& J, int KS, int row,
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
       if (lane == 0 && tl + u < tn) out[size_t(tl + u) * ostride] = acc[u];
