@@ -7,7 +7,7 @@
 //   routing  every CTA waits for the counter, then builds the whole routing
 //            table itself in shared memory (logits from the partial sums,
 //            top-k, bucketing, sub-slots): no second grid-wide round trip;
-//   phase 1  gate/up units, then down units, then combine blocks, balanced
+//   phase 1  gate/up units, then down units, then combine pieces, balanced
 //            over the CTAs in closed form (FusedSched), run by the item engine
 //            (engine.cuh): the producer warp streams items through TMA stages,
 //            16 consumer warps compute, a signal warp publishes results.
@@ -44,20 +44,22 @@ namespace {
 //   order, so early indices depend on early gate/up units) first fill the
 //   CTAs that got one big unit fewer, q = ceil(c1/c2) each, spread
 //   round-robin over them, then the rest go round-robin over all CTAs;
-//   combine blocks go to CTAs G-1, G-2, ... (those with the least work).
-// A CTA runs its big units, then its small units, then its combine blocks:
-// big units never wait, small units wait only on big units, combine blocks
+//   combine pieces (kCombineRows output columns each) go to CTAs G-1, G-2,
+//   ... (those with the least work).
+// A CTA runs its big units, then its small units, then its combine pieces:
+// big units never wait, small units wait only on big units, combine pieces
 // only on small units, so every wait is on work that is already queued ahead.
 struct FusedSched {
   const DecodeArgs* A;
   const RouteTable* RT;
-  int T, ngr, nrb, nss_sh, nss, nA, nB, nC, nD;
+  int T, ngr, nrb, ncp, nss_sh, nss, nA, nB, nC, nD;
   int G, c, NB, NS, r, q, atot, nb, qa, qb, ne;
 
   __device__ FusedSched(const DecodeArgs* a, const RouteTable* rt) : A(a), RT(rt) {
     T = A->R.T;
     ngr = A->C.inter / 64;
     nrb = A->C.hidden / kUnitRows;
+    ncp = A->C.hidden / kCombineRows;
     nss_sh = A->has_shared ? (T + kMaxTok - 1) / kMaxTok : 0;
     nss = RT->nss;
     nA = nss_sh * ngr;
@@ -78,9 +80,9 @@ struct FusedSched {
     if (c >= r && q > 0 && c - r < atot) qa = min(q, (atot - (c - r) + (G - r) - 1) / (G - r));
     // phase-B small units: i = atot + m*G + c < NS
     qb = NS - atot > c ? (NS - atot - c + G - 1) / G : 0;
-    // combine block e on CTA G-1 - (e mod G)
+    // combine piece e on CTA G-1 - (e mod G)
     const int cc = G - 1 - c;
-    ne = nrb > cc ? (nrb - cc + G - 1) / G : 0;
+    ne = ncp > cc ? (ncp - cc + G - 1) / G : 0;
   }
   __device__ int n_units() const { return nb + qa + qb + ne; }
   __device__ UnitInfo unit(int j) const {
@@ -96,7 +98,7 @@ struct FusedSched {
     r_.kind = kItemCombine;
     r_.blk = e;
     r_.signal = -1;
-    r_.wait_ctr = kCtlRb + e;
+    r_.wait_ctr = kCtlRb + e * kCombineRows / kUnitRows;
     r_.wait_target = nss + nss_sh;
     return r_;
   }
@@ -165,7 +167,7 @@ struct FusedSched {
     combine_rows(A->C.tg[1].y, A->C.tg[1].yhalf, RT->w, A->has_shared ? A->C.tg[3].y : nullptr,
                  A->has_shared ? A->C.tg[3].y + A->C.tg[3].yhalf : nullptr,
                  A->has_shared && A->R.gq ? RT->sg : nullptr, A->out, T, A->k, A->C.hidden,
-                 A->R.f16 != 0, blk, threadIdx.x, kConsumers);
+                 A->R.f16 != 0, blk * kCombineRows, kCombineRows, threadIdx.x, kConsumers);
   }
 };
 

@@ -342,45 +342,6 @@ __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* w
   }
 }
 
-// Group-count dispatch (CK = 512, 256 or 128).
-template <int FMT, bool F16A, bool SPLIT>
-__device__ __forceinline__ void compute_item_any(const TileGeo& tg, const uint8_t* wst,
-                                                 const uint8_t* op, const OpLayout& L, int c,
-                                                 int tile, int kh, uint32_t mg,
-                                                 float (&acc)[4]) {
-  if (tg.ng == 8)
-    compute_item<FMT, F16A, SPLIT, 8>(tg, wst, op, L, c, tile, kh, mg, acc);
-  else if (tg.ng == 4)
-    compute_item<FMT, F16A, SPLIT, 4>(tg, wst, op, L, c, tile, kh, mg, acc);
-  else
-    compute_item<FMT, F16A, SPLIT, 2>(tg, wst, op, L, c, tile, kh, mg, acc);
-}
-
-// One item of matrix slot `mat` (0/2 gate/up, 1/3 down); slots 0/1 hold
-// format FMT, slots 2/3 format FMT_SH.  With FMT_SH == FMT both share one
-// copy of the code.
-template <int FMT, int FMT_SH, bool F16A>
-__device__ __forceinline__ void compute_mat(const EngineCfg& C, int mat, const uint8_t* wst,
-                                            const uint8_t* op, int c, int tile, int kh,
-                                            float (&acc)[4]) {
-  const TileGeo& tg = C.geo[mat].t;
-  const OpLayout L = op_layout(tg);
-  const bool down = mat & 1;
-  // the down operand (h) is bf16 whatever the activation type
-  const uint32_t mg = (F16A && !down) ? C.magic_f16 : C.magic_bf16;
-  if (FMT_SH == FMT || mat < 2) {
-    if (down)
-      compute_item_any<FMT, false, true>(tg, wst, op, L, c, tile, kh, mg, acc);
-    else
-      compute_item_any<FMT, F16A, false>(tg, wst, op, L, c, tile, kh, mg, acc);
-  } else {
-    if (down)
-      compute_item_any<FMT_SH, false, true>(tg, wst, op, L, c, tile, kh, mg, acc);
-    else
-      compute_item_any<FMT_SH, F16A, false>(tg, wst, op, L, c, tile, kh, mg, acc);
-  }
-}
-
 }  // namespace moe
 
 namespace moe {
@@ -475,6 +436,68 @@ struct Ring {
     }
   }
 };
+
+// ---------------------------------------------------------------------------
+// A unit's MMA pass: wait for the operand buffer, then for every k-chunk wait
+// for its stage, run compute_item and release the stage.  The format, group
+// count and operand split are resolved once per unit (unit_mat), so the chunk
+// loop carries no per-item dispatch or layout arithmetic.
+template <int FMT, bool F16A, bool SPLIT, int NG>
+__device__ __forceinline__ void unit_items(const TileGeo& tg, uint32_t mg, EngineSmem& E,
+                                           const EngineMem& M, Ring& R, const uint8_t* op,
+                                           uint64_t* op_full, unsigned op_parity, int tile,
+                                           int kh, int* status, float (&acc)[4]) {
+  const OpLayout L = op_layout(tg);
+  const int nch = tg.nch;
+  mbar_wait_bounded(op_full, op_parity, &E.skip, status);
+  for (int c = 0; c < nch; ++c) {
+    mbar_wait_bounded(&E.full[R.slot], R.use & 1, &E.skip, status);
+    compute_item<FMT, F16A, SPLIT, NG>(tg, M.stages + (size_t)R.slot * M.SB, op, L, c, tile, kh,
+                                       mg, acc);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&E.empty[R.slot]);
+    R.next();
+  }
+}
+
+template <int FMT, bool F16A, bool SPLIT>
+__device__ __forceinline__ void unit_ng(const TileGeo& tg, uint32_t mg, EngineSmem& E,
+                                        const EngineMem& M, Ring& R, const uint8_t* op,
+                                        uint64_t* op_full, unsigned op_parity, int tile, int kh,
+                                        int* status, float (&acc)[4]) {
+  if (tg.ng == 8)
+    unit_items<FMT, F16A, SPLIT, 8>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, status, acc);
+  else if (tg.ng == 4)
+    unit_items<FMT, F16A, SPLIT, 4>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, status, acc);
+  else
+    unit_items<FMT, F16A, SPLIT, 2>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, status, acc);
+}
+
+// Matrix slot `mat` (0/2 gate/up, 1/3 down); slots 0/1 hold format FMT,
+// slots 2/3 format FMT_SH (with FMT_SH == FMT both share one copy of the
+// code).  The down operand (h) is split bf16 whatever the activation type.
+template <int FMT, int FMT_SH, bool F16A>
+__device__ __forceinline__ void unit_mat(const EngineCfg& C, int mat, EngineSmem& E,
+                                         const EngineMem& M, Ring& R, const uint8_t* op,
+                                         uint64_t* op_full, unsigned op_parity, int tile, int kh,
+                                         float (&acc)[4]) {
+  const TileGeo& tg = C.geo[mat].t;
+  const bool down = mat & 1;
+  const uint32_t mg = (F16A && !down) ? C.magic_f16 : C.magic_bf16;
+  if (FMT_SH == FMT || mat < 2) {
+    if (down)
+      unit_ng<FMT, false, true>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, C.status, acc);
+    else
+      unit_ng<FMT, F16A, false>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, C.status, acc);
+  } else {
+    if (down)
+      unit_ng<FMT_SH, false, true>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, C.status,
+                                   acc);
+    else
+      unit_ng<FMT_SH, F16A, false>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, C.status,
+                                   acc);
+  }
+}
 
 // ---------------------------------------------------------------------------
 // Producer (warp kProducerWarp, all 32 lanes).
@@ -716,16 +739,9 @@ __device__ void consumer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
     }
     const int my_orow = lane < u.cnt ? unit_out_row(u, sch.perm(), lane) : 0;
     const uint8_t* op = M.ops + (size_t)B.slot * M.OB;
-    mbar_wait_bounded(&E.op_full[B.slot], B.use & 1, &E.skip, C.status);
     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-    for (int c = 0; c < u.nch; ++c) {
-      mbar_wait_bounded(&E.full[R.slot], R.use & 1, &E.skip, C.status);
-      compute_mat<FMT, FMT_SH, F16A>(C, u.mat, M.stages + (size_t)R.slot * M.SB, op, c, tile, kh,
-                                     acc);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&E.empty[R.slot]);
-      R.next();
-    }
+    unit_mat<FMT, FMT_SH, F16A>(C, u.mat, E, M, R, op, &E.op_full[B.slot], B.use & 1, tile, kh,
+                                acc);
     if (lane == 0) mbar_arrive(&E.op_empty[B.slot]);
     B.next();
     if (u.kind == kItemDown)
@@ -737,28 +753,40 @@ __device__ void consumer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
 }
 
 // ---------------------------------------------------------------------------
-// Weighted combine of one 128-row block of the output, for all T tokens:
+// Weighted combine of output columns [h0, h0 + nh), for all T tokens:
 //   out[t, h] = round( sum_j w[t, j] * y[t*k + j, h]  +  s_t * ysh[t, h] )
 // an fp32 fma chain in slot order with the shared slot last; y (and ysh when
 // ysh2 is given) come as two k-half planes, added plane 0 + plane 1 first.
-// y and ysh are read through L2 (written by other CTAs).  `nthr` threads.
+// y and ysh are read through L2 (written by other CTAs); every load of one
+// output is issued before the chain starts (k <= kMaxTopK).  `nthr` threads.
+constexpr int kMaxTopK = 8;
+constexpr int kCombineRows = 64;  // columns of one combine piece
 __device__ __forceinline__ void combine_rows(const float* y, size_t yhalf, const float* w,
                                              const float* ysh, const float* ysh2,
                                              const float* sg, uint16_t* out, int T, int k, int H,
-                                             bool f16, int blk, int tid, int nthr) {
-  for (int v = tid; v < T * kUnitRows; v += nthr) {
-    const int t = v >> 7;
-    const int h = blk * kUnitRows + (v & 127);
-    float acc = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const size_t a = (size_t)(t * k + j) * H + h;
-      acc = fmaf(w[t * k + j], __ldcg(y + a) + __ldcg(y + yhalf + a), acc);
+                                             bool f16, int h0, int nh, int tid, int nthr) {
+  for (int v = tid; v < T * nh; v += nthr) {
+    const int t = v / nh;
+    const int h = h0 + (v - t * nh);
+    float ya[kMaxTopK], yb[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        const size_t a = (size_t)(t * k + j) * H + h;
+        ya[j] = __ldcg(y + a);
+        yb[j] = __ldcg(y + yhalf + a);
+      }
     }
+    float vs = 0.f;
     if (ysh) {
       const size_t a = (size_t)t * H + h;
-      const float vs = ysh2 ? __ldcg(ysh + a) + __ldcg(ysh2 + a) : __ldcg(ysh + a);
-      acc = fmaf(sg ? sg[t] : 1.f, vs, acc);
+      vs = ysh2 ? __ldcg(ysh + a) + __ldcg(ysh2 + a) : __ldcg(ysh + a);
     }
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) acc = fmaf(w[t * k + j], ya[j] + yb[j], acc);
+    if (ysh) acc = fmaf(sg ? sg[t] : 1.f, vs, acc);
     out[(size_t)t * H + h] = float_to_act_bits(acc, f16);
   }
 }

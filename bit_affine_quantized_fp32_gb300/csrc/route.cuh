@@ -71,22 +71,27 @@ __device__ __forceinline__ void router_warp(const RouterJob& J, int KS, int row,
       router_load_w4(J.fmt, J.q, J.s, J.b, row, J.H, k, w[i]);
   }
   pre();
-  // 8 tokens per pass: every x load of a pass is issued before its sums
+  // 8 tokens per pass: every x load of a pass is issued before its sums (a
+  // token past the end re-reads the last row; its sum is not written)
   for (int tl = 0; tl < tn; tl += 8) {
+    uint2 xv[8][NI];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint16_t* xr = xs + size_t(min(tl + u, tn - 1)) * J.H + kq + 4 * lane;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) xv[u][i] = *reinterpret_cast<const uint2*>(xr + 128 * i);
+    }
     float acc[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       acc[u] = 0.f;
-      if (tl + u < tn) {
-        const uint16_t* xr = xs + size_t(tl + u) * J.H;
 #pragma unroll
-        for (int i = 0; i < NI; ++i) {
-          const uint2 v = *reinterpret_cast<const uint2*>(xr + kq + 128 * i + 4 * lane);
-          acc[u] = fmaf(w[i][0], act_to_float(uint16_t(v.x & 0xFFFF), J.f16), acc[u]);
-          acc[u] = fmaf(w[i][1], act_to_float(uint16_t(v.x >> 16), J.f16), acc[u]);
-          acc[u] = fmaf(w[i][2], act_to_float(uint16_t(v.y & 0xFFFF), J.f16), acc[u]);
-          acc[u] = fmaf(w[i][3], act_to_float(uint16_t(v.y >> 16), J.f16), acc[u]);
-        }
+      for (int i = 0; i < NI; ++i) {
+        const uint2 v = xv[u][i];
+        acc[u] = fmaf(w[i][0], act_to_float(uint16_t(v.x & 0xFFFF), J.f16), acc[u]);
+        acc[u] = fmaf(w[i][1], act_to_float(uint16_t(v.x >> 16), J.f16), acc[u]);
+        acc[u] = fmaf(w[i][2], act_to_float(uint16_t(v.y & 0xFFFF), J.f16), acc[u]);
+        acc[u] = fmaf(w[i][3], act_to_float(uint16_t(v.y >> 16), J.f16), acc[u]);
       }
     }
 #pragma unroll
@@ -164,6 +169,12 @@ __device__ __forceinline__ void router_rows_cta(const RouterJob& J, int KS, int 
   const int rl = wid / KS, q = wid - rl * KS;
   const int row = rb * RPB + rl;
   const int nrows = J.E + (J.gq ? 1 : 0);
+  // the bias of this thread's first finalisation, fetched before the sums
+  float bias0 = 0.f;
+  if (J.bias && int(threadIdx.x) < RPB * J.T) {
+    const int row2 = rb * RPB + int(threadIdx.x) / J.T;
+    if (row2 < J.E) bias0 = J.bias[row2];
+  }
   if (wid < RPB * KS && row < nrows) router_warp_any(J, KS, row, q, xs, J.T, part + wid * J.T, 1, pre);
   __syncthreads();
   for (int i = threadIdx.x; i < RPB * J.T; i += blockDim.x) {
@@ -172,8 +183,8 @@ __device__ __forceinline__ void router_rows_cta(const RouterJob& J, int KS, int 
     if (row2 >= nrows) continue;
     const float* p = part + (r2 * KS) * J.T + tl;
     if (row2 < J.E)
-      J.logits[size_t(tl) * J.E + row2] =
-          router_finalize(p, J.T, KS, J.bias ? J.bias + row2 : nullptr);
+      J.logits[size_t(tl) * J.E + row2] = router_finalize(
+          p, J.T, KS, J.bias ? (i == int(threadIdx.x) ? &bias0 : J.bias + row2) : nullptr);
     else
       J.gate_logit[tl] = router_finalize(p, J.T, KS, nullptr);
   }

@@ -86,7 +86,7 @@ __global__ void k_xsum(const uint16_t* __restrict__ x, int T, int H, int f16, Ti
 
 __global__ void __launch_bounds__(256) k_combine(const CombineArgs A) {
   combine_rows(A.y, A.yhalf, A.w, A.ysh, A.ysh2, A.sg, A.out, A.T, A.k, A.H, A.f16 != 0,
-               blockIdx.x, threadIdx.x, blockDim.x);
+               blockIdx.x * kCombineRows, kCombineRows, threadIdx.x, blockDim.x);
 }
 
 // dst = a + b elementwise (the two k-half planes of a down projection)
@@ -175,7 +175,7 @@ cudaError_t launch_add_planes(const float* a, const float* b, float* dst, long n
 
 cudaError_t launch_combine(const CombineArgs& A, cudaStream_t st) {
   if (A.T <= 0) return cudaSuccess;
-  k_combine<<<A.H / kUnitRows, 256, 0, st>>>(A);
+  k_combine<<<A.H / kCombineRows, 256, 0, st>>>(A);
   return cudaGetLastError();
 }
 
