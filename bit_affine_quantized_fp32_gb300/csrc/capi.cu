@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "decode.h"
+#include "prefill.h"
 
 namespace moe {
 int router_ks(int H);
@@ -249,9 +250,49 @@ moe_status run_bank(const moe_expert_bank* bank, const SubSlots& ss, int max_ss,
 // the given workspace layout: activation sums -> gate/up units (SwiGLU) ->
 // down units into the two planes of the workspace's shared-expert output
 // (L.ysh); y_out (nullable) receives their sum.
+// The prefill form (tcgen05 expert GEMMs) serves T > MOE_DECODE_MAX_TOKENS
+// unless the caller forces the decode form or the shape does not fit it.
+bool use_prefill(const moe_expert_bank* b, int T, int flags) {
+  return T > MOE_DECODE_MAX_TOKENS && !(flags & MOE_FLAG_FORCE_DECODE) &&
+         prefill_smem(geo13(b).t, 0) > 0 && prefill_smem(geo2(b).t, 1) > 0;
+}
+
+// One expert of a bank over T tokens in the prefill form: h (bf16) into the
+// workspace, y (fp32) straight into y_out.
+moe_status run_expert_prefill(const moe_expert_bank* bank, int expert, const void* x, bool f16,
+                              int T, float* y_out, void* ws, const WsLayout& L,
+                              cudaStream_t stream) {
+  const int H = bank->hidden, I = bank->inter;
+  const MatGeo g13 = geo13(bank), g2 = geo2(bank);
+  PrefillJob J{};
+  J.g = g13.t;
+  J.base = g13.base;
+  J.fixed_e = expert;
+  J.fixed_T = T;
+  J.B = static_cast<const uint16_t*>(x);
+  J.ldB = H;
+  J.h = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh));
+  J.hl = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl));
+  J.ldh = h_pitch(I);
+  J.status = static_cast<int*>(ws);
+  MOE_CUDA(launch_prefill(J, 0, f16, sm_count(), stream), "prefill gate/up kernel");
+  PrefillJob D = J;
+  D.g = g2.t;
+  D.base = g2.base;
+  D.B = J.h;
+  D.Blo = J.hl;
+  D.ldB = h_pitch(I);
+  D.y = y_out;
+  D.ldy = H;
+  MOE_CUDA(launch_prefill(D, 1, false, sm_count(), stream), "prefill down kernel");
+  return MOE_OK;
+}
+
 moe_status run_expert_mlp(const moe_expert_bank* bank, int expert, const void* x, bool f16,
                           int T, float* h_out, float* y_out, void* ws, const WsLayout& L,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, int flags = 0) {
+  if (!h_out && y_out && use_prefill(bank, T, flags))
+    return run_expert_prefill(bank, expert, x, f16, T, y_out, ws, L, stream);
   const int H = bank->hidden;
   float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
   MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, f16, geo13(bank).t, xsum, stream),
@@ -444,6 +485,57 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
   const WsLayout L = ws_layout(T, E, top_k, H, I);
   if ((s = check_ws(ws, ws_bytes, L.total))) return s;
   const bool f16 = act == MOE_FMT_F16;
+  if (use_prefill(experts, T, flags)) {
+    // tiles of up to kPfTile bucket positions per expert, then the two GEMMs
+    int* nt = reinterpret_cast<int*>(wsp(ws, L.nss));
+    int* te = reinterpret_cast<int*>(wsp(ws, L.ss_e));
+    int* to = reinterpret_cast<int*>(wsp(ws, L.ss_off));
+    int* tc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
+    MOE_CUDA(launch_subslots(bucket_offsets, E, nt, te, to, tc, stream, kPfTile), "tile kernel");
+    const MatGeo g13 = geo13(experts), g2 = geo2(experts);
+    PrefillJob J{};
+    J.g = g13.t;
+    J.base = g13.base;
+    J.n_tiles = nt;
+    J.te = te;
+    J.toff = to;
+    J.tcnt = tc;
+    J.B = static_cast<const uint16_t*>(x);
+    J.ldB = H;
+    J.gather = 1;
+    J.perm = bucket_perm;
+    J.k = top_k;
+    J.h = reinterpret_cast<uint16_t*>(wsp(ws, L.hh));
+    J.hl = reinterpret_cast<uint16_t*>(wsp(ws, L.hl));
+    J.ldh = h_pitch(I);
+    J.status = static_cast<int*>(ws);
+    MOE_CUDA(launch_prefill(J, 0, f16, sm_count(), stream), "prefill gate/up kernel");
+    PrefillJob D = J;
+    D.g = g2.t;
+    D.base = g2.base;
+    D.B = J.h;
+    D.Blo = J.hl;
+    D.ldB = h_pitch(I);
+    D.gather = 0;
+    D.y = reinterpret_cast<float*>(wsp(ws, L.y));
+    D.ldy = H;
+    D.scatter = 1;
+    MOE_CUDA(launch_prefill(D, 1, false, sm_count(), stream), "prefill down kernel");
+    CombineArgs C{};
+    C.y = D.y;
+    C.yhalf = 0;  // one plane
+    C.w = topk_w;
+    C.ysh = y_shared;
+    C.ysh2 = nullptr;
+    C.sg = shared_gate_w;
+    C.out = static_cast<uint16_t*>(out);
+    C.T = T;
+    C.k = top_k;
+    C.H = H;
+    C.f16 = f16;
+    MOE_CUDA(launch_combine(C, stream), "combine kernel");
+    return ok();
+  }
   float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
   MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, f16, geo13(experts).t, xsum,
                        stream),
@@ -582,7 +674,7 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
   float* ysh = nullptr;
   if (shared) {
     ysh = reinterpret_cast<float*>(wsp(ws, L.ysh));
-    s = run_expert_mlp(shared, 0, x, act == MOE_FMT_F16, T, nullptr, ysh, ws, L, stream);
+    s = run_expert_mlp(shared, 0, x, act == MOE_FMT_F16, T, nullptr, ysh, ws, L, stream, flags);
     if (s) return s;
   }
   return moe_experts_forward(experts, x, act, T, top_k, idx, w, offs, perm, ysh,

@@ -755,8 +755,9 @@ __device__ void consumer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
 // ---------------------------------------------------------------------------
 // Weighted combine of output columns [h0, h0 + nh), for all T tokens:
 //   out[t, h] = round( sum_j w[t, j] * y[t*k + j, h]  +  s_t * ysh[t, h] )
-// an fp32 fma chain in slot order with the shared slot last; y (and ysh when
-// ysh2 is given) come as two k-half planes, added plane 0 + plane 1 first.
+// an fp32 fma chain in slot order with the shared slot last; y comes as two
+// k-half planes added plane 0 + plane 1 first (one plane when yhalf == 0),
+// ysh likewise when ysh2 is given.
 // y and ysh are read through L2 (written by other CTAs); every load of one
 // output is issued before the chain starts (k <= kMaxTopK).  `nthr` threads.
 constexpr int kMaxTopK = 8;
@@ -774,7 +775,7 @@ __device__ __forceinline__ void combine_rows(const float* y, size_t yhalf, const
       if (j < k) {
         const size_t a = (size_t)(t * k + j) * H + h;
         ya[j] = __ldcg(y + a);
-        yb[j] = __ldcg(y + yhalf + a);
+        if (yhalf) yb[j] = __ldcg(y + yhalf + a);
       }
     }
     float vs = 0.f;
@@ -785,7 +786,7 @@ __device__ __forceinline__ void combine_rows(const float* y, size_t yhalf, const
     float acc = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
-      if (j < k) acc = fmaf(w[t * k + j], ya[j] + yb[j], acc);
+      if (j < k) acc = fmaf(w[t * k + j], yhalf ? ya[j] + yb[j] : ya[j], acc);
     if (ysh) acc = fmaf(sg ? sg[t] : 1.f, vs, acc);
     out[(size_t)t * H + h] = float_to_act_bits(acc, f16);
   }

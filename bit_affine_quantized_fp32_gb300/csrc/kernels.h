@@ -85,7 +85,7 @@ cudaError_t launch_topk(const float* logits, const float* gate_logit, int T, int
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets,
                           int32_t* perm, cudaStream_t st);
 cudaError_t launch_subslots(const int32_t* offsets, int E, int* nss, int* se, int* so, int* sc,
-                            cudaStream_t st);
+                            cudaStream_t st, int run = kMaxTok);
 
 // formats
 cudaError_t launch_pack(int fmt, const uint8_t* codes, int rows, int cols, uint32_t* packed,

@@ -1,0 +1,421 @@
+// prefill.cu -- the expert GEMMs of a prefill window on tcgen05.
+//
+// For T > 32 tokens an expert sees up to hundreds of rows, so its weights are
+// dequantised once per tile of kPfTile rows and fed to the tensor cores:
+// D[128 weight rows x N tokens] += A[128 x 64] * B[N x 64]^T per 64-column
+// group, 16-bit operands in shared memory, fp32 accumulators in tensor memory.
+// One persistent CTA per SM, 15 warps:
+//   warps 0-3   epilogue: tensor memory -> registers (thread = weight row),
+//               SwiGLU -> bf16 h (mode 0) or fp32 y rows (mode 1);
+//   warps 4-11  dequantisation: one weight item (128 rows x CK columns, the
+//               kernel-tiled layout) per raw stage, one 64-column group at a
+//               time into an A stage, w = fma(s, q, b) in fp32 split into a
+//               bf16 hi part and a bf16 lo part w - hi (fp16 for fp16
+//               activations);
+//   warp 12     TMA bulk copies of the raw weight items (2 stages);
+//   warp 13     the operand rows of each group into a B stage (cp.async, 16 B
+//               pieces placed in the tensor core's K-major layout; h as hi
+//               and lo rows);
+//   warp 14     allocates tensor memory and issues the MMAs (one thread);
+//               tcgen05.commit frees A/B stages and hands accumulators over.
+// Per 16 columns the MMAs add A_hi B + A_lo B (gate/up; x is exact) or
+// A_hi B_hi + A_hi B_lo + A_lo B_hi (down), so the operands carry ~16
+// significant bits.  Two accumulators of kPfTile columns let the epilogue of
+// one unit overlap the MMAs of the next.  Every wait is bounded (one second,
+// then the status word gets MOE_ERR_TIMEOUT and the remaining waits return at
+// once).
+//
+// Sources: "qwen3_5_moe on native CUDA with 3-bit routed experts ... #803"
+// (prefill windows through grouped expert GEMMs, SwiGLU epilogue).
+
+#include "prefill.h"
+#include "engine.cuh"
+#include "umma.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kPfRaw = 2;                    // raw weight-item stages
+constexpr int kPfA = 128 * 64 * 2;           // 128 rows x 64 columns, 16-bit
+constexpr int kPfB = kPfTile * 64 * 2;
+constexpr int kPfKBlk = 64;                  // columns per MMA group (4 x K16)
+constexpr int kPfStagesMax = 3;
+// A/B stages per mode: [A hi][A lo][B] (gate/up, 3 stages) or
+// [A hi][A lo][B hi][B lo] (down, 2 stages)
+__host__ __device__ constexpr int pf_stages(int mode) { return mode == 0 ? 3 : 2; }
+__host__ __device__ constexpr int pf_stage_bytes(int mode) {
+  return mode == 0 ? 2 * kPfA + kPfB : 2 * kPfA + 2 * kPfB;
+}
+
+__host__ __device__ inline int raw_stage_bytes(const TileGeo& g) {
+  return (g.item_bytes + 1023) & ~1023;
+}
+
+struct PfSmem {
+  uint64_t raw_full[kPfRaw], raw_empty[kPfRaw];
+  uint64_t a_full[kPfStagesMax], b_full[kPfStagesMax], ab_empty[kPfStagesMax];
+  uint64_t acc_full[2], acc_empty[2];
+  uint32_t tmem;
+  int skip;
+  float xch[64][9];  // up rows handed to the gate rows in the SwiGLU epilogue
+};
+
+struct PfUnit {
+  int e, off, cnt, m;
+};
+
+__device__ __forceinline__ int pf_tiles(const PrefillJob& J) {
+  return J.n_tiles ? __ldcg(J.n_tiles) : (J.fixed_T + kPfTile - 1) / kPfTile;
+}
+
+__device__ __forceinline__ PfUnit pf_unit(const PrefillJob& J, int u) {
+  const int nblk = J.g.nblk;
+  const int t = u / nblk;
+  PfUnit r;
+  r.m = u - t * nblk;
+  if (J.n_tiles) {
+    r.e = __ldcg(J.te + t);
+    r.off = __ldcg(J.toff + t);
+    r.cnt = __ldcg(J.tcnt + t);
+  } else {
+    r.e = J.fixed_e;
+    r.off = kPfTile * t;
+    r.cnt = min(kPfTile, J.fixed_T - kPfTile * t);
+  }
+  return r;
+}
+
+// Two fp32 values -> a packed pair of 16-bit hi parts and of lo parts
+// (v - hi), bf16 or fp16.
+__device__ __forceinline__ void split2(float a, float b, bool f16, uint32_t& hi, uint32_t& lo) {
+  if (f16) {
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+  }
+}
+
+// One 8-code word (codes in nibble order [0 2 4 6 1 3 5 7]) -> 8 dequantised
+// values in column order, w = fma(s, 128 + q, b - 128 s) in fp32, as hi and
+// lo 16-bit parts.
+__device__ __forceinline__ void dequant_word(uint32_t w, float s, float b128, bool f16, uint4& hi,
+                                             uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t p;
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;\n" : "=r"(p) : "r"(w >> (4 * j)));
+    const float c0 = __uint_as_float(p << 16), c1 = __uint_as_float(p & 0xFFFF0000u);
+    split2(fmaf(s, c0, b128), fmaf(s, c1, b128), f16, h[j], l[j]);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Group G of the raw item into an A stage: thread (tile w, lane l) converts
+// its four words -- rows 16w + g and 16w + g + 8, columns 16t .. 16t + 15 of
+// the group -- into the K-major layout (one 16-byte piece per word).
+template <int FMT>
+__device__ __forceinline__ void dequant_group(const TileGeo& g, const uint8_t* raw, int G,
+                                              uint8_t* A, uint8_t* Alo, int w, int l, bool f16) {
+  const int NG = g.ng;
+  const int gq = l >> 2, t = l & 3;
+  uint32_t W0, W1, W2, W3;
+  if constexpr (FMT == MOE_FMT_AFFINE3_G64) {
+    const uint32_t* pl = reinterpret_cast<const uint32_t*>(raw + (w * NG + G) * 384) + l;
+    planes_to_words(pl[0], pl[32], pl[64], W0, W1, W2, W3);
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4*>(raw + (w * NG + G) * 512 + l * 16);
+    W0 = v.x;
+    W1 = v.y;
+    W2 = v.z;
+    W3 = v.w;
+  }
+  const uint8_t* sc = raw + g.code_bytes;
+  float s0, s1, b0, b1;
+  if constexpr (FMT == MOE_FMT_W4A16_SYM_G128) {
+    const uint32_t sv =
+        *reinterpret_cast<const uint32_t*>(sc + ((w * 8 + gq) * (NG / 2) + (G >> 1)) * 4);
+    const float2 sf = half2_bits_to_float2(sv);
+    s0 = sf.x;
+    s1 = sf.y;
+    b0 = -136.f * s0;  // w = s (u - 8) with the stored nibble u; operand is 128 + u
+    b1 = -136.f * s1;
+  } else {
+    const uint2 sv = *reinterpret_cast<const uint2*>(sc + ((w * 8 + gq) * NG + G) * 8);
+    const float2 p0 = half2_bits_to_float2(sv.x), p1 = half2_bits_to_float2(sv.y);
+    s0 = p0.x;
+    s1 = p1.x;
+    b0 = fmaf(-128.f, s0, p0.y);
+    b1 = fmaf(-128.f, s1, p1.y);
+  }
+  const int r0 = 16 * w + gq, r1 = r0 + 8;
+  const uint32_t WW[4] = {W0, W1, W2, W3};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i < 2 ? r0 : r1;
+    uint4 hi, lo;
+    dequant_word(WW[i], i < 2 ? s0 : s1, i < 2 ? b0 : b1, f16, hi, lo);
+    const int o = umma_off(r, 16 * t + 8 * (i & 1), kPfKBlk);
+    *reinterpret_cast<uint4*>(A + o) = hi;
+    *reinterpret_cast<uint4*>(Alo + o) = lo;
+  }
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+
+template <int FMT, int MODE, bool F16>
+__global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant__ PrefillJob J) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ PfSmem S;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const TileGeo& g = J.g;
+  constexpr int NS = pf_stages(MODE), SB = pf_stage_bytes(MODE);
+  const int RB = raw_stage_bytes(g);
+  uint8_t* raw = smem;
+  uint8_t* stages = smem + kPfRaw * RB;  // stage s: [A hi][A lo][B (hi)][B lo]
+  if (tid == 0) {
+    for (int i = 0; i < kPfRaw; ++i) {
+      mbar_init(&S.raw_full[i], 1);
+      mbar_init(&S.raw_empty[i], 8);
+    }
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&S.a_full[i], 8);
+      mbar_init(&S.b_full[i], 32);
+      mbar_init(&S.ab_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.acc_full[i], 1);
+      mbar_init(&S.acc_empty[i], 4);
+    }
+    S.skip = 0;
+  }
+  if (warp == 14) tmem_alloc(&S.tmem, 2 * kPfTile);
+  fence_proxy_async();
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tbase = S.tmem;
+  const int nunits = pf_tiles(J) * g.nblk;
+  const int G = gridDim.x;
+  const int NG = g.ng, nch = g.nch, nks = nch * NG;
+  int* status = J.status;
+
+  if (warp == 12) {
+    // ---- raw weight items
+    int ri = 0;
+    for (int u = blockIdx.x; u < nunits; u += G) {
+      const PfUnit U = pf_unit(J, u);
+      for (int c = 0; c < nch; ++c, ++ri) {
+        const int rs = ri % kPfRaw;
+        if (lane == 0) {
+          if (ri >= kPfRaw)
+            mbar_wait_bounded(&S.raw_empty[rs], ((ri / kPfRaw) - 1) & 1, &S.skip, status);
+          mbar_expect_tx(&S.raw_full[rs], unsigned(g.item_bytes));
+          bulk_g2s(raw + rs * RB,
+                   J.base + (size_t)U.e * g.expert_bytes +
+                       (size_t)(U.m * nch + c) * g.item_bytes,
+                   unsigned(g.item_bytes), &S.raw_full[rs]);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0)  // the last copies have landed before the CTA may exit
+      for (int i = max(0, ri - kPfRaw); i < ri; ++i)
+        mbar_wait_bounded(&S.raw_full[i % kPfRaw], (i / kPfRaw) & 1, &S.skip, status);
+  } else if (warp == 13) {
+    // ---- operand rows, one 64-column group per stage
+    int ks = 0;
+    for (int u = blockIdx.x; u < nunits; u += G) {
+      const PfUnit U = pf_unit(J, u);
+      for (int q = 0; q < nks; ++q, ++ks) {
+        const int s = ks % NS;
+        if (ks >= NS) mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.skip, status);
+        const int k0 = q * kPfKBlk;
+        uint8_t* B = stages + s * SB + 2 * kPfA;
+        for (int i = lane; i < U.cnt * 8; i += 32) {
+          const int n = i >> 3, ch = i & 7;
+          const int row = (MODE == 0 && J.gather) ? __ldg(J.perm + U.off + n) / J.k : U.off + n;
+          const size_t src = (size_t)row * J.ldB + k0 + ch * 8;
+          cp_async16(B + umma_off(n, ch * 8, kPfKBlk), J.B + src);
+          if (MODE == 1) cp_async16(B + kPfB + umma_off(n, ch * 8, kPfKBlk), J.Blo + src);
+        }
+        cp_async_arrive_noinc(&S.b_full[s]);
+      }
+    }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+  } else if (warp == 14) {
+    // ---- MMA issue (one thread)
+    if (lane == 0) {
+      int ks = 0, ui = 0;
+      for (int u = blockIdx.x; u < nunits; u += G, ++ui) {
+        const PfUnit U = pf_unit(J, u);
+        const int a = ui & 1;
+        if (ui >= 2) mbar_wait_bounded(&S.acc_empty[a], ((ui >> 1) - 1) & 1, &S.skip, status);
+        tmem_fence_after();
+        const int N = max(16, (U.cnt + 15) & ~15);
+        const uint32_t idesc = (MODE == 0 && F16)
+                                   ? (umma_idesc_bf16(128, N) & ~((7u << 7) | (7u << 10)))
+                                   : umma_idesc_bf16(128, N);
+        const uint32_t d = tbase + uint32_t(a * kPfTile);
+        constexpr uint32_t kSbo = (kPfKBlk / 8) * 128;
+        for (int q = 0; q < nks; ++q, ++ks) {
+          const int s = ks % NS;
+          mbar_wait_bounded(&S.a_full[s], (ks / NS) & 1, &S.skip, status);
+          mbar_wait_bounded(&S.b_full[s], (ks / NS) & 1, &S.skip, status);
+          fence_proxy_async();
+          tmem_fence_after();
+          const uint32_t ah = smem_u32(stages + s * SB), al = ah + kPfA;
+          const uint32_t bh = ah + 2 * kPfA, bl = bh + kPfB;
+#pragma unroll
+          for (int kk = 0; kk < kPfKBlk / 16; ++kk) {
+            const uint32_t o = kk * 256;
+            const uint64_t dah = umma_desc(ah + o, 128, kSbo), dal = umma_desc(al + o, 128, kSbo);
+            const uint64_t dbh = umma_desc(bh + o, 128, kSbo);
+            umma_bf16(d, dah, dbh, idesc, q > 0 || kk > 0);
+            umma_bf16(d, dal, dbh, idesc, true);
+            if (MODE == 1) umma_bf16(d, dah, umma_desc(bl + o, 128, kSbo), idesc, true);
+          }
+          umma_commit(&S.ab_empty[s]);
+        }
+        umma_commit(&S.acc_full[a]);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---- dequantisation: warp 4 + w takes M-tile w
+    const int w = warp - 4;
+    int ri = 0, ks = 0;
+    for (int u = blockIdx.x; u < nunits; u += G) {
+      const PfUnit U = pf_unit(J, u);
+      (void)U;
+      for (int c = 0; c < nch; ++c, ++ri) {
+        const int rs = ri % kPfRaw;
+        mbar_wait_bounded(&S.raw_full[rs], (ri / kPfRaw) & 1, &S.skip, status);
+        for (int Gi = 0; Gi < NG; ++Gi, ++ks) {
+          const int s = ks % NS;
+          if (ks >= NS) mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.skip, status);
+          uint8_t* A = stages + s * SB;
+          dequant_group<FMT>(g, raw + rs * RB, Gi, A, A + kPfA, w, lane, MODE == 0 && F16);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.a_full[s]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.raw_empty[rs]);
+      }
+    }
+  } else {
+    // ---- epilogue: thread r = tensor-memory lane r = weight row r of the block
+    const int r = tid;
+    int ui = 0;
+    for (int u = blockIdx.x; u < nunits; u += G, ++ui) {
+      const PfUnit U = pf_unit(J, u);
+      const int a = ui & 1;
+      mbar_wait_bounded(&S.acc_full[a], (ui >> 1) & 1, &S.skip, status);
+      tmem_fence_after();
+      const uint32_t tl = tbase + (uint32_t(32 * warp) << 16) + uint32_t(a * kPfTile);
+      for (int c8 = 0; c8 < U.cnt; c8 += 8) {
+        float v[8];
+        tmem_ld8(tl + uint32_t(c8), v);
+        if (MODE == 0) {
+          // rows 0-63 are gate rows 64 m + r, rows 64-127 the matching up rows
+          if (r >= 64) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) S.xch[r - 64][j] = v[j];
+          }
+          epi_bar();
+          if (r < 64) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int n = c8 + j;
+              if (n < U.cnt) {
+                const float ga = v[j], up = S.xch[r][j];
+                const float hv = ga / (1.f + expf(-ga)) * up;
+                const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                const size_t at = (size_t)(U.off + n) * J.ldh + 64 * U.m + r;
+                J.h[at] = __bfloat16_as_ushort(hb);
+                J.hl[at] = __bfloat16_as_ushort(__float2bfloat16_rn(hv - __bfloat162float(hb)));
+              }
+            }
+          }
+          epi_bar();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int n = c8 + j;
+            if (n < U.cnt) {
+              const int row = J.scatter ? __ldg(J.perm + U.off + n) : U.off + n;
+              J.y[(size_t)row * J.ldy + 128 * U.m + r] = v[j];
+            }
+          }
+        }
+      }
+      tmem_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.acc_empty[a]);
+    }
+  }
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  if (warp == 14) tmem_dealloc(tbase, 2 * kPfTile);
+}
+
+template <int FMT, int MODE, bool F16>
+cudaError_t launch_t(const PrefillJob& J, int sms, cudaStream_t st) {
+  const int smem = prefill_smem(J.g, MODE);
+  if (smem <= 0) return cudaErrorInvalidValue;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured[dev] < smem) {
+    e = cudaFuncSetAttribute(k_prefill<FMT, MODE, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = smem;
+  }
+  k_prefill<FMT, MODE, F16><<<sms, kPfThreads, smem, st>>>(J);
+  return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t launch_fmt(const PrefillJob& J, int mode, bool f16a, int sms, cudaStream_t st) {
+  if (mode == 1) return launch_t<FMT, 1, false>(J, sms, st);
+  return f16a ? launch_t<FMT, 0, true>(J, sms, st) : launch_t<FMT, 0, false>(J, sms, st);
+}
+
+}  // namespace
+
+int prefill_smem(const TileGeo& g, int mode) {
+  if (g.K % kPfKBlk != 0) return 0;
+  const int bytes = kPfRaw * raw_stage_bytes(g) + pf_stages(mode) * pf_stage_bytes(mode);
+  return bytes + int(sizeof(PfSmem)) + 1024 <= kEngineSmemMax ? bytes : 0;
+}
+
+cudaError_t launch_prefill(const PrefillJob& J, int mode, bool f16a, int sms, cudaStream_t st) {
+  switch (J.g.fmt) {
+    case MOE_FMT_AFFINE4_G64: return launch_fmt<MOE_FMT_AFFINE4_G64>(J, mode, f16a, sms, st);
+    case MOE_FMT_AFFINE3_G64: return launch_fmt<MOE_FMT_AFFINE3_G64>(J, mode, f16a, sms, st);
+    case MOE_FMT_W4A16_SYM_G128: return launch_fmt<MOE_FMT_W4A16_SYM_G128>(J, mode, f16a, sms, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

@@ -29,9 +29,10 @@ __global__ void __launch_bounds__(1024) k_bucket(const int32_t* __restrict__ idx
 }
 
 __global__ void __launch_bounds__(256) k_subslots(const int32_t* __restrict__ offsets, int E,
-                                                  int* nss, int* se, int* so, int* sc) {
+                                                  int* nss, int* se, int* so, int* sc,
+                                                  int run) {
   __shared__ int wcount[8];
-  subslots_cta(offsets, E, nss, se, so, sc, wcount);
+  subslots_cta(offsets, E, nss, se, so, sc, wcount, run);
 }
 
 }  // namespace
@@ -71,8 +72,8 @@ cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offs
 }
 
 cudaError_t launch_subslots(const int32_t* offsets, int E, int* nss, int* se, int* so, int* sc,
-                            cudaStream_t st) {
-  k_subslots<<<1, 256, 0, st>>>(offsets, E, nss, se, so, sc);
+                            cudaStream_t st, int run) {
+  k_subslots<<<1, 256, 0, st>>>(offsets, E, nss, se, so, sc, run);
   return cudaGetLastError();
 }
 

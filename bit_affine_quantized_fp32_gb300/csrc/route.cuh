@@ -381,10 +381,12 @@ __device__ __forceinline__ void bucket_cta(const int32_t* idx, int N, int E, int
 }
 
 // Sub-slots from the bucket offsets: every active expert (ascending id) is
-// cut into runs of at most 8 bucket positions.  Needs blockDim.x >= 256 (the
-// first 256 threads scan).
+// cut into runs of at most `run` bucket positions (8 for the decode units, the
+// N tile for the prefill GEMMs).  Needs blockDim.x >= 256 (the first 256
+// threads scan).
 __device__ __forceinline__ void subslots_cta(const int32_t* offsets, int E, int* nss, int* se,
-                                             int* so, int* sc, int* wcount /* 8 ints of smem */) {
+                                             int* so, int* sc, int* wcount /* 8 ints of smem */,
+                                             int run = 8) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int c = 0, off = 0, nsub = 0, incl = 0;
   if (tid < 256) {
@@ -392,7 +394,7 @@ __device__ __forceinline__ void subslots_cta(const int32_t* offsets, int E, int*
       off = __ldcg(offsets + tid);
       c = __ldcg(offsets + tid + 1) - off;
     }
-    nsub = (c + 7) >> 3;
+    nsub = (c + run - 1) / run;
     incl = nsub;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -408,8 +410,8 @@ __device__ __forceinline__ void subslots_cta(const int32_t* offsets, int E, int*
     const int base = pre + incl - nsub;
     for (int i = 0; i < nsub; ++i) {
       se[base + i] = tid;
-      so[base + i] = off + 8 * i;
-      sc[base + i] = min(8, c - 8 * i);
+      so[base + i] = off + run * i;
+      sc[base + i] = min(run, c - run * i);
     }
     if (tid == 0) {
       int tot = 0;

@@ -492,3 +492,55 @@ def test_fused_alternating_shapes(capi):
         part, _, _ = g.forward(g.x[:T].contiguous())
         assert torch.equal(part, full[:T])
     assert capi.moe_get_device_status(g.ws) == 0
+
+
+# ---------------------------------------------------------------------------
+# Prefill form (T > 32): the tcgen05 expert GEMMs with bf16 operands and fp32
+# accumulation; the tolerance is the layer's (bf16 rounding of the dequantised
+# weights and of h stays well inside it).
+
+PREFILL_CASES = [
+    # Zipf routing: the busiest experts take more than one 128-token tile
+    dict(T=300, E=16, k=4, H=256, I=128, expert_fmt="affine4_g64", shared_fmt="affine4_g64",
+         gate_fmt="affine8_g64", zipf=True, seed=41),
+    dict(T=200, E=8, k=2, H=512, I=256, expert_fmt="affine3_g64", router_fmt="affine8_g64",
+         shared_fmt="affine4_g64", gate_fmt="affine8_g64", seed=42),
+    dict(T=160, E=16, k=8, H=512, I=256, expert_fmt="w4a16_g128", shared_fmt="w4a16_g128",
+         gate_fmt="bf16", act="f16", seed=43),
+    # the smallest prefill call; four experts hold every token (tiles of 33)
+    dict(T=33, E=4, k=4, H=256, I=128, expert_fmt="affine4_g64", seed=44),
+    # 300 tokens per expert: three tiles each, the last one ragged
+    dict(T=600, E=4, k=2, H=256, I=128, expert_fmt="affine4_g64", shared_fmt="affine4_g64",
+         seed=45),
+]
+
+
+@pytest.mark.parametrize("cfg", PREFILL_CASES,
+                         ids=lambda c: f"T{c['T']}_E{c['E']}_{c['expert_fmt']}")
+def test_prefill_layer(capi, cfg):
+    L = synth.gen_layer(**cfg)
+    g = Hn.GpuLayer(L)
+    out, idx, _ = g.forward()
+    ref = Hn.oracle_layer(L, idx_override=idx.cpu().numpy())
+    Hn.assert_layer_close(Hn.to_np(out), ref["out"])
+    # the decode form of the same call agrees with the oracle too
+    out_d, idx_d, _ = g.forward(flags=1)
+    assert Hn.torch().equal(idx, idx_d)
+    Hn.assert_layer_close(Hn.to_np(out_d), ref["out"])
+
+
+def test_prefill_full_size_sampled(capi):
+    """The 512-token prefill window at full size (E=256, hidden 2048, inter
+    512, Zipf routing, shared expert): every token computed on the GPU, a
+    seeded sample of tokens checked against the oracle (a token's output
+    depends on its own row and routing only)."""
+    import dataclasses
+    L = synth.workload("prefill512_affine4_zipf")
+    g = Hn.GpuLayer(L)
+    out, idx, _ = g.forward()
+    assert capi.moe_get_device_status(g.ws) == 0
+    rng = np.random.default_rng(512)
+    pick = np.sort(rng.choice(L.T, size=40, replace=False))
+    Ls = dataclasses.replace(L, T=len(pick), x=L.x[pick])
+    ref = Hn.oracle_layer(Ls, idx_override=idx.cpu().numpy()[pick])
+    Hn.assert_layer_close(Hn.to_np(out)[pick], ref["out"])
