@@ -238,21 +238,40 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       for (int i = max(0, ri - kPfRaw); i < ri; ++i)
         mbar_wait_bounded(&S.raw_full[i % kPfRaw], (i / kPfRaw) & 1, &S.skip, status);
   } else if (warp == 13) {
-    // ---- operand rows, one 64-column group per stage
+    // ---- operand rows, one 64-column group per stage; lane l copies rows
+    // l, l + 32, ... of the tile, their addresses resolved once per unit
+    constexpr int RPL = kPfTile / 32;
     int ks = 0;
     for (int u = blockIdx.x; u < nunits; u += G) {
       const PfUnit U = pf_unit(J, u);
+      size_t rofs[RPL];
+#pragma unroll
+      for (int i = 0; i < RPL; ++i) {
+        const int n = lane + 32 * i;
+        const int row = n < U.cnt ? ((MODE == 0 && J.gather) ? __ldg(J.perm + U.off + n) / J.k
+                                                             : U.off + n)
+                                  : 0;
+        rofs[i] = (size_t)row * J.ldB;
+      }
       for (int q = 0; q < nks; ++q, ++ks) {
         const int s = ks % NS;
         if (ks >= NS) mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.skip, status);
         const int k0 = q * kPfKBlk;
         uint8_t* B = stages + s * SB + 2 * kPfA;
-        for (int i = lane; i < U.cnt * 8; i += 32) {
-          const int n = i >> 3, ch = i & 7;
-          const int row = (MODE == 0 && J.gather) ? __ldg(J.perm + U.off + n) / J.k : U.off + n;
-          const size_t src = (size_t)row * J.ldB + k0 + ch * 8;
-          cp_async16(B + umma_off(n, ch * 8, kPfKBlk), J.B + src);
-          if (MODE == 1) cp_async16(B + kPfB + umma_off(n, ch * 8, kPfKBlk), J.Blo + src);
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) {
+          const int n = lane + 32 * i;
+          if (n < U.cnt) {
+            const uint16_t* src = J.B + rofs[i] + k0;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) cp_async16(B + umma_off(n, ch * 8, kPfKBlk), src + ch * 8);
+            if (MODE == 1) {
+              const uint16_t* srl = J.Blo + rofs[i] + k0;
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch)
+                cp_async16(B + kPfB + umma_off(n, ch * 8, kPfKBlk), srl + ch * 8);
+            }
+          }
         }
         cp_async_arrive_noinc(&S.b_full[s]);
       }

@@ -7,10 +7,11 @@ namespace moe {
 
 namespace {
 
+// blockIdx.x: router block (rows), blockIdx.y: run of kRouterTT tokens
 __global__ void __launch_bounds__(256) k_router(const RouterJob J, int KS) {
   __shared__ float part[8 * kRouterTT];
-  for (int t0 = 0; t0 < J.T; t0 += kRouterTT)
-    router_block(J, KS, blockIdx.x, part, J.x + size_t(t0) * J.H, t0, min(kRouterTT, J.T - t0));
+  const int t0 = blockIdx.y * kRouterTT;
+  router_block(J, KS, blockIdx.x, part, J.x + size_t(t0) * J.H, t0, min(kRouterTT, J.T - t0));
 }
 
 __global__ void k_topk(const float* __restrict__ logits, const float* __restrict__ gate_logit,
@@ -54,7 +55,8 @@ cudaError_t launch_router(const RouterJob& J, cudaStream_t st) {
   if (J.T <= 0) return cudaSuccess;
   const int KS = router_ks(J.H);
   if (KS == 0) return cudaErrorInvalidValue;
-  k_router<<<router_blocks(J.E, J.gq != nullptr, J.H), 256, 0, st>>>(J, KS);
+  k_router<<<dim3(router_blocks(J.E, J.gq != nullptr, J.H), (J.T + kRouterTT - 1) / kRouterTT),
+             256, 0, st>>>(J, KS);
   return cudaGetLastError();
 }
 

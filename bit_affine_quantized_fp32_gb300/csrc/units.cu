@@ -84,9 +84,16 @@ __global__ void k_xsum(const uint16_t* __restrict__ x, int T, int H, int f16, Ti
   xsum_task(x, H, f16 != 0, g13, xsum, task);
 }
 
+// blockIdx.x: 64-column piece, blockIdx.y: run of kCombineTok tokens
+constexpr int kCombineTok = 16;
 __global__ void __launch_bounds__(256) k_combine(const CombineArgs A) {
-  combine_rows(A.y, A.yhalf, A.w, A.ysh, A.ysh2, A.sg, A.out, A.T, A.k, A.H, A.f16 != 0,
-               blockIdx.x * kCombineRows, kCombineRows, threadIdx.x, blockDim.x);
+  const int t0 = blockIdx.y * kCombineTok;
+  const int Tn = min(kCombineTok, A.T - t0);
+  const size_t kh = size_t(A.k) * A.H;
+  combine_rows(A.y + t0 * kh, A.yhalf, A.w + t0 * A.k, A.ysh ? A.ysh + size_t(t0) * A.H : nullptr,
+               A.ysh2 ? A.ysh2 + size_t(t0) * A.H : nullptr, A.sg ? A.sg + t0 : nullptr,
+               A.out + size_t(t0) * A.H, Tn, A.k, A.H, A.f16 != 0, blockIdx.x * kCombineRows,
+               kCombineRows, threadIdx.x, blockDim.x);
 }
 
 // dst = a + b elementwise (the two k-half planes of a down projection)
@@ -175,7 +182,7 @@ cudaError_t launch_add_planes(const float* a, const float* b, float* dst, long n
 
 cudaError_t launch_combine(const CombineArgs& A, cudaStream_t st) {
   if (A.T <= 0) return cudaSuccess;
-  k_combine<<<A.H / kCombineRows, 256, 0, st>>>(A);
+  k_combine<<<dim3(A.H / kCombineRows, (A.T + kCombineTok - 1) / kCombineTok), 256, 0, st>>>(A);
   return cudaGetLastError();
 }
 
