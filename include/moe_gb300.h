@@ -124,11 +124,16 @@ typedef struct moe_expert_bank {
 } moe_expert_bank;
 
 /* flags of moe_experts_forward / moe_layer_forward */
-#define MOE_FLAG_FORCE_DECODE 1   /* use the decode (grouped GEMV) kernels at any T */
+#define MOE_FLAG_FORCE_DECODE 1   /* use the decode (grouped GEMV) form at any T */
 #define MOE_FLAG_UNFUSED 2        /* moe_layer_forward: one launch per step instead of the
                                      single persistent decode launch (same results) */
 
-/* Decode path is taken for n_tokens <= MOE_DECODE_MAX_TOKENS. */
+/* The decode form (grouped GEMV on exact integer codes) serves n_tokens <=
+ * MOE_DECODE_MAX_TOKENS; above it the prefill form runs the expert GEMMs on
+ * the tensor cores (tcgen05) over tiles of up to 128 tokens of one expert,
+ * with the dequantised weights and h as bf16 hi + lo parts (fp16 parts for
+ * fp16 activations) and fp32 accumulation -- the same values to within the
+ * layer's tolerance, not the same bits as the decode form. */
 #define MOE_DECODE_MAX_TOKENS 32
 
 /* Human-readable name of a status; never NULL. */
@@ -229,8 +234,10 @@ moe_status moe_shared_expert(const moe_expert_bank* shared, const void* x, int a
  * the activation type.  y_shared/shared_gate_w nullable (no shared slot when
  * y_shared is NULL; weight 1 when only shared_gate_w is NULL).
  * Routing inputs are moe_route's outputs (or any valid equivalent).
- * Every token's output row depends only on that token's inputs: a row is
- * bit-identical whatever the other rows of the call ([547-win]).       */
+ * In the decode form every token's output row depends only on that token's
+ * inputs: a row is bit-identical whatever the other rows of the call
+ * ([547-win]); the prefill form (T > 32) matches it to within the layer's
+ * tolerance.                                                             */
 moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, int act,
                                int n_tokens, int top_k, const int32_t* topk_idx,
                                const float* topk_w, const int32_t* bucket_offsets,
