@@ -486,12 +486,24 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
   if ((s = check_ws(ws, ws_bytes, L.total))) return s;
   const bool f16 = act == MOE_FMT_F16;
   if (use_prefill(experts, T, flags)) {
-    // tiles of up to kPfTile bucket positions per expert, then the two GEMMs
-    int* nt = reinterpret_cast<int*>(wsp(ws, L.nss));
-    int* te = reinterpret_cast<int*>(wsp(ws, L.ss_e));
-    int* to = reinterpret_cast<int*>(wsp(ws, L.ss_off));
-    int* tc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
-    MOE_CUDA(launch_subslots(bucket_offsets, E, nt, te, to, tc, stream, kPfTile), "tile kernel");
+    // Experts with more than kPfLight assignments: tiles of up to kPfTile
+    // bucket positions through the tensor-core GEMMs (second y plane set to
+    // 0); the others: sub-slots of 8 through the decode units.  One combine
+    // over the two y planes.
+    float* y = reinterpret_cast<float*>(wsp(ws, L.y));
+    const size_t yhalf = size_t(T) * top_k * H;
+    int* nt = reinterpret_cast<int*>(wsp(ws, L.pt_n));
+    int* te = reinterpret_cast<int*>(wsp(ws, L.pt_e));
+    int* to = reinterpret_cast<int*>(wsp(ws, L.pt_off));
+    int* tc = reinterpret_cast<int*>(wsp(ws, L.pt_cnt));
+    MOE_CUDA(launch_subslots(bucket_offsets, E, nt, te, to, tc, stream, kPfTile, kPfLight),
+             "tile kernel");
+    int* nss = reinterpret_cast<int*>(wsp(ws, L.nss));
+    int* se = reinterpret_cast<int*>(wsp(ws, L.ss_e));
+    int* so = reinterpret_cast<int*>(wsp(ws, L.ss_off));
+    int* sc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
+    MOE_CUDA(launch_subslots(bucket_offsets, E, nss, se, so, sc, stream, kMaxTok, 0, kPfLight),
+             "sub-slot kernel");
     const MatGeo g13 = geo13(experts), g2 = geo2(experts);
     PrefillJob J{};
     J.g = g13.t;
@@ -517,13 +529,22 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
     D.Blo = J.hl;
     D.ldB = h_pitch(I);
     D.gather = 0;
-    D.y = reinterpret_cast<float*>(wsp(ws, L.y));
+    D.y = y;
     D.ldy = H;
+    D.yzero = yhalf;
     D.scatter = 1;
     MOE_CUDA(launch_prefill(D, 1, false, sm_count(), stream), "prefill down kernel");
+    float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
+    MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, f16, g13.t, xsum, stream),
+             "activation sums");
+    const SubSlots ss{nss, se, so, sc, 0, 0};
+    s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
+                 bucket_perm, top_k, J.h, J.hl, reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr,
+                 y, yhalf, kRowsScatter, static_cast<int*>(ws), stream);
+    if (s) return s;
     CombineArgs C{};
-    C.y = D.y;
-    C.yhalf = 0;  // one plane
+    C.y = y;
+    C.yhalf = yhalf;
     C.w = topk_w;
     C.ysh = y_shared;
     C.ysh2 = nullptr;

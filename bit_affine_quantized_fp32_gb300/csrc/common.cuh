@@ -39,6 +39,10 @@ struct WsLayout {
   size_t sh_hl;       // u16 [T][I+8]
   size_t sh_hsum;     // f32 [T][ldh]
   size_t ysh;         // f32 [2][T][H]
+  size_t pt_n;        // i32 [1]   prefill tiles (experts with many assignments)
+  size_t pt_e;        // i32 [maxss] expert of each tile
+  size_t pt_off;      // i32 [maxss] first bucket position
+  size_t pt_cnt;      // i32 [maxss] rows (1..128)
   size_t total;
 };
 
@@ -88,6 +92,10 @@ inline WsLayout ws_layout(long T, long E, long k, long H, long I) {
   L.sh_hl = take(2 * T * (I + 8));
   L.sh_hsum = take(4 * T * ldh);
   L.ysh = take(4 * 2 * T * H);
+  L.pt_n = take(4);
+  L.pt_e = take(4 * mss);
+  L.pt_off = take(4 * mss);
+  L.pt_cnt = take(4 * mss);
   L.total = o;
   return L;
 }

@@ -84,8 +84,10 @@ cudaError_t launch_topk(const float* logits, const float* gate_logit, int T, int
                         int32_t* idx, float* w, float* sg, cudaStream_t st);
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets,
                           int32_t* perm, cudaStream_t st);
+// Sub-slots (runs of at most `run` bucket positions) of the experts with
+// more than cmin and at most cmax assignments.
 cudaError_t launch_subslots(const int32_t* offsets, int E, int* nss, int* se, int* so, int* sc,
-                            cudaStream_t st, int run = kMaxTok);
+                            cudaStream_t st, int run = kMaxTok, int cmin = 0, int cmax = 1 << 30);
 
 // formats
 cudaError_t launch_pack(int fmt, const uint8_t* codes, int rows, int cols, uint32_t* packed,

@@ -379,7 +379,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
             const int n = c8 + j;
             if (n < U.cnt) {
               const int row = J.scatter ? __ldg(J.perm + U.off + n) : U.off + n;
-              J.y[(size_t)row * J.ldy + 128 * U.m + r] = v[j];
+              const size_t at = (size_t)row * J.ldy + 128 * U.m + r;
+              J.y[at] = v[j];
+              if (J.yzero) J.y[at + J.yzero] = 0.f;
             }
           }
         }

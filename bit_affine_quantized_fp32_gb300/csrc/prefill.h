@@ -7,6 +7,10 @@ namespace moe {
 
 constexpr int kPfTile = 128;   // tokens per N tile (tensor-memory columns per accumulator)
 constexpr int kPfThreads = 480;
+// Experts with at most this many assignments in a prefill call go to the
+// decode units instead (each tensor-core unit dequantises a whole weight
+// block whatever its rows; the decode units cost per 8 rows).
+constexpr int kPfLight = 40;
 
 // One prefill GEMM launch over a tile list: each tile is <= kPfTile rows of
 // one expert; every (tile, 128-row weight block) is a unit.
@@ -37,6 +41,8 @@ struct PrefillJob {
   int ldh;
   float* y;                  // mode 1 output (fp32), ldy elements apart
   int ldy;
+  size_t yzero;              // mode 1: when > 0, 0 is also stored at y[i + yzero] (the
+                             //         second k-half plane the decode units would write)
   int scatter;               // mode 1: output row = perm[off + n] (else off + n)
   int* status;
 };

@@ -31,9 +31,9 @@ __global__ void __launch_bounds__(1024) k_bucket(const int32_t* __restrict__ idx
 
 __global__ void __launch_bounds__(256) k_subslots(const int32_t* __restrict__ offsets, int E,
                                                   int* nss, int* se, int* so, int* sc,
-                                                  int run) {
+                                                  int run, int cmin, int cmax) {
   __shared__ int wcount[8];
-  subslots_cta(offsets, E, nss, se, so, sc, wcount, run);
+  subslots_cta(offsets, E, nss, se, so, sc, wcount, run, cmin, cmax);
 }
 
 }  // namespace
@@ -74,8 +74,8 @@ cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offs
 }
 
 cudaError_t launch_subslots(const int32_t* offsets, int E, int* nss, int* se, int* so, int* sc,
-                            cudaStream_t st, int run) {
-  k_subslots<<<1, 256, 0, st>>>(offsets, E, nss, se, so, sc, run);
+                            cudaStream_t st, int run, int cmin, int cmax) {
+  k_subslots<<<1, 256, 0, st>>>(offsets, E, nss, se, so, sc, run, cmin, cmax);
   return cudaGetLastError();
 }
 

@@ -380,19 +380,20 @@ __device__ __forceinline__ void bucket_cta(const int32_t* idx, int N, int E, int
   }
 }
 
-// Sub-slots from the bucket offsets: every active expert (ascending id) is
-// cut into runs of at most `run` bucket positions (8 for the decode units, the
-// N tile for the prefill GEMMs).  Needs blockDim.x >= 256 (the first 256
-// threads scan).
+// Sub-slots from the bucket offsets: every active expert (ascending id) with
+// more than cmin and at most cmax assignments is cut into runs of at most
+// `run` bucket positions (8 for the decode units, the N tile for the prefill
+// GEMMs).  Needs blockDim.x >= 256 (the first 256 threads scan).
 __device__ __forceinline__ void subslots_cta(const int32_t* offsets, int E, int* nss, int* se,
                                              int* so, int* sc, int* wcount /* 8 ints of smem */,
-                                             int run = 8) {
+                                             int run = 8, int cmin = 0, int cmax = 1 << 30) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int c = 0, off = 0, nsub = 0, incl = 0;
   if (tid < 256) {
     if (tid < E) {
       off = __ldcg(offsets + tid);
       c = __ldcg(offsets + tid + 1) - off;
+      if (c <= cmin || c > cmax) c = 0;
     }
     nsub = (c + run - 1) / run;
     incl = nsub;
