@@ -204,7 +204,7 @@ static __device__ __noinline__ bool wait_counter(const int* p, int target, volat
     if (*skip) return false;
     if (global_ns() - t0 > kWaitLimitNs) break;
     __nanosleep(ns);
-    if (ns < 256) ns <<= 1;
+    if (ns < 64) ns <<= 1;
   }
   *skip = 1;
   atomicExch(status, int(MOE_ERR_TIMEOUT));
