@@ -368,9 +368,10 @@ def run_gpu(args, ws_world, rank, local):
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
     # one persistent launch per layer call for decode batches (<= 32 tokens);
-    # the prefill form: routing (3), shared expert (2), tiles, gate/up, down,
-    # combine
-    launches_per_step = 1 if T <= 32 else 3 + (2 if cfg["shared_fmt"] else 0) + 4
+    # the prefill form: routing (3), shared expert (2), tiles and sub-slots
+    # (2), tensor-core gate/up and down (2), activation sums, decode units for
+    # the light experts (2), combine
+    launches_per_step = 1 if T <= 32 else 3 + (2 if cfg["shared_fmt"] else 0) + 8
     line = {
         "metric": "MoE-layer tokens/s (decode batch %d, %s)" % (T, cfg["expert_fmt"]),
         "value": round(value, 1),
