@@ -147,13 +147,19 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second
 // Wait for phase `parity` of an mbarrier; after kWaitLimitNs, record a timeout
 // and return false.  `skip` (shared) turns every later wait into a no-op once
 // a timeout has happened, so the kernel finishes (with garbage results)
-// quickly.
+// quickly.  By default the warp polls (the decode engine's waits are short and
+// a suspended warp wakes late); sleep = true lets the hardware suspend it
+// between polls (long waits of otherwise idle roles).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity,
-                                                  volatile int* skip, int* status) {
-  if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+                                                  volatile int* skip, int* status,
+                                                  bool sleep = false) {
+  auto poll = [&]() {
+    return sleep ? mbar_try_wait_sleep(bar, parity, 100000u) : mbar_try_wait(bar, parity);
+  };
+  if (poll()) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (poll()) return true;
     if (*skip) return false;
     if (global_ns() - t0 > kWaitLimitNs) break;
   }

@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         const int rs = ri % kPfRaw;
         if (lane == 0) {
           if (ri >= kPfRaw)
-            mbar_wait_bounded(&S.raw_empty[rs], ((ri / kPfRaw) - 1) & 1, &S.skip, status);
+            mbar_wait_bounded(&S.raw_empty[rs], ((ri / kPfRaw) - 1) & 1, &S.skip, status, true);
           mbar_expect_tx(&S.raw_full[rs], unsigned(g.item_bytes));
           bulk_g2s(raw + rs * RB,
                    J.base + (size_t)U.e * g.expert_bytes +
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
     }
     if (lane == 0)  // the last copies have landed before the CTA may exit
       for (int i = max(0, ri - kPfRaw); i < ri; ++i)
-        mbar_wait_bounded(&S.raw_full[i % kPfRaw], (i / kPfRaw) & 1, &S.skip, status);
+        mbar_wait_bounded(&S.raw_full[i % kPfRaw], (i / kPfRaw) & 1, &S.skip, status, true);
   } else if (warp == 13) {
     // ---- operand rows, one 64-column group per stage; lane l copies rows
     // l, l + 32, ... of the tile, their addresses resolved once per unit
@@ -255,7 +255,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       }
       for (int q = 0; q < nks; ++q, ++ks) {
         const int s = ks % NS;
-        if (ks >= NS) mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.skip, status);
+        if (ks >= NS)
+          mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.skip, status, true);
         const int k0 = q * kPfKBlk;
         uint8_t* B = stages + s * SB + 2 * kPfA;
 #pragma unroll
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       for (int u = blockIdx.x; u < nunits; u += G, ++ui) {
         const PfUnit U = pf_unit(J, u);
         const int a = ui & 1;
-        if (ui >= 2) mbar_wait_bounded(&S.acc_empty[a], ((ui >> 1) - 1) & 1, &S.skip, status);
+        if (ui >= 2) mbar_wait_bounded(&S.acc_empty[a], ((ui >> 1) - 1) & 1, &S.skip, status, true);
         tmem_fence_after();
         const int N = max(16, (U.cnt + 15) & ~15);
         const uint32_t idesc = (MODE == 0 && F16)
@@ -294,8 +295,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         constexpr uint32_t kSbo = (kPfKBlk / 8) * 128;
         for (int q = 0; q < nks; ++q, ++ks) {
           const int s = ks % NS;
-          mbar_wait_bounded(&S.a_full[s], (ks / NS) & 1, &S.skip, status);
-          mbar_wait_bounded(&S.b_full[s], (ks / NS) & 1, &S.skip, status);
+          mbar_wait_bounded(&S.a_full[s], (ks / NS) & 1, &S.skip, status, true);
+          mbar_wait_bounded(&S.b_full[s], (ks / NS) & 1, &S.skip, status, true);
           fence_proxy_async();
           tmem_fence_after();
           const uint32_t ah = smem_u32(stages + s * SB), al = ah + kPfA;
@@ -324,10 +325,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       (void)U;
       for (int c = 0; c < nch; ++c, ++ri) {
         const int rs = ri % kPfRaw;
-        mbar_wait_bounded(&S.raw_full[rs], (ri / kPfRaw) & 1, &S.skip, status);
+        mbar_wait_bounded(&S.raw_full[rs], (ri / kPfRaw) & 1, &S.skip, status, true);
         for (int Gi = 0; Gi < NG; ++Gi, ++ks) {
           const int s = ks % NS;
-          if (ks >= NS) mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.skip, status);
+          if (ks >= NS)
+          mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.skip, status, true);
           uint8_t* A = stages + s * SB;
           dequant_group<FMT>(g, raw + rs * RB, Gi, A, A + kPfA, w, lane, MODE == 0 && F16);
           fence_proxy_async();
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
     for (int u = blockIdx.x; u < nunits; u += G, ++ui) {
       const PfUnit U = pf_unit(J, u);
       const int a = ui & 1;
-      mbar_wait_bounded(&S.acc_full[a], (ui >> 1) & 1, &S.skip, status);
+      mbar_wait_bounded(&S.acc_full[a], (ui >> 1) & 1, &S.skip, status, true);
       tmem_fence_after();
       const uint32_t tl = tbase + (uint32_t(32 * warp) << 16) + uint32_t(a * kPfTile);
       for (int c8 = 0; c8 < U.cnt; c8 += 8) {

@@ -38,7 +38,11 @@ __global__ void __launch_bounds__(256) k_subslots(const int32_t* __restrict__ of
 
 }  // namespace
 
+// k-splits of a router row: the fewest with at most 2 x 128 columns per warp
+// (short dependent chains), else at most 4 x 128.
 int router_ks(int H) {
+  for (int ks = 1; ks <= 8; ks <<= 1)
+    if (H % (ks * 128) == 0 && H / (ks * 128) <= 2) return ks;
   for (int ks = 1; ks <= 8; ks <<= 1)
     if (H % (ks * 128) == 0 && H / (ks * 128) <= 4) return ks;
   return 0;
