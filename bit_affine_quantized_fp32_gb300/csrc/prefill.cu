@@ -265,7 +265,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
           if (n < U.cnt) {
             const uint16_t* src = J.B + rofs[i] + k0;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) cp_async16(B + umma_off(n, ch * 8, kPfKBlk), src + ch * 8);
+            for (int ch = 0; ch < 8; ++ch)
+              cp_async16(B + umma_off(n, ch * 8, kPfKBlk), src + ch * 8);
             if (MODE == 1) {
               const uint16_t* srl = J.Blo + rofs[i] + k0;
 #pragma unroll
