@@ -33,7 +33,9 @@
 // Parity status: every function here is pinned by the CPU tests (format
 // round trips and hand-derived words, exact dequant, brute-force top-k,
 // closed-form softmax, bucketing invariants, one-expert layer = dense
-// SwiGLU MLP through numpy, width-widening equality).  None is unpinned.
+// SwiGLU MLP through numpy, width-widening equality, bf16 rounding against
+// torch's conversion, fp32 combine cases that only the fused multiply-add,
+// the slot order or the shared slot's place decide).  None is unpinned.
 
 #include <cmath>
 #include <cstdint>
@@ -553,6 +555,59 @@ int oracle_moe_layer(const LayerArgs* A) {
   if (A->sg) std::memcpy(A->sg, sg.data(), sizeof(double) * T);
   if (A->y_slots) std::memcpy(A->y_slots, yslots.data(), sizeof(double) * T * k * H);
   if (A->y_shared) std::memcpy(A->y_shared, ysh.data(), sizeof(double) * T * H);
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// The combine in the engine's own precision [803-gate]: the slots' fma sum in
+// fp32 -- slot order, the shared slot last -- rounded once to bf16.  Given the
+// slots' outputs and weights as fp32 values, every bit of the result is fixed
+// by IEEE arithmetic, so a device combine fed the same inputs can be compared
+// byte for byte.  Rounding to bf16 is to nearest, ties to even; a NaN becomes
+// the quiet NaN 0x7FC0.
+//   y [T*k][H], w [T][k], ysh [T][H] (nullable), sg [T] (nullable: weight 1),
+//   out [T][H] bf16 bit patterns.
+static uint16_t f32_to_bf16_rne(float v) {
+  uint32_t u;
+  std::memcpy(&u, &v, 4);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0;
+  const uint32_t bias = 0x7FFFu + ((u >> 16) & 1u);
+  return uint16_t((u + bias) >> 16);
+}
+
+static float bf16_to_f32(uint16_t b) {
+  const uint32_t u = uint32_t(b) << 16;
+  float v;
+  std::memcpy(&v, &u, 4);
+  return v;
+}
+
+int oracle_round_bf16(long n, const float* in, float* out) {
+  for (long i = 0; i < n; ++i) out[i] = bf16_to_f32(f32_to_bf16_rne(in[i]));
+  return 0;
+}
+
+int oracle_combine_f32(long T, long k, long H, const float* y, const float* w,
+                       const float* ysh, const float* sg, uint16_t* out) {
+  if (T < 0 || k < 1 || H < 0) return -1;
+  for (long t = 0; t < T; ++t)
+    for (long h = 0; h < H; ++h) {
+      float acc = 0.f;
+      for (long j = 0; j < k; ++j) acc = std::fmaf(w[t * k + j], y[(t * k + j) * H + h], acc);
+      if (ysh) acc = std::fmaf(sg ? sg[t] : 1.f, ysh[t * H + h], acc);
+      out[t * H + h] = f32_to_bf16_rne(acc);
+    }
+  return 0;
+}
+
+// The rounding chain that paragraph lists for the engine's routing: slot
+// weights rounded to bf16, the shared slot weighted by bf16(sigmoid(bf16(g)))
+// (the sigmoid evaluated in fp64 on the bf16 gate logit).
+int oracle_chain_gate_weight(long T, const float* g, float* s) {
+  for (long t = 0; t < T; ++t) {
+    const double gb = bf16_to_f32(f32_to_bf16_rne(g[t]));
+    s[t] = bf16_to_f32(f32_to_bf16_rne(float(1.0 / (1.0 + std::exp(-gb)))));
+  }
   return 0;
 }
 

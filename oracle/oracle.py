@@ -74,6 +74,9 @@ def lib():
         L.oracle_down.argtypes = [i32, i64, i64, P, P, P, i64, P, P]
         L.oracle_bucket.argtypes = [i64, i64, i64, P, P, P, P, P, P]
         L.oracle_moe_layer.argtypes = [P]
+        L.oracle_round_bf16.argtypes = [i64, P, P]
+        L.oracle_combine_f32.argtypes = [i64, i64, i64, P, P, P, P, P]
+        L.oracle_chain_gate_weight.argtypes = [i64, P, P]
         L.oracle_value_bytes.restype = i64
         L.oracle_value_bytes.argtypes = [i32, i64, i64]
         _lib = L
@@ -286,4 +289,40 @@ def moe_layer(x: np.ndarray, k: int, router: dict, experts: dict, shared: dict |
     a.y_slots = P(out["y_slots"]) if want_slots else None
     a.y_shared, a.out = P(out["y_shared"]), P(out["out"])
     _check(lib().oracle_moe_layer(ctypes.byref(a)), "moe_layer")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# The engine's fp32 precision (byte-exact references)
+
+def round_bf16(a) -> np.ndarray:
+    """fp32 values rounded to bf16 (nearest, ties to even), returned as fp32."""
+    a = _c(a, np.float32)
+    out = np.empty_like(a)
+    _check(lib().oracle_round_bf16(a.size, _p(a), _p(out)), "round_bf16")
+    return out
+
+
+def combine_f32(y, w, ysh=None, sg=None) -> np.ndarray:
+    """The slots' fp32 fma sum (slot order, shared slot last), rounded once to
+    bf16; y [T*k, H], w [T, k], ysh [T, H] or None, sg [T] or None.  Returns
+    the bf16 bit patterns [T, H] as uint16."""
+    w = _c(w, np.float32)
+    T, k = w.shape
+    y = _c(y, np.float32)
+    H = y.shape[1]
+    assert y.shape == (T * k, H)
+    ysh = None if ysh is None else _c(ysh, np.float32)
+    sg = None if sg is None else _c(sg, np.float32)
+    out = np.empty((T, H), np.uint16)
+    _check(lib().oracle_combine_f32(T, k, H, _p(y), _p(w), _p(ysh), _p(sg), _p(out)),
+           "combine_f32")
+    return out
+
+
+def chain_gate_weight(g) -> np.ndarray:
+    """bf16(sigmoid(bf16(g))) per token, as fp32."""
+    g = _c(g, np.float32)
+    out = np.empty_like(g)
+    _check(lib().oracle_chain_gate_weight(g.size, _p(g), _p(out)), "chain_gate_weight")
     return out

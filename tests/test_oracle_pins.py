@@ -514,3 +514,86 @@ def test_bucket_invariants():
             assert np.all(flat[seg] == e)
             assert np.all(np.diff(seg) > 0)
         assert np.array_equal(active, np.unique(flat))
+
+
+# --------------------------------------------------------------------------
+# The engine's own precision: bf16 rounding and the fp32 combine
+# ("Progress on the 4-bit gate": the slots' fma sum rounded once to bf16; the
+# routing's bf16 rounding chain)
+
+def test_round_bf16_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(7)
+    v = np.concatenate([
+        rng.standard_normal(4096).astype(np.float32) * np.float32(1e3),
+        np.array([0.0, -0.0, np.inf, -np.inf, 1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8,
+                  -(1 + 2 ** -8), 2 ** -126, 2 ** -133, 3.3895e38, 65504.0], np.float32)])
+    ours = O.round_bf16(v)
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(ours.view(np.uint32), ref.view(np.uint32))
+    # ties go to the even neighbour
+    assert O.round_bf16(np.array([1 + 2 ** -8], np.float32))[0] == 1.0
+    assert O.round_bf16(np.array([1 + 3 * 2 ** -8], np.float32))[0] == 1 + 2 ** -6
+    # NaN stays NaN
+    assert np.isnan(O.round_bf16(np.array([np.nan], np.float32))[0])
+
+
+def bf16_bits(x: float) -> int:
+    return int(np.array([x], np.float32).view(np.uint32)[0] >> 16)
+
+
+def test_combine_f32_single_slot_is_rounding():
+    y = np.array([[1.0, 1 + 2 ** -8, -3.25, 1e-3]], np.float32)
+    out = O.combine_f32(y, np.array([[1.0]], np.float32))
+    expect = O.round_bf16(y[0]).view(np.uint32) >> 16
+    assert np.array_equal(out[0].astype(np.uint32), expect)
+
+
+def test_combine_f32_uses_fused_multiply_add():
+    # w1*y1 = 1 + 2^-11 + 2^-24 exactly; a rounded product loses the 2^-24,
+    # which the fused multiply-add keeps after the first slot cancels 1 + 2^-11
+    a = 1 + 2 ** -12
+    y = np.array([[-(1 + 2 ** -11)], [a]], np.float32)
+    w = np.array([[1.0, a]], np.float32)
+    out = O.combine_f32(y, w)
+    assert int(out[0, 0]) == bf16_bits(2 ** -24)
+
+
+def test_combine_f32_slot_order_and_shared_last():
+    # fp32 sums do not associate: (1e8 + 1) - 1e8 = 0 in slot order, while
+    # 1e8 - 1e8 + 1 would give 1
+    y = np.array([[1e8], [1.0], [-1e8]], np.float32)
+    out = O.combine_f32(y, np.ones((1, 3), np.float32))
+    assert int(out[0, 0]) == bf16_bits(0.0)
+    # the shared slot comes after every routed slot: (1e8 - 1e8) + 1 = 1
+    y2 = np.array([[1e8], [-1e8]], np.float32)
+    out = O.combine_f32(y2, np.ones((1, 2), np.float32), ysh=np.array([[1.0]], np.float32),
+                        sg=np.array([1.0], np.float32))
+    assert int(out[0, 0]) == bf16_bits(1.0)
+    # without sg the shared slot has weight 1
+    out = O.combine_f32(y2, np.ones((1, 2), np.float32), ysh=np.array([[1.0]], np.float32))
+    assert int(out[0, 0]) == bf16_bits(1.0)
+
+
+def test_combine_f32_agrees_with_fp64_layer_combine():
+    # on random data the fp32 chain is the fp64 sum to within the bf16 step
+    rng = np.random.default_rng(11)
+    T, k, H = 3, 8, 64
+    y = rng.standard_normal((T * k, H)).astype(np.float32)
+    w = rng.dirichlet(np.ones(k), size=T).astype(np.float32)
+    ysh = rng.standard_normal((T, H)).astype(np.float32)
+    sg = rng.uniform(0, 1, T).astype(np.float32)
+    out = O.combine_f32(y, w, ysh, sg).astype(np.uint32) << 16
+    got = out.view(np.float32)
+    ref = np.einsum("tk,tkh->th", w.astype(np.float64), y.reshape(T, k, H).astype(np.float64))
+    ref += sg[:, None].astype(np.float64) * ysh
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2 ** -8 + 1e-6)
+
+
+def test_chain_gate_weight_closed_forms():
+    s = O.chain_gate_weight(np.array([0.0, 40.0, -40.0, 1.0], np.float32))
+    assert s[0] == 0.5
+    assert s[1] == 1.0
+    assert 0.0 <= s[2] < 2 ** -50
+    # sigmoid(1) = 0.7310585786... -> bf16 0.73046875 (0x3F3B)
+    assert int(np.array([s[3]], np.float32).view(np.uint32)[0] >> 16) == 0x3F3B
