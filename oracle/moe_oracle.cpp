@@ -35,7 +35,10 @@
 // closed-form softmax, bucketing invariants, one-expert layer = dense
 // SwiGLU MLP through numpy, width-widening equality, bf16 rounding against
 // torch's conversion, fp32 combine cases that only the fused multiply-add,
-// the slot order or the shared slot's place decide).  None is unpinned.
+// the slot order or the shared slot's place decide, 2/5/6-bit streams over
+// every code at every position, exact dequantisation at every width, the
+// same codes at every width giving the same weights and layer output).  None
+// is unpinned.
 
 #include <cmath>
 #include <cstdint>
@@ -60,6 +63,9 @@ enum OFmt {
   O_AFFINE4_G64 = 4,  // MLX affine 4-bit, group 64
   O_AFFINE3_G64 = 5,  // MLX affine 3-bit, group 64 (LSB-first bit stream)
   O_W4A16_G128 = 6,   // compressed-tensors int4 symmetric, group 128: w = s*q
+  O_AFFINE2_G64 = 7,  // MLX affine at the other widths the loader reads [803-fp64]
+  O_AFFINE5_G64 = 8,
+  O_AFFINE6_G64 = 9,
 };
 
 int code_bits(int fmt) {
@@ -68,6 +74,9 @@ int code_bits(int fmt) {
     case O_AFFINE4_G64: return 4;
     case O_AFFINE3_G64: return 3;
     case O_W4A16_G128: return 4;
+    case O_AFFINE2_G64: return 2;
+    case O_AFFINE5_G64: return 5;
+    case O_AFFINE6_G64: return 6;
     default: return 0;
   }
 }
@@ -76,7 +85,10 @@ int group_size(int fmt) {
   switch (fmt) {
     case O_AFFINE8_G64:
     case O_AFFINE4_G64:
-    case O_AFFINE3_G64: return 64;
+    case O_AFFINE3_G64:
+    case O_AFFINE2_G64:
+    case O_AFFINE5_G64:
+    case O_AFFINE6_G64: return 64;
     case O_W4A16_G128: return 128;
     default: return 0;
   }
@@ -120,16 +132,20 @@ double bf16_bits_to_double(uint16_t b) {
   return sign ? -v : v;
 }
 
-// One code out of a packed row.  Affine 8/4-bit and W4A16: 32/bits codes per
-// little-endian uint32, code i of a word at bits [bits*i, bits*i + bits).
-// Affine 3-bit: the row is one LSB-first bit stream; code c occupies stream
-// bits [3c, 3c+3), which may straddle two words.
+// One code out of a packed row.  Affine 8/4/2-bit and W4A16: 32/bits codes
+// per little-endian uint32, code i of a word at bits [bits*i, bits*i + bits).
+// Affine 3/5/6-bit (widths that do not divide 32): the row is one LSB-first
+// bit stream; code c occupies stream bits [bits*c, bits*c + bits), which may
+// straddle two words.  (Both rules are the same stream for widths dividing
+// 32; the pages state the 3-bit stream, and 5/6-bit are read the same way.)
+bool stream_width(int fmt) { return 32 % code_bits(fmt) != 0; }
+
 uint32_t get_code(int fmt, const uint32_t* row_words, long c) {
   int bits = code_bits(fmt);
-  if (fmt == O_AFFINE3_G64) {
+  if (stream_width(fmt)) {
     uint32_t v = 0;
-    for (int i = 0; i < 3; ++i) {
-      long bit = 3 * c + i;
+    for (int i = 0; i < bits; ++i) {
+      long bit = (long)bits * c + i;
       uint32_t b = (row_words[bit / 32] >> (bit % 32)) & 1u;
       v |= b << i;
     }
@@ -142,9 +158,9 @@ uint32_t get_code(int fmt, const uint32_t* row_words, long c) {
 
 void put_code(int fmt, uint32_t* row_words, long c, uint32_t v) {
   int bits = code_bits(fmt);
-  if (fmt == O_AFFINE3_G64) {
-    for (int i = 0; i < 3; ++i) {
-      long bit = 3 * c + i;
+  if (stream_width(fmt)) {
+    for (int i = 0; i < bits; ++i) {
+      long bit = (long)bits * c + i;
       uint32_t b = (v >> i) & 1u;
       row_words[bit / 32] |= b << (bit % 32);
     }

@@ -6,7 +6,9 @@ this module, and this module imports nothing from the library.
 
 Arrays are numpy.  Bit patterns of fp16 / bf16 values travel as ``uint16``
 arrays; packed codes as ``uint32`` arrays.  Format names are the plain strings
-``"f32" "bf16" "f16" "affine8_g64" "affine4_g64" "affine3_g64" "w4a16_g128"``.
+``"f32" "bf16" "f16" "affine8_g64" "affine4_g64" "affine3_g64" "w4a16_g128"``
+and the other MLX affine widths ``"affine2_g64" "affine5_g64" "affine6_g64"``
+(oracle only: the library's kernels read 8/4/3-bit and W4A16).
 """
 
 from __future__ import annotations
@@ -30,9 +32,14 @@ FMT = {
     "affine4_g64": 4,
     "affine3_g64": 5,
     "w4a16_g128": 6,
+    "affine2_g64": 7,
+    "affine5_g64": 8,
+    "affine6_g64": 9,
 }
-BITS = {"affine8_g64": 8, "affine4_g64": 4, "affine3_g64": 3, "w4a16_g128": 4}
-GROUP = {"affine8_g64": 64, "affine4_g64": 64, "affine3_g64": 64, "w4a16_g128": 128}
+BITS = {"affine8_g64": 8, "affine4_g64": 4, "affine3_g64": 3, "w4a16_g128": 4,
+        "affine2_g64": 2, "affine5_g64": 5, "affine6_g64": 6}
+GROUP = {"affine8_g64": 64, "affine4_g64": 64, "affine3_g64": 64, "w4a16_g128": 128,
+         "affine2_g64": 64, "affine5_g64": 64, "affine6_g64": 64}
 
 
 def build(force: bool = False) -> Path:

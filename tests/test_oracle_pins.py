@@ -78,7 +78,8 @@ def test_pack_w4a16_offset_binary():
     assert np.all(w[0, 1:] == 0)
 
 
-@pytest.mark.parametrize("fmt", ["affine8_g64", "affine4_g64", "affine3_g64", "w4a16_g128"])
+@pytest.mark.parametrize("fmt", ["affine8_g64", "affine4_g64", "affine3_g64", "w4a16_g128",
+                                 "affine2_g64", "affine5_g64", "affine6_g64"])
 def test_pack_every_code_every_position_bitstream(fmt):
     """A single code v at column c lands at stream bits [b*c, b*c + b) as v
     (offset-binary for W4A16), for every v and every position of a 64/128 group."""
@@ -597,3 +598,71 @@ def test_chain_gate_weight_closed_forms():
     assert 0.0 <= s[2] < 2 ** -50
     # sigmoid(1) = 0.7310585786... -> bf16 0.73046875 (0x3F3B)
     assert int(np.array([s[3]], np.float32).view(np.uint32)[0] >> 16) == 0x3F3B
+
+
+
+# --------------------------------------------------------------------------
+# MLX affine at the other widths the pages' loader reads (2/5/6-bit; oracle
+# only for now): one LSB-first bit stream per row, as for 3-bit
+
+WIDE = ["affine2_g64", "affine5_g64", "affine6_g64"]
+
+
+@pytest.mark.parametrize("fmt", WIDE)
+def test_pack_random_rows_bitstream_other_widths(fmt):
+    rng = np.random.default_rng(21)
+    bits, cols = O.BITS[fmt], 192
+    codes = rng.integers(0, 1 << bits, size=(7, cols), dtype=np.int32)
+    words = O.pack(fmt, codes)
+    assert words.shape == (7, cols * bits // 32)
+    for r in range(codes.shape[0]):
+        acc = 0
+        for c in range(cols):
+            acc |= int(codes[r, c]) << (bits * c)
+        assert stream_int(words[r]) == acc
+    assert np.array_equal(O.unpack(fmt, words, cols), codes)
+    with pytest.raises(ValueError):
+        O.pack(fmt, np.full((1, 64), 1 << bits, np.int32))
+
+
+@pytest.mark.parametrize("fmt", WIDE)
+def test_dequant_other_widths_exact(fmt):
+    rng = np.random.default_rng(22)
+    bits, rows, cols = O.BITS[fmt], 6, 256
+    codes = rng.integers(0, 1 << bits, size=(rows, cols), dtype=np.int32)
+    s = (np.abs(rng.standard_normal((rows, cols // 64))) * 0.01).astype(np.float16)
+    b = (rng.standard_normal((rows, cols // 64)) * 0.1).astype(np.float16)
+    got = O.dequant(fmt, O.pack(fmt, codes), s.view(np.uint16), b.view(np.uint16), rows, cols)
+    for r in range(rows):
+        for c in range(0, cols, 37):
+            want = Fraction(float(s[r, c // 64])) * codes[r, c] + Fraction(float(b[r, c // 64]))
+            assert Fraction(got[r, c]) == want
+
+
+def test_same_codes_at_every_width_dequantise_equally():
+    # codes 0..3 stored at every width from 2 to 8 bits decode to the same
+    # weights (the widening control, across all widths)
+    rng = np.random.default_rng(23)
+    rows, cols = 3, 128
+    codes = rng.integers(0, 4, size=(rows, cols), dtype=np.int32)
+    s = (np.abs(rng.standard_normal((rows, cols // 64))) * 0.01).astype(np.float16).view(np.uint16)
+    b = (rng.standard_normal((rows, cols // 64)) * 0.1).astype(np.float16).view(np.uint16)
+    ref = O.dequant("affine2_g64", O.pack("affine2_g64", codes), s, b, rows, cols)
+    for fmt in ["affine3_g64", "affine4_g64", "affine5_g64", "affine6_g64", "affine8_g64"]:
+        got = O.dequant(fmt, O.pack(fmt, codes), s, b, rows, cols)
+        assert np.array_equal(got, ref), fmt
+
+
+def test_layer_codes_widened_across_widths_equal():
+    # the same 2-bit codes as 2-, 5- and 6-bit experts give the same layer output
+    L = synth.gen_layer(T=3, E=6, k=2, H=128, I=64, expert_fmt="affine3_g64", seed=24)
+    outs = []
+    for fmt in ["affine2_g64", "affine5_g64", "affine6_g64"]:
+        bank = synth.ExpertBank(fmt, L.E, L.I, L.H)
+        for src, dst in ((L.experts.w13, bank.w13), (L.experts.w2, bank.w2)):
+            for m in src:
+                dst.append(synth.QMatrix(fmt, m.rows, m.cols, codes=m.codes & 3,
+                                         scales=m.scales, biases=m.biases))
+        L2 = synth.LayerInputs(**{**L.__dict__, "experts": bank})
+        outs.append(_layer(L2)["out"])
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
