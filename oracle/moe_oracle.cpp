@@ -251,11 +251,31 @@ void matvec_rows(const double* W, long rows, long cols, const double* x, long T,
     }
 }
 
+// bf16 from fp32: round to nearest, ties to even; a NaN becomes the quiet NaN
+// 0x7FC0.  bf16 is the top half of the fp32 encoding, so widening is exact.
+static uint16_t f32_to_bf16_rne(float v) {
+  uint32_t u;
+  std::memcpy(&u, &v, 4);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0;
+  const uint32_t bias = 0x7FFFu + ((u >> 16) & 1u);
+  return uint16_t((u + bias) >> 16);
+}
+
+static float bf16_to_f32(uint16_t b) {
+  const uint32_t u = uint32_t(b) << 16;
+  float v;
+  std::memcpy(&v, &u, 4);
+  return v;
+}
+
+// An fp64 value through the engine's storage types: first fp32, then bf16.
+double via_f32_bf16(double v) { return (double)bf16_to_f32(f32_to_bf16_rne((float)v)); }
+
 }  // namespace
 
 extern "C" {
 
-int oracle_abi_version() { return 1; }
+int oracle_abi_version() { return 2; }
 
 int oracle_set_threads(int n) {
 #ifdef _OPENMP
@@ -332,17 +352,27 @@ int oracle_fp16_to_double(long n, const uint16_t* h, double* out) {
 // Router logits [803-gate]: l[t, e] = sum_h W_r[e, h] * x[t, h] + bias[e].
 // W_r is fp32, bf16 or affine-8 g64 (the 3-bit checkpoint's 8-bit router,
 // [803-run]).  bias (nullable) is a per-expert logit offset.
-int oracle_router_logits(int wfmt, long E, long H, const void* wq, const uint16_t* ws,
-                         const uint16_t* wb, const float* bias, long T,
-                         const double* x, double* logits) {
+// bf16_rows: the dequantised rows are first rounded to bf16 (through fp32),
+// as the engine stores its 8-bit router rows after loading them [803-gate].
+static int router_logits(int wfmt, long E, long H, const void* wq, const uint16_t* ws,
+                         const uint16_t* wb, const float* bias, long T, const double* x,
+                         double* logits, bool bf16_rows) {
   std::vector<double> W((size_t)E * H);
   int rc = dequant(wfmt, E, H, wq, ws, wb, W.data());
   if (rc) return rc;
+  if (bf16_rows)
+    for (double& v : W) v = via_f32_bf16(v);
   matvec_rows(W.data(), E, H, x, T, logits);
   if (bias)
     for (long t = 0; t < T; ++t)
       for (long e = 0; e < E; ++e) logits[t * E + e] += (double)bias[e];
   return 0;
+}
+
+int oracle_router_logits(int wfmt, long E, long H, const void* wq, const uint16_t* ws,
+                         const uint16_t* wb, const float* bias, long T,
+                         const double* x, double* logits) {
+  return router_logits(wfmt, E, H, wq, ws, wb, bias, T, x, logits, false);
 }
 
 // Top-k and routing weights [803-gate].  Experts are ordered by (logit desc,
@@ -370,19 +400,32 @@ int oracle_topk(long T, long E, long k, const double* logits, int32_t* idx, doub
 
 // Shared-expert gate [803-gate]: g_t = sum_h w_g[h] x[t, h] over the shared
 // gate row (affine-8 g64, bf16 or fp32), weight s_t = sigmoid(g_t).
-int oracle_shared_gate(int gfmt, long H, const void* gq, const uint16_t* gs,
+// bf16_chain: the gate row is rounded to bf16 like the router rows, and the
+// weight becomes bf16(sigmoid(bf16(g))) [803-gate] (sigmoid in fp64).
+static int shared_gate(int gfmt, long H, const void* gq, const uint16_t* gs,
                        const uint16_t* gb, long T, const double* x, double* logit,
-                       double* sg) {
+                       double* sg, bool bf16_chain) {
   std::vector<double> g((size_t)H);
   int rc = dequant(gfmt, 1, H, gq, gs, gb, g.data());
   if (rc) return rc;
+  if (bf16_chain)
+    for (double& v : g) v = via_f32_bf16(v);
   for (long t = 0; t < T; ++t) {
     double acc = 0.0;
     for (long h = 0; h < H; ++h) acc += g[h] * x[t * H + h];
     if (logit) logit[t] = acc;
-    sg[t] = 1.0 / (1.0 + std::exp(-acc));
+    if (bf16_chain)
+      sg[t] = via_f32_bf16(1.0 / (1.0 + std::exp(-via_f32_bf16(acc))));
+    else
+      sg[t] = 1.0 / (1.0 + std::exp(-acc));
   }
   return 0;
+}
+
+int oracle_shared_gate(int gfmt, long H, const void* gq, const uint16_t* gs,
+                       const uint16_t* gb, long T, const double* x, double* logit,
+                       double* sg) {
+  return shared_gate(gfmt, H, gq, gs, gb, T, x, logit, sg, false);
 }
 
 // One expert's SwiGLU MLP [803-gate] on dequantised weights.  w13 holds the
@@ -458,6 +501,9 @@ int oracle_bucket(long T, long k, long E, const int32_t* idx, int32_t* counts,
 // idx_override (nullable) replaces the computed top-k indices (weights are
 // then the softmax of this oracle's own logits over those indices); used
 // when fp32 logits on the GPU resolve a near tie differently.
+// round_bf16 selects the engine's bf16 rounding chain for the routing inputs
+// (router and gate rows, slot weights, shared weight); the logits, the
+// experts and the weighted sum stay fp64 and out stays unrounded.
 struct LayerArgs {
   long T, E, k, H, I;
   const double* x;                 // [T][H]
@@ -481,13 +527,18 @@ struct LayerArgs {
   double* y_slots;                 // [T][k][H]
   double* y_shared;                // [T][H]
   double* out;                     // [T][H]
+  // 1: the engine's bf16 rounding chain [803-gate] -- router and gate rows
+  // rounded to bf16, slot weights bf16(w), shared weight
+  // bf16(sigmoid(bf16(g))); 0: weights and gate kept exact.
+  int round_bf16;
 };
 
 int oracle_moe_layer(const LayerArgs* A) {
   const long T = A->T, E = A->E, k = A->k, H = A->H, I = A->I;
+  const bool rb = A->round_bf16 != 0;
   std::vector<double> logits((size_t)T * E);
-  int rc = oracle_router_logits(A->router_fmt, E, H, A->router_q, A->router_s, A->router_b,
-                                A->logit_bias, T, A->x, logits.data());
+  int rc = router_logits(A->router_fmt, E, H, A->router_q, A->router_s, A->router_b,
+                         A->logit_bias, T, A->x, logits.data(), rb);
   if (rc) return rc;
   std::vector<int32_t> idx((size_t)T * k);
   std::vector<double> w((size_t)T * k);
@@ -506,10 +557,12 @@ int oracle_moe_layer(const LayerArgs* A) {
       }
     }
   }
+  if (rb)
+    for (double& v : w) v = via_f32_bf16(v);
   std::vector<double> sg((size_t)T, 1.0);
   if (A->gate_q) {
-    rc = oracle_shared_gate(A->gate_fmt, H, A->gate_q, A->gate_s, A->gate_b, T, A->x,
-                            nullptr, sg.data());
+    rc = shared_gate(A->gate_fmt, H, A->gate_q, A->gate_s, A->gate_b, T, A->x, nullptr,
+                     sg.data(), rb);
     if (rc) return rc;
   }
 
@@ -575,6 +628,12 @@ int oracle_moe_layer(const LayerArgs* A) {
 }
 
 // ---------------------------------------------------------------------------
+// fp32 values rounded to bf16 (nearest, ties to even) and widened back.
+int oracle_round_bf16(long n, const float* in, float* out) {
+  for (long i = 0; i < n; ++i) out[i] = bf16_to_f32(f32_to_bf16_rne(in[i]));
+  return 0;
+}
+
 // The combine in the engine's own precision [803-gate]: the slots' fma sum in
 // fp32 -- slot order, the shared slot last -- rounded once to bf16.  Given the
 // slots' outputs and weights as fp32 values, every bit of the result is fixed
@@ -583,26 +642,6 @@ int oracle_moe_layer(const LayerArgs* A) {
 // the quiet NaN 0x7FC0.
 //   y [T*k][H], w [T][k], ysh [T][H] (nullable), sg [T] (nullable: weight 1),
 //   out [T][H] bf16 bit patterns.
-static uint16_t f32_to_bf16_rne(float v) {
-  uint32_t u;
-  std::memcpy(&u, &v, 4);
-  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0;
-  const uint32_t bias = 0x7FFFu + ((u >> 16) & 1u);
-  return uint16_t((u + bias) >> 16);
-}
-
-static float bf16_to_f32(uint16_t b) {
-  const uint32_t u = uint32_t(b) << 16;
-  float v;
-  std::memcpy(&v, &u, 4);
-  return v;
-}
-
-int oracle_round_bf16(long n, const float* in, float* out) {
-  for (long i = 0; i < n; ++i) out[i] = bf16_to_f32(f32_to_bf16_rne(in[i]));
-  return 0;
-}
-
 int oracle_combine_f32(long T, long k, long H, const float* y, const float* w,
                        const float* ysh, const float* sg, uint16_t* out) {
   if (T < 0 || k < 1 || H < 0) return -1;
@@ -616,8 +655,8 @@ int oracle_combine_f32(long T, long k, long H, const float* y, const float* w,
   return 0;
 }
 
-// The rounding chain that paragraph lists for the engine's routing: slot
-// weights rounded to bf16, the shared slot weighted by bf16(sigmoid(bf16(g)))
+// The engine's rounding chain for the shared slot [803-gate]: slot weights
+// rounded to bf16, the shared slot weighted by bf16(sigmoid(bf16(g)))
 // (the sigmoid evaluated in fp64 on the bf16 gate logit).
 int oracle_chain_gate_weight(long T, const float* g, float* s) {
   for (long t = 0; t < T; ++t) {

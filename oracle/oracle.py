@@ -42,6 +42,10 @@ GROUP = {"affine8_g64": 64, "affine4_g64": 64, "affine3_g64": 64, "w4a16_g128": 
          "affine2_g64": 64, "affine5_g64": 64, "affine6_g64": 64}
 
 
+# Layout version of the structures passed by pointer (LayerArgs).
+ABI_VERSION = 2
+
+
 def build(force: bool = False) -> Path:
     """Compile the oracle into ``oracle/libmoe_oracle.so`` (g++, OpenMP when present)."""
     if LIB.exists() and not force and LIB.stat().st_mtime >= SRC.stat().st_mtime:
@@ -65,6 +69,9 @@ def lib():
     if _lib is None:
         build()
         L = ctypes.CDLL(str(LIB))
+        if L.oracle_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"{LIB} is ABI {L.oracle_abi_version()}, this module wants "
+                               f"{ABI_VERSION}: rebuild it with oracle.build(force=True)")
         P = ctypes.c_void_p
         i64 = ctypes.c_long
         i32 = ctypes.c_int
@@ -243,18 +250,22 @@ class _LayerArgs(ctypes.Structure):
                 ("gate_fmt", ctypes.c_int), ("gate_q", P), ("gate_s", P), ("gate_b", P),
                 ("idx_override", P),
                 ("logits", P), ("idx", P), ("w", P), ("sg", P), ("y_slots", P),
-                ("y_shared", P), ("out", P)]
+                ("y_shared", P), ("out", P),
+                ("round_bf16", ctypes.c_int)]
 
 
 def moe_layer(x: np.ndarray, k: int, router: dict, experts: dict, shared: dict | None = None,
               gate: dict | None = None, logit_bias=None, idx_override=None,
-              want_slots: bool = False) -> dict:
+              want_slots: bool = False, round_bf16: bool = False) -> dict:
     """Whole layer in fp64.
 
     x: float64 [T, H] (already decoded activations).
     router: {'fmt','q','s','b','rows'=E,'cols'=H}.
     experts: {'fmt','E','I','w13','s13','b13','w2','s2','b2'} (per-expert blocks stacked).
     shared: same keys for one expert (or None); gate: matrix dict (or None).
+    round_bf16: the engine's bf16 rounding chain for the routing inputs
+    (router and gate rows rounded to bf16, w -> bf16(w), the shared weight
+    bf16(sigmoid(bf16(g)))); logits, experts and the sum stay fp64.
     """
     x = _c(x, np.float64)
     T, H = x.shape
@@ -295,6 +306,7 @@ def moe_layer(x: np.ndarray, k: int, router: dict, experts: dict, shared: dict |
     a.logits, a.idx, a.w, a.sg = P(out["logits"]), P(out["idx"]), P(out["w"]), P(out["sg"])
     a.y_slots = P(out["y_slots"]) if want_slots else None
     a.y_shared, a.out = P(out["y_shared"]), P(out["out"])
+    a.round_bf16 = int(bool(round_bf16))
     _check(lib().oracle_moe_layer(ctypes.byref(a)), "moe_layer")
     return out
 

@@ -602,6 +602,126 @@ def test_chain_gate_weight_closed_forms():
 
 
 # --------------------------------------------------------------------------
+# The layer under the engine's bf16 rounding chain (round_bf16=True): router
+# and gate rows rounded to bf16, slot weights bf16(w), shared weight
+# bf16(sigmoid(bf16(g))).  Values below are worked by hand from the bf16
+# encoding (8 significant bits, round to nearest even).
+
+def _is_bf16(v) -> bool:
+    f = np.asarray(v, np.float64).astype(np.float32)
+    return bool(np.all(f.astype(np.float64) == np.asarray(v, np.float64))
+                and np.all((f.view(np.uint32) & 0xFFFF) == 0))
+
+
+def test_layer_round_bf16_closed_form():
+    # the slot-order case above under the chain: the router entry ln 3
+    # (fp32 0x3F8C9F54) is stored as bf16 0x3F8D = 1 + 13/128, so the
+    # weights are sigmoid(+-141/128) = 0.750554.. and 0.249446.., which round
+    # to 0.75 (0x3F40) and 255/1024 (0x3E7F); expert 0 is zero, so
+    # out = 0.75 * M(x) exactly
+    H, I, E = 128, 64, 4
+    L = synth.gen_layer(T=1, E=E, k=2, H=H, I=I, expert_fmt="affine4_g64", seed=12)
+    x_bits = np.zeros((1, H), np.uint16)
+    x_bits[0, 0] = 0x3F80
+    L.x = x_bits
+    W = np.zeros((E, H), np.float32)
+    W[:, 0] = [0.0, math.log(3.0), -30.0, -40.0]
+    L.router = synth.QMatrix("f32", E, H, values=W)
+    z = L.experts.w13[0]
+    L.experts.w13[0] = synth.QMatrix(z.fmt, z.rows, z.cols, codes=np.zeros_like(z.codes),
+                                     scales=np.zeros_like(z.scales), biases=np.zeros_like(z.biases))
+    r = _layer(L, round_bf16=True)
+    assert list(r["idx"][0]) == [1, 0]
+    assert r["logits"][0, 1] == 1 + 13 / 128
+    assert list(r["w"][0]) == [0.75, 255 / 1024]
+    x = O.act_to_double("bf16", L.x)
+    _, M = _np_swiglu(_dense(L.experts.w13[1]), _dense(L.experts.w2[1]), x)
+    assert np.allclose(r["out"], 0.75 * M, rtol=1e-12, atol=1e-15)
+    # without the chain slot 1 keeps 1 / (exp(l1) + 1) ~ 1/4, l1 = fp32(ln 3):
+    # the 255/1024 above comes from the router row's rounding
+    r0 = _layer(L)
+    assert abs(r0["w"][0, 1] - 0.25) < 1e-8
+
+
+def test_layer_round_bf16_flat_row_thirds():
+    # a zero router gives a flat row: ids 0..k-1 and weights 1/3, stored as
+    # bf16 0x3EAB = 171/512 (1/3 = fp32 0x3EAAAAAB rounds up)
+    L = synth.gen_layer(T=3, E=6, k=3, H=128, I=64, expert_fmt="affine4_g64", seed=21)
+    L.router = synth.QMatrix("f32", 6, 128, values=np.zeros((6, 128), np.float32))
+    r = _layer(L, round_bf16=True)
+    assert np.all(r["idx"] == np.array([0, 1, 2], np.int32))
+    assert np.all(r["w"] == 171 / 512)
+    assert np.all(_layer(L)["w"] == 1 / 3)
+
+
+def test_layer_round_bf16_gate_closed_forms():
+    # gate row (1, 3 * 2^-9, 0, ...) in bf16: s_t = bf16(sigmoid(bf16(g_t)));
+    # x = 0 -> g = 0 -> 1/2; x = e_0 -> g = 1 -> sigmoid 0.73106.. -> 187/256;
+    # x = e_0 + e_1 -> g = 1 + 3 * 2^-9, which bf16 holds only as 1 + 2^-7
+    # (0.75 ulp rounds up), sigmoid 0.73259.. -> 188/256 (rounding after the
+    # sigmoid alone would give sigmoid(g) = 0.73220.. -> 187/256)
+    H = 128
+    L = synth.gen_layer(T=3, E=4, k=2, H=H, I=64, expert_fmt="affine4_g64",
+                        shared_fmt="affine4_g64", gate_fmt="bf16", seed=22)
+    g_row = np.zeros((1, H), np.uint16)
+    g_row[0, :2] = [0x3F80, 0x3BC0]
+    L.gate = synth.QMatrix("bf16", 1, H, values=g_row)
+    x_bits = np.zeros((3, H), np.uint16)
+    x_bits[1, 0] = 0x3F80
+    x_bits[2, :2] = 0x3F80
+    L.x = x_bits
+    r = _layer(L, round_bf16=True)
+    assert list(r["sg"]) == [0.5, 187 / 256, 188 / 256]
+    r0 = _layer(L)
+    assert r0["sg"][0] == 0.5
+    assert abs(r0["sg"][1] - 1 / (1 + math.exp(-1.0))) < 1e-15
+
+
+def test_layer_round_bf16_gate_row_rounded():
+    # gate row (1 + 2^-8 + 2^-10, -1, 0, ...) in fp32 and x = (8, 8, 0, ...):
+    # the chain stores the first entry as bf16 1 + 2^-7 (0.625 ulp rounds up),
+    # so g = 8 * 2^-7 = 1/16 and s = bf16(sigmoid(1/16)) = bf16(0.515620..)
+    # = 132/256; the exact row gives g = 2^-5 + 2^-7 and s = sigmoid(g)
+    H = 128
+    L = synth.gen_layer(T=1, E=4, k=2, H=H, I=64, expert_fmt="affine4_g64",
+                        shared_fmt="affine4_g64", gate_fmt="f32", seed=23)
+    g_row = np.zeros((1, H), np.float32)
+    g_row[0, :2] = [1 + 2 ** -8 + 2 ** -10, -1.0]
+    L.gate = synth.QMatrix("f32", 1, H, values=g_row)
+    x_bits = np.zeros((1, H), np.uint16)
+    x_bits[0, :2] = 0x4100  # 8.0
+    L.x = x_bits
+    assert _layer(L, round_bf16=True)["sg"][0] == 132 / 256
+    assert abs(_layer(L)["sg"][0] - 1 / (1 + math.exp(-(2 ** -5 + 2 ** -7)))) < 1e-15
+
+
+def test_layer_round_bf16_weights_are_bf16_and_used_in_out():
+    L = synth.gen_layer(T=6, E=16, k=4, H=256, I=64, expert_fmt="affine4_g64",
+                        shared_fmt="affine4_g64", gate_fmt="affine8_g64", seed=24)
+    r = _layer(L, round_bf16=True, want_slots=True)
+    assert _is_bf16(r["w"]) and _is_bf16(r["sg"])
+    # the chain moves each weight by at most half a bf16 ulp of the exact one
+    # when the picks agree (the router rows differ by their own rounding)
+    r0 = _layer(L)
+    if np.array_equal(r["idx"], r0["idx"]):
+        assert np.all(np.abs(r["w"] - r0["w"]) <= 2 ** -8 * r0["w"] + 2 ** -8 * 0.02)
+    ref = np.einsum("tk,tkh->th", r["w"], r["y_slots"]) + r["sg"][:, None] * r["y_shared"]
+    assert np.allclose(r["out"], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_layer_round_bf16_is_identity_on_bf16_exact_routing():
+    # a zero router (flat row, k = 8: weights 1/8) and a zero gate row
+    # (weight 1/2) are bf16 values already: the chain changes nothing
+    L = synth.gen_layer(T=2, E=8, k=8, H=128, I=64, expert_fmt="affine4_g64",
+                        shared_fmt="affine4_g64", gate_fmt="affine8_g64", seed=25)
+    L.router = synth.QMatrix("bf16", 8, 128, values=np.zeros((8, 128), np.uint16))
+    L.gate = synth.QMatrix("bf16", 1, 128, values=np.zeros((1, 128), np.uint16))
+    a, b = _layer(L, round_bf16=True), _layer(L)
+    assert np.all(a["w"] == 0.125) and np.all(a["sg"] == 0.5)
+    assert np.array_equal(a["out"], b["out"])
+
+
+# --------------------------------------------------------------------------
 # MLX affine at the other widths the pages' loader reads (2/5/6-bit; oracle
 # only for now): one LSB-first bit stream per row, as for 3-bit
 
