@@ -37,7 +37,8 @@
 // torch's conversion, fp32 combine cases that only the fused multiply-add,
 // the slot order or the shared slot's place decide, 2/5/6-bit streams over
 // every code at every position, exact dequantisation at every width, the
-// same codes at every width giving the same weights and layer output).  None
+// same codes at every width giving the same weights and layer output, the
+// layer's bf16 rounding-chain option on hand-worked bf16 closed forms).  None
 // is unpinned.
 
 #include <cmath>
