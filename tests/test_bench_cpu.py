@@ -1,0 +1,60 @@
+"""Host-side arithmetic of bench.py (no GPU): the algorithmic bytes behind the
+roofline figure and the guard that drops a stale DRAM-traffic record."""
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+# bytes per quantisation group, from the formats' definitions: codes at their
+# width, then one fp16 scale (and one fp16 bias for the affine formats)
+@pytest.mark.parametrize("fmt,per_group,G", [
+    ("affine8_g64", 64 + 4, 64),
+    ("affine4_g64", 32 + 4, 64),
+    ("affine3_g64", 24 + 4, 64),
+    ("w4a16_g128", 64 + 2, 128),
+])
+def test_matrix_bytes_per_group(fmt, per_group, G):
+    for rows, cols in [(1, 2048), (256, 2048), (2048, 512), (1024, 256)]:
+        assert bench.matrix_bytes(fmt, rows, cols) == rows * cols // G * per_group
+
+
+def test_matrix_bytes_dense_and_absent():
+    assert bench.matrix_bytes("f32", 256, 2048) == 2 * 1024 * 1024
+    assert bench.matrix_bytes("bf16", 1, 2048) == 4096
+    assert bench.matrix_bytes("f16", 3, 8) == 48
+    assert bench.matrix_bytes(None, 256, 2048) == 0
+
+
+def test_expert_bytes_at_layer_shape():
+    # gate, up and down of one expert: 3 * 512 * 2048 = 3,145,728 weights
+    n = 3 * 512 * 2048
+    assert bench.expert_bytes("affine4_g64") == n // 64 * 36 == 1_769_472
+    assert bench.expert_bytes("affine3_g64") == n // 64 * 28 == 1_376_256
+    assert bench.expert_bytes("w4a16_g128") == n // 128 * 66 == 1_622_016
+
+
+def test_kernel_source_hash_tracks_every_source():
+    base = bench.kernel_source_hash()
+    assert base == bench.kernel_source_hash()
+    real = lambda rel: open(os.path.join(ROOT, rel), "rb").read()  # noqa: E731
+    for target in ("include/moe_gb300.h", "bit_affine_quantized_fp32_gb300/csrc/decode.cu"):
+        changed = lambda rel, t=target: real(rel) + (b" " if rel == t else b"")  # noqa: E731
+        assert bench.kernel_source_hash(changed) != base
+
+
+def test_captured_traffic_needs_matching_sources(tmp_path, monkeypatch):
+    rec = {"source_sha256": "0" * 64, "dram_bytes_per_launch": 123}
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "k_decode_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda read=None: "f" * 64)
+    assert bench.captured_traffic() is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda read=None: "0" * 64)
+    assert bench.captured_traffic() == 123
