@@ -383,7 +383,11 @@ def run_gpu(args, ws_world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16 x, 4-bit codes, fp32 accumulate" if act == "bf16" else "f16 x, int4 codes, fp32 accumulate",
+        "dtype": act,
+        "arith": (("%s activations times the exact integer codes (mma.sync), fp32 "
+                   "accumulation, per-group scale and bias in fp32" % act) if T <= 32 else
+                  "dequantised weights and h as 16-bit hi + lo parts (tcgen05), fp32 "
+                  "accumulation in tensor memory"),
         "data": "synthetic (seeded; random-init weights of the layer's shapes)",
         "config": {"workload": args.workload, "tokens": T, "experts": E, "top_k": K_TOP,
                    "hidden": H, "inter": I, "expert_fmt": cfg["expert_fmt"],
