@@ -197,29 +197,42 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 
-class Bank:
+class RawBank:
+    """Weight bank b of a workload in its canonical stored form (the seeded
+    generators' tensors on `device`); the oracle reads these.  No library
+    call is made here."""
     def __init__(self, cfg: dict, b: int, device):
-        import torch
-        from bit_affine_quantized_fp32_gb300 import capi, synth
+        from bit_affine_quantized_fp32_gb300 import synth
         seed = 1000 + 97 * b + cfg["seed"]
         self.cfg = cfg
-        r = synth.device_matrix(cfg["router_fmt"], E, H, seed, device)
-        self.router = capi.QMatrix(cfg["router_fmt"], E, H, r["q"], r["s"], r["b"])
+        self.raw = {"router": synth.device_matrix(cfg["router_fmt"], E, H, seed, device),
+                    "experts": synth.device_bank(cfg["expert_fmt"], E, I, H, seed + 2, device)}
         self.bias = synth.device_zipf_bias(E, seed + 1, device) if cfg["zipf"] else None
-        ex = synth.device_bank(cfg["expert_fmt"], E, I, H, seed + 2, device)
+        if cfg["shared_fmt"]:
+            self.raw["shared"] = synth.device_bank(cfg["shared_fmt"], 1, I, H, seed + 3, device)
+        if cfg["gate_fmt"]:
+            self.raw["gate"] = synth.device_matrix(cfg["gate_fmt"], 1, H, seed + 4, device)
+
+
+class Bank(RawBank):
+    """The same bank as the library's handles, experts repacked to the tiled
+    layout on the GPU."""
+    def __init__(self, cfg: dict, b: int, device):
+        import torch
+        from bit_affine_quantized_fp32_gb300 import capi
+        super().__init__(cfg, b, device)
+        r, ex = self.raw["router"], self.raw["experts"]
+        self.router = capi.QMatrix(cfg["router_fmt"], E, H, r["q"], r["s"], r["b"])
         self.experts = capi.ExpertBank(cfg["expert_fmt"], E, I, H, ex["w13"], ex["s13"], ex["b13"],
                                        ex["w2"], ex["s2"], ex["b2"]).tiled()
-        self.raw = {"router": r, "experts": ex}
         self.shared = self.gate = None
         if cfg["shared_fmt"]:
-            sh = synth.device_bank(cfg["shared_fmt"], 1, I, H, seed + 3, device)
+            sh = self.raw["shared"]
             self.shared = capi.ExpertBank(cfg["shared_fmt"], 1, I, H, sh["w13"], sh["s13"],
                                           sh["b13"], sh["w2"], sh["s2"], sh["b2"]).tiled()
-            self.raw["shared"] = sh
         if cfg["gate_fmt"]:
-            g = synth.device_matrix(cfg["gate_fmt"], 1, H, seed + 4, device)
+            g = self.raw["gate"]
             self.gate = capi.QMatrix(cfg["gate_fmt"], 1, H, g["q"], g["s"], g["b"])
-            self.raw["gate"] = g
         torch.cuda.synchronize()
 
 
@@ -485,7 +498,10 @@ def xs_to_np(xs, act):
 
 def run_reference(args, ws_world, rank, local):
     """The oracle as it stands on the host cores, on the GPU arm's workload:
-    each step is one token of the batch through the whole layer."""
+    each step is one token of the batch through the whole layer.  The inputs
+    come from the same seeded generators as the GPU arm's, on the GPU when
+    there is one (the same values), else on the CPU (same laws); the library
+    is not used."""
     import torch
     from bit_affine_quantized_fp32_gb300 import synth
     cfg = dict(synth.WORKLOADS[args.workload])
@@ -494,10 +510,7 @@ def run_reference(args, ws_world, rank, local):
     device = torch.device("cuda", local) if have_gpu else torch.device("cpu")
     if have_gpu:
         torch.cuda.set_device(local)
-    bank = Bank(cfg, 0, device) if have_gpu else None
-    if bank is None:
-        print(json.dumps({"impl": "reference", "unavailable": "needs the device-side generators"}))
-        return
+    bank = RawBank(cfg, 0, device)
     xs = [synth.device_x(T, H, cfg["act"], 500 + 31 * i, device) for i in range(16)]
     xs_np = xs_to_np(xs, cfg["act"])
     time_oracle(bank, cfg, xs_np, 0, max_steps=max(0, args.warmup))
@@ -509,7 +522,7 @@ def run_reference(args, ws_world, rank, local):
         "value": round(tps, 3), "unit": "tokens/s", "n_gpus": ws_world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(el * 1e3 / max(1, steps), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)",
+        "data": "synthetic (seeded; generated on the %s)" % ("GPU" if have_gpu else "CPU"),
         "config": {"workload": args.workload, "tokens": T, "experts": E, "top_k": K_TOP,
                    "hidden": H, "inter": I, "parallelism": "host cores"},
         "cpu_baseline": {"value": round(tps, 3), "unit": "tokens/s", "cores": cores,

@@ -1,7 +1,9 @@
-"""Host-side arithmetic of bench.py (no GPU): the algorithmic bytes behind the
-roofline figure and the guard that drops a stale DRAM-traffic record."""
+"""bench.py without a GPU: the algorithmic bytes behind the roofline figure,
+the guard that drops a stale DRAM-traffic record, and the oracle (reference)
+arm's JSON line."""
 import json
 import os
+import subprocess
 import sys
 
 import pytest
@@ -58,3 +60,27 @@ def test_captured_traffic_needs_matching_sources(tmp_path, monkeypatch):
     assert bench.captured_traffic() is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda read=None: "0" * 64)
     assert bench.captured_traffic() == 123
+
+
+def test_reference_arm_line_on_cpu():
+    # the oracle arm needs no GPU and no library: inputs from the seeded
+    # generators on the CPU, one token per step through the whole layer
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "2", "--warmup", "1"], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in rec, key
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 1 and rec["steps"] == 2
+    assert rec["value"] > 0 and rec["unit"] == "tokens/s" and rec["higher_is_better"] is True
+    cb = rec["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == rec["value"]
+    assert cb["sample"]
+    assert rec["e2e"] == {"value": rec["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
+    assert rec["config"]["workload"] == bench.DEFAULT_WORKLOAD

@@ -71,5 +71,4 @@ def test_reference_arm_two_ranks_rank0_only():
     assert len(lines) == 1, r.stdout
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference"
-    # on a host without a GPU the arm says why it cannot run
-    assert "unavailable" in rec or rec.get("n_gpus") == 2
+    assert rec["n_gpus"] == 2 and rec["value"] > 0 and rec["steps"] == 1
