@@ -47,7 +47,6 @@ def parse():
     p.add_argument("--banks", type=int, default=8)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
-    p.add_argument("--sweep", action="store_true", help="also time the other decode workloads")
     return p.parse_args()
 
 
