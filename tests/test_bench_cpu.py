@@ -84,3 +84,16 @@ def test_reference_arm_line_on_cpu():
     assert rec["e2e"] == {"value": rec["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                           "d2h_bytes_per_step": 0}
     assert rec["config"]["workload"] == bench.DEFAULT_WORKLOAD
+
+
+def test_clock_record_parsing():
+    idle = "0, 2070, 2070, 150.00, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active"
+    capped = "0, 1965, 2070, 1398.20, 0x0000000000000004, Not Active, Not Active, Not Active, Active"
+    hot = "0, 1500, 2070, 900.00, 0x0000000000000020, Not Active, Not Active, Active, Not Active"
+    r = bench.parse_clock_lines([idle, capped, idle, "garbage", "", "0, [N/A], 2070"])
+    assert r == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                 "samples": 3}
+    r = bench.parse_clock_lines([hot, idle])
+    assert r["reasons"] == ["sw_thermal_slowdown"] and r["sm_mhz"] == (1500 + 2070) / 2
+    assert bench.parse_clock_lines([]) == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                                           "samples": 0}
