@@ -2,7 +2,7 @@
 //
 // A plain, slow, fp64 CPU reference of the routed-expert MoE layer over
 // low-bit affine-quantised weights.  Only the test suite, the package's
-// smoke() check and the CPU-baseline leg of bench.py may load it; the
+// smoke() check and bench.py's CPU-baseline and reference legs may load it; the
 // library's GPU path never does, and this file shares no code, header,
 // table or constant with the CUDA sources.
 //

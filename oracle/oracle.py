@@ -1,7 +1,7 @@
 """ctypes wrapper around the fp64 CPU oracle (``moe_oracle.cpp``).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
-CPU-baseline leg of ``bench.py`` use it.  The library's GPU path never imports
+CPU-baseline and reference legs of ``bench.py`` use it.  The library's GPU path never imports
 this module, and this module imports nothing from the library.
 
 Arrays are numpy.  Bit patterns of fp16 / bf16 values travel as ``uint16``
