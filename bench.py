@@ -34,6 +34,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "decode8_affine4_shared_zipf"
+OTHER_WORKLOADS = ["decode1_affine4", "decode4_affine3", "decode32_w4a16",
+                   "prefill512_affine4_zipf"]
 E, K_TOP, H, I = 256, 8, 2048, 512
 
 
@@ -44,9 +46,14 @@ def parse():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--also", default=",".join(OTHER_WORKLOADS),
+                   help="comma list of further workloads measured in the same run "
+                        "(summarised under 'workloads'), or 'none'")
+    p.add_argument("--other-steps", type=int, default=2000)
     p.add_argument("--banks", type=int, default=8)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--cpu-seconds", type=float, default=8.0,
+                   help="seconds of oracle work at all threads, and again at one thread")
     return p.parse_args()
 
 
@@ -105,17 +112,18 @@ def kernel_source_hash(read=None) -> str:
     return h.hexdigest()
 
 
-def captured_traffic():
-    """DRAM bytes per launch of the fused kernel from the committed ncu
-    summary, or None when the kernel sources changed since that capture."""
-    p = os.path.join(ROOT, "profiles", "k_decode_traffic.json")
+def captured_traffic(workload: str = DEFAULT_WORKLOAD):
+    """DRAM bytes per layer call of `workload` from the committed ncu record
+    (profiles/traffic_<workload>.json), or None when there is none or the
+    kernel sources changed since that capture."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
     try:
         rec = json.load(open(p))
     except (OSError, ValueError):
         return None
     if rec.get("source_sha256") != kernel_source_hash():
         return None
-    return int(rec["dram_bytes_per_launch"])
+    return int(rec["dram_bytes_per_step"])
 
 
 def matrix_bytes(fmt: str | None, rows: int, cols: int) -> int:
@@ -242,18 +250,45 @@ class Bank(RawBank):
         torch.cuda.synchronize()
 
 
-def run_gpu(args, ws_world, rank, local):
+def load_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def step_flops(cfg: dict, T: int) -> float:
+    """Algorithmic FLOPs of one layer call: every routed (token, expert) pair
+    and the shared expert run three I x H matrix-vector products (2 flops per
+    weight), the router one E x H."""
+    per_pair = 2.0 * 3 * I * H
+    return (T * K_TOP * per_pair + (T * per_pair if cfg["shared_fmt"] else 0.0)
+            + 2.0 * E * H * T + (2.0 * H * T if cfg["gate_fmt"] else 0.0))
+
+
+def launches_per_step(cfg: dict, T: int) -> int:
+    # one persistent launch per decode call (T <= 32); the prefill form:
+    # routing (router, top-k, bucket), the shared expert's two tensor-core
+    # GEMMs, tiles and sub-slots (2), the routed tensor-core GEMMs (2),
+    # activation sums, decode units for the light experts (2), combine
+    if T <= 32:
+        return 1
+    return 3 + (2 if cfg["shared_fmt"] else 0) + 8
+
+
+def measure(name: str, steps: int, warmup: int, nbanks: int, ws_world: int, rank: int,
+            device, keep: bool = False) -> dict:
+    """Time `steps` layer calls of workload `name` (after `warmup`), device-only
+    and end to end; returns the figures of one JSON line (and, with keep, the
+    banks and inputs for the CPU baseline)."""
     import torch
-    from bit_affine_quantized_fp32_gb300 import build as B
-    B.build()
     from bit_affine_quantized_fp32_gb300 import capi, synth
 
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    cfg = dict(synth.WORKLOADS[args.workload])
+    cfg = dict(synth.WORKLOADS[name])
     T = cfg["T"]
     act = cfg["act"]
-    banks = [Bank(cfg, b, device) for b in range(args.banks)]
+    banks = [Bank(cfg, b, device) for b in range(nbanks)]
     n_in = 16
     xs = [synth.device_x(T, H, act, 500 + 31 * i + rank, device) for i in range(n_in)]
     wsb = capi.moe_workspace_bytes(T, E, K_TOP, H, I)
@@ -284,86 +319,113 @@ def run_gpu(args, ws_world, rank, local):
              (expert_bytes(cfg["shared_fmt"]) if cfg["shared_fmt"] else 0) + 2 * T * H * 2)
     step_bytes = [u * eb + fixed for u in U]
 
-    def bytes_for(steps):
-        return sum(step_bytes[i % pairs] for i in range(steps))
+    def bytes_for(n):
+        return sum(step_bytes[i % pairs] for i in range(n))
 
-    # eager warm-up (sets kernel attributes outside capture)
-    for i in range(3):
+    for i in range(3):  # eager warm-up (sets kernel attributes outside capture)
         step(i)
     torch.cuda.synchronize()
 
     G = 64
 
-    def capture(n, start):
+    def capture(fn, n):
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream(device=device)
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
             with torch.cuda.graph(g, stream=s):
-                for j in range(n):
-                    step(start + j)
+                fn(n)
         torch.cuda.current_stream().wait_stream(s)
         return g
 
-    g_main = capture(G, 0)
-    rem = args.steps % G
-    g_rem = capture(rem, 0) if rem else None
-    wrem = args.warmup % G
-    g_wrem = capture(wrem, 0) if wrem else None
+    def plain(n):
+        for j in range(n):
+            step(j)
 
-    def run_steps(n, main, remg):
+    graphs = {}
+
+    def run_steps(fn, n):
         for _ in range(n // G):
-            main.replay()
+            graphs.setdefault((fn, G), capture(fn, G)).replay()
         if n % G:
-            remg.replay()
+            graphs.setdefault((fn, n % G), capture(fn, n % G)).replay()
 
-    # warm-up steps (untimed)
-    run_steps(args.warmup, g_main, g_wrem)
+    # bring clocks and memory out of their idle states with ~0.3 s of untimed
+    # calls before the counted warm-up steps
+    t_pre = time.perf_counter()
+    while time.perf_counter() - t_pre < 0.3:
+        run_steps(plain, G)
+        torch.cuda.synchronize()
+    run_steps(plain, warmup)
     torch.cuda.synchronize()
     barrier(ws_world)
 
-    clocks = ClockSampler(local)
-    clocks.start()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    graphs.setdefault((plain, G), capture(plain, G))
+    if steps % G:
+        graphs.setdefault((plain, steps % G), capture(plain, steps % G))
+    clocks = ClockSampler(device.index or 0)
+    clocks.start()
     barrier(ws_world)
     torch.cuda.synchronize()
     ev0.record()
-    run_steps(args.steps, g_main, g_rem)
+    run_steps(plain, steps)
     ev1.record()
     torch.cuda.synchronize()
     barrier(ws_world)
     ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
     ms_max = max_over_ranks(ms, ws_world)
-    tokens = T * args.steps * ws_world
-    value = tokens / (ms_max / 1e3)
-    step_ms = ms_max / args.steps
-    gbs = bytes_for(args.steps) / (ms / 1e3) / 1e9
+    value = T * steps * ws_world / (ms_max / 1e3)
 
-    # end to end through the C ABI with host buffers: pinned x in, out back, every step
+    # End to end through the C ABI with host buffers, every step: x from
+    # pinned host memory in, the output back to pinned host memory.  The
+    # copies of step j + 1 (in) and j (out) run on two copy streams while the
+    # layer call of step j runs, double-buffered on the device.
     x_host = [xs[i].cpu().pin_memory() for i in range(n_in)]
-    out_host = torch.empty((T, H), dtype=out.dtype).pin_memory()
-    x_dev = torch.empty_like(xs[0])
+    out_host = [torch.empty((T, H), dtype=out.dtype).pin_memory() for _ in range(2)]
+    xd = [torch.empty_like(xs[0]) for _ in range(2)]
+    od = [torch.empty_like(out) for _ in range(2)]
 
-    def e2e_step(i):
-        x_dev.copy_(x_host[i % n_in], non_blocking=True)
-        step(i, x=x_dev)
-        out_host.copy_(out, non_blocking=True)
+    def e2e(n):
+        main = torch.cuda.current_stream()
+        cin, cout = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+        cin.wait_stream(main)
+        cout.wait_stream(main)
+        k_done = [None] * n
+        h_done = [None] * (n + 1)
+        d_done = [None] * n
 
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    ge = torch.cuda.CUDAGraph()
-    s = torch.cuda.Stream(device=device)
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(ge, stream=s):
-            for j in range(G):
-                e2e_step(j)
-    torch.cuda.current_stream().wait_stream(s)
+        def h2d(j):
+            with torch.cuda.stream(cin):
+                if j >= 2:
+                    cin.wait_event(k_done[j - 2])
+                xd[j % 2].copy_(x_host[j % n_in], non_blocking=True)
+                h_done[j] = torch.cuda.Event()
+                h_done[j].record(cin)
+
+        h2d(0)
+        for j in range(n):
+            if j + 1 < n:
+                h2d(j + 1)
+            main.wait_event(h_done[j])
+            if j >= 2:
+                main.wait_event(d_done[j - 2])
+            step(j, x=xd[j % 2], o=od[j % 2])
+            k_done[j] = torch.cuda.Event()
+            k_done[j].record(main)
+            with torch.cuda.stream(cout):
+                cout.wait_event(k_done[j])
+                out_host[j % 2].copy_(od[j % 2], non_blocking=True)
+                d_done[j] = torch.cuda.Event()
+                d_done[j].record(cout)
+        main.wait_stream(cin)
+        main.wait_stream(cout)
+
+    n_e2e = max(G, (steps // G) * G)
+    ge = capture(e2e, G)
     ge.replay()
     torch.cuda.synchronize()
-    n_e2e = max(G, (args.steps // G) * G)
     barrier(ws_world)
     ev0.record()
     for _ in range(n_e2e // G):
@@ -373,43 +435,47 @@ def run_gpu(args, ws_world, rank, local):
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), ws_world)
     e2e_value = T * n_e2e * ws_world / (e2e_ms / 1e3)
 
-    # correctness of the timed configuration: the last step's output is finite
-    assert torch.isfinite(out.float()).all()
+    # the timed configuration ran cleanly: the last outputs are finite and the
+    # workspace reports no timeout
+    assert torch.isfinite(out.float()).all() and torch.isfinite(od[0].float()).all()
     assert capi.moe_get_device_status(ws) == 0
 
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except OSError:
-        pass
-    peak = float(peaks.get("hbm_gbs", 6800.0))
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-
-    # one persistent launch per layer call for decode batches (<= 32 tokens);
-    # the prefill form: routing (3), shared expert (2), tiles and sub-slots
-    # (2), tensor-core gate/up and down (2), activation sums, decode units for
-    # the light experts (2), combine
-    launches_per_step = 1 if T <= 32 else 3 + (2 if cfg["shared_fmt"] else 0) + 8
-    line = {
-        "metric": "MoE-layer tokens/s (%s %d, %s)" % (
-            "decode batch" if T <= 32 else "prefill window", T, cfg["expert_fmt"]),
-        "value": round(value, 1),
-        "unit": "tokens/s",
-        "n_gpus": ws_world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(step_ms, 6),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": act,
-        "arith": (("%s activations times the exact integer codes (mma.sync), fp32 "
-                   "accumulation, per-group scale and bias in fp32" % act) if T <= 32 else
-                  "dequantised weights and h as 16-bit hi + lo parts (tcgen05), fp32 "
-                  "accumulation in tensor memory"),
-        "data": "synthetic (seeded; random-init weights of the layer's shapes)",
-        "config": {"workload": args.workload, "tokens": T, "experts": E, "top_k": K_TOP,
+    peaks = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    hbm_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    gbs = bytes_for(steps) / (ms / 1e3) / 1e9
+    step_ms = ms_max / steps
+    if T <= 32:
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(gbs / hbm, 4), "traffic": captured_traffic(name),
+                "kernel": "k_decode: the whole layer in one persistent launch",
+                "peak_source": hbm_src, "target_frac": 0.70,
+                "algorithmic_bytes_per_step": round(float(np.mean(step_bytes)))}
+    else:
+        tf = float(peaks.get("bf16_tflops", 1900.0))
+        tf_sus = float(peaks.get("bf16_tflops_sustained", tf))
+        fl = step_flops(cfg, T)
+        tfs = fl / (step_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(tfs, 2), "peak": tf, "unit": "TFLOP/s",
+                "frac": round(tfs / tf, 4), "frac_of_sustained": round(tfs / tf_sus, 4),
+                "traffic": captured_traffic(name),
+                "kernel": "whole step (all launches of one layer call; the tcgen05 expert "
+                          "GEMMs lead)",
+                "peak_source": "measured" if "bf16_tflops" in peaks else "fallback",
+                "target_frac": 0.50, "algorithmic_flops_per_step": fl,
+                "hbm": {"achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                        "frac": round(gbs / hbm, 4),
+                        "algorithmic_bytes_per_step": round(float(np.mean(step_bytes)))}}
+    res = {
+        "name": name, "cfg": cfg, "T": T, "value": value, "ms_per_step": step_ms,
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
+                "copies": "pinned host x in and out back every step, on two copy streams "
+                          "overlapping the neighbouring steps' layer calls"},
+        "gpu_launches": launches_per_step(cfg, T) * steps,
+        "clocks": clk,
+        "config": {"workload": name, "tokens": T, "experts": E, "top_k": K_TOP,
                    "hidden": H, "inter": I, "expert_fmt": cfg["expert_fmt"],
                    "router_fmt": cfg["router_fmt"], "shared_fmt": cfg["shared_fmt"],
                    "gate_fmt": cfg["gate_fmt"], "zipf": cfg["zipf"],
@@ -417,19 +483,76 @@ def run_gpu(args, ws_world, rank, local):
                    "l2": "inputs larger than L2 (%d rotating weight banks, %.1f GB)" % (
                        len(banks), len(banks) * (E * eb + fixed) / 1e9),
                    "experts_touched_mean": round(float(np.mean(U)), 2)},
-        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gbs / peak, 4),
-                     "traffic": captured_traffic() if T <= 32 else None,
-                     "kernel": ("k_decode: the whole layer in one persistent launch" if T <= 32
-                                else "whole step (all launches of one layer call)"),
-                     "peak_source": peak_src,
-                     "algorithmic_bytes_per_step": round(float(np.mean(step_bytes)))},
-        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
     }
-    return line, banks, xs, cfg
+    if keep:
+        res["banks"], res["xs"] = banks, xs
+    else:
+        del banks, xs
+        graphs.clear()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return res
+
+
+def metric_name(T: int, fmt: str) -> str:
+    return "MoE-layer tokens/s (%s %d, %s)" % ("decode batch" if T <= 32 else "prefill window",
+                                               T, fmt)
+
+
+def arith_note(T: int, act: str) -> str:
+    if T <= 32:
+        return ("%s activations times the exact integer codes (mma.sync), fp32 accumulation, "
+                "per-group scale and bias in fp32" % act)
+    return ("dequantised weights and h as 16-bit hi + lo parts (tcgen05), fp32 accumulation "
+            "in tensor memory")
+
+
+def run_gpu(args, ws_world, rank, local):
+    import torch
+    from bit_affine_quantized_fp32_gb300 import build as B
+    B.build()
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    head = measure(args.workload, args.steps, args.warmup, args.banks, ws_world, rank, device,
+                   keep=True)
+    others = {}
+    for name in ([] if args.also == "none" else args.also.split(",")):
+        if name == args.workload or not name:
+            continue
+        T = int(__import__("bit_affine_quantized_fp32_gb300.synth",
+                           fromlist=["WORKLOADS"]).WORKLOADS[name]["T"])
+        n = args.other_steps if T <= 32 else max(64, args.other_steps // 4)
+        r = measure(name, n, args.warmup, args.banks, ws_world, rank, device)
+        others[name] = {"metric": metric_name(r["T"], r["cfg"]["expert_fmt"]),
+                        "value": round(r["value"], 1), "unit": "tokens/s",
+                        "ms_per_step": round(r["ms_per_step"], 6), "steps": n,
+                        "roofline": r["roofline"], "e2e": r["e2e"],
+                        "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
+                        "config": r["config"]}
+    line = {
+        "metric": metric_name(head["T"], head["cfg"]["expert_fmt"]),
+        "value": round(head["value"], 1),
+        "unit": "tokens/s",
+        "n_gpus": ws_world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(head["ms_per_step"], 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": head["cfg"]["act"],
+        "arith": arith_note(head["T"], head["cfg"]["act"]),
+        "data": "synthetic (seeded; random-init weights of the layer's shapes)",
+        "config": head["config"],
+        "roofline": head["roofline"],
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+    }
+    if others:
+        line["workloads"] = others
+    return line, head["banks"], head["xs"], head["cfg"]
 
 
 # ---------------------------------------------------------------------------
@@ -469,10 +592,10 @@ def oracle_inputs(bank, cfg):
 
 
 def time_oracle(bank, cfg, xs_np, seconds: float, max_steps: int | None = None,
-                tokens_per_step: int = 1):
+                tokens_per_step: int = 1, threads: int = 0):
     from oracle import oracle as O
     O.build()
-    cores = O.set_threads(0)
+    cores = O.set_threads(threads)
     r, ex, sh, g, bias = oracle_inputs(bank, cfg)
     done_tokens, steps = 0, 0
     t0 = time.perf_counter()
@@ -553,10 +676,15 @@ def main():
         xs_np = xs_to_np(xs, cfg["act"])
         tps, cores, steps, el = time_oracle(banks[0], cfg, xs_np, args.cpu_seconds,
                                             tokens_per_step=cfg["T"])
+        tps1, _, steps1, el1 = time_oracle(banks[0], cfg, xs_np, args.cpu_seconds,
+                                           tokens_per_step=cfg["T"], threads=1)
         line["cpu_baseline"] = {"value": round(tps, 3), "unit": "tokens/s", "cores": cores,
                                 "kind": "oracle",
                                 "sample": f"{steps} full decode batches of {cfg['T']} tokens "
-                                          f"on weight bank 0 ({el:.1f} s, fp64 C++ oracle)"}
+                                          f"on weight bank 0 ({el:.1f} s, fp64 C++ oracle, "
+                                          f"OpenMP over the batch's experts)",
+                                "single_thread": {"value": round(tps1, 3), "cores": 1,
+                                                  "sample": f"{steps1} batches ({el1:.1f} s)"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_world > 1:

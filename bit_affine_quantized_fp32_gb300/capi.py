@@ -19,11 +19,12 @@ FMT = {"f32": 0, "bf16": 1, "f16": 2, "affine8_g64": 3, "affine4_g64": 4,
        "affine3_g64": 5, "w4a16_g128": 6}
 MOE_FLAG_FORCE_DECODE = 1
 MOE_FLAG_UNFUSED = 2
+MOE_FLAG_ROUND_BF16 = 4
 MOE_DECODE_MAX_TOKENS = 32
 
 EXPORTS = [
     "moe_status_string", "moe_last_error", "moe_workspace_bytes", "moe_workspace_init",
-    "moe_get_device_status", "moe_route", "moe_route_static", "moe_topk_softmax", "moe_bucket",
+    "moe_workspace_set_wait_limit", "moe_get_device_status", "moe_route", "moe_route_static", "moe_topk_softmax", "moe_bucket",
     "moe_expert_mlp", "moe_shared_expert", "moe_experts_forward", "moe_layer_forward",
     "moe_pack_affine8_g64", "moe_unpack_affine8_g64", "moe_pack_affine4_g64",
     "moe_unpack_affine4_g64", "moe_pack_affine3_g64", "moe_unpack_affine3_g64",
@@ -63,8 +64,10 @@ def _load():
     L.moe_workspace_bytes.restype = c_size_t
     L.moe_workspace_bytes.argtypes = [c_int] * 5
     L.moe_workspace_init.argtypes = [P, c_size_t, P]
+    L.moe_workspace_set_wait_limit.argtypes = [P, c_size_t, ctypes.c_uint, P]
     L.moe_get_device_status.argtypes = [P, c_size_t, P, P]
-    L.moe_route.argtypes = [P, P, P, P, c_int, c_int, c_int, P, P, P, P, P, P, P, c_size_t, P]
+    L.moe_route.argtypes = [P, P, P, P, c_int, c_int, c_int, P, P, P, P, P, P, c_int, P, c_size_t,
+                            P]
     L.moe_route_static.argtypes = [P, P, P, P, c_int, c_int, c_int, P, P, P, P, P, P]
     L.moe_topk_softmax.argtypes = [P, c_int, c_int, c_int, P, P, P]
     L.moe_bucket.argtypes = [P, c_int, c_int, c_int, P, P, P]
@@ -171,6 +174,11 @@ def moe_workspace_init(ws, stream=None):
     _check(lib.moe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def moe_workspace_set_wait_limit(ws, limit_us: int, stream=None):
+    _check(lib.moe_workspace_set_wait_limit(_ptr(ws), ws.numel() * ws.element_size(),
+                                            int(limit_us), _stream(stream)))
+
+
 def moe_get_device_status(ws, stream=None) -> int:
     v = ctypes.c_int(-1)
     _check(lib.moe_get_device_status(_ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(v),
@@ -179,11 +187,12 @@ def moe_get_device_status(ws, stream=None) -> int:
 
 
 def moe_route(router: QMatrix, logit_bias, shared_gate: QMatrix | None, x, top_k: int, logits,
-              topk_idx, topk_w, shared_gate_w, bucket_offsets, bucket_perm, ws, stream=None):
+              topk_idx, topk_w, shared_gate_w, bucket_offsets, bucket_perm, ws, stream=None,
+              flags: int = 0):
     _check(lib.moe_route(router.ref(), _ptr(logit_bias), _ref(shared_gate), _ptr(x), act_code(x),
                          x.shape[0], top_k, _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
-                         _ptr(shared_gate_w), _ptr(bucket_offsets), _ptr(bucket_perm), _ptr(ws),
-                         ws.numel() * ws.element_size(), _stream(stream)))
+                         _ptr(shared_gate_w), _ptr(bucket_offsets), _ptr(bucket_perm), flags,
+                         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_route_static(router: QMatrix, logit_bias, shared_gate: QMatrix | None, x, top_k: int,

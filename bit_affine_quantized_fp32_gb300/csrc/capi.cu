@@ -6,19 +6,81 @@
 // refuses any width its kernels do not read (comment "Progress on the 4-bit
 // gate", last paragraph).
 
+#include <cuda.h>
+
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
 #include "decode.h"
+#include "host.h"
 #include "prefill.h"
 
 namespace moe {
 int router_ks(int H);
+
+// The driver's cuCtxGetCurrent and cuCtxGetId, reached through the runtime's
+// entry-point query (the library links no driver library of its own).
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
+  unsigned long long id = 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
 }
+
+cudaError_t ensure_dynamic_smem(const void* func, int bytes) {
+  struct Done {
+    unsigned long long ctx;
+    const void* func;
+    int bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Done> done;
+  unsigned long long ctx = current_context_id();
+  std::lock_guard<std::mutex> lock(mu);
+  if (ctx)
+    for (const Done& d : done)
+      if (d.ctx == ctx && d.func == func && d.bytes >= bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (!ctx) ctx = current_context_id();  // the call above made the primary context current
+  if (ctx) {
+    for (Done& d : done)
+      if (d.ctx == ctx && d.func == func) {
+        d.bytes = bytes;
+        return cudaSuccess;
+      }
+    done.push_back(Done{ctx, func, bytes});
+  }
+  return cudaSuccess;
+}
+
+}  // namespace moe
 
 using namespace moe;
 
@@ -343,6 +405,17 @@ moe_status moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
   return ok();
 }
 
+moe_status moe_workspace_set_wait_limit(void* ws, size_t ws_bytes, unsigned limit_us,
+                                        cudaStream_t stream) {
+  moe_status s = check_ws(ws, ws_bytes, kCtlBytes);
+  if (s) return s;
+  if (limit_us > 0x7FFFFFFFu)
+    return fail(MOE_ERR_INVALID_ARG, "limit_us=%u exceeds 2^31 - 1", limit_us);
+  MOE_CUDA(launch_store_word(static_cast<int*>(ws) + kCtlWaitLimit, int(limit_us), stream),
+           "wait-limit store");
+  return ok();
+}
+
 moe_status moe_get_device_status(void* ws, size_t ws_bytes, int* device_status,
                                  cudaStream_t stream) {
   moe_status s = check_ws(ws, ws_bytes, kCtlBytes);
@@ -366,7 +439,7 @@ moe_status moe_topk_softmax(const float* logits, int n_tokens, int n_experts, in
   if (n_tokens > 0 && (!logits || !topk_idx || !topk_w))
     return fail(MOE_ERR_INVALID_ARG, "logits/topk_idx/topk_w must not be NULL");
   MOE_CUDA(launch_topk(logits, nullptr, n_tokens, n_experts, top_k, topk_idx, topk_w, nullptr,
-                       stream),
+                       false, stream),
            "top-k kernel");
   return ok();
 }
@@ -390,9 +463,11 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
                      const moe_qmatrix* shared_gate, const void* x, int act, int n_tokens,
                      int top_k, float* logits, int32_t* topk_idx, float* topk_w,
                      float* shared_gate_w, int32_t* bucket_offsets, int32_t* bucket_perm,
-                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+                     int flags, void* ws, size_t ws_bytes, cudaStream_t stream) {
   moe_status s;
   if (!router) return fail(MOE_ERR_INVALID_ARG, "router is NULL");
+  if (flags & ~MOE_FLAG_ROUND_BF16) return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  const bool rb = (flags & MOE_FLAG_ROUND_BF16) != 0;
   const int E = router->rows, H = router->cols, T = n_tokens;
   if (T < 0) return fail(MOE_ERR_INVALID_ARG, "n_tokens=%d < 0", T);
   if (E < 1 || E > 256) return fail(MOE_ERR_INVALID_ARG, "router rows (experts)=%d not in 1..256", E);
@@ -429,9 +504,10 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
   R.H = H;
   R.logits = lg;
   R.gate_logit = gl;
+  R.round_bf16 = rb;
   MOE_CUDA(launch_router(R, stream), "router kernel");
   MOE_CUDA(launch_topk(lg, shared_gate ? gl : nullptr, T, E, top_k, topk_idx, topk_w,
-                       shared_gate ? shared_gate_w : nullptr, stream),
+                       shared_gate ? shared_gate_w : nullptr, rb, stream),
            "top-k kernel");
   MOE_CUDA(launch_bucket(topk_idx, T, top_k, E, bucket_offsets, bucket_perm, stream),
            "bucket kernel");
@@ -476,7 +552,9 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
   if (T < 0) return fail(MOE_ERR_INVALID_ARG, "n_tokens=%d < 0", T);
   if (top_k < 1 || top_k > 8 || top_k > E)
     return fail(MOE_ERR_INVALID_ARG, "top_k=%d not in 1..min(8, n_experts)", top_k);
-  if (flags & ~MOE_FLAG_FORCE_DECODE) return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if (flags & ~(MOE_FLAG_FORCE_DECODE | MOE_FLAG_ROUND_BF16))
+    return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  const bool rb = (flags & MOE_FLAG_ROUND_BF16) != 0;
   if (T == 0) return ok();
   if (!x || !topk_idx || !topk_w || !bucket_offsets || !bucket_perm || !out)
     return fail(MOE_ERR_INVALID_ARG, "x, routing and out pointers must not be NULL");
@@ -554,6 +632,7 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
     C.k = top_k;
     C.H = H;
     C.f16 = f16;
+    C.round_bf16 = rb;
     MOE_CUDA(launch_combine(C, stream), "combine kernel");
     return ok();
   }
@@ -587,6 +666,7 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
   C.k = top_k;
   C.H = H;
   C.f16 = f16;
+  C.round_bf16 = rb;
   MOE_CUDA(launch_combine(C, stream), "combine kernel");
   return ok();
 }
@@ -613,8 +693,9 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
   const WsLayout L = ws_layout(T, E, top_k, H, I);
   if ((s = check_ws(ws, ws_bytes, L.total))) return s;
   if (T == 0) return ok();
-  if (flags & ~(MOE_FLAG_FORCE_DECODE | MOE_FLAG_UNFUSED))
+  if (flags & ~(MOE_FLAG_FORCE_DECODE | MOE_FLAG_UNFUSED | MOE_FLAG_ROUND_BF16))
     return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  const bool rb = (flags & MOE_FLAG_ROUND_BF16) != 0;
   if (!(flags & MOE_FLAG_UNFUSED) && T <= MOE_DECODE_MAX_TOKENS) {
     // validate what moe_route / moe_experts_forward would, then one launch
     if ((s = check_hidden(H))) return s;
@@ -642,6 +723,7 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
     A.R.T = T;
     A.R.E = E;
     A.R.H = H;
+    A.R.round_bf16 = rb;
     int* status = static_cast<int*>(ws);
     uint16_t* hh = reinterpret_cast<uint16_t*>(wsp(ws, L.hh));
     uint16_t* hl = reinterpret_cast<uint16_t*>(wsp(ws, L.hl));
@@ -690,7 +772,8 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
   int32_t* offs = reinterpret_cast<int32_t*>(wsp(ws, L.offsets));
   int32_t* perm = reinterpret_cast<int32_t*>(wsp(ws, L.perm));
   s = moe_route(router, logit_bias, shared_gate, x, act, T, top_k, nullptr, idx, w,
-                shared_gate ? sgw : nullptr, offs, perm, ws, ws_bytes, stream);
+                shared_gate ? sgw : nullptr, offs, perm, flags & MOE_FLAG_ROUND_BF16, ws, ws_bytes,
+                stream);
   if (s) return s;
   float* ysh = nullptr;
   if (shared) {
@@ -700,7 +783,8 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
   }
   return moe_experts_forward(experts, x, act, T, top_k, idx, w, offs, perm, ysh,
                              shared && shared_gate ? sgw : nullptr, out,
-                             flags & MOE_FLAG_FORCE_DECODE, ws, ws_bytes, stream);
+                             flags & (MOE_FLAG_FORCE_DECODE | MOE_FLAG_ROUND_BF16), ws, ws_bytes,
+                             stream);
 }
 
 #define MOE_PACK_PAIR(NAME, FMT, CT)                                                           \
@@ -800,8 +884,9 @@ moe_status moe_unrepack_bank(const moe_expert_bank* tiled, void* w13, void* s13,
 // scratch buffer -- the fp32 logits and shared-gate logits between the router
 // kernel and the top-k kernel -- lives in this file-scope device array.
 // Nothing in it has to start at zero: every element a call reads was written
-// earlier in the same call.  There is one array per device, so calls that
-// overlap in time on one device (two streams, two host threads) race on it.
+// earlier in the same call.  There is one copy of the array per CUDA context
+// (it belongs to the module loaded into that context), so calls that overlap
+// in time within one context (two streams, two host threads) race on it.
 namespace {
 
 constexpr int kStaticRouteMaxLogits = 32 * 256;  // T * E of at most 32 tokens x 256 experts
@@ -809,22 +894,33 @@ constexpr int kStaticRouteMaxTokens = 32;        // shared-gate logits
 __device__ __align__(256) float g_static_route_scratch[kStaticRouteMaxLogits +
                                                        kStaticRouteMaxTokens];
 
-// The array's device address, looked up once per device with that device
-// current.  The first call on a device does this set-up (a synchronous
-// runtime query), so it should run before any stream capture.
+// The array's device address in the current context.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress once per context (the first call in a context does
+// this synchronous runtime query, so it should come before any stream
+// capture) and cached under the context's id: after cudaDeviceReset, or in a
+// driver-API context, the module is loaded again and the array may sit
+// elsewhere.
 moe_status static_route_scratch(float** out) {
+  struct Entry {
+    unsigned long long ctx;
+    float* addr;
+  };
   static std::mutex mu;
-  static float* addr[64] = {nullptr};
-  int dev = 0;
-  MOE_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(MOE_ERR_CUDA, "device ordinal %d out of range", dev);
+  static std::vector<Entry> cache;
+  unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    MOE_CUDA(cudaGetSymbolAddress(&p, g_static_route_scratch), "cudaGetSymbolAddress");
-    addr[dev] = static_cast<float*>(p);
-  }
-  *out = addr[dev];
+  if (ctx)
+    for (const Entry& c : cache)
+      if (c.ctx == ctx) {
+        *out = c.addr;
+        return MOE_OK;
+      }
+  void* p = nullptr;
+  MOE_CUDA(cudaGetSymbolAddress(&p, g_static_route_scratch), "cudaGetSymbolAddress");
+  if (!ctx) ctx = current_context_id();  // the lookup made the primary context current
+  if (ctx) cache.push_back(Entry{ctx, static_cast<float*>(p)});
+  *out = static_cast<float*>(p);
   return MOE_OK;
 }
 
@@ -880,7 +976,7 @@ moe_status moe_route_static(const moe_qmatrix* router, const float* logit_bias,
   R.gate_logit = scratch + kStaticRouteMaxLogits;
   MOE_CUDA(launch_router(R, stream), "router kernel");
   MOE_CUDA(launch_topk(R.logits, shared_gate ? R.gate_logit : nullptr, T, E, top_k, topk_idx,
-                       topk_w, shared_gate ? shared_gate_w : nullptr, stream),
+                       topk_w, shared_gate ? shared_gate_w : nullptr, false, stream),
            "top-k kernel");
   MOE_CUDA(launch_bucket(topk_idx, T, top_k, E, bucket_offsets, bucket_perm, stream),
            "bucket kernel");

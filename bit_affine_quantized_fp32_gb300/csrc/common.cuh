@@ -12,6 +12,11 @@ namespace moe {
 
 constexpr int kWarp = 32;
 
+// Control words of a workspace (int32 indices into its first 16 KiB, which
+// moe_workspace_init zeroes).
+constexpr int kCtlStatus = 0;      // device status: MOE_OK or MOE_ERR_TIMEOUT
+constexpr int kCtlWaitLimit = 36;  // limit of every bounded wait, microseconds (0: 1 s)
+
 // ---------------------------------------------------------------------------
 // Workspace layout.  Every region is 256-byte aligned; the layout depends only
 // on the call's shape, so any workspace of moe_workspace_bytes(max_tokens, ...)
@@ -113,6 +118,11 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
 
 __device__ __forceinline__ float act_to_float(uint16_t v, bool f16) {
   return f16 ? half_bits_to_float(v) : bf16_bits_to_float(v);
+}
+
+// v rounded to bf16 (nearest, ties to even) and widened back to fp32.
+__device__ __forceinline__ float round_bf16(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
 }
 
 __device__ __forceinline__ uint16_t float_to_act_bits(float v, bool f16) {

@@ -31,6 +31,7 @@
 
 #include "route.cuh"
 #include "decode.h"
+#include "host.h"
 
 namespace moe {
 
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   const int T = A.R.T, H = A.R.H, NE = A.R.E;
   const bool gate = A.R.gq != nullptr;
   const int E1 = NE + (gate ? 1 : 0);
-  engine_init(E, P.S);
+  engine_init(E, P.S, A.ctrl);
   const EngineMem M{smem, smem + P.nob * P.OB, P.OB, P.nob, P.SB, P.S};
   fence_proxy_async();
   __syncthreads();
@@ -221,13 +222,14 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   const int n_tasks = nrb_router + nx;
 
   // ---- routing, redundantly in every CTA
-  if (tid == 0) wait_counter(ctrl + kCtlPhase0, n_tasks, &E.skip, status);
+  if (tid == 0) wait_counter(ctrl + kCtlPhase0, n_tasks, &E.wc, status);
   __syncthreads();
   {
     int(*wc)[256] = reinterpret_cast<int(*)[256]>(smem);
     const bool first = blockIdx.x == 0;
     route_table_cta(A.R.logits, gate ? A.R.gate_logit : nullptr, T, NE, A.k,
-                    first ? A.user_idx : nullptr, first ? A.user_w : nullptr, wc, RT);
+                    first ? A.user_idx : nullptr, first ? A.user_w : nullptr, wc, RT,
+                    A.R.round_bf16 != 0);
   }
   fence_proxy_async();  // routing scratch (generic writes) before TMA reuses it
   __syncthreads();
@@ -263,19 +265,8 @@ cudaError_t launch_decode_t(const DecodeArgs& A, int sms, cudaStream_t st) {
   const EnginePlan P = decode_plan(A);
   if (P.S < 2) return cudaErrorInvalidValue;
   const int smem = P.bytes();
-  // raise the dynamic shared-memory limit once per device (not a stream
-  // operation, so later calls can be captured in graphs)
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const cudaError_t e = ensure_dynamic_smem((const void*)k_decode<FMT, FMT_SH, F16A>, smem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (configured[dev] < smem) {
-    e = cudaFuncSetAttribute(k_decode<FMT, FMT_SH, F16A>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = smem;
-  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(unsigned(sms));
   cfg.blockDim = dim3(kEngineThreads);

@@ -142,30 +142,58 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, unsigned pari
   return ok != 0;
 }
 
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // default: one second
+constexpr unsigned long long kDrainLimitNs = 100000000ull;  // copies in flight at exit
 
-// Wait for phase `parity` of an mbarrier; after kWaitLimitNs, record a timeout
-// and return false.  `skip` (shared) turns every later wait into a no-op once
-// a timeout has happened, so the kernel finishes (with garbage results)
-// quickly.  By default the warp polls (the decode engine's waits are short and
-// a suspended warp wakes late); sleep = true lets the hardware suspend it
-// between polls (long waits of otherwise idle roles).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity,
-                                                  volatile int* skip, int* status,
-                                                  bool sleep = false) {
+// Bounded-wait control of one CTA (shared memory): the limit of every wait,
+// read once at kernel start from the workspace control word kCtlWaitLimit
+// (microseconds; 0 selects the one-second default), and the flag set after
+// the first timeout, which turns every later wait of the CTA into a no-op so
+// that the kernel finishes (with garbage results) quickly.
+struct WaitCtl {
+  unsigned long long limit_ns;
+  int skip;
+};
+
+// One thread; `ctrl` is the workspace's control region (nullable: default).
+__device__ __forceinline__ void wait_ctl_init(WaitCtl& w, const int* ctrl) {
+  const int us = ctrl ? *(volatile const int*)(ctrl + kCtlWaitLimit) : 0;
+  w.limit_ns = us > 0 ? 1000ull * unsigned(us) : kWaitLimitNs;
+  w.skip = 0;
+}
+
+// Wait for phase `parity` of an mbarrier; after the CTA's limit, record a
+// timeout and return false.  By default the warp polls (the decode engine's
+// waits are short and a suspended warp wakes late); sleep = true lets the
+// hardware suspend it between polls (long waits of otherwise idle roles).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity, WaitCtl* w,
+                                                  int* status, bool sleep = false) {
   auto poll = [&]() {
     return sleep ? mbar_try_wait_sleep(bar, parity, 100000u) : mbar_try_wait(bar, parity);
   };
   if (poll()) return true;
-  const unsigned long long t0 = global_ns();
+  volatile int* skip = &w->skip;
+  const unsigned long long t0 = global_ns(), lim = w->limit_ns;
   for (;;) {
     if (poll()) return true;
     if (*skip) return false;
-    if (global_ns() - t0 > kWaitLimitNs) break;
+    if (global_ns() - t0 > lim) break;
   }
   *skip = 1;
   atomicExch(status, int(MOE_ERR_TIMEOUT));
   return false;
+}
+
+// Wait for the completion of a copy this CTA issued (its barrier phase
+// `parity`) before the CTA exits; unlike the other waits it does not give up
+// after a timeout elsewhere in the CTA, only after kDrainLimitNs.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 10000u)) return true;
+    if (global_ns() - t0 > kDrainLimitNs) return false;
+  }
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -198,17 +226,18 @@ __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
 }
 
-// Bounded wait (one thread) until *p >= target; after kWaitLimitNs records a
-// timeout and sets *skip.  Returns at once when *skip is already set.
-static __device__ __noinline__ bool wait_counter(const int* p, int target, volatile int* skip,
+// Bounded wait (one thread) until *p >= target; after the CTA's limit records
+// a timeout and sets the skip flag.  Returns at once when the flag is set.
+static __device__ __noinline__ bool wait_counter(const int* p, int target, WaitCtl* w,
                                                  int* status) {
   if (ld_acquire(p) >= target) return true;
-  const unsigned long long t0 = global_ns();
+  volatile int* skip = &w->skip;
+  const unsigned long long t0 = global_ns(), lim = w->limit_ns;
   unsigned ns = 32;
   for (;;) {
     if (ld_acquire(p) >= target) return true;
     if (*skip) return false;
-    if (global_ns() - t0 > kWaitLimitNs) break;
+    if (global_ns() - t0 > lim) break;
     __nanosleep(ns);
     if (ns < 64) ns <<= 1;
   }
@@ -401,12 +430,13 @@ struct EngineSmem {
   uint64_t op_empty[2];
   uint64_t epi_full[kEpiRing];    // unit results written (consumers -> signal warp)
   uint64_t epi_empty[kEpiRing];   // unit published (signal warp -> consumers)
-  int skip;                       // set after the first timeout
+  WaitCtl wc;                     // wait limit and timeout flag
   float red[2][8][32][4];         // epilogue: accumulators by k-half, tile, lane
   float part[kConsumerWarps];     // epilogue: per-warp partial sums
 };
 
-__device__ __forceinline__ void engine_init(EngineSmem& E, int S) {
+// `ctrl`: the workspace's control region (the wait limit).
+__device__ __forceinline__ void engine_init(EngineSmem& E, int S, const int* ctrl) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&E.full[s], 1);
@@ -420,7 +450,7 @@ __device__ __forceinline__ void engine_init(EngineSmem& E, int S) {
       mbar_init(&E.epi_full[b], kConsumerWarps);
       mbar_init(&E.epi_empty[b], 1);
     }
-    E.skip = 0;
+    wait_ctl_init(E.wc, ctrl);
   }
 }
 
@@ -455,9 +485,9 @@ __device__ __forceinline__ void unit_items(const TileGeo& tg, uint32_t mg, Engin
                                            int kh, int* status, float (&acc)[4]) {
   const OpLayout L = op_layout(tg);
   const int nch = tg.nch;
-  mbar_wait_bounded(op_full, op_parity, &E.skip, status);
+  mbar_wait_bounded(op_full, op_parity, &E.wc, status);
   for (int c = 0; c < nch; ++c) {
-    mbar_wait_bounded(&E.full[R.slot], R.use & 1, &E.skip, status);
+    mbar_wait_bounded(&E.full[R.slot], R.use & 1, &E.wc, status);
     compute_item<FMT, F16A, SPLIT, NG>(tg, M.stages + (size_t)R.slot * M.SB, op, L, c, tile, kh,
                                        mg, acc);
     __syncwarp();
@@ -524,12 +554,12 @@ __device__ __forceinline__ void produce_weights(const MatGeo& g, const UnitInfo&
 __device__ __forceinline__ void produce_operands(const EngineCfg& C, const MatSource& src,
                                                  const UnitInfo& u, const int* perm, int k,
                                                  uint8_t* ob, uint64_t* full, const int* ctrl,
-                                                 volatile int* skip) {
+                                                 WaitCtl* wc) {
   const int lane = threadIdx.x & 31;
   const TileGeo& tg = C.geo[u.mat].t;
   const OpLayout L = op_layout(tg);
   if (u.wait_ctr >= 0) {
-    if (lane == 0) wait_counter(ctrl + u.wait_ctr, u.wait_target, skip, C.status);
+    if (lane == 0) wait_counter(ctrl + u.wait_ctr, u.wait_target, wc, C.status);
     __syncwarp();
     fence_proxy_async_global();
   }
@@ -567,9 +597,15 @@ __device__ void producer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
   const int lane = threadIdx.x & 31;
   Ring R{0, 0, M.S}, B{0, 0, M.nob};
   const int nu = sch.n_units();
+  // A stage (operand buffer) is refilled once the consumers released it and
+  // its previous fill has landed -- immediate unless a timeout let the
+  // consumers skip their wait: one fill per barrier phase.
   auto take_stage = [&]() -> uint8_t* {
     if (R.use > 0) {
-      if (lane == 0) mbar_wait_bounded(&E.empty[R.slot], (R.use - 1) & 1, &E.skip, C.status);
+      if (lane == 0) {
+        mbar_wait_bounded(&E.empty[R.slot], (R.use - 1) & 1, &E.wc, C.status);
+        mbar_drain(&E.full[R.slot], (R.use - 1) & 1);
+      }
       __syncwarp();
     }
     return M.stages + (size_t)R.slot * M.SB;
@@ -579,7 +615,7 @@ __device__ void producer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
     if (u.kind == kItemCombine) {
       take_stage();
       if (lane == 0) {
-        wait_counter(ctrl + u.wait_ctr, u.wait_target, &E.skip, C.status);
+        wait_counter(ctrl + u.wait_ctr, u.wait_target, &E.wc, C.status);
         mbar_arrive(&E.full[R.slot]);
       }
       __syncwarp();
@@ -590,27 +626,31 @@ __device__ void producer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
     produce_weights(g, u, 0, take_stage(), &E.full[R.slot]);
     R.next();
     if (B.use > 0) {
-      if (lane == 0) mbar_wait_bounded(&E.op_empty[B.slot], (B.use - 1) & 1, &E.skip, C.status);
+      if (lane == 0) {
+        mbar_wait_bounded(&E.op_empty[B.slot], (B.use - 1) & 1, &E.wc, C.status);
+        mbar_drain(&E.op_full[B.slot], (B.use - 1) & 1);
+      }
       __syncwarp();
     }
     produce_operands(C, sch.source(u.mat), u, sch.perm(), sch.topk(),
-                     M.ops + (size_t)B.slot * M.OB, &E.op_full[B.slot], ctrl, &E.skip);
+                     M.ops + (size_t)B.slot * M.OB, &E.op_full[B.slot], ctrl, &E.wc);
     B.next();
     for (int c = 1; c < u.nch; ++c) {
       produce_weights(g, u, c, take_stage(), &E.full[R.slot]);
       R.next();
     }
   }
-  // wait (bounded) until the last copies have landed: every stage and
-  // operand buffer's most recent fill
+  // wait until the last copies have landed (every stage and operand buffer's
+  // most recent fill), also after a timeout: the CTA may not exit with copies
+  // into its shared memory in flight
   if (lane == 0) {
     for (int s = 0; s < M.S; ++s) {
       const int uses = R.use + (s < R.slot ? 1 : 0);
-      if (uses > 0) mbar_wait_bounded(&E.full[s], (uses - 1) & 1, &E.skip, C.status);
+      if (uses > 0) mbar_drain(&E.full[s], (uses - 1) & 1);
     }
     for (int b = 0; b < M.nob; ++b) {
       const int uses = B.use + (b < B.slot ? 1 : 0);
-      if (uses > 0) mbar_wait_bounded(&E.op_full[b], (uses - 1) & 1, &E.skip, C.status);
+      if (uses > 0) mbar_drain(&E.op_full[b], (uses - 1) & 1);
     }
   }
   __syncwarp();
@@ -698,7 +738,7 @@ __device__ __forceinline__ void epi_publish(EngineSmem& E, Ring& P, const UnitIn
   if (u.signal < 0) return;
   __syncwarp();
   if ((threadIdx.x & 31) == 0) {
-    if (P.use > 0) mbar_wait_bounded(&E.epi_empty[P.slot], (P.use - 1) & 1, &E.skip, status);
+    if (P.use > 0) mbar_wait_bounded(&E.epi_empty[P.slot], (P.use - 1) & 1, &E.wc, status);
     mbar_arrive(&E.epi_full[P.slot]);
   }
   P.next();
@@ -713,7 +753,7 @@ __device__ void signal_run(EngineSmem& E, const Sched& sch, int* ctrl, int* stat
     const UnitInfo u = sch.unit(j);
     if (u.kind == kItemCombine || u.signal < 0) continue;
     if (lane == 0) {
-      mbar_wait_bounded(&E.epi_full[P.slot], P.use & 1, &E.skip, status);
+      mbar_wait_bounded(&E.epi_full[P.slot], P.use & 1, &E.wc, status);
       red_release_add(ctrl + u.signal, 1);
       mbar_arrive(&E.epi_empty[P.slot]);
     }
@@ -736,7 +776,7 @@ __device__ void consumer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
   for (int j = 0; j < nu; ++j) {
     const UnitInfo u = sch.unit(j);
     if (u.kind == kItemCombine) {
-      mbar_wait_bounded(&E.full[R.slot], R.use & 1, &E.skip, C.status);
+      mbar_wait_bounded(&E.full[R.slot], R.use & 1, &E.wc, C.status);
       __syncwarp();
       if (lane == 0) mbar_arrive(&E.empty[R.slot]);
       R.next();
@@ -763,7 +803,8 @@ __device__ void consumer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
 //   out[t, h] = round( sum_j w[t, j] * y[t*k + j, h]  +  s_t * ysh[t, h] )
 // an fp32 fma chain in slot order with the shared slot last; y comes as two
 // k-half planes added plane 0 + plane 1 first (one plane when yhalf == 0),
-// ysh likewise when ysh2 is given.
+// ysh likewise when ysh2 is given.  rb rounds the weights w and sg to bf16
+// first (the engine's bf16 rounding chain; idempotent on rounded weights).
 // y and ysh are read through L2 (written by other CTAs); every load of one
 // output is issued before the chain starts (k <= kMaxTopK).  `nthr` threads.
 constexpr int kMaxTopK = 8;
@@ -771,7 +812,8 @@ constexpr int kCombineRows = 64;  // columns of one combine piece
 __device__ __forceinline__ void combine_rows(const float* y, size_t yhalf, const float* w,
                                              const float* ysh, const float* ysh2,
                                              const float* sg, uint16_t* out, int T, int k, int H,
-                                             bool f16, int h0, int nh, int tid, int nthr) {
+                                             bool f16, int h0, int nh, int tid, int nthr,
+                                             bool rb = false) {
   for (int v = tid; v < T * nh; v += nthr) {
     const int t = v / nh;
     const int h = h0 + (v - t * nh);
@@ -792,8 +834,11 @@ __device__ __forceinline__ void combine_rows(const float* y, size_t yhalf, const
     float acc = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
-      if (j < k) acc = fmaf(w[t * k + j], yhalf ? ya[j] + yb[j] : ya[j], acc);
-    if (ysh) acc = fmaf(sg ? sg[t] : 1.f, vs, acc);
+      if (j < k) {
+        const float wj = rb ? round_bf16(w[t * k + j]) : w[t * k + j];
+        acc = fmaf(wj, yhalf ? ya[j] + yb[j] : ya[j], acc);
+      }
+    if (ysh) acc = fmaf(sg ? (rb ? round_bf16(sg[t]) : sg[t]) : 1.f, vs, acc);
     out[(size_t)t * H + h] = float_to_act_bits(acc, f16);
   }
 }

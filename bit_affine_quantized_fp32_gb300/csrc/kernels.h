@@ -46,8 +46,11 @@ struct CombineArgs {
   const float* sg;   // [T] or nullptr (weight 1)
   uint16_t* out;     // [T][H]
   int T, k, H, f16;
+  int round_bf16;    // w and sg rounded to bf16 before the sum
 };
 cudaError_t launch_combine(const CombineArgs& A, cudaStream_t st);
+// *p = v, stream-ordered (a workspace control word)
+cudaError_t launch_store_word(int* p, int v, cudaStream_t st);
 cudaError_t launch_add_planes(const float* a, const float* b, float* dst, long n,
                               cudaStream_t st);
 
@@ -76,12 +79,14 @@ struct RouterJob {
   int T, E, H;
   float* logits;            // [T][E]
   float* gate_logit;        // [T] (when gq)
+  int round_bf16;           // router and gate rows rounded to bf16 before the dot products
 };
 int router_ks(int H);
 int router_blocks(int E, bool gate, int H);
 cudaError_t launch_router(const RouterJob& J, cudaStream_t st);
+// round_bf16: slot weights bf16(w) and shared weight bf16(sigmoid(bf16(g)))
 cudaError_t launch_topk(const float* logits, const float* gate_logit, int T, int E, int k,
-                        int32_t* idx, float* w, float* sg, cudaStream_t st);
+                        int32_t* idx, float* w, float* sg, bool round_bf16, cudaStream_t st);
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets,
                           int32_t* perm, cudaStream_t st);
 // Sub-slots (runs of at most `run` bucket positions) of the experts with

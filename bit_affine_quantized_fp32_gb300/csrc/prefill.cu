@@ -29,6 +29,7 @@
 // (prefill windows through grouped expert GEMMs, SwiGLU epilogue).
 
 #include "prefill.h"
+#include "host.h"
 #include "engine.cuh"
 #include "umma.cuh"
 
@@ -57,7 +58,7 @@ struct PfSmem {
   uint64_t a_full[kPfStagesMax], b_full[kPfStagesMax], ab_empty[kPfStagesMax];
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem;
-  int skip;
+  WaitCtl wc;
   float xch[64][9];  // up rows handed to the gate rows in the SwiGLU epilogue
 };
 
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       mbar_init(&S.acc_full[i], 1);
       mbar_init(&S.acc_empty[i], 4);
     }
-    S.skip = 0;
+    wait_ctl_init(S.wc, J.status);
   }
   if (warp == 14) tmem_alloc(&S.tmem, 2 * kPfTile);
   fence_proxy_async();
@@ -223,8 +224,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       for (int c = 0; c < nch; ++c, ++ri) {
         const int rs = ri % kPfRaw;
         if (lane == 0) {
-          if (ri >= kPfRaw)
-            mbar_wait_bounded(&S.raw_empty[rs], ((ri / kPfRaw) - 1) & 1, &S.skip, status, true);
+          if (ri >= kPfRaw) {
+            mbar_wait_bounded(&S.raw_empty[rs], ((ri / kPfRaw) - 1) & 1, &S.wc, status, true);
+            // the stage's previous copy has landed (immediate unless a timeout
+            // let the consumers skip their wait): one copy per barrier phase
+            mbar_drain(&S.raw_full[rs], ((ri / kPfRaw) - 1) & 1);
+          }
           mbar_expect_tx(&S.raw_full[rs], unsigned(g.item_bytes));
           bulk_g2s(raw + rs * RB,
                    J.base + (size_t)U.e * g.expert_bytes +
@@ -234,9 +239,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         __syncwarp();
       }
     }
-    if (lane == 0)  // the last copies have landed before the CTA may exit
+    // the last copies have landed before the CTA may exit, also after a timeout
+    if (lane == 0)
       for (int i = max(0, ri - kPfRaw); i < ri; ++i)
-        mbar_wait_bounded(&S.raw_full[i % kPfRaw], (i / kPfRaw) & 1, &S.skip, status, true);
+        mbar_drain(&S.raw_full[i % kPfRaw], (i / kPfRaw) & 1);
   } else if (warp == 13) {
     // ---- operand rows, one 64-column group per stage; lane l copies rows
     // l, l + 32, ... of the tile, their addresses resolved once per unit
@@ -256,7 +262,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       for (int q = 0; q < nks; ++q, ++ks) {
         const int s = ks % NS;
         if (ks >= NS)
-          mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.skip, status, true);
+          mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status, true);
         const int k0 = q * kPfKBlk;
         uint8_t* B = stages + s * SB + 2 * kPfA;
 #pragma unroll
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       for (int u = blockIdx.x; u < nunits; u += G, ++ui) {
         const PfUnit U = pf_unit(J, u);
         const int a = ui & 1;
-        if (ui >= 2) mbar_wait_bounded(&S.acc_empty[a], ((ui >> 1) - 1) & 1, &S.skip, status, true);
+        if (ui >= 2) mbar_wait_bounded(&S.acc_empty[a], ((ui >> 1) - 1) & 1, &S.wc, status, true);
         tmem_fence_after();
         const int N = max(16, (U.cnt + 15) & ~15);
         const uint32_t idesc = (MODE == 0 && F16)
@@ -296,8 +302,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         constexpr uint32_t kSbo = (kPfKBlk / 8) * 128;
         for (int q = 0; q < nks; ++q, ++ks) {
           const int s = ks % NS;
-          mbar_wait_bounded(&S.a_full[s], (ks / NS) & 1, &S.skip, status, true);
-          mbar_wait_bounded(&S.b_full[s], (ks / NS) & 1, &S.skip, status, true);
+          mbar_wait_bounded(&S.a_full[s], (ks / NS) & 1, &S.wc, status, true);
+          mbar_wait_bounded(&S.b_full[s], (ks / NS) & 1, &S.wc, status, true);
           fence_proxy_async();
           tmem_fence_after();
           const uint32_t ah = smem_u32(stages + s * SB), al = ah + kPfA;
@@ -315,6 +321,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         }
         umma_commit(&S.acc_full[a]);
       }
+      // every MMA has completed before tensor memory is released, also after
+      // a timeout: the last commit arrives once all earlier MMAs are done
+      if (ui > 0) mbar_drain(&S.acc_full[(ui - 1) & 1], ((ui - 1) >> 1) & 1);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -326,11 +335,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       (void)U;
       for (int c = 0; c < nch; ++c, ++ri) {
         const int rs = ri % kPfRaw;
-        mbar_wait_bounded(&S.raw_full[rs], (ri / kPfRaw) & 1, &S.skip, status, true);
+        mbar_wait_bounded(&S.raw_full[rs], (ri / kPfRaw) & 1, &S.wc, status, true);
         for (int Gi = 0; Gi < NG; ++Gi, ++ks) {
           const int s = ks % NS;
           if (ks >= NS)
-          mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.skip, status, true);
+          mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status, true);
           uint8_t* A = stages + s * SB;
           dequant_group<FMT>(g, raw + rs * RB, Gi, A, A + kPfA, w, lane, MODE == 0 && F16);
           fence_proxy_async();
@@ -348,7 +357,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
     for (int u = blockIdx.x; u < nunits; u += G, ++ui) {
       const PfUnit U = pf_unit(J, u);
       const int a = ui & 1;
-      mbar_wait_bounded(&S.acc_full[a], (ui >> 1) & 1, &S.skip, status, true);
+      mbar_wait_bounded(&S.acc_full[a], (ui >> 1) & 1, &S.wc, status, true);
       tmem_fence_after();
       const uint32_t tl = tbase + (uint32_t(32 * warp) << 16) + uint32_t(a * kPfTile);
       for (int c8 = 0; c8 < U.cnt; c8 += 8) {
@@ -404,17 +413,8 @@ template <int FMT, int MODE, bool F16>
 cudaError_t launch_t(const PrefillJob& J, int sms, cudaStream_t st) {
   const int smem = prefill_smem(J.g, MODE);
   if (smem <= 0) return cudaErrorInvalidValue;
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const cudaError_t e = ensure_dynamic_smem((const void*)k_prefill<FMT, MODE, F16>, smem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (configured[dev] < smem) {
-    e = cudaFuncSetAttribute(k_prefill<FMT, MODE, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = smem;
-  }
   k_prefill<FMT, MODE, F16><<<sms, kPfThreads, smem, st>>>(J);
   return cudaGetLastError();
 }

@@ -16,10 +16,10 @@ __global__ void __launch_bounds__(256) k_router(const RouterJob J, int KS) {
 
 __global__ void k_topk(const float* __restrict__ logits, const float* __restrict__ gate_logit,
                        int T, int E, int k, int32_t* __restrict__ idx, float* __restrict__ w,
-                       float* __restrict__ sg) {
+                       float* __restrict__ sg, int rb) {
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
-  topk_warp<false>(logits, gate_logit, t, E, k, idx, w, sg, nullptr, nullptr);
+  topk_warp<false>(logits, gate_logit, t, E, k, idx, w, sg, nullptr, nullptr, rb != 0);
 }
 
 __global__ void __launch_bounds__(1024) k_bucket(const int32_t* __restrict__ idx, int N, int E,
@@ -65,9 +65,9 @@ cudaError_t launch_router(const RouterJob& J, cudaStream_t st) {
 }
 
 cudaError_t launch_topk(const float* logits, const float* gate_logit, int T, int E, int k,
-                        int32_t* idx, float* w, float* sg, cudaStream_t st) {
+                        int32_t* idx, float* w, float* sg, bool round_bf16, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
-  k_topk<<<(T + 7) / 8, 256, 0, st>>>(logits, gate_logit, T, E, k, idx, w, sg);
+  k_topk<<<(T + 7) / 8, 256, 0, st>>>(logits, gate_logit, T, E, k, idx, w, sg, round_bf16);
   return cudaGetLastError();
 }
 

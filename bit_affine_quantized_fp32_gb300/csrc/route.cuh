@@ -21,7 +21,7 @@ constexpr int kRouterTT = 64;  // tokens per pass of a router block
 // Four consecutive weights of row r at column k (k % 4 == 0) as fp32.
 __device__ __forceinline__ void router_load_w4(int fmt, const void* q, const uint16_t* s,
                                                const uint16_t* b, int r, int H, int k,
-                                               float (&w)[4]) {
+                                               float (&w)[4], bool rb) {
   if (fmt == MOE_FMT_F32) {
     const float4 v =
         *reinterpret_cast<const float4*>(static_cast<const float*>(q) + size_t(r) * H + k);
@@ -41,6 +41,10 @@ __device__ __forceinline__ void router_load_w4(int fmt, const void* q, const uin
     const float bi = half_bits_to_float(b[gi]);
 #pragma unroll
     for (int j = 0; j < 4; ++j) w[j] = fmaf(sc, float((word >> (8 * j)) & 0xFFu), bi);
+  }
+  if (rb) {  // the engine's bf16 rounding chain: rows stored as bf16
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = round_bf16(w[j]);
   }
 }
 
@@ -66,9 +70,9 @@ __device__ __forceinline__ void router_warp(const RouterJob& J, int KS, int row,
   for (int i = 0; i < NI; ++i) {
     const int k = kq + 128 * i + 4 * lane;
     if (gate)
-      router_load_w4(J.gfmt, J.gq, J.gs, J.gb, 0, J.H, k, w[i]);
+      router_load_w4(J.gfmt, J.gq, J.gs, J.gb, 0, J.H, k, w[i], J.round_bf16 != 0);
     else
-      router_load_w4(J.fmt, J.q, J.s, J.b, row, J.H, k, w[i]);
+      router_load_w4(J.fmt, J.q, J.s, J.b, row, J.H, k, w[i], J.round_bf16 != 0);
   }
   pre();
   // 8 tokens per pass: every x load of a pass is issued before its sums (a
@@ -213,10 +217,11 @@ __device__ __forceinline__ float key_value(unsigned hi) {
 // head.  Then w_j = exp(l_j - l_0) / sum over the k, the exponentials by lanes
 // 0..k-1 in parallel and the sum in slot order.  Lanes 0..k-1 write
 // idx/w[t*k + j] (and idx2/w2 when given); lane 0 writes sg[t] from the gate
-// logit gl when has_gate.
+// logit gl when has_gate.  rb (the engine's bf16 rounding chain): each slot
+// weight is stored as bf16(w) and the shared weight as bf16(sigmoid(bf16(gl))).
 __device__ __forceinline__ void topk_select(unsigned long long (&key)[8], int t, int k,
                                             int32_t* idx, float* w, float* sg, bool has_gate,
-                                            float gl, int32_t* idx2, float* w2) {
+                                            float gl, int32_t* idx2, float* w2, bool rb) {
   const int lane = threadIdx.x & 31;
   // sorting network (descending), 19 compare-exchanges
 #define MOE_CX(a, b)                                  \
@@ -265,13 +270,14 @@ __device__ __forceinline__ void topk_select(unsigned long long (&key)[8], int t,
     if (r < k) den += er;
   }
   if (lane < k) {
-    const float wr = ex / den;
+    const float wr = rb ? round_bf16(ex / den) : ex / den;
     idx[size_t(t) * k + lane] = my_e;
     w[size_t(t) * k + lane] = wr;
     if (idx2) idx2[size_t(t) * k + lane] = my_e;
     if (w2) w2[size_t(t) * k + lane] = wr;
   }
-  if (lane == 0 && has_gate && sg) sg[t] = 1.f / (1.f + expf(-gl));
+  if (lane == 0 && has_gate && sg)
+    sg[t] = rb ? round_bf16(1.f / (1.f + expf(-round_bf16(gl)))) : 1.f / (1.f + expf(-gl));
 }
 
 // Top-k + weights of token t by one warp from fp32 logits [T][E] (E <= 256),
@@ -280,7 +286,7 @@ __device__ __forceinline__ void topk_select(unsigned long long (&key)[8], int t,
 template <bool SMEM = false>
 __device__ __forceinline__ void topk_warp(const float* logits, const float* gate_logit, int t,
                                           int E, int k, int32_t* idx, float* w, float* sg,
-                                          int32_t* idx2, float* w2) {
+                                          int32_t* idx2, float* w2, bool rb) {
   const int lane = threadIdx.x & 31;
   const float* row = logits + size_t(t) * E;
   float v[8];
@@ -306,7 +312,7 @@ __device__ __forceinline__ void topk_warp(const float* logits, const float* gate
   }
   float gl = 0.f;
   if (gate_logit) gl = SMEM ? gate_logit[t] : __ldcg(gate_logit + t);
-  topk_select(key, t, k, idx, w, sg, gate_logit != nullptr, gl, idx2, w2);
+  topk_select(key, t, k, idx, w, sg, gate_logit != nullptr, gl, idx2, w2, rb);
 }
 
 // Shared memory of bucket_cta for NW warps.
@@ -451,14 +457,15 @@ struct RouteTable {
 // outputs.  All threads of the CTA call it (blockDim.x >= 256).
 __device__ __forceinline__ void route_table_cta(const float* logits, const float* gate_logit,
                                                 int T, int E, int k, int32_t* user_idx,
-                                                float* user_w, int (*wc)[256], RouteTable& S) {
+                                                float* user_w, int (*wc)[256], RouteTable& S,
+                                                bool rb) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int NT = blockDim.x, NW = NT >> 5;
   for (int i = tid; i < 256; i += NT) S.cnt[i] = 0;
   for (int i = tid; i < 8 * 256; i += NT) wc[i >> 8][i & 255] = 0;
   __syncthreads();
   for (int t = wid; t < T; t += NW)
-    topk_warp<false>(logits, gate_logit, t, E, k, S.idx, S.w, S.sg, user_idx, user_w);
+    topk_warp<false>(logits, gate_logit, t, E, k, S.idx, S.w, S.sg, user_idx, user_w, rb);
   __syncthreads();
   const int N = T * k;
   const int e_a = tid < N ? S.idx[tid] : -1;

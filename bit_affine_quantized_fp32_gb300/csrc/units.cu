@@ -9,6 +9,7 @@
 // epilogue, decode rows summed in fp32, the slots' fma sum rounded once.
 
 #include "kernels.h"
+#include "host.h"
 
 namespace moe {
 
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
     k_units(const __grid_constant__ UnitJob J, const EnginePlan P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ EngineSmem E;
-  engine_init(E, P.S);
+  engine_init(E, P.S, J.C.status);
   fence_proxy_async();
   __syncthreads();
   const EngineMem M{smem, smem + P.nob * P.OB, P.OB, P.nob, P.SB, P.S};
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(256) k_combine(const CombineArgs A) {
   combine_rows(A.y + t0 * kh, A.yhalf, A.w + t0 * A.k, A.ysh ? A.ysh + size_t(t0) * A.H : nullptr,
                A.ysh2 ? A.ysh2 + size_t(t0) * A.H : nullptr, A.sg ? A.sg + t0 : nullptr,
                A.out + size_t(t0) * A.H, Tn, A.k, A.H, A.f16 != 0, blockIdx.x * kCombineRows,
-               kCombineRows, threadIdx.x, blockDim.x);
+               kCombineRows, threadIdx.x, blockDim.x, A.round_bf16 != 0);
 }
 
 // dst = a + b elementwise (the two k-half planes of a down projection)
@@ -103,25 +104,16 @@ __global__ void k_add_planes(const float* __restrict__ a, const float* __restric
   if (i < n) dst[i] = a[i] + b[i];
 }
 
+__global__ void k_store_word(int* p, int v) { *p = v; }
+
 template <int FMT, bool F16A>
 cudaError_t launch_units_t(const UnitJob& J, int sms, cudaStream_t st) {
   const TileGeo geos[1] = {J.C.geo[J.mat].t};
   const EnginePlan P = engine_plan(geos, 1, int(sizeof(EngineSmem)));
   if (P.S < 2) return cudaErrorInvalidValue;
   const int smem = P.bytes();
-  // raise the dynamic shared-memory limit once per device (cudaFuncSetAttribute
-  // is not a stream operation, so it stays out of captured graphs afterwards)
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const cudaError_t e = ensure_dynamic_smem((const void*)k_units<FMT, F16A>, smem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (configured[dev] < smem) {
-    e = cudaFuncSetAttribute(k_units<FMT, F16A>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = smem;
-  }
   const int grid = J.max_units < sms ? J.max_units : sms;
   if (grid <= 0) return cudaSuccess;
   k_units<FMT, F16A><<<grid, kEngineThreads, smem, st>>>(J, P);
@@ -177,6 +169,11 @@ cudaError_t launch_add_planes(const float* a, const float* b, float* dst, long n
                               cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   k_add_planes<<<unsigned((n + 255) / 256), 256, 0, st>>>(a, b, dst, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_store_word(int* p, int v, cudaStream_t st) {
+  k_store_word<<<1, 1, 0, st>>>(p, v);
   return cudaGetLastError();
 }
 

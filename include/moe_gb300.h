@@ -127,6 +127,17 @@ typedef struct moe_expert_bank {
 #define MOE_FLAG_FORCE_DECODE 1   /* use the decode (grouped GEMV) form at any T */
 #define MOE_FLAG_UNFUSED 2        /* moe_layer_forward: one launch per step instead of the
                                      single persistent decode launch (same results) */
+/* The engine's bf16 rounding chain ([803-gate]: router and combine checked
+ * byte-equal against a host reference, weights within a bf16 step).  In
+ * moe_route and moe_layer_forward: the router and shared-gate rows are
+ * rounded to bf16 (through their fp32 value, nearest, ties to even) before
+ * the dot products, each slot weight is stored as bf16(w), and the shared
+ * weight as bf16(sigmoid(bf16(g))); logits, softmax and sums stay fp32.  In
+ * moe_experts_forward (and the layer's combine): the given slot and shared
+ * weights are rounded to bf16 before the fp32 fma chain (a no-op on weights
+ * moe_route already rounded).  Without the flag the weights stay fp32 and
+ * the only rounding is the final cast to the activation type.            */
+#define MOE_FLAG_ROUND_BF16 4
 
 /* The decode form (grouped GEMV on exact integer codes) serves n_tokens <=
  * MOE_DECODE_MAX_TOKENS; above it the prefill form runs the expert GEMMs on
@@ -150,6 +161,19 @@ size_t moe_workspace_bytes(int max_tokens, int n_experts, int top_k, int hidden,
  * allocating a workspace, before its first use, and again after a call
  * reported MOE_ERR_TIMEOUT through moe_get_device_status. */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Limit of every bounded device-side wait (a CTA waiting for another CTA's
+ * results, or for its own copies) of later calls on this workspace, in
+ * microseconds; 0 restores the default of one second.  A wait that runs out
+ * records MOE_ERR_TIMEOUT in the workspace's status word and makes the rest
+ * of its CTA's waits return at once, so the launch ends (its outputs are then
+ * garbage); the workspace must be re-initialised before the next call.  The
+ * pages' counterpart is the serving engine's wall-clock guard with an error
+ * event on shutdown ([547-win]).  Stream-ordered (a one-thread kernel writes
+ * the control word); moe_workspace_init resets it to the default.
+ *   limit_us  0 .. 2^31 - 1, else MOE_ERR_INVALID_ARG.                   */
+moe_status moe_workspace_set_wait_limit(void* ws, size_t ws_bytes, unsigned limit_us,
+                                        cudaStream_t stream);
 
 /* Read and clear the device status word of a workspace (synchronises the
  * stream).  *device_status receives MOE_OK or MOE_ERR_TIMEOUT. */
@@ -175,25 +199,30 @@ moe_status moe_get_device_status(void* ws, size_t ws_bytes, int* device_status,
  *   top_k        1..8, <= E;  E <= 256
  *   logits       nullable [T, E] fp32 output
  *   topk_idx [T, k] int32, topk_w [T, k] fp32, shared_gate_w nullable [T]
+ *   flags        0 or MOE_FLAG_ROUND_BF16 (the engine's bf16 rounding chain)
  */
 moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
                      const moe_qmatrix* shared_gate, const void* x, int act, int n_tokens,
                      int top_k, float* logits, int32_t* topk_idx, float* topk_w,
                      float* shared_gate_w, int32_t* bucket_offsets, int32_t* bucket_perm,
-                     void* ws, size_t ws_bytes, cudaStream_t stream);
+                     int flags, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* moe_route without a workspace, for callers that cannot hand the library
  * memory (no device allocator of their own, or no allocation allowed once
  * serving).  The pages have no counterpart to this entry point: it is
  * moe_route (same kernels, same results) with its one scratch buffer -- the
  * fp32 logits between the router and top-k kernels -- in a static device
- * array of 32 * 256 + 32 floats per device; no logits output.
+ * array of 32 * 256 + 32 floats; no logits output.  The array belongs to the
+ * library's module as loaded into a CUDA context, so there is one copy per
+ * context (module instance), not per device.
  *   Limits: n_tokens <= 32 and n_tokens * experts <= 8192, else
  *           MOE_ERR_WORKSPACE before anything is launched.
- *   The first call on a device looks the array's address up (a synchronous
- *   runtime query), so make it before any stream capture.
+ *   The first call in a context looks the array's address up (a synchronous
+ *   runtime query, cached under the context's id; after cudaDeviceReset or in
+ *   another context it is looked up again), so make it before any stream
+ *   capture.
  *   Nothing in the array needs to start at zero.  Calls that overlap in time
- *   on one device (other streams, other host threads) race on the array. */
+ *   within one context (other streams, other host threads) race on it. */
 moe_status moe_route_static(const moe_qmatrix* router, const float* logit_bias,
                             const moe_qmatrix* shared_gate, const void* x, int act,
                             int n_tokens, int top_k, int32_t* topk_idx, float* topk_w,
@@ -234,6 +263,8 @@ moe_status moe_shared_expert(const moe_expert_bank* shared, const void* x, int a
  * the activation type.  y_shared/shared_gate_w nullable (no shared slot when
  * y_shared is NULL; weight 1 when only shared_gate_w is NULL).
  * Routing inputs are moe_route's outputs (or any valid equivalent).
+ * flags: MOE_FLAG_FORCE_DECODE, MOE_FLAG_ROUND_BF16 (weights rounded to bf16
+ * before the sum).
  * In the decode form every token's output row depends only on that token's
  * inputs: a row is bit-identical whatever the other rows of the call
  * ([547-win]); the prefill form (T > 32) matches it to within the layer's
@@ -248,6 +279,7 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
 /* The whole layer in one call: route, shared expert, routed experts, combine.
  * shared (nullable) is a one-expert bank; shared_gate nullable.
  * topk_idx/topk_w nullable outputs [T, k].
+ * flags: MOE_FLAG_FORCE_DECODE, MOE_FLAG_UNFUSED, MOE_FLAG_ROUND_BF16.
  * For n_tokens <= MOE_DECODE_MAX_TOKENS the layer runs as ONE persistent
  * cooperative launch (one CTA per SM) whose phases synchronise through
  * counters in the workspace; every wait is bounded and reports

@@ -51,15 +51,30 @@ def test_kernel_source_hash_tracks_every_source():
 
 
 def test_captured_traffic_needs_matching_sources(tmp_path, monkeypatch):
-    rec = {"source_sha256": "0" * 64, "dram_bytes_per_launch": 123}
+    rec = {"source_sha256": "0" * 64, "dram_bytes_per_step": 123}
     prof = tmp_path / "profiles"
     prof.mkdir()
-    (prof / "k_decode_traffic.json").write_text(json.dumps(rec))
+    (prof / "traffic_decode1_affine4.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "kernel_source_hash", lambda read=None: "f" * 64)
-    assert bench.captured_traffic() is None
+    assert bench.captured_traffic("decode1_affine4") is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda read=None: "0" * 64)
-    assert bench.captured_traffic() == 123
+    assert bench.captured_traffic("decode1_affine4") == 123
+    assert bench.captured_traffic("decode4_affine3") is None      # no record
+
+
+def test_step_flops_of_the_prefill_window():
+    # 512 tokens x 8 routed experts and the shared expert, three 512 x 2048
+    # products each at 2 flops per weight, plus the 256 x 2048 router and the
+    # gate row: 29.5 GFLOP
+    from bit_affine_quantized_fp32_gb300 import synth
+    cfg = synth.WORKLOADS["prefill512_affine4_zipf"]
+    per = 2 * 3 * 512 * 2048
+    assert bench.step_flops(cfg, 512) == 512 * 8 * per + 512 * per + 2 * 256 * 2048 * 512 + \
+        2 * 2048 * 512
+    assert abs(bench.step_flops(cfg, 512) / 1e9 - 29.5) < 0.1
+    assert bench.launches_per_step(cfg, 512) == 13
+    assert bench.launches_per_step(synth.WORKLOADS["decode8_affine4_shared_zipf"], 8) == 1
 
 
 def test_reference_arm_line_on_cpu():

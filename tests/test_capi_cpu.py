@@ -135,16 +135,24 @@ def test_route_validation(capi):
     P = 1 << 21
     r = Q(capi.FMT["affine4_g64"], 256, 2048, 0, P, P, P)   # 4-bit router is not read
     rc = capi.lib.moe_route(ctypes.byref(r), None, None, P, 1, 4, 8, None, P, P, None, P, P,
-                            P, 1 << 30, None)
+                            0, P, 1 << 30, None)
     assert rc == 2 and b"router" in capi.lib.moe_last_error()
     r = Q(capi.FMT["f32"], 300, 2048, 0, P, None, None)     # > 256 experts
     rc = capi.lib.moe_route(ctypes.byref(r), None, None, P, 1, 4, 8, None, P, P, None, P, P,
-                            P, 1 << 30, None)
+                            0, P, 1 << 30, None)
     assert rc == 1
     r = Q(capi.FMT["f32"], 256, 2048, 0, P, None, None)
     rc = capi.lib.moe_route(ctypes.byref(r), None, None, P, 7, 4, 8, None, P, P, None, P, P,
-                            P, 1 << 30, None)                # activation format 7
+                            0, P, 1 << 30, None)                # activation format 7
     assert rc == 2
+    rc = capi.lib.moe_route(ctypes.byref(r), None, None, P, 1, 4, 8, None, P, P, None, P, P,
+                            8, P, 1 << 30, None)                # unknown flag
+    assert rc == 1 and b"flags" in capi.lib.moe_last_error()
+
+
+def test_wait_limit_validation(capi):
+    assert capi.lib.moe_workspace_set_wait_limit(None, 1 << 20, 5, None) == 3
+    assert capi.lib.moe_workspace_set_wait_limit(1 << 21, 1 << 20, 1 << 31, None) == 1
 
 
 def test_pack_validation(capi):

@@ -5,6 +5,10 @@ Collected last on purpose: it must pass both alone in a fresh process and
 after every other GPU test.
 """
 
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 
@@ -66,11 +70,10 @@ def test_route_static_equals_route(capi, c):
         assert torch.equal(got["idx"], ref["idx"])
         assert torch.equal(got["offsets"], ref["offsets"])
         assert torch.equal(got["perm"], ref["perm"])
-        # same kernels and arithmetic: equal; the test tolerance is the bound
-        assert np.allclose(got["w"].cpu().numpy(), ref["w"].cpu().numpy(), rtol=1e-6, atol=0)
+        # same kernels and arithmetic: the same bits
+        assert torch.equal(got["w"], ref["w"])
         if gate:
-            assert np.allclose(got["sg"].cpu().numpy(), ref["sg"].cpu().numpy(), rtol=1e-6,
-                               atol=0)
+            assert torch.equal(got["sg"], ref["sg"])
 
 
 def test_route_static_refuses_oversize(capi):
@@ -83,3 +86,14 @@ def test_route_static_refuses_oversize(capi):
         capi.moe_route_static(router, None, None, x, 4, o["idx"], o["w"], None, o["offsets"],
                               o["perm"])
     assert e.value.status == 3 and "static scratch" in str(e.value)
+
+
+def test_route_static_per_context(capi):
+    """The static array belongs to the module as loaded into one CUDA context:
+    a child process (driver-API contexts, no torch) routes in the primary
+    context, in a context of its own and in the primary context again, and
+    moe_route_static equals moe_route bit for bit in each."""
+    script = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_ctx_route_static.py")
+    r = subprocess.run([sys.executable, script], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    assert "route_static contexts ok" in r.stdout
