@@ -12,10 +12,16 @@ namespace moe {
 
 constexpr int kWarp = 32;
 
-// Control words of a workspace (int32 indices into its first 16 KiB, which
-// moe_workspace_init zeroes).
+// Control region of a workspace (its first kCtlBytes, which
+// moe_workspace_init zeroes): int32 control words, then (from byte
+// kCtlTaggedOffset) the fused decode kernel's router logits, one 64-bit word
+// per (token, router row) holding the call's generation number in the high
+// half and the fp32 logit in the low half.
 constexpr int kCtlStatus = 0;      // device status: MOE_OK or MOE_ERR_TIMEOUT
 constexpr int kCtlWaitLimit = 36;  // limit of every bounded wait, microseconds (0: 1 s)
+constexpr int kCtlTaggedOffset = 16384;
+constexpr int kTaggedRows = 32 * 260;  // tokens x (experts + shared gate), rounded
+constexpr int kCtlBytes = kCtlTaggedOffset + 8 * kTaggedRows;
 
 // ---------------------------------------------------------------------------
 // Workspace layout.  Every region is 256-byte aligned; the layout depends only
@@ -23,7 +29,7 @@ constexpr int kCtlWaitLimit = 36;  // limit of every bounded wait, microseconds 
 // bytes serves every call with n_tokens <= max_tokens.  Sums are kept in the
 // padded per-chunk layout of engine.cuh (ldx / ldh floats per row).
 struct WsLayout {
-  size_t ctrl;        // int32 control words ([0] device status), 16 KiB
+  size_t ctrl;        // control region (kCtlBytes): words, tagged logits
   size_t logits;      // f32 [T][E]
   size_t gate_logit;  // f32 [T]
   size_t idx;         // i32 [T][k]
@@ -76,7 +82,7 @@ inline WsLayout ws_layout(long T, long E, long k, long H, long I) {
   const long P = T * k;
   const long mss = max_subslots(T, E, k);
   const long ldx = padded_sums_ld(H), ldh = padded_sums_ld(I);
-  L.ctrl = take(16384);
+  L.ctrl = take(kCtlBytes);
   L.logits = take(4 * T * E);
   L.gate_logit = take(4 * T);
   L.idx = take(4 * P);
@@ -206,6 +212,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// Bring `bytes` (a multiple of 16, 16-byte aligned) at src into L2 ahead of
+// a later copy, without waiting for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   uint32_t ok;
   asm volatile(

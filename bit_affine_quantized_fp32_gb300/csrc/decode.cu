@@ -1,27 +1,38 @@
 // decode.cu -- the whole decode layer in one persistent launch.
 //
-// One CTA per SM, co-resident (cooperative launch), 18 warps each.
-//   phase 0  router tasks (one router row x one k-split, partial sums for all
-//            tokens) and activation-sum tasks, spread over every warp of the
-//            grid; each finished task adds 1 to a workspace counter;
-//   routing  every CTA waits for the counter, then builds the whole routing
-//            table itself in shared memory (logits from the partial sums,
-//            top-k, bucketing, sub-slots): no second grid-wide round trip;
-//   phase 1  gate/up units, then down units, then combine pieces, balanced
-//            over the CTAs in closed form (FusedSched), run by the item engine
-//            (engine.cuh): the producer warp streams items through TMA stages,
-//            16 consumer warps compute, a signal warp publishes results.
+// One CTA per SM, co-resident (cooperative launch), 19 warps each.
+//   start    the producer claims its first unit from the grid's queue; the
+//            first ceil(T/8) * I/64 queue entries are the shared expert's
+//            gate/up units, which need no routing, so a CTA that drew one
+//            starts streaming its weight items at once;
+//   phase 0  router rows (one k-split of one row per warp) and activation-sum
+//            tasks spread over the grid; every logit is published as one
+//            64-bit word tagged with the call's generation number, the
+//            activation-sum tasks are counted;
+//   routing  every CTA polls the tagged logits until all carry this call's
+//            generation, then builds the whole routing table itself in shared
+//            memory (top-k, bucketing, sub-slots): no fence, no grid-wide
+//            counter and no second round trip;
+//   phase 1  the item engine (engine.cuh) over the queue: shared gate/up,
+//            routed gate/up (sub-slot major), shared down, routed down,
+//            combine pieces.  Each producer claims the next queue entry with
+//            one atomic as soon as it has published the previous one, so the
+//            grid balances itself; a unit waits only on units earlier in the
+//            queue (down on its sub-slot's gate/up units, a combine piece on
+//            the down units of its rows), which are claimed and never wait
+//            on later ones.
 // Producers of data never wait: a finished gate/up or down unit adds 1 to a
-// counter with a release reduction.  Only the producer warp polls, just
+// counter with a release reduction.  Only the operand warp polls, just
 // before it copies operands that other CTAs write (h rows, y rows for the
 // combine); weights are fetched ahead regardless.  The arithmetic is the
 // standalone kernels' (same device functions), so outputs are identical bit
 // for bit.
 //
-// Every wait is bounded: after about a second it writes MOE_ERR_TIMEOUT to the
-// workspace status word and every later wait of the CTA returns at once, so
-// the launch ends (with garbage output; the workspace must then be
-// re-initialised).  The last CTA to leave zeroes the counters.
+// Every wait is bounded: after the workspace's limit (one second by default)
+// it writes MOE_ERR_TIMEOUT to the workspace status word and every later wait
+// of the CTA returns at once, so the launch ends (with garbage output; the
+// workspace must then be re-initialised).  The last CTA to leave zeroes the
+// counters.
 //
 // Sources: "qwen3_5_moe on native CUDA with 3-bit routed experts ... #803",
 // comment "Progress on the 4-bit gate" (routing, grouped experts with a SwiGLU
@@ -37,24 +48,45 @@ namespace moe {
 
 namespace {
 
-// The units of one CTA, resolved from the CTA's own routing table.  Work is
-// balanced in closed form (every CTA computes the same assignment):
-//   gate/up units ("big", c1 items each; shared expert first, then routed in
-//   sub-slot order) go round-robin: big unit b to CTA b mod G;
-//   down units ("small", c2 items each; shared first, then routed in sub-slot
-//   order, so early indices depend on early gate/up units) first fill the
-//   CTAs that got one big unit fewer, q = ceil(c1/c2) each, spread
-//   round-robin over them, then the rest go round-robin over all CTAs;
-//   combine pieces (kCombineRows output columns each) go to CTAs G-1, G-2,
-//   ... (those with the least work).
-// A CTA runs its big units, then its small units, then its combine pieces:
-// big units never wait, small units wait only on big units, combine pieces
-// only on small units, so every wait is on work that is already queued ahead.
+// Shared-expert gate/up unit v (queue entries 0 .. ceil(T/8) * I/64 - 1):
+// decodable before routing.
+// Activation-sum tasks of a call (one per token and 128 columns); gate/up
+// operands wait until they are all done.
+__device__ __forceinline__ int n_xsum_tasks(const DecodeArgs& A) {
+  return A.R.T * (A.R.H >> 7);
+}
+
+__device__ __forceinline__ UnitInfo shared_gateup_unit(const DecodeArgs& A, int v) {
+  const int ngr = A.C.inter / 64;
+  const int ss = v / ngr;
+  UnitInfo r{};
+  r.kind = kItemGateUp;
+  r.mat = 2;
+  r.e = 0;
+  r.blk = v - ss * ngr;
+  r.off = kMaxTok * ss;
+  r.cnt = min(kMaxTok, A.R.T - kMaxTok * ss);
+  r.nch = A.C.geo[2].t.nch;
+  r.rows = kRowsDirect;
+  r.signal = kSharedReady + ss;
+  r.wait_ctr = kCtlXsum;
+  r.wait_target = n_xsum_tasks(A);
+  return r;
+}
+
+__device__ __forceinline__ int n_shared_gateup(const DecodeArgs& A) {
+  return A.has_shared ? ((A.R.T + kMaxTok - 1) / kMaxTok) * (A.C.inter / 64) : 0;
+}
+
+// The grid's queue, resolved from the CTA's own routing table:
+//   [nA shared gate/up][nB routed gate/up][nC shared down][nD routed down]
+//   [ncp combine pieces]
+// gate/up and down units sub-slot major, so a sub-slot's blocks are claimed
+// together; claims come from one atomic counter in the workspace.
 struct FusedSched {
   const DecodeArgs* A;
   const RouteTable* RT;
   int T, ngr, nrb, ncp, nss_sh, nss, nA, nB, nC, nD;
-  int G, c, NB, NS, r, q, atot, nb, qa, qb, ne;
 
   __device__ FusedSched(const DecodeArgs* a, const RouteTable* rt) : A(a), RT(rt) {
     T = A->R.T;
@@ -67,99 +99,58 @@ struct FusedSched {
     nB = nss * ngr;
     nC = nss_sh * nrb;
     nD = nss * nrb;
-    G = gridDim.x;
-    c = blockIdx.x;
-    NB = nA + nB;
-    NS = nC + nD;
-    const int c1 = A->C.geo[0].t.nch, c2 = A->C.geo[1].t.nch;
-    r = NB % G;
-    q = r ? (c1 + c2 - 1) / c2 : 0;
-    atot = min(NS, (G - r) * q);
-    nb = NB / G + (c < r ? 1 : 0);
-    // phase-A small units of CTA c: i = k*(G-r) + (c-r), k < q, i < atot
-    qa = 0;
-    if (c >= r && q > 0 && c - r < atot) qa = min(q, (atot - (c - r) + (G - r) - 1) / (G - r));
-    // phase-B small units: i = atot + m*G + c < NS
-    qb = NS - atot > c ? (NS - atot - c + G - 1) / G : 0;
-    // combine piece e on CTA G-1 - (e mod G)
-    const int cc = G - 1 - c;
-    ne = ncp > cc ? (ncp - cc + G - 1) / G : 0;
   }
-  __device__ int n_units() const { return nb + qa + qb + ne; }
-  __device__ UnitInfo unit(int j) const {
-    UnitInfo r_{};
-    r_.wait_ctr = -1;
-    if (j < nb) return big(c + j * G);
-    j -= nb;
-    if (j < qa) return small(j * (G - r) + (c - r));
-    j -= qa;
-    if (j < qb) return small(atot + j * G + c);
-    j -= qb;
-    const int e = (G - 1 - c) + j * G;
-    r_.kind = kItemCombine;
-    r_.blk = e;
-    r_.signal = -1;
-    r_.wait_ctr = kCtlRb + e * kCombineRows / kUnitRows;
-    r_.wait_target = nss + nss_sh;
-    return r_;
-  }
-  __device__ UnitInfo big(int v) const {
-    UnitInfo r_{};
-    r_.wait_ctr = -1;
-    r_.kind = kItemGateUp;
-    if (v < nA) {
-      const int ss = v / ngr;
-      r_.mat = 2;
-      r_.e = 0;
-      r_.blk = v - ss * ngr;
-      r_.off = kMaxTok * ss;
-      r_.cnt = min(kMaxTok, T - kMaxTok * ss);
-      r_.nch = A->C.geo[2].t.nch;
-      r_.rows = kRowsDirect;
-      r_.signal = kSharedReady + ss;
-      return r_;
+  __device__ int claim(int) const { return atomicAdd(A->ctrl + kCtlQueue, 1); }
+  __device__ bool unit(int j, UnitInfo& r) const {
+    r = UnitInfo{};
+    if (j < nA) {
+      r = shared_gateup_unit(*A, j);
+      return true;
     }
-    v -= nA;
-    const int ss = v / ngr;
-    r_.mat = 0;
-    r_.e = RT->ss_e[ss];
-    r_.blk = v - ss * ngr;
-    r_.off = RT->ss_off[ss];
-    r_.cnt = RT->ss_cnt[ss];
-    r_.nch = A->C.geo[0].t.nch;
-    r_.rows = kRowsGather;
-    r_.signal = kCtlReady + ss;
-    return r_;
-  }
-  __device__ UnitInfo small(int v) const {
-    UnitInfo r_{};
-    r_.kind = kItemDown;
-    r_.wait_target = ngr;
-    if (v < nC) {
+    j -= nA;
+    if (j < nB) {
+      const int ss = j / ngr;
+      r.kind = kItemGateUp;
+      r.mat = 0;
+      r.e = RT->ss_e[ss];
+      r.blk = j - ss * ngr;
+      r.off = RT->ss_off[ss];
+      r.cnt = RT->ss_cnt[ss];
+      r.nch = A->C.geo[0].t.nch;
+      r.rows = kRowsGather;
+      r.signal = kCtlReady + ss;
+      r.wait_ctr = kCtlXsum;
+      r.wait_target = n_xsum_tasks(*A);
+      return true;
+    }
+    j -= nB;
+    if (j < nC + nD) {
+      const bool sh = j < nC;
+      const int v = sh ? j : j - nC;
       const int ss = v / nrb;
-      r_.mat = 3;
-      r_.e = 0;
-      r_.blk = v - ss * nrb;
-      r_.off = kMaxTok * ss;
-      r_.cnt = min(kMaxTok, T - kMaxTok * ss);
-      r_.nch = A->C.geo[3].t.nch;
-      r_.rows = kRowsDirect;
-      r_.signal = kCtlRb + r_.blk;
-      r_.wait_ctr = kSharedReady + ss;
-      return r_;
+      r.kind = kItemDown;
+      r.mat = sh ? 3 : 1;
+      r.e = sh ? 0 : RT->ss_e[ss];
+      r.blk = v - ss * nrb;
+      r.off = sh ? kMaxTok * ss : RT->ss_off[ss];
+      r.cnt = sh ? min(kMaxTok, T - kMaxTok * ss) : RT->ss_cnt[ss];
+      r.nch = A->C.geo[r.mat].t.nch;
+      r.rows = sh ? kRowsDirect : kRowsScatter;
+      r.signal = kCtlRb + r.blk;
+      r.wait_ctr = (sh ? kSharedReady : kCtlReady) + ss;
+      r.wait_target = ngr;
+      return true;
     }
-    v -= nC;
-    const int ss = v / nrb;
-    r_.mat = 1;
-    r_.e = RT->ss_e[ss];
-    r_.blk = v - ss * nrb;
-    r_.off = RT->ss_off[ss];
-    r_.cnt = RT->ss_cnt[ss];
-    r_.nch = A->C.geo[1].t.nch;
-    r_.rows = kRowsScatter;
-    r_.signal = kCtlRb + r_.blk;
-    r_.wait_ctr = kCtlReady + ss;
-    return r_;
+    j -= nC + nD;
+    if (j < ncp) {
+      r.kind = kItemCombine;
+      r.blk = j;
+      r.signal = -1;
+      r.wait_ctr = kCtlRb + j * kCombineRows / kUnitRows;
+      r.wait_target = nss + nss_sh;
+      return true;
+    }
+    return false;
   }
   __device__ const MatSource& source(int mat) const { return A->src[mat]; }
   __device__ const int* perm() const { return RT->perm; }
@@ -180,6 +171,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   __shared__ RouteTable RT;
   __shared__ float RT_part[kConsumerWarps * 32];  // router partials [warp][T]
   __shared__ int last;
+  __shared__ unsigned s_gen;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x;
   int* ctrl = A.ctrl;
@@ -187,25 +179,47 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   const int T = A.R.T, H = A.R.H, NE = A.R.E;
   const bool gate = A.R.gq != nullptr;
   const int E1 = NE + (gate ? 1 : 0);
+  // this call's generation number: the tag of its published logits
+  if (tid == 0) s_gen = unsigned(*(volatile const int*)(ctrl + kCtlGen)) + 1u;
   engine_init(E, P.S, A.ctrl);
   const EngineMem M{smem, smem + P.nob * P.OB, P.OB, P.nob, P.SB, P.S};
   fence_proxy_async();
   __syncthreads();
+  const unsigned gen = s_gen;
+  unsigned long long* tagged =
+      reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ctrl) + kCtlTaggedOffset);
+  const int TS = (NE + 2) & ~1;  // row stride of the tagged logits (even: 16-byte pairs)
+
+  // ---- start: the producer's first claim; a shared-expert gate/up unit
+  // (no routing needed) starts streaming its weight items now
+  ProducerStart pst{0, 0};
+  if (warp == kProducerWarp) {
+    int j0 = 0;
+    if (lane == 0) j0 = atomicAdd(ctrl + kCtlQueue, 1);
+    j0 = __shfl_sync(0xffffffffu, j0, 0);
+    pst.j = j0;
+    if (j0 < n_shared_gateup(A)) {
+      const UnitInfo u = shared_gateup_unit(A, j0);
+      pst.issued = min(P.S, u.nch);
+      for (int c = 0; c < pst.issued; ++c)
+        produce_weights(A.C.geo[u.mat], u, c, M.stages + (size_t)c * M.SB, &E.full[c]);
+    }
+  }
 
   // ---- phase 0: router rows and activation sums
-  // Router blocks of RPB rows x KS k-splits (one warp each, rows finalised in
-  // shared memory), as few rows per CTA as the grid allows so that each SM
-  // streams little of the router; x is read through L2 together with the
-  // weights.  Activation-sum tasks go to the CTAs without router rows.
+  // Router blocks of RPB rows x KS k-splits (one warp each), as few rows per
+  // CTA as the grid allows so that each SM streams little of the router; x
+  // is read through L2 together with the weights.  Each logit is published
+  // as a tagged word (no fence, no counter).  Activation-sum tasks go to the
+  // CTAs without router rows and are counted.
   const int KS = A.KS;
   const int RPB = max(1, min(kConsumerWarps / KS, (E1 + G - 1) / G));
   const int nrb_router = (E1 + RPB - 1) / RPB;
-  const int nx = T * (H >> 7);
+  const int nx = n_xsum_tasks(A);
   int done = 0;
-  for (int rb = blockIdx.x; rb < nrb_router; rb += G) {
-    router_rows_cta(A.R, KS, RPB * KS, rb, RT_part, A.R.x, NoPre());
-    if (tid == 0) red_release_add(ctrl + kCtlPhase0, 1);
-  }
+  if (warp < kConsumerWarps)
+    for (int rb = blockIdx.x; rb < nrb_router; rb += G)
+      router_rows_cta(A.R, KS, RPB, rb, RT_part, tagged, TS, gen);
   {
     const int free_ctas = nrb_router < G ? G - nrb_router : G;
     const int first = nrb_router < G ? nrb_router : 0;
@@ -218,18 +232,15 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
     }
   }
   __syncwarp();
-  if (lane == 0 && done) red_release_add(ctrl + kCtlPhase0, done);
-  const int n_tasks = nrb_router + nx;
+  if (lane == 0 && done) red_release_add(ctrl + kCtlXsum, done);
 
-  // ---- routing, redundantly in every CTA
-  if (tid == 0) wait_counter(ctrl + kCtlPhase0, n_tasks, &E.wc, status);
-  __syncthreads();
+  // ---- routing, redundantly in every CTA, from the tagged logits
   {
     int(*wc)[256] = reinterpret_cast<int(*)[256]>(smem);
     const bool first = blockIdx.x == 0;
-    route_table_cta(A.R.logits, gate ? A.R.gate_logit : nullptr, T, NE, A.k,
-                    first ? A.user_idx : nullptr, first ? A.user_w : nullptr, wc, RT,
-                    A.R.round_bf16 != 0);
+    route_table_cta(nullptr, nullptr, T, NE, A.k, first ? A.user_idx : nullptr,
+                    first ? A.user_w : nullptr, wc, RT, A.R.round_bf16 != 0, tagged, TS, gen,
+                    gate, &E.wc, status);
   }
   fence_proxy_async();  // routing scratch (generic writes) before TMA reuses it
   __syncthreads();
@@ -238,7 +249,9 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   {
     const FusedSched sch(&A, &RT);
     if (warp == kProducerWarp)
-      producer_run(A.C, E, M, sch, ctrl);
+      producer_run(A.C, E, M, sch, pst);
+    else if (warp == kOperandWarp)
+      operand_run(A.C, E, M, sch, ctrl);
     else if (warp == kSignalWarp)
       signal_run(E, sch, ctrl, status);
     else
@@ -255,7 +268,11 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   }
   __syncthreads();
   if (last) {
-    if (tid == 0) ctrl[kCtlPhase0] = 0;
+    if (tid == 0) {
+      ctrl[kCtlXsum] = 0;
+      ctrl[kCtlQueue] = 0;
+      ctrl[kCtlGen] = int(gen);
+    }
     for (int i = kCtlReady + tid; i < kCtlEnd; i += kEngineThreads) ctrl[i] = 0;
   }
 }

@@ -8,15 +8,16 @@ namespace moe {
 // Control words (int32 indices into the workspace's control region).  They
 // start at zero (moe_workspace_init); the last CTA of every fused call zeroes
 // them again, except the exit counter, which only ever grows.
-constexpr int kCtlPhase0 = 32;       // router and activation-sum tasks finished
+constexpr int kCtlXsum = 32;         // activation-sum tasks finished
+constexpr int kCtlQueue = 33;        // the grid's unit queue: next entry to claim
+constexpr int kCtlGen = 34;          // generation number of the last completed call
 constexpr int kCtlExit = 35;         // CTAs finished (monotonic)
 static_assert(kCtlWaitLimit > kCtlExit && kCtlWaitLimit < 64, "control word clash");
 constexpr int kCtlReady = 64;        // [296]: 64-row h groups done per routed sub-slot
 constexpr int kSharedReady = kCtlReady + 296;  // [24]: same for the shared sub-slots
 constexpr int kCtlRb = kCtlReady + 320;        // [64]: down units done per 128-row block
 constexpr int kCtlEnd = kCtlRb + 64;
-constexpr int kCtlBytes = 16384;
-static_assert(kCtlEnd * 4 <= kCtlBytes, "control region too small");
+static_assert(kCtlEnd * 4 <= kCtlTaggedOffset, "control words overlap the tagged logits");
 
 struct DecodeArgs {
   RouterJob R;          // router, shared gate, bias, x, T, E, H, f16

@@ -2,23 +2,27 @@
 // by the standalone expert kernels (units.cu) and the fused layer kernel
 // (decode.cu).
 //
-// A CTA has 18 warps: warps 0..15 are the consumers, warp 16 the producer,
-// warp 17 the signal warp (it publishes finished units to other CTAs, so the
-// consumers never wait on a gpu-scope release).
+// A CTA has 19 warps: warps 0..15 are the consumers, warp 16 the producer
+// (weights), warp 17 the operand warp, warp 18 the signal warp.
 // Work comes as "units": one sub-slot (<= 8 tokens of one expert) times one
 // 128-row block of a matrix, streamed as k-chunk "items".  An item is a
 // contiguous block of the kernel-tiled bank (codes + scales, tiled.cuh); the
 // unit's operand rows (x, or h as bf16 hi + lo, full K) and their per-64-group
 // sums sit in one of two operand buffers for the whole unit.
-//   producer: for each item, waits until its stage is free (empty barrier)
-//             and fills it with one TMA bulk copy that completes on the
-//             stage's full barrier; once per unit it fills an operand buffer
-//             the same way (one copy per x row, or three block copies for h);
-//             it alone waits on other CTAs (operands produced in the kernel).
-//   consumers: wait for the full barrier, run the MMA pass over the item,
-//             release the stage, and after the last item of a unit reduce and
-//             write the unit's result (SwiGLU -> h, or y).
-// There is no CTA-wide barrier in the item loop; consumers synchronise only
+//   producer: claims units from the schedule (a queue shared by the grid in
+//             the fused kernel), publishes each into a ring of unit
+//             descriptors in shared memory, and streams its weight items by
+//             TMA bulk copy into the stage ring (waiting only until a stage
+//             is free), so weights keep flowing while operands wait;
+//   operand:  per unit, waits for the unit's dependency on other CTAs (h
+//             rows, y rows for a combine piece) if any, then fills an operand
+//             buffer (one copy per x row, or three block copies for h);
+//   consumers: wait for the operand buffer and each item's stage, run the MMA
+//             pass, release the stage, and after the last item reduce and
+//             write the unit's result (SwiGLU -> h, or y);
+//   signal:   publishes finished units to other CTAs with a release
+//             reduction, so no consumer waits on a gpu-scope release.
+// There is no CTA-wide barrier in the unit loop; consumers synchronise only
 // among themselves in a unit's epilogue.
 //
 // Warp w of the consumers owns the 16-row M-tile (w & 7) and the k-half
@@ -29,8 +33,8 @@
 // integers (fp32 accumulation, exact products); s and b are applied in fp32.
 // Every output element is one MMA column with a fixed k-order and fixed fp32
 // reductions, so a token's result never depends on the other tokens of the
-// call or on its sub-slot, and the fused and standalone kernels (same device
-// functions) give the same bits.
+// call, on its sub-slot or on the CTA that runs the unit, and the fused and
+// standalone kernels (same device functions) give the same bits.
 //
 // Source: "qwen3_5_moe on native CUDA with 3-bit routed experts ... #803",
 // comment "Progress on the 4-bit gate" (grouped affine experts with a SwiGLU
@@ -45,9 +49,12 @@ namespace moe {
 
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = 32 * kConsumerWarps;     // 512
-constexpr int kEngineThreads = kConsumers + 64;     // + producer and signal warps
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kSignalWarp = kConsumerWarps + 1;
+constexpr int kProducerWarp = kConsumerWarps;       // weights
+constexpr int kOperandWarp = kConsumerWarps + 1;    // operand rows
+constexpr int kSignalWarp = kConsumerWarps + 2;     // publishes finished units
+constexpr int kEngineThreads = kConsumers + 96;
+constexpr int kUnitRing = 16;                       // unit descriptors in flight
+constexpr int kRingReaders = kConsumerWarps + 2;    // consumer, operand and signal warps
 constexpr int kEpiRing = 4;
 constexpr int kUnitRows = 128;
 constexpr int kMaxTok = 8;
@@ -73,7 +80,13 @@ __host__ __device__ inline int sums_pos(const TileGeo& t, int j) {
   return (j / t.ng) * sums_ngp(t) + j % t.ng;
 }
 
-enum : int { kItemGateUp = 0, kItemDown = 1, kItemCombine = 2 };
+// A unit covers a 128-row block (gate/up: 64 gate rows + their 64 up rows);
+// the consumers split it as 8 M-tiles x 2 groups of k.
+constexpr int kTiles = 8, kKsplit = 2;
+
+
+
+enum : int { kItemGateUp = 0, kItemDown = 1, kItemCombine = 2, kItemEnd = 3 };
 
 // A weight stage holds one tiled item.
 __host__ __device__ inline int stage_bytes(const TileGeo& t) { return align128i(t.item_bytes); }
@@ -222,6 +235,25 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   return v;
 }
 
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// two consecutive 64-bit words (16-byte aligned), each read single-copy atomically
+__device__ __forceinline__ void ld_relaxed_v2u64(const unsigned long long* p, unsigned long long& a,
+                                                 unsigned long long& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];\n"
+               : "=l"(a), "=l"(b)
+               : "l"(p)
+               : "memory");
+}
+
 __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
 }
@@ -278,39 +310,41 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t v) {
   return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
-// One k-chunk item (chunk c) for consumer warp (tile, kh): groups
-// [kh*NG/2, (kh+1)*NG/2) of M-tile `tile`, added into acc.  NG = CK/64 is a
-// compile-time constant so the group loop unrolls completely (a rolled loop
-// costs several times the instructions).  wst is the weight stage, op the
-// unit's operand buffer.  acc[0]: (row g, token 2t), acc[1]: (g, 2t+1),
-// acc[2]: (g+8, 2t), acc[3]: (g+8, 2t+1).  Operand columns of tokens >= cnt
-// hold whatever the buffer held before; MMA columns are independent, so they
-// only touch accumulators that are never written out.
-template <int FMT, bool F16A, bool SPLIT, int NG>
+// One k-chunk item (chunk c) for consumer warp (tile, ks): the item's stage
+// holds TILES M-tiles (codes: tile t, group G at (t * NG + G) * CB; then the
+// scales of the TILES tiles), and the warp takes the groups G = ks, ks +
+// KSPLIT, ... < NG of its tile, added into acc.  NG = CK/64 is a compile-time
+// constant so the group loop unrolls completely (a rolled loop costs several
+// times the instructions).  op is the unit's operand buffer.  acc[0]: (row g,
+// token 2t), acc[1]: (g, 2t+1), acc[2]: (g+8, 2t), acc[3]: (g+8, 2t+1).
+// Operand columns of tokens >= cnt hold whatever the buffer held before; MMA
+// columns are independent, so they only touch accumulators that are never
+// written out.
+template <int FMT, bool F16A, bool SPLIT, int NG, int TILES, int KSPLIT>
 __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* wst,
                                              const uint8_t* op, const OpLayout& L, int c,
-                                             int tile, int kh, uint32_t mg, float (&acc)[4]) {
+                                             int tile, int ks, uint32_t mg, float (&acc)[4]) {
   constexpr int CB = FMT == MOE_FMT_AFFINE3_G64 ? 384 : 512;
-  constexpr int GH = NG / 2;
   constexpr int NGP = (NG + 3) & ~3;
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, t = lane & 3;
-  const int G0 = kh * GH;
-  const uint8_t* codes = wst + (tile * NG + G0) * CB;
-  const int xo = gq * L.bpitch + c * NG * 128 + G0 * 128 + 32 * t;
+  const int xo = gq * L.bpitch + c * NG * 128 + 32 * t;
   const uint8_t* xrow = op + L.x + xo;
   const uint8_t* xlrow = op + L.xlo + xo;
-  const float* xs0 = reinterpret_cast<const float*>(op + L.xs) + (2 * t) * L.lds + c * NGP + G0;
+  const float* xs0 = reinterpret_cast<const float*>(op + L.xs) + (2 * t) * L.lds + c * NGP;
   const float* xs1 = xs0 + L.lds;
-  const uint8_t* sc = wst + 8 * NG * CB;
+  const uint8_t* sc = wst + TILES * NG * CB;
 #pragma unroll
-  for (int G = 0; G < GH; ++G) {
+  for (int i = 0; i < (NG + KSPLIT - 1) / KSPLIT; ++i) {
+    const int G = ks + KSPLIT * i;
+    if (NG % KSPLIT != 0 && G >= NG) break;
+    const uint8_t* codes = wst + (tile * NG + G) * CB;
     uint32_t w0, w1, w2, w3;
     if constexpr (FMT == MOE_FMT_AFFINE3_G64) {
-      const uint32_t* pl = reinterpret_cast<const uint32_t*>(codes + G * 384) + lane;
+      const uint32_t* pl = reinterpret_cast<const uint32_t*>(codes) + lane;
       planes_to_words(pl[0], pl[32], pl[64], w0, w1, w2, w3);
     } else {
-      const uint4 v = *reinterpret_cast<const uint4*>(codes + G * 512 + lane * 16);
+      const uint4 v = *reinterpret_cast<const uint4*>(codes + lane * 16);
       w0 = v.x;
       w1 = v.y;
       w2 = v.z;
@@ -343,8 +377,8 @@ __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* w
     }
     float s0, s1, b0, b1;
     if constexpr (FMT == MOE_FMT_W4A16_SYM_G128) {
-      const uint32_t sv = *reinterpret_cast<const uint32_t*>(
-          sc + ((tile * 8 + gq) * (NG / 2) + ((G0 + G) >> 1)) * 4);
+      const uint32_t sv =
+          *reinterpret_cast<const uint32_t*>(sc + ((tile * 8 + gq) * (NG / 2) + (G >> 1)) * 4);
       const float2 sf = half2_bits_to_float2(sv);
       s0 = sf.x;
       s1 = sf.y;
@@ -353,8 +387,7 @@ __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* w
       b0 = (F16A ? -8.f : -136.f) * s0;
       b1 = (F16A ? -8.f : -136.f) * s1;
     } else {
-      const uint2 sv =
-          *reinterpret_cast<const uint2*>(sc + ((tile * 8 + gq) * NG + G0 + G) * 8);
+      const uint2 sv = *reinterpret_cast<const uint2*>(sc + ((tile * 8 + gq) * NG + G) * 8);
       const float2 p0 = half2_bits_to_float2(sv.x), p1 = half2_bits_to_float2(sv.y);
       s0 = p0.x;
       b0 = p0.y;
@@ -430,6 +463,9 @@ struct EngineSmem {
   uint64_t op_empty[2];
   uint64_t epi_full[kEpiRing];    // unit results written (consumers -> signal warp)
   uint64_t epi_empty[kEpiRing];   // unit published (signal warp -> consumers)
+  uint64_t ring_full[kUnitRing];  // unit descriptor published (producer -> readers)
+  uint64_t ring_empty[kUnitRing]; // descriptor read by every reader warp
+  UnitInfo ring[kUnitRing];
   WaitCtl wc;                     // wait limit and timeout flag
   float red[2][8][32][4];         // epilogue: accumulators by k-half, tile, lane
   float part[kConsumerWarps];     // epilogue: per-warp partial sums
@@ -449,6 +485,10 @@ __device__ __forceinline__ void engine_init(EngineSmem& E, int S, const int* ctr
     for (int b = 0; b < kEpiRing; ++b) {
       mbar_init(&E.epi_full[b], kConsumerWarps);
       mbar_init(&E.epi_empty[b], 1);
+    }
+    for (int b = 0; b < kUnitRing; ++b) {
+      mbar_init(&E.ring_full[b], 1);
+      mbar_init(&E.ring_empty[b], kRingReaders);
     }
     wait_ctl_init(E.wc, ctrl);
   }
@@ -476,20 +516,23 @@ struct Ring {
 // ---------------------------------------------------------------------------
 // A unit's MMA pass: wait for the operand buffer, then for every k-chunk wait
 // for its stage, run compute_item and release the stage.  The format, group
-// count and operand split are resolved once per unit (unit_mat), so the chunk
-// loop carries no per-item dispatch or layout arithmetic.
+// count, operand split and warp split are resolved once per unit (unit_mat),
+// so the chunk loop carries no per-item dispatch or layout arithmetic.  Warp
+// w takes M-tile w % 8 and k-group w / 8.
 template <int FMT, bool F16A, bool SPLIT, int NG>
 __device__ __forceinline__ void unit_items(const TileGeo& tg, uint32_t mg, EngineSmem& E,
                                            const EngineMem& M, Ring& R, const uint8_t* op,
-                                           uint64_t* op_full, unsigned op_parity, int tile,
-                                           int kh, int* status, float (&acc)[4]) {
+                                           uint64_t* op_full, unsigned op_parity, int* status,
+                                           float (&acc)[4]) {
+  const int warp = threadIdx.x >> 5;
+  const int tile = warp % kTiles, ks = warp / kTiles;
   const OpLayout L = op_layout(tg);
   const int nch = tg.nch;
   mbar_wait_bounded(op_full, op_parity, &E.wc, status);
   for (int c = 0; c < nch; ++c) {
     mbar_wait_bounded(&E.full[R.slot], R.use & 1, &E.wc, status);
-    compute_item<FMT, F16A, SPLIT, NG>(tg, M.stages + (size_t)R.slot * M.SB, op, L, c, tile, kh,
-                                       mg, acc);
+    compute_item<FMT, F16A, SPLIT, NG, kTiles, kKsplit>(tg, M.stages + (size_t)R.slot * M.SB, op,
+                                                        L, c, tile, ks, mg, acc);
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&E.empty[R.slot]);
     R.next();
@@ -499,14 +542,14 @@ __device__ __forceinline__ void unit_items(const TileGeo& tg, uint32_t mg, Engin
 template <int FMT, bool F16A, bool SPLIT>
 __device__ __forceinline__ void unit_ng(const TileGeo& tg, uint32_t mg, EngineSmem& E,
                                         const EngineMem& M, Ring& R, const uint8_t* op,
-                                        uint64_t* op_full, unsigned op_parity, int tile, int kh,
-                                        int* status, float (&acc)[4]) {
+                                        uint64_t* op_full, unsigned op_parity, int* status,
+                                        float (&acc)[4]) {
   if (tg.ng == 8)
-    unit_items<FMT, F16A, SPLIT, 8>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, status, acc);
+    unit_items<FMT, F16A, SPLIT, 8>(tg, mg, E, M, R, op, op_full, op_parity, status, acc);
   else if (tg.ng == 4)
-    unit_items<FMT, F16A, SPLIT, 4>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, status, acc);
+    unit_items<FMT, F16A, SPLIT, 4>(tg, mg, E, M, R, op, op_full, op_parity, status, acc);
   else
-    unit_items<FMT, F16A, SPLIT, 2>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, status, acc);
+    unit_items<FMT, F16A, SPLIT, 2>(tg, mg, E, M, R, op, op_full, op_parity, status, acc);
 }
 
 // Matrix slot `mat` (0/2 gate/up, 1/3 down); slots 0/1 hold format FMT,
@@ -515,37 +558,72 @@ __device__ __forceinline__ void unit_ng(const TileGeo& tg, uint32_t mg, EngineSm
 template <int FMT, int FMT_SH, bool F16A>
 __device__ __forceinline__ void unit_mat(const EngineCfg& C, int mat, EngineSmem& E,
                                          const EngineMem& M, Ring& R, const uint8_t* op,
-                                         uint64_t* op_full, unsigned op_parity, int tile, int kh,
+                                         uint64_t* op_full, unsigned op_parity,
                                          float (&acc)[4]) {
   const TileGeo& tg = C.geo[mat].t;
   const bool down = mat & 1;
   const uint32_t mg = (F16A && !down) ? C.magic_f16 : C.magic_bf16;
   if (FMT_SH == FMT || mat < 2) {
     if (down)
-      unit_ng<FMT, false, true>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, C.status, acc);
+      unit_ng<FMT, false, true>(tg, mg, E, M, R, op, op_full, op_parity, C.status, acc);
     else
-      unit_ng<FMT, F16A, false>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, C.status, acc);
+      unit_ng<FMT, F16A, false>(tg, mg, E, M, R, op, op_full, op_parity, C.status, acc);
   } else {
     if (down)
-      unit_ng<FMT_SH, false, true>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, C.status,
-                                   acc);
+      unit_ng<FMT_SH, false, true>(tg, mg, E, M, R, op, op_full, op_parity, C.status, acc);
     else
-      unit_ng<FMT_SH, F16A, false>(tg, mg, E, M, R, op, op_full, op_parity, tile, kh, C.status,
-                                   acc);
+      unit_ng<FMT_SH, F16A, false>(tg, mg, E, M, R, op, op_full, op_parity, C.status, acc);
   }
+}
+
+// ---------------------------------------------------------------------------
+// The unit ring: the producer publishes unit descriptors in claim order; the
+// consumer, operand and signal warps read them in the same order.
+//
+// A schedule (Sched) provides
+//   claim(n)    the queue index of this CTA's n-th claim (producer lane 0);
+//   unit(j, u)  the unit at queue index j, false past the end;
+//   source(mat), perm(), topk(), combine(blk).
+
+__device__ __forceinline__ void ring_put(EngineSmem& E, int pos, const UnitInfo& u,
+                                         int* status) {
+  const int s = pos % kUnitRing;
+  if (pos >= kUnitRing)
+    mbar_wait_bounded(&E.ring_empty[s], ((pos / kUnitRing) - 1) & 1, &E.wc, status);
+  E.ring[s] = u;
+  mbar_arrive(&E.ring_full[s]);  // release: the descriptor is visible to the readers
+}
+
+// The unit at ring position pos (every lane of a reader warp); after a
+// timeout the reader ends its loop (kItemEnd).
+__device__ __forceinline__ UnitInfo ring_take(EngineSmem& E, int pos, int* status) {
+  const int s = pos % kUnitRing;
+  UnitInfo u;
+  if (mbar_wait_bounded(&E.ring_full[s], (pos / kUnitRing) & 1, &E.wc, status)) {
+    u = E.ring[s];
+  } else {
+    u = UnitInfo{};
+    u.kind = kItemEnd;
+  }
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&E.ring_empty[s]);
+  return u;
 }
 
 // ---------------------------------------------------------------------------
 // Producer (warp kProducerWarp, all 32 lanes).
 
 // Weight item (u, c) into a stage: one bulk copy.
+__device__ __forceinline__ const uint8_t* item_src(const MatGeo& g, const UnitInfo& u, int c) {
+  return g.base + (size_t)u.e * g.t.expert_bytes + (size_t)(u.blk * g.t.nch + c) * g.t.item_bytes;
+}
+
 __device__ __forceinline__ void produce_weights(const MatGeo& g, const UnitInfo& u, int c,
                                                 uint8_t* st, uint64_t* full) {
   if ((threadIdx.x & 31) == 0) {
-    const int bytes = g.t.item_bytes;
-    mbar_expect_tx(full, unsigned(bytes));
-    bulk_g2s(st, g.base + (size_t)u.e * g.t.expert_bytes + (size_t)(u.blk * g.t.nch + c) * bytes,
-             unsigned(bytes), full);
+    const unsigned bytes = unsigned(g.t.item_bytes);
+    mbar_expect_tx(full, bytes);
+    bulk_g2s(st, item_src(g, u, c), bytes, full);
   }
 }
 
@@ -589,17 +667,38 @@ __device__ __forceinline__ void produce_operands(const EngineCfg& C, const MatSo
   }
 }
 
-// The producer's loop over a schedule (sch.n_units(), sch.unit(j)): per unit,
-// the first weight item, then the operands, then the other items.
+// Items [c0, nch) of unit u into L2 (one thread), so that their later copies
+// into a stage come from L2.
+__device__ __forceinline__ void prefetch_unit(const EngineCfg& C, const UnitInfo& u, int c0) {
+  if (u.kind != kItemGateUp && u.kind != kItemDown) return;
+  const MatGeo& g = C.geo[u.mat];
+  for (int c = c0; c < u.nch; ++c) bulk_prefetch_l2(item_src(g, u, c), unsigned(g.t.item_bytes));
+}
+
+// Where the producer starts: its first claimed queue index, and how many of
+// that unit's weight items it already issued into stages 0.. (the fused
+// kernel fills the stages with a routing-independent unit before routing).
+struct ProducerStart {
+  int j;
+  int issued;
+};
+
+// The producer's loop: publish the unit, claim the next one (the atomic is in
+// flight while this unit's items are issued), stream this unit's weight items
+// into the stage ring, then prefetch the next unit's items into L2 -- which
+// keeps enough bytes in flight for HBM (the stage ring alone holds too few)
+// without queueing copies that are needed now behind prefetches.  The call's
+// very first copy is left to land before the rest of the first unit's stages
+// go out: every CTA starts at once, and a CTA's first item would otherwise
+// share HBM with all the grid's later stages and land with them.
 template <class Sched>
 __device__ void producer_run(const EngineCfg& C, EngineSmem& E, const EngineMem& M,
-                             const Sched& sch, const int* ctrl) {
+                             const Sched& sch, ProducerStart st) {
   const int lane = threadIdx.x & 31;
-  Ring R{0, 0, M.S}, B{0, 0, M.nob};
-  const int nu = sch.n_units();
-  // A stage (operand buffer) is refilled once the consumers released it and
-  // its previous fill has landed -- immediate unless a timeout let the
-  // consumers skip their wait: one fill per barrier phase.
+  Ring R{st.issued % M.S, st.issued / M.S, M.S};
+  // A stage is refilled once the consumers released it and its previous fill
+  // has landed -- immediate unless a timeout let the consumers skip their
+  // wait: one fill per barrier phase.
   auto take_stage = [&]() -> uint8_t* {
     if (R.use > 0) {
       if (lane == 0) {
@@ -610,21 +709,57 @@ __device__ void producer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
     }
     return M.stages + (size_t)R.slot * M.SB;
   };
-  for (int j = 0; j < nu; ++j) {
-    const UnitInfo u = sch.unit(j);
-    if (u.kind == kItemCombine) {
-      take_stage();
-      if (lane == 0) {
-        wait_counter(ctrl + u.wait_ctr, u.wait_target, &E.wc, C.status);
-        mbar_arrive(&E.full[R.slot]);
+  int cur = st.j, first = st.issued;
+  for (int pos = 0, n = 1;; ++pos, ++n) {
+    UnitInfo u;
+    const bool more = sch.unit(cur, u);
+    if (!more) u.kind = kItemEnd;
+    if (lane == 0) ring_put(E, pos, u, C.status);
+    __syncwarp();
+    if (!more) break;
+    int nxt = 0;
+    if (lane == 0) nxt = sch.claim(n);
+    if (u.kind != kItemCombine) {
+      const MatGeo& g = C.geo[u.mat];
+      for (int c = first; c < u.nch; ++c) {
+        produce_weights(g, u, c, take_stage(), &E.full[R.slot]);
+        R.next();
+        if (pos == 0 && c == 0) {  // the call's first copy lands first
+          if (lane == 0) mbar_wait_bounded(&E.full[0], 0, &E.wc, C.status);
+          __syncwarp();
+        }
       }
-      __syncwarp();
-      R.next();
-      continue;
     }
-    const MatGeo& g = C.geo[u.mat];
-    produce_weights(g, u, 0, take_stage(), &E.full[R.slot]);
-    R.next();
+    first = 0;
+    cur = __shfl_sync(0xffffffffu, nxt, 0);
+    if (lane == 0) {
+      UnitInfo t;
+      if (sch.unit(cur, t)) prefetch_unit(C, t, 0);
+    }
+  }
+  // wait until the last copies have landed (every stage's most recent fill),
+  // also after a timeout: the CTA may not exit with copies into its shared
+  // memory in flight
+  if (lane == 0)
+    for (int s = 0; s < M.S; ++s) {
+      const int uses = R.use + (s < R.slot ? 1 : 0);
+      if (uses > 0) mbar_drain(&E.full[s], (uses - 1) & 1);
+    }
+  __syncwarp();
+}
+
+// The operand warp's loop: per unit, an operand buffer once the consumers
+// released it (and its previous fill landed), after the unit's dependency
+// on other CTAs.  A combine piece gets an empty fill that only signals that
+// its y rows are complete.
+template <class Sched>
+__device__ void operand_run(const EngineCfg& C, EngineSmem& E, const EngineMem& M,
+                            const Sched& sch, const int* ctrl) {
+  const int lane = threadIdx.x & 31;
+  Ring B{0, 0, M.nob};
+  for (int pos = 0;; ++pos) {
+    const UnitInfo u = ring_take(E, pos, C.status);
+    if (u.kind == kItemEnd) break;
     if (B.use > 0) {
       if (lane == 0) {
         mbar_wait_bounded(&E.op_empty[B.slot], (B.use - 1) & 1, &E.wc, C.status);
@@ -632,27 +767,23 @@ __device__ void producer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
       }
       __syncwarp();
     }
-    produce_operands(C, sch.source(u.mat), u, sch.perm(), sch.topk(),
-                     M.ops + (size_t)B.slot * M.OB, &E.op_full[B.slot], ctrl, &E.wc);
+    if (u.kind == kItemCombine) {
+      if (lane == 0) {
+        wait_counter(ctrl + u.wait_ctr, u.wait_target, &E.wc, C.status);
+        mbar_arrive(&E.op_full[B.slot]);
+      }
+      __syncwarp();
+    } else {
+      produce_operands(C, sch.source(u.mat), u, sch.perm(), sch.topk(),
+                       M.ops + (size_t)B.slot * M.OB, &E.op_full[B.slot], ctrl, &E.wc);
+    }
     B.next();
-    for (int c = 1; c < u.nch; ++c) {
-      produce_weights(g, u, c, take_stage(), &E.full[R.slot]);
-      R.next();
-    }
   }
-  // wait until the last copies have landed (every stage and operand buffer's
-  // most recent fill), also after a timeout: the CTA may not exit with copies
-  // into its shared memory in flight
-  if (lane == 0) {
-    for (int s = 0; s < M.S; ++s) {
-      const int uses = R.use + (s < R.slot ? 1 : 0);
-      if (uses > 0) mbar_drain(&E.full[s], (uses - 1) & 1);
-    }
+  if (lane == 0)
     for (int b = 0; b < M.nob; ++b) {
       const int uses = B.use + (b < B.slot ? 1 : 0);
       if (uses > 0) mbar_drain(&E.op_full[b], (uses - 1) & 1);
     }
-  }
   __syncwarp();
 }
 
@@ -660,7 +791,8 @@ __device__ void producer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
 // Consumer epilogues (all 512 consumer threads).
 
 // SwiGLU of a gate/up unit: warps with tile < 4 hold gate rows 64 blk + 16
-// tile + {g, g+8}, tiles 4..7 the matching up rows; k-halves are added first.
+// tile + {g, g+8}, tiles 4..7 the matching up rows; the k-groups are added
+// first, in order.
 //   h = a / (1 + exp(-a)) * u,  hi = bf16(h), lo = bf16(h - hi)
 // stored at output row out_row(n), columns 64 blk + r, and the padded sum
 // over the 64 rows of (hi + lo) in a fixed tree (32 rows by shuffles, then
@@ -669,9 +801,9 @@ __device__ __forceinline__ void epilogue_gateup(const EngineCfg& C, EngineSmem& 
                                                 const UnitInfo& u, int my_orow,
                                                 const float (&acc)[4]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int tile = warp & 7, kh = warp >> 3;
+  const int tile = warp % kTiles, ks = warp / kTiles;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) E.red[kh][tile][lane][i] = acc[i];
+  for (int i = 0; i < 4; ++i) E.red[ks][tile][lane][i] = acc[i];
   consumer_sync();
   const MatTarget& T = C.tg[u.mat];
   const int I = C.inter;
@@ -748,9 +880,10 @@ template <class Sched>
 __device__ void signal_run(EngineSmem& E, const Sched& sch, int* ctrl, int* status) {
   const int lane = threadIdx.x & 31;
   Ring P{0, 0, kEpiRing};
-  const int nu = sch.n_units();
-  for (int j = 0; j < nu; ++j) {
-    const UnitInfo u = sch.unit(j);
+  (void)sch;
+  for (int pos = 0;; ++pos) {
+    const UnitInfo u = ring_take(E, pos, status);
+    if (u.kind == kItemEnd) break;
     if (u.kind == kItemCombine || u.signal < 0) continue;
     if (lane == 0) {
       mbar_wait_bounded(&E.epi_full[P.slot], P.use & 1, &E.wc, status);
@@ -763,31 +896,29 @@ __device__ void signal_run(EngineSmem& E, const Sched& sch, int* ctrl, int* stat
 }
 
 // ---------------------------------------------------------------------------
-// Consumers' loop over the same schedule as the producer.  sch.combine(blk)
-// runs a combine unit (fused kernel only).
+// Consumers' loop over the units of the ring.  sch.combine(blk) runs a
+// combine piece (fused kernel only).
 template <int FMT, int FMT_SH, bool F16A, class Sched>
 __device__ void consumer_run(const EngineCfg& C, EngineSmem& E, const EngineMem& M,
                              const Sched& sch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int tile = warp & 7, kh = warp >> 3;
+  const int lane = threadIdx.x & 31;
   Ring R{0, 0, M.S}, B{0, 0, M.nob}, P{0, 0, kEpiRing};
   float acc[4];
-  const int nu = sch.n_units();
-  for (int j = 0; j < nu; ++j) {
-    const UnitInfo u = sch.unit(j);
+  for (int pos = 0;; ++pos) {
+    const UnitInfo u = ring_take(E, pos, C.status);
+    if (u.kind == kItemEnd) break;
     if (u.kind == kItemCombine) {
-      mbar_wait_bounded(&E.full[R.slot], R.use & 1, &E.wc, C.status);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&E.empty[R.slot]);
-      R.next();
+      mbar_wait_bounded(&E.op_full[B.slot], B.use & 1, &E.wc, C.status);
       sch.combine(u.blk);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&E.op_empty[B.slot]);
+      B.next();
       continue;
     }
     const int my_orow = lane < u.cnt ? unit_out_row(u, sch.perm(), lane) : 0;
     const uint8_t* op = M.ops + (size_t)B.slot * M.OB;
     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-    unit_mat<FMT, FMT_SH, F16A>(C, u.mat, E, M, R, op, &E.op_full[B.slot], B.use & 1, tile, kh,
-                                acc);
+    unit_mat<FMT, FMT_SH, F16A>(C, u.mat, E, M, R, op, &E.op_full[B.slot], B.use & 1, acc);
     if (lane == 0) mbar_arrive(&E.op_empty[B.slot]);
     B.next();
     if (u.kind == kItemDown)

@@ -159,40 +159,140 @@ __device__ __forceinline__ void router_block(const RouterJob& J, int KS, int rb,
   __syncthreads();
 }
 
-// The fused kernel's router block rb: rows [rb*RPB, rb*RPB + RPB) with
-// RPB = NW / KS, warp (row, q) running router_warp for all T tokens into
-// part [NW][T] (shared), then every (row, token) finalised in split order
-// (router_finalize, as router_block does) into J.logits / J.gate_logit.
-// All threads of the CTA call it; it ends with a barrier.
-template <class Pre>
-__device__ __forceinline__ void router_rows_cta(const RouterJob& J, int KS, int NW, int rb,
-                                                float* part, const uint16_t* xs,
-                                                const Pre& pre) {
+// Split q of R consecutive router rows row0.. (rows >= nrows skipped; the
+// shared-gate row is row E) for all T tokens of J.x, by one warp: every
+// weight of the split in registers, then for each pass of 8 tokens the x
+// values loaded once and used for all R rows.  Per (row, token) the sum has
+// the lane order and xor tree of router_warp, so the partials are the same
+// bits.  Lane 0 writes part[(r * KS + q) * T + t].
+template <int NI, int R>
+__device__ __forceinline__ void router_warp_rows(const RouterJob& J, int KS, int row0, int nrows,
+                                                 int q, float* part) {
+  const int lane = threadIdx.x & 31;
+  const int kq = q * (J.H / KS);
+  const int T = J.T;
+  float w[R][NI][4];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int row = row0 + r < nrows ? row0 + r : row0;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int k = kq + 128 * i + 4 * lane;
+      if (row >= J.E)
+        router_load_w4(J.gfmt, J.gq, J.gs, J.gb, 0, J.H, k, w[r][i], J.round_bf16 != 0);
+      else
+        router_load_w4(J.fmt, J.q, J.s, J.b, row, J.H, k, w[r][i], J.round_bf16 != 0);
+    }
+  }
+  for (int tl = 0; tl < T; tl += 8) {
+    uint2 xv[8][NI];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint16_t* xr = J.x + size_t(min(tl + u, T - 1)) * J.H + kq + 4 * lane;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) xv[u][i] = *reinterpret_cast<const uint2*>(xr + 128 * i);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float acc[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc[u] = 0.f;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          const uint2 v = xv[u][i];
+          acc[u] = fmaf(w[r][i][0], act_to_float(uint16_t(v.x & 0xFFFF), J.f16), acc[u]);
+          acc[u] = fmaf(w[r][i][1], act_to_float(uint16_t(v.x >> 16), J.f16), acc[u]);
+          acc[u] = fmaf(w[r][i][2], act_to_float(uint16_t(v.y & 0xFFFF), J.f16), acc[u]);
+          acc[u] = fmaf(w[r][i][3], act_to_float(uint16_t(v.y >> 16), J.f16), acc[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+        if (lane == 0 && tl + u < T && row0 + r < nrows)
+          part[size_t(r * KS + q) * T + tl + u] = acc[u];
+      }
+    }
+  }
+}
+
+// Rows two at a time when a warp's split is at most 2 x 128 columns (the
+// weights of both rows stay in registers), else one at a time.
+__device__ __forceinline__ void router_warp_rows_any(const RouterJob& J, int KS, int row0,
+                                                     int R, int nrows, int q, float* part) {
+  const int NI_ = J.H / (KS * 128);
+  for (int r0 = 0; r0 < R;) {
+    float* pr = part + size_t(r0) * KS * J.T;
+    if (NI_ <= 2 && R - r0 >= 2) {
+      if (NI_ == 1)
+        router_warp_rows<1, 2>(J, KS, row0 + r0, nrows, q, pr);
+      else
+        router_warp_rows<2, 2>(J, KS, row0 + r0, nrows, q, pr);
+      r0 += 2;
+    } else {
+      if (NI_ == 1)
+        router_warp_rows<1, 1>(J, KS, row0 + r0, nrows, q, pr);
+      else if (NI_ == 2)
+        router_warp_rows<2, 1>(J, KS, row0 + r0, nrows, q, pr);
+      else if (NI_ == 3)
+        router_warp_rows<3, 1>(J, KS, row0 + r0, nrows, q, pr);
+      else
+        router_warp_rows<4, 1>(J, KS, row0 + r0, nrows, q, pr);
+      r0 += 1;
+    }
+  }
+}
+
+// The fused kernel's router block rb: rows [rb*RPB, rb*RPB + RPB) (the
+// shared-gate row is row E), warp (r, q) computing split q of row r into
+// part [RPB * KS][T] (shared; RPB * KS * T <= 512 floats), then every
+// (row, token) finalised in split order (router_finalize, as router_block
+// does).  Threads 0..511 (the consumer warps) call it; it synchronises them
+// with named barrier 2 only, so the CTA's other warps go on meanwhile.
+// With `tagged` set, each logit (and the shared-gate logit, row E) is
+// published instead as one 64-bit word tagged[t * TS + row] = gen << 32 |
+// bits(logit): a reader that sees the call's generation number sees the
+// final value, so no fence or counter is needed.
+__device__ __forceinline__ void router_rows_cta(const RouterJob& J, int KS, int RPB, int rb,
+                                                float* part, unsigned long long* tagged = nullptr,
+                                                int TS = 0, unsigned gen = 0) {
   const int wid = threadIdx.x >> 5;
-  const int RPB = NW / KS;
-  const int rl = wid / KS, q = wid - rl * KS;
-  const int row = rb * RPB + rl;
   const int nrows = J.E + (J.gq ? 1 : 0);
+  const int row0 = rb * RPB;
   // the bias of this thread's first finalisation, fetched before the sums
   float bias0 = 0.f;
   if (J.bias && int(threadIdx.x) < RPB * J.T) {
-    const int row2 = rb * RPB + int(threadIdx.x) / J.T;
+    const int row2 = row0 + int(threadIdx.x) / J.T;
     if (row2 < J.E) bias0 = J.bias[row2];
   }
-  if (wid < RPB * KS && row < nrows) router_warp_any(J, KS, row, q, xs, J.T, part + wid * J.T, 1, pre);
-  __syncthreads();
-  for (int i = threadIdx.x; i < RPB * J.T; i += blockDim.x) {
+  // warp (r, q) computes split q of row row0 + r: one row per warp keeps the
+  // dependent chains short (x is read through L2 once per row)
+  if (wid < RPB * KS) {
+    const int r = wid / KS, q = wid - r * KS;
+    router_warp_rows_any(J, KS, row0 + r, 1, nrows, q, part + size_t(r) * KS * J.T);
+  }
+  asm volatile("bar.sync 2, 512;\n" ::: "memory");
+  for (int i = threadIdx.x; i < RPB * J.T; i += 512) {
     const int r2 = i / J.T, tl = i - r2 * J.T;
-    const int row2 = rb * RPB + r2;
+    const int row2 = row0 + r2;
     if (row2 >= nrows) continue;
     const float* p = part + (r2 * KS) * J.T + tl;
-    if (row2 < J.E)
-      J.logits[size_t(tl) * J.E + row2] = router_finalize(
-          p, J.T, KS, J.bias ? (i == int(threadIdx.x) ? &bias0 : J.bias + row2) : nullptr);
+    const float v =
+        row2 < J.E ? router_finalize(p, J.T, KS,
+                                     J.bias ? (i == int(threadIdx.x) ? &bias0 : J.bias + row2)
+                                            : nullptr)
+                   : router_finalize(p, J.T, KS, nullptr);
+    if (tagged)
+      st_relaxed_u64(tagged + size_t(tl) * TS + row2,
+                     (static_cast<unsigned long long>(gen) << 32) | __float_as_uint(v));
+    else if (row2 < J.E)
+      J.logits[size_t(tl) * J.E + row2] = v;
     else
-      J.gate_logit[tl] = router_finalize(p, J.T, KS, nullptr);
+      J.gate_logit[tl] = v;
   }
-  __syncthreads();
+  asm volatile("bar.sync 2, 512;\n" ::: "memory");
 }
 
 // Ranking key of (logit v, expert id): a larger key ranks first.  The high
@@ -240,7 +340,9 @@ __device__ __forceinline__ void topk_select(unsigned long long (&key)[8], int t,
 #undef MOE_CX
   int my_e = 0;
   float my_v = 0.f, top = 0.f;
-#pragma unroll
+  // rounds as a rolled loop: this code runs once per call, so a small
+  // footprint matters more than the loop overhead
+#pragma unroll 1
   for (int r = 0; r < 8; ++r) {
     if (r < k) {
       const unsigned hi = unsigned(key[0] >> 32), lo = unsigned(key[0]);
@@ -313,6 +415,67 @@ __device__ __forceinline__ void topk_warp(const float* logits, const float* gate
   float gl = 0.f;
   if (gate_logit) gl = SMEM ? gate_logit[t] : __ldcg(gate_logit + t);
   topk_select(key, t, k, idx, w, sg, gate_logit != nullptr, gl, idx2, w2, rb);
+}
+
+// topk_warp on logits published as tagged words (router_rows_cta): the warp
+// polls token t's row until every word carries generation `gen`, bounded by
+// the CTA's wait limit (on a timeout it records MOE_ERR_TIMEOUT and goes on
+// with whatever it read).  Row stride TS (even), the shared-gate logit at
+// column E when has_gate.
+__device__ __forceinline__ void topk_warp_tagged(const unsigned long long* tagged, int TS,
+                                                 unsigned gen, bool has_gate, int t, int E, int k,
+                                                 int32_t* idx, float* w, float* sg, int32_t* idx2,
+                                                 float* w2, bool rb, WaitCtl* wc, int* status) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long* row = tagged + size_t(t) * TS;
+  float v[8];
+  float gl = 0.f;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    bool ok = true;
+    if (8 * lane + 8 <= E) {
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        unsigned long long a, b;
+        ld_relaxed_v2u64(row + 8 * lane + i, a, b);
+        ok = ok && unsigned(a >> 32) == gen && unsigned(b >> 32) == gen;
+        v[i] = __uint_as_float(unsigned(a));
+        v[i + 1] = __uint_as_float(unsigned(b));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[i] = 0.f;
+        if (8 * lane + i < E) {
+          const unsigned long long a = ld_relaxed_u64(row + 8 * lane + i);
+          ok = ok && unsigned(a >> 32) == gen;
+          v[i] = __uint_as_float(unsigned(a));
+        }
+      }
+    }
+    if (has_gate && lane == 0) {
+      const unsigned long long a = ld_relaxed_u64(row + E);
+      ok = ok && unsigned(a >> 32) == gen;
+      gl = __uint_as_float(unsigned(a));
+    }
+    if (__all_sync(0xffffffffu, ok)) break;
+    if (*(volatile int*)&wc->skip) break;
+    __nanosleep(100);  // every CTA polls the same lines: keep L2 free for the writers
+    if (global_ns() - t0 > wc->limit_ns) {
+      if (lane == 0) {
+        wc->skip = 1;
+        atomicExch(status, int(MOE_ERR_TIMEOUT));
+      }
+      break;
+    }
+  }
+  unsigned long long key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = 8 * lane + i;
+    key[i] = e < E ? rank_key(v[i], e) : 0ull;
+  }
+  topk_select(key, t, k, idx, w, sg, has_gate, gl, idx2, w2, rb);
 }
 
 // Shared memory of bucket_cta for NW warps.
@@ -455,17 +618,27 @@ struct RouteTable {
 // logits [T][E] and gate_logit [T] (nullable) written by other CTAs; wc:
 // 8*256 ints of shared scratch.  user_idx/user_w (nullable) receive the top-k
 // outputs.  All threads of the CTA call it (blockDim.x >= 256).
+// With `tagged` set, the logits come from tagged words of generation gen
+// (row stride TS) instead, polled until they are all published.
 __device__ __forceinline__ void route_table_cta(const float* logits, const float* gate_logit,
                                                 int T, int E, int k, int32_t* user_idx,
                                                 float* user_w, int (*wc)[256], RouteTable& S,
-                                                bool rb) {
+                                                bool rb, const unsigned long long* tagged = nullptr,
+                                                int TS = 0, unsigned gen = 0,
+                                                bool has_gate = false, WaitCtl* wctl = nullptr,
+                                                int* status = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int NT = blockDim.x, NW = NT >> 5;
   for (int i = tid; i < 256; i += NT) S.cnt[i] = 0;
   for (int i = tid; i < 8 * 256; i += NT) wc[i >> 8][i & 255] = 0;
   __syncthreads();
-  for (int t = wid; t < T; t += NW)
-    topk_warp<false>(logits, gate_logit, t, E, k, S.idx, S.w, S.sg, user_idx, user_w, rb);
+  for (int t = wid; t < T; t += NW) {
+    if (tagged)
+      topk_warp_tagged(tagged, TS, gen, has_gate, t, E, k, S.idx, S.w, S.sg, user_idx, user_w,
+                       rb, wctl, status);
+    else
+      topk_warp<false>(logits, gate_logit, t, E, k, S.idx, S.w, S.sg, user_idx, user_w, rb);
+  }
   __syncthreads();
   const int N = T * k;
   const int e_a = tid < N ? S.idx[tid] : -1;

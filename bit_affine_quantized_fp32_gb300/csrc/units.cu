@@ -19,22 +19,20 @@ __device__ __forceinline__ int subslot_count(const SubSlots& S) {
   return S.n ? __ldcg(S.n) : (S.fixed_T + kMaxTok - 1) / kMaxTok;
 }
 
-// The units of this CTA: u = blockIdx.x + j * gridDim.x over n_subslots x
-// blocks, sub-slot major.
+// The units of this CTA: claims n = 0, 1, ... are queue indices
+// blockIdx.x + n * gridDim.x over n_subslots x blocks, sub-slot major.
 struct JobSched {
   const UnitJob* J;
-  int nblk, nu;
+  int nblk, total;
   __device__ explicit JobSched(const UnitJob* j) : J(j) {
     nblk = J->C.geo[J->mat].t.nblk;
-    const int total = subslot_count(J->ss) * nblk;
-    const int b = blockIdx.x, G = gridDim.x;
-    nu = total > b ? (total - b + G - 1) / G : 0;
+    total = subslot_count(J->ss) * nblk;
   }
-  __device__ int n_units() const { return nu; }
-  __device__ UnitInfo unit(int j) const {
-    const int u = blockIdx.x + j * gridDim.x;
+  __device__ int claim(int n) const { return blockIdx.x + n * gridDim.x; }
+  __device__ bool unit(int u, UnitInfo& r) const {
+    r = UnitInfo{};
+    if (u >= total) return false;
     const int ss = u / nblk;
-    UnitInfo r;
     r.kind = (J->mat & 1) ? kItemDown : kItemGateUp;
     r.mat = J->mat;
     r.blk = u - ss * nblk;
@@ -52,7 +50,7 @@ struct JobSched {
     r.signal = -1;
     r.wait_ctr = -1;
     r.wait_target = 0;
-    return r;
+    return true;
   }
   __device__ const MatSource& source(int) const { return J->src; }
   __device__ const int* perm() const { return J->perm; }
@@ -72,10 +70,13 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   const JobSched sch(&J);
   const int warp = threadIdx.x >> 5;
   if (warp == kProducerWarp)
-    producer_run(J.C, E, M, sch, nullptr);
-  else if (warp < kConsumerWarps)
+    producer_run(J.C, E, M, sch, ProducerStart{sch.claim(0), 0});
+  else if (warp == kOperandWarp)
+    operand_run(J.C, E, M, sch, nullptr);
+  else if (warp == kSignalWarp)
+    signal_run(E, sch, nullptr, J.C.status);  // reads the ring; nothing to publish
+  else
     consumer_run<FMT, FMT, F16A>(J.C, E, M, sch);
-  // the signal warp has nothing to publish in a standalone launch
 }
 
 __global__ void k_xsum(const uint16_t* __restrict__ x, int T, int H, int f16, TileGeo g13,
