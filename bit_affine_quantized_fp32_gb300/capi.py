@@ -16,7 +16,10 @@ from pathlib import Path
 LIB_PATH = Path(__file__).resolve().parent / "libmoe_gb300.so"
 
 FMT = {"f32": 0, "bf16": 1, "f16": 2, "affine8_g64": 3, "affine4_g64": 4,
-       "affine3_g64": 5, "w4a16_g128": 6}
+       "affine3_g64": 5, "w4a16_g128": 6, "affine2_g64": 7, "affine5_g64": 8,
+       "affine6_g64": 9}
+PACKED = ("affine8_g64", "affine4_g64", "affine3_g64", "w4a16_g128", "affine2_g64",
+          "affine5_g64", "affine6_g64")
 MOE_FLAG_FORCE_DECODE = 1
 MOE_FLAG_UNFUSED = 2
 MOE_FLAG_ROUND_BF16 = 4
@@ -28,7 +31,9 @@ EXPORTS = [
     "moe_expert_mlp", "moe_shared_expert", "moe_experts_forward", "moe_layer_forward",
     "moe_pack_affine8_g64", "moe_unpack_affine8_g64", "moe_pack_affine4_g64",
     "moe_unpack_affine4_g64", "moe_pack_affine3_g64", "moe_unpack_affine3_g64",
-    "moe_pack_w4a16_g128", "moe_unpack_w4a16_g128", "moe_tiled_bytes", "moe_repack_bank",
+    "moe_pack_w4a16_g128", "moe_unpack_w4a16_g128", "moe_pack_affine2_g64",
+    "moe_unpack_affine2_g64", "moe_pack_affine5_g64", "moe_unpack_affine5_g64",
+    "moe_pack_affine6_g64", "moe_unpack_affine6_g64", "moe_tiled_bytes", "moe_repack_bank",
     "moe_unrepack_bank", "moe_dequant",
 ]
 LAYOUT_CANONICAL = 0
@@ -77,7 +82,7 @@ def _load():
                                       c_size_t, P]
     L.moe_layer_forward.argtypes = [P, P, P, P, P, P, c_int, c_int, c_int, P, P, P, c_int, P,
                                     c_size_t, P]
-    for n in ("affine8_g64", "affine4_g64", "affine3_g64", "w4a16_g128"):
+    for n in PACKED:
         getattr(L, f"moe_pack_{n}").argtypes = [P, c_int, c_int, P, P]
         getattr(L, f"moe_unpack_{n}").argtypes = [P, c_int, c_int, P, P]
     L.moe_tiled_bytes.restype = c_size_t

@@ -120,6 +120,9 @@ const char* fmt_name(int f) {
     case MOE_FMT_AFFINE4_G64: return "AFFINE4_G64";
     case MOE_FMT_AFFINE3_G64: return "AFFINE3_G64";
     case MOE_FMT_W4A16_SYM_G128: return "W4A16_SYM_G128";
+    case MOE_FMT_AFFINE2_G64: return "AFFINE2_G64";
+    case MOE_FMT_AFFINE5_G64: return "AFFINE5_G64";
+    case MOE_FMT_AFFINE6_G64: return "AFFINE6_G64";
     default: return "unknown";
   }
 }
@@ -130,8 +133,17 @@ int fmt_bits(int f) {
     case MOE_FMT_AFFINE4_G64: return 4;
     case MOE_FMT_AFFINE3_G64: return 3;
     case MOE_FMT_W4A16_SYM_G128: return 4;
+    case MOE_FMT_AFFINE2_G64: return 2;
+    case MOE_FMT_AFFINE5_G64: return 5;
+    case MOE_FMT_AFFINE6_G64: return 6;
     default: return 0;
   }
+}
+
+// Expert formats of the fused decode launch and of the prefill GEMMs; the
+// other widths run the launch-per-step decode form (same results as fused).
+bool fused_format(int f) {
+  return f == MOE_FMT_AFFINE4_G64 || f == MOE_FMT_AFFINE3_G64 || f == MOE_FMT_W4A16_SYM_G128;
 }
 
 int fmt_group(int f) { return f == MOE_FMT_W4A16_SYM_G128 ? 128 : 64; }
@@ -194,10 +206,12 @@ moe_status check_hidden(int H) {
 moe_status check_bank_shape(const moe_expert_bank* b, const char* what) {
   if (!b) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", what);
   const int f = b->fmt;
-  if (f != MOE_FMT_AFFINE4_G64 && f != MOE_FMT_AFFINE3_G64 && f != MOE_FMT_W4A16_SYM_G128)
+  if (f != MOE_FMT_AFFINE4_G64 && f != MOE_FMT_AFFINE3_G64 && f != MOE_FMT_W4A16_SYM_G128 &&
+      f != MOE_FMT_AFFINE2_G64 && f != MOE_FMT_AFFINE5_G64 && f != MOE_FMT_AFFINE6_G64 &&
+      f != MOE_FMT_AFFINE8_G64)
     return fail(MOE_ERR_UNSUPPORTED_FORMAT,
-                "%s: expert format %s (%d) is not read by the expert kernels (AFFINE4_G64, "
-                "AFFINE3_G64, W4A16_SYM_G128 are)",
+                "%s: expert format %s (%d) is not read by the expert kernels (AFFINE2/3/4/5/6/"
+                "8_G64 and W4A16_SYM_G128 are)",
                 what, fmt_name(f), f);
   if (b->n_experts <= 0 || b->n_experts > 256)
     return fail(MOE_ERR_INVALID_ARG, "%s: n_experts=%d not in 1..256", what, b->n_experts);
@@ -315,7 +329,7 @@ moe_status run_bank(const moe_expert_bank* bank, const SubSlots& ss, int max_ss,
 // The prefill form (tcgen05 expert GEMMs) serves T > MOE_DECODE_MAX_TOKENS
 // unless the caller forces the decode form or the shape does not fit it.
 bool use_prefill(const moe_expert_bank* b, int T, int flags) {
-  return T > MOE_DECODE_MAX_TOKENS && !(flags & MOE_FLAG_FORCE_DECODE) &&
+  return T > MOE_DECODE_MAX_TOKENS && !(flags & MOE_FLAG_FORCE_DECODE) && fused_format(b->fmt) &&
          prefill_smem(geo13(b).t, 0) > 0 && prefill_smem(geo2(b).t, 1) > 0;
 }
 
@@ -696,7 +710,8 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
   if (flags & ~(MOE_FLAG_FORCE_DECODE | MOE_FLAG_UNFUSED | MOE_FLAG_ROUND_BF16))
     return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
   const bool rb = (flags & MOE_FLAG_ROUND_BF16) != 0;
-  if (!(flags & MOE_FLAG_UNFUSED) && T <= MOE_DECODE_MAX_TOKENS) {
+  if (!(flags & MOE_FLAG_UNFUSED) && T <= MOE_DECODE_MAX_TOKENS && fused_format(experts->fmt) &&
+      (!shared || fused_format(shared->fmt))) {
     // validate what moe_route / moe_experts_forward would, then one launch
     if ((s = check_hidden(H))) return s;
     if ((s = check_router_matrix(router, "router", E, H))) return s;
@@ -818,6 +833,9 @@ MOE_PACK_PAIR(affine8_g64, MOE_FMT_AFFINE8_G64, uint8_t)
 MOE_PACK_PAIR(affine4_g64, MOE_FMT_AFFINE4_G64, uint8_t)
 MOE_PACK_PAIR(affine3_g64, MOE_FMT_AFFINE3_G64, uint8_t)
 MOE_PACK_PAIR(w4a16_g128, MOE_FMT_W4A16_SYM_G128, int8_t)
+MOE_PACK_PAIR(affine2_g64, MOE_FMT_AFFINE2_G64, uint8_t)
+MOE_PACK_PAIR(affine5_g64, MOE_FMT_AFFINE5_G64, uint8_t)
+MOE_PACK_PAIR(affine6_g64, MOE_FMT_AFFINE6_G64, uint8_t)
 
 size_t moe_tiled_bytes(int fmt, int n_experts, int inter, int hidden, int which) {
   moe_expert_bank b{};
@@ -986,7 +1004,7 @@ moe_status moe_route_static(const moe_qmatrix* router, const float* logit_bias,
 moe_status moe_dequant(const moe_qmatrix* m, float* w, cudaStream_t stream) {
   if (!m || !w) return fail(MOE_ERR_INVALID_ARG, "dequant: NULL argument");
   const int f = m->fmt;
-  if (f < MOE_FMT_F32 || f > MOE_FMT_W4A16_SYM_G128)
+  if (f < MOE_FMT_F32 || f > MOE_FMT_AFFINE6_G64)
     return fail(MOE_ERR_UNSUPPORTED_FORMAT, "dequant: format %d is not read", f);
   if (m->rows < 0 || m->cols < 0) return fail(MOE_ERR_INVALID_ARG, "dequant: negative shape");
   const int bits = fmt_bits(f);

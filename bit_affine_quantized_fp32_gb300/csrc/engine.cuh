@@ -306,6 +306,40 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t v, uint32_t magic) {
   }
 }
 
+// code_pair with the pair's high bits (at [4,6) and [20,22)) added: codes up
+// to 6 bits stay exact (bf16 128 + q for q < 128, fp16 1024 + q).
+template <bool F16A>
+__device__ __forceinline__ uint32_t code_pair_hb(uint32_t v, uint32_t hb, uint32_t magic) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;\n" : "=r"(r) : "r"(v), "r"(hb | magic));
+  if constexpr (F16A) {
+    __half2 h = *reinterpret_cast<__half2*>(&r);
+    const __half2 off = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+    h = __hsub2(h, off);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    return r;
+  }
+}
+
+// Two nibbles as the exact 16-bit values q (no +128 offset): the high nibble
+// pair of an 8-bit code, whose second MMA is scaled by 16.
+template <bool F16A>
+__device__ __forceinline__ uint32_t code_pair_exact(uint32_t v, uint32_t magic) {
+  uint32_t r = code_pair<F16A>(v, magic);
+  if constexpr (!F16A) {
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&r);
+    const __nv_bfloat162 off = __halves2bfloat162(__ushort_as_bfloat16(0x4300),
+                                                  __ushort_as_bfloat16(0x4300));
+    b = __hsub2(b, off);
+    r = *reinterpret_cast<uint32_t*>(&b);
+  }
+  return r;
+}
+
+// shift right by s (left by -s), s a compile-time constant after inlining
+__device__ __forceinline__ uint32_t shr_signed(uint32_t v, int s) { return s >= 0 ? v >> s : v << -s; }
+
 __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t v) {
   return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
@@ -324,7 +358,8 @@ template <int FMT, bool F16A, bool SPLIT, int NG, int TILES, int KSPLIT>
 __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* wst,
                                              const uint8_t* op, const OpLayout& L, int c,
                                              int tile, int ks, uint32_t mg, float (&acc)[4]) {
-  constexpr int CB = FMT == MOE_FMT_AFFINE3_G64 ? 384 : 512;
+  constexpr int CB = tiled_cb(FMT);
+  constexpr int BITS = tiled_bits(FMT);
   constexpr int NGP = (NG + 3) & ~3;
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, t = lane & 3;
@@ -339,29 +374,50 @@ __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* w
     const int G = ks + KSPLIT * i;
     if (NG % KSPLIT != 0 && G >= NG) break;
     const uint8_t* codes = wst + (tile * NG + G) * CB;
-    uint32_t w0, w1, w2, w3;
-    if constexpr (FMT == MOE_FMT_AFFINE3_G64) {
+    // the lane's four nibble words (low 4 bits of its 32 codes) and what
+    // the format keeps above them
+    uint32_t w[4], hw[4] = {0u, 0u, 0u, 0u}, p0 = 0u, p1 = 0u;
+    if constexpr (BITS <= 3) {
       const uint32_t* pl = reinterpret_cast<const uint32_t*>(codes) + lane;
-      planes_to_words(pl[0], pl[32], pl[64], w0, w1, w2, w3);
+      planes_to_words(pl[0], pl[32], BITS == 3 ? pl[64] : 0u, w[0], w[1], w[2], w[3]);
     } else {
       const uint4 v = *reinterpret_cast<const uint4*>(codes + lane * 16);
-      w0 = v.x;
-      w1 = v.y;
-      w2 = v.z;
-      w3 = v.w;
+      w[0] = v.x;
+      w[1] = v.y;
+      w[2] = v.z;
+      w[3] = v.w;
+      if constexpr (BITS == 5 || BITS == 6) {
+        const uint32_t* hp = reinterpret_cast<const uint32_t*>(codes + 512) + lane;
+        p0 = hp[0];
+        if constexpr (BITS == 6) p1 = hp[32];
+      } else if constexpr (BITS == 8) {
+        const uint4 h = *reinterpret_cast<const uint4*>(codes + 512 + lane * 16);
+        hw[0] = h.x;
+        hw[1] = h.y;
+        hw[2] = h.z;
+        hw[3] = h.w;
+      }
     }
+    // the code pair in nibbles m and m + 4 of word x, as an MMA register
+    auto pr = [&](int x, int m) -> uint32_t {
+      const uint32_t v = w[x] >> (4 * m);
+      if constexpr (BITS == 5) {
+        return code_pair_hb<F16A>(v, shr_signed(p0, 4 * x + m - 4) & 0x00100010u, mg);
+      } else if constexpr (BITS == 6) {
+        return code_pair_hb<F16A>(
+            v, shr_signed(x < 2 ? p0 : p1, 2 * (4 * (x & 1) + m) - 4) & 0x00300030u, mg);
+      } else {
+        return code_pair<F16A>(v, mg);
+      }
+    };
     const uint4 xa = *reinterpret_cast<const uint4*>(xrow + G * 128);
     const uint4 xb = *reinterpret_cast<const uint4*>(xrow + G * 128 + 16);
     // k-step m takes code pairs (4m, 4m+1) and (4m+2, 4m+3) of the lane's 16
     // codes: nibbles (m&1)*2 and (m&1)*2+1 of word W0/W1 (row g), W2/W3 (g+8)
-    const uint32_t A00 = code_pair<F16A>(w0, mg), A01 = code_pair<F16A>(w2, mg);
-    const uint32_t A02 = code_pair<F16A>(w0 >> 4, mg), A03 = code_pair<F16A>(w2 >> 4, mg);
-    const uint32_t A10 = code_pair<F16A>(w0 >> 8, mg), A11 = code_pair<F16A>(w2 >> 8, mg);
-    const uint32_t A12 = code_pair<F16A>(w0 >> 12, mg), A13 = code_pair<F16A>(w2 >> 12, mg);
-    const uint32_t A20 = code_pair<F16A>(w1, mg), A21 = code_pair<F16A>(w3, mg);
-    const uint32_t A22 = code_pair<F16A>(w1 >> 4, mg), A23 = code_pair<F16A>(w3 >> 4, mg);
-    const uint32_t A30 = code_pair<F16A>(w1 >> 8, mg), A31 = code_pair<F16A>(w3 >> 8, mg);
-    const uint32_t A32 = code_pair<F16A>(w1 >> 12, mg), A33 = code_pair<F16A>(w3 >> 12, mg);
+    const uint32_t A00 = pr(0, 0), A01 = pr(2, 0), A02 = pr(0, 1), A03 = pr(2, 1);
+    const uint32_t A10 = pr(0, 2), A11 = pr(2, 2), A12 = pr(0, 3), A13 = pr(2, 3);
+    const uint32_t A20 = pr(1, 0), A21 = pr(3, 0), A22 = pr(1, 1), A23 = pr(3, 1);
+    const uint32_t A30 = pr(1, 2), A31 = pr(3, 2), A32 = pr(1, 3), A33 = pr(3, 3);
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     mma16816<F16A>(d, A00, A01, A02, A03, xa.x, xa.y);
     mma16816<F16A>(d, A10, A11, A12, A13, xa.z, xa.w);
@@ -374,6 +430,26 @@ __device__ __forceinline__ void compute_item(const TileGeo& tg, const uint8_t* w
       mma16816<F16A>(d, A10, A11, A12, A13, la.z, la.w);
       mma16816<F16A>(d, A20, A21, A22, A23, lb.x, lb.y);
       mma16816<F16A>(d, A30, A31, A32, A33, lb.z, lb.w);
+    }
+    if constexpr (BITS == 8) {
+      // the high nibbles as exact values: q = lo + 16 hi, so the group's
+      // bracket is d_lo + 16 d_hi
+      auto hp = [&](int x, int m) -> uint32_t { return code_pair_exact<F16A>(hw[x] >> (4 * m), mg); };
+      float dh[4] = {0.f, 0.f, 0.f, 0.f};
+      mma16816<F16A>(dh, hp(0, 0), hp(2, 0), hp(0, 1), hp(2, 1), xa.x, xa.y);
+      mma16816<F16A>(dh, hp(0, 2), hp(2, 2), hp(0, 3), hp(2, 3), xa.z, xa.w);
+      mma16816<F16A>(dh, hp(1, 0), hp(3, 0), hp(1, 1), hp(3, 1), xb.x, xb.y);
+      mma16816<F16A>(dh, hp(1, 2), hp(3, 2), hp(1, 3), hp(3, 3), xb.z, xb.w);
+      if constexpr (SPLIT) {
+        const uint4 la = *reinterpret_cast<const uint4*>(xlrow + G * 128);
+        const uint4 lb = *reinterpret_cast<const uint4*>(xlrow + G * 128 + 16);
+        mma16816<F16A>(dh, hp(0, 0), hp(2, 0), hp(0, 1), hp(2, 1), la.x, la.y);
+        mma16816<F16A>(dh, hp(0, 2), hp(2, 2), hp(0, 3), hp(2, 3), la.z, la.w);
+        mma16816<F16A>(dh, hp(1, 0), hp(3, 0), hp(1, 1), hp(3, 1), lb.x, lb.y);
+        mma16816<F16A>(dh, hp(1, 2), hp(3, 2), hp(1, 3), hp(3, 3), lb.z, lb.w);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d[q] = fmaf(16.f, dh[q], d[q]);
     }
     float s0, s1, b0, b1;
     if constexpr (FMT == MOE_FMT_W4A16_SYM_G128) {

@@ -22,8 +22,17 @@ __host__ __device__ inline int fmt_bits(int fmt) {
     case MOE_FMT_AFFINE4_G64: return 4;
     case MOE_FMT_AFFINE3_G64: return 3;
     case MOE_FMT_W4A16_SYM_G128: return 4;
+    case MOE_FMT_AFFINE2_G64: return 2;
+    case MOE_FMT_AFFINE5_G64: return 5;
+    case MOE_FMT_AFFINE6_G64: return 6;
     default: return 0;
   }
+}
+
+// widths whose codes straddle word boundaries (a row is one bit stream)
+__host__ __device__ inline bool fmt_stream(int fmt) {
+  const int b = fmt_bits(fmt);
+  return b == 3 || b == 5 || b == 6;
 }
 
 // one thread per packed word
@@ -36,11 +45,11 @@ __global__ void k_pack(int fmt, const uint8_t* __restrict__ codes, int rows, int
   const long r = i / wpr, j = i - r * wpr;
   const uint8_t* row = codes + r * cols;
   uint32_t v = 0;
-  if (fmt == MOE_FMT_AFFINE3_G64) {
+  if (fmt_stream(fmt)) {
     for (int b = 0; b < 32; ++b) {
       const long s = j * 32 + b;
-      const uint32_t code = row[s / 3];
-      v |= ((code >> (s % 3)) & 1u) << b;
+      const uint32_t code = row[s / bits];
+      v |= ((code >> (s % bits)) & 1u) << b;
     }
   } else {
     const int per = 32 / bits;
@@ -55,15 +64,15 @@ __global__ void k_pack(int fmt, const uint8_t* __restrict__ codes, int rows, int
 }
 
 __device__ __forceinline__ uint32_t get_code(int fmt, const uint32_t* row, long c) {
-  if (fmt == MOE_FMT_AFFINE3_G64) {
-    const long s = 3 * c;
+  const int bits = fmt_bits(fmt);
+  if (fmt_stream(fmt)) {
+    const long s = long(bits) * c;
     const long w = s >> 5;
     const int b = int(s & 31);
     uint32_t v = row[w] >> b;
-    if (b > 29) v |= row[w + 1] << (32 - b);
-    return v & 7u;
+    if (b > 32 - bits) v |= row[w + 1] << (32 - b);
+    return v & ((1u << bits) - 1u);
   }
-  const int bits = fmt_bits(fmt);
   const int per = 32 / bits;
   return (row[c / per] >> (bits * (c % per))) & ((1u << bits) - 1u);
 }
@@ -141,8 +150,7 @@ __device__ __forceinline__ TiledPos tiled_pos(const TileGeo& g, int e, int r, in
   const int c = k / g.CK, kk = k % g.CK;
   const int G = kk / 64, t = (kk % 64) / 16, half = (kk % 16) / 8;
   TiledPos p;
-  p.block = tiled_item(g, e, blk, c) +
-            (long long)(w * g.ng + G) * (g.fmt == MOE_FMT_AFFINE3_G64 ? 384 : 512);
+  p.block = tiled_item(g, e, blk, c) + (long long)(w * g.ng + G) * tiled_cb(g.fmt);
   p.lane = (sub & 7) * 4 + t;
   p.widx = (sub >> 3) * 2 + half;
   p.nib = tiled_nib(k % 8);
@@ -166,25 +174,41 @@ __global__ void k_repack_codes(TileGeo g, int E, const uint32_t* __restrict__ wc
   const int r0 = tiled_row(g, blk, w) + gq;
   const int k0 = c * g.CK + 64 * G + 16 * t;
   const long wpr = long(g.K) * fmt_bits(g.fmt) / 32;
-  uint32_t W[4];
+  // low 4 bits of each code as the nibble words W0..W3, the rest per format
+  uint32_t W[4], HW[4] = {0, 0, 0, 0}, P5 = 0, P6[2] = {0, 0};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int r = r0 + (j >> 1) * 8;
     const uint32_t* row = wc + ((long long)e * g.rows + r) * wpr;
     const int ks = k0 + 8 * (j & 1);
     uint32_t v = 0;
-    for (int q2 = 0; q2 < 8; ++q2) v |= get_code(g.fmt, row, ks + q2) << (4 * tiled_nib(q2));
+    for (int q2 = 0; q2 < 8; ++q2) {
+      const uint32_t code = get_code(g.fmt, row, ks + q2);
+      const int n = tiled_nib(q2);
+      v |= (code & 15u) << (4 * n);
+      HW[j] |= (code >> 4) << (4 * n);
+      P5 |= ((code >> 4) & 1u) << plane5_pos(j, n);
+      P6[j >> 1] |= ((code >> 4) & 3u) << plane6_pos(j, n);
+    }
     W[j] = v;
   }
-  uint8_t* blkp = out + tiled_item(g, e, blk, c);
-  if (g.fmt == MOE_FMT_AFFINE3_G64) {
-    uint32_t* pl = reinterpret_cast<uint32_t*>(blkp + (long long)(w * g.ng + G) * 384) + lane;
+  uint8_t* blkp = out + tiled_item(g, e, blk, c) + (long long)(w * g.ng + G) * tiled_cb(g.fmt);
+  uint32_t* pl = reinterpret_cast<uint32_t*>(blkp) + lane;
+  const int bits = tiled_bits(g.fmt);
+  if (bits == 2 || bits == 3) {
     pl[0] = planes_l(W[0], W[1]);
     pl[32] = planes_l(W[2], W[3]);
-    pl[64] = planes_h(W[0], W[1], W[2], W[3]);
+    if (bits == 3) pl[64] = planes_h(W[0], W[1], W[2], W[3]);
   } else {
-    *reinterpret_cast<uint4*>(blkp + (long long)(w * g.ng + G) * 512 + lane * 16) =
-        make_uint4(W[0], W[1], W[2], W[3]);
+    *reinterpret_cast<uint4*>(blkp + lane * 16) = make_uint4(W[0], W[1], W[2], W[3]);
+    uint32_t* hp = reinterpret_cast<uint32_t*>(blkp + 512) + lane;
+    if (bits == 5) hp[0] = P5;
+    if (bits == 6) {
+      hp[0] = P6[0];
+      hp[32] = P6[1];
+    }
+    if (bits == 8)
+      *reinterpret_cast<uint4*>(blkp + 512 + lane * 16) = make_uint4(HW[0], HW[1], HW[2], HW[3]);
   }
 }
 
@@ -226,16 +250,24 @@ __global__ void k_repack_scales(TileGeo g, int E, const uint16_t* __restrict__ s
 __device__ __forceinline__ uint32_t tiled_code(const TileGeo& g, const uint8_t* tl, int e, int r,
                                                int k) {
   const TiledPos p = tiled_pos(g, e, r, k);
-  uint32_t W;
-  if (g.fmt == MOE_FMT_AFFINE3_G64) {
-    const uint32_t* pl = reinterpret_cast<const uint32_t*>(tl + p.block) + p.lane;
+  const int bits = tiled_bits(g.fmt);
+  const uint32_t* pl = reinterpret_cast<const uint32_t*>(tl + p.block) + p.lane;
+  if (bits == 2 || bits == 3) {
     uint32_t w0, w1, w2, w3;
-    planes_to_words(pl[0], pl[32], pl[64], w0, w1, w2, w3);
-    W = p.widx == 0 ? w0 : p.widx == 1 ? w1 : p.widx == 2 ? w2 : w3;
-  } else {
-    W = reinterpret_cast<const uint32_t*>(tl + p.block + p.lane * 16)[p.widx];
+    planes_to_words(pl[0], pl[32], bits == 3 ? pl[64] : 0u, w0, w1, w2, w3);
+    const uint32_t W = p.widx == 0 ? w0 : p.widx == 1 ? w1 : p.widx == 2 ? w2 : w3;
+    return (W >> (4 * p.nib)) & 15u;
   }
-  return (W >> (4 * p.nib)) & 15u;
+  const uint32_t lo =
+      (reinterpret_cast<const uint32_t*>(tl + p.block + p.lane * 16)[p.widx] >> (4 * p.nib)) & 15u;
+  const uint32_t* hp = reinterpret_cast<const uint32_t*>(tl + p.block + 512) + p.lane;
+  uint32_t hi = 0;
+  if (bits == 5) hi = (hp[0] >> plane5_pos(p.widx, p.nib)) & 1u;
+  if (bits == 6) hi = (hp[32 * (p.widx >> 1)] >> plane6_pos(p.widx, p.nib)) & 3u;
+  if (bits == 8)
+    hi = (reinterpret_cast<const uint32_t*>(tl + p.block + 512 + p.lane * 16)[p.widx] >>
+          (4 * p.nib)) & 15u;
+  return lo | (hi << 4);
 }
 
 // one thread per canonical packed word
@@ -250,13 +282,14 @@ __global__ void k_unrepack_codes(TileGeo g, int E, const uint8_t* __restrict__ t
   const int j = int(i - er * wpr);
   const int e = int(er / g.rows), r = int(er % g.rows);
   uint32_t v = 0;
-  if (g.fmt == MOE_FMT_AFFINE3_G64) {
+  if (fmt_stream(g.fmt)) {
     for (int b = 0; b < 32; ++b) {
       const long s = long(j) * 32 + b;
-      v |= ((tiled_code(g, tl, e, r, int(s / 3)) >> (s % 3)) & 1u) << b;
+      v |= ((tiled_code(g, tl, e, r, int(s / bits)) >> (s % bits)) & 1u) << b;
     }
   } else {
-    for (int q = 0; q < 8; ++q) v |= tiled_code(g, tl, e, r, 8 * j + q) << (4 * q);
+    const int per = 32 / bits;
+    for (int q = 0; q < per; ++q) v |= tiled_code(g, tl, e, r, per * j + q) << (bits * q);
   }
   wc[i] = v;
 }

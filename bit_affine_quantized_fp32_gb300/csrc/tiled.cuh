@@ -17,14 +17,25 @@
 // nibbles hold codes [0 2 4 6 1 3 5 7]: nibbles i and i+4 are the adjacent
 // pair (2i, 2i+1), which is how an MMA register takes two k-values, so the
 // activations stay in their natural order.
-//   4-bit / W4A16: 16 bytes [W0 W1 W2 W3] per lane, (w, G) blocks of 512 B.
-//   3-bit: three 32-bit planes per (w, G) block of 384 B, plane p holding
-//     lane l's word at p*128 + 4l:
+// A (w, G) code block holds exactly the codes' bits (128 * bits bytes), the
+// words W0..W3 above holding each code's low 4 bits:
+//   4-bit / W4A16: 16 bytes [W0 W1 W2 W3] per lane, blocks of 512 B.
+//   3-bit: three 32-bit planes per block of 384 B, plane p holding lane l's
+//     word at p*128 + 4l:
 //       L01 = (W0 & 0x33333333) | (W1 & 0x33333333) << 2      (bits 0-1)
 //       L23 = (W2 & 0x33333333) | (W3 & 0x33333333) << 2
 //       H   = (W0 >> 2 & 0x11111111) | (W1 >> 1 & 0x22222222)
 //           | (W2 & 0x44444444) | (W3 << 1 & 0x88888888)        (bit 2)
-//     i.e. exactly 3 bits per code, no padding.
+//   2-bit: the planes L01 and L23 alone (256 B).
+//   5-bit: [W0..W3] per lane (512 B), then a plane (128 B) of bit 4: bit 4 of
+//     the code in nibble n of Wx sits at bit 4x + (n & 3) + 16 (n >> 2), so
+//     (plane >> (4x + m - 4)) puts the bits of the code pair in nibbles m and
+//     m + 4 at bits 4 and 20, next to the low nibbles.
+//   6-bit: [W0..W3] (512 B), then two planes (bits 4-5 of the codes of W0,W1
+//     and of W2,W3): bits 4-5 of the code in nibble n of Wx at bit
+//     2 (4 (x & 1) + (n & 3)) + 16 (n >> 2) of plane x >> 1.
+//   8-bit: [W0..W3] of the low nibbles, then the same 16 bytes per lane of
+//     the high nibbles (1024 B).
 // Scales of an item (fp16), one run per (w, g) so that a lane's groups are
 // contiguous:
 //   affine: entry (w, g, G) = [s(r0), b(r0), s(r1), b(r1)] of 64-group G,
@@ -53,6 +64,18 @@ struct TileGeo {
   long long expert_bytes;
 };
 
+// bits per code of an expert format
+__host__ __device__ constexpr int tiled_bits(int fmt) {
+  return fmt == MOE_FMT_AFFINE2_G64   ? 2
+         : fmt == MOE_FMT_AFFINE3_G64 ? 3
+         : fmt == MOE_FMT_AFFINE5_G64 ? 5
+         : fmt == MOE_FMT_AFFINE6_G64 ? 6
+         : fmt == MOE_FMT_AFFINE8_G64 ? 8
+                                      : 4;
+}
+// bytes of one (w, G) code block
+__host__ __device__ constexpr int tiled_cb(int fmt) { return 128 * tiled_bits(fmt); }
+
 __host__ __device__ inline int tiled_chunk(int K) {
   return K % 512 == 0 ? 512 : (K % 256 == 0 ? 256 : 128);
 }
@@ -68,7 +91,7 @@ __host__ __device__ inline TileGeo tile_geo(int fmt, int inter, int hidden, int 
   g.nch = g.K / g.CK;
   g.ng = g.CK / 64;
   g.nblk = down ? hidden / 128 : inter / 64;
-  g.code_bytes = 8 * g.ng * (fmt == MOE_FMT_AFFINE3_G64 ? 384 : 512);
+  g.code_bytes = 8 * g.ng * tiled_cb(fmt);
   g.sc_bytes = fmt == MOE_FMT_W4A16_SYM_G128 ? 8 * (g.ng / 2) * 8 * 4 : 8 * g.ng * 8 * 8;
   g.item_bytes = g.code_bytes + g.sc_bytes;
   g.expert_bytes = (long long)g.nblk * g.nch * g.item_bytes;
@@ -91,6 +114,13 @@ __host__ __device__ inline uint32_t planes_l(uint32_t wa, uint32_t wb) {
 __host__ __device__ inline uint32_t planes_h(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
   return ((w0 >> 2) & 0x11111111u) | ((w1 >> 1) & 0x22222222u) | (w2 & 0x44444444u) |
          ((w3 << 1) & 0x88888888u);
+}
+
+// Bit position, in a 5-bit block's bit-4 plane, of the code in nibble n of
+// word x; in a 6-bit block's plane x >> 1, of bit 4 of that code (bit 5 next).
+__host__ __device__ inline int plane5_pos(int x, int n) { return 4 * x + (n & 3) + 16 * (n >> 2); }
+__host__ __device__ inline int plane6_pos(int x, int n) {
+  return 2 * (4 * (x & 1) + (n & 3)) + 16 * (n >> 2);
 }
 
 // Inverse of the planes: the four 8-code words of a 3-bit fragment.

@@ -154,6 +154,10 @@ cudaError_t launch_units(const UnitJob& J, bool f16a, int sms, cudaStream_t st) 
     case MOE_FMT_AFFINE4_G64: return launch_fmt<MOE_FMT_AFFINE4_G64>(J, f, sms, st);
     case MOE_FMT_AFFINE3_G64: return launch_fmt<MOE_FMT_AFFINE3_G64>(J, f, sms, st);
     case MOE_FMT_W4A16_SYM_G128: return launch_fmt<MOE_FMT_W4A16_SYM_G128>(J, f, sms, st);
+    case MOE_FMT_AFFINE2_G64: return launch_fmt<MOE_FMT_AFFINE2_G64>(J, f, sms, st);
+    case MOE_FMT_AFFINE5_G64: return launch_fmt<MOE_FMT_AFFINE5_G64>(J, f, sms, st);
+    case MOE_FMT_AFFINE6_G64: return launch_fmt<MOE_FMT_AFFINE6_G64>(J, f, sms, st);
+    case MOE_FMT_AFFINE8_G64: return launch_fmt<MOE_FMT_AFFINE8_G64>(J, f, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

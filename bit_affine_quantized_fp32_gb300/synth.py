@@ -35,11 +35,17 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-BITS = {"affine8_g64": 8, "affine4_g64": 4, "affine3_g64": 3, "w4a16_g128": 4}
-GROUP = {"affine8_g64": 64, "affine4_g64": 64, "affine3_g64": 64, "w4a16_g128": 128}
+BITS = {"affine8_g64": 8, "affine4_g64": 4, "affine3_g64": 3, "w4a16_g128": 4,
+        "affine2_g64": 2, "affine5_g64": 5, "affine6_g64": 6}
+GROUP = {"affine8_g64": 64, "affine4_g64": 64, "affine3_g64": 64, "w4a16_g128": 128,
+         "affine2_g64": 64, "affine5_g64": 64, "affine6_g64": 64}
+# scale laws |N(0, sigma)|: the 3- and 4-bit values of the workloads; the other
+# widths keep the weights' spread of the 4-bit law (sigma = 0.064 / 2^bits)
 SCALE_SIGMA = {"affine8_g64": 2.7e-4, "affine4_g64": 0.004, "affine3_g64": 0.008,
-               "w4a16_g128": 0.004}
-BIAS_NOISE = {"affine8_g64": 1e-4, "affine4_g64": 1e-4, "affine3_g64": 0.0}
+               "w4a16_g128": 0.004, "affine2_g64": 0.016, "affine5_g64": 0.002,
+               "affine6_g64": 0.001}
+BIAS_NOISE = {"affine8_g64": 1e-4, "affine4_g64": 1e-4, "affine3_g64": 0.0,
+              "affine2_g64": 1e-4, "affine5_g64": 1e-4, "affine6_g64": 1e-4}
 
 
 def f32_to_bf16_bits(a) -> np.ndarray:

@@ -19,6 +19,11 @@
  *               int4 symmetric weights, group 128, no zero point, fp16 compute.
  *   [1329]      "Sage-A1.5 (qwen3_5 MoE 35B-A3B) on the XPU backend ... #1329",
  *               Proposal: 256 experts with top-8, grouped MoE decode.
+ *   [803-fp64]  same issue, "Affine experts at other widths": the loader reads
+ *               MLX affine experts at further widths, checked per projection
+ *               against fp64.
+ *   [803-widen] same issue, comment "The 3-bit width is up as #972": the same
+ *               codes at a wider width give the same results (the control).
  *   [547-win]   "Native server: --backend xpu for Nemotron on Intel Arc",
  *               update comment: a one-row window equals the decode step bit
  *               for bit; 512-row prefill windows.
@@ -66,7 +71,11 @@ typedef enum moe_status {
  *   AFFINE3_G64  MLX affine 3-bit: each row is one LSB-first bit stream, code
  *                c at stream bits [3c, 3c+3) (codes may straddle two words;
  *                32 codes fill 3 words exactly)
- *     affine dequantisation: w = scale * q + bias, q unsigned   [803-run]
+ *   AFFINE2_G64, AFFINE5_G64, AFFINE6_G64  MLX affine at the other widths the
+ *                pages' loader reads, rows as LSB-first bit streams as for
+ *                3-bit (code c at bits [bc, bc+b)); 2-bit is 16 codes per word
+ *     affine dequantisation: w = scale * q + bias, q unsigned   [803-run],
+ *                                                                [803-fp64]
  *   W4A16_SYM_G128  compressed-tensors pack-quantized int4: 8 nibbles per
  *                word LSB-first, stored u = q + 8 (q in -8..7), w = scale * q,
  *                no bias                                          [w4a16]
@@ -78,7 +87,10 @@ typedef enum moe_format {
   MOE_FMT_AFFINE8_G64 = 3,
   MOE_FMT_AFFINE4_G64 = 4,
   MOE_FMT_AFFINE3_G64 = 5,
-  MOE_FMT_W4A16_SYM_G128 = 6
+  MOE_FMT_W4A16_SYM_G128 = 6,
+  MOE_FMT_AFFINE2_G64 = 7,
+  MOE_FMT_AFFINE5_G64 = 8,
+  MOE_FMT_AFFINE6_G64 = 9
 } moe_format;
 
 /* One matrix [rows, cols] in any format.  For F32/BF16/F16 qweight holds the
@@ -245,9 +257,14 @@ moe_status moe_bucket(const int32_t* topk_idx, int n_tokens, int top_k, int n_ex
  *   h_out nullable [T, inter] fp32, y_out [T, hidden] fp32.
  * moe_shared_expert is the same for expert 0 of a one-expert bank:
  *   y_shared [T, hidden] fp32.
- * Banks must be TILED (moe_repack_bank).  Formats: AFFINE4_G64,
- * AFFINE3_G64 (hidden and inter multiples of 128), W4A16_SYM_G128 (multiples
- * of 256); inter <= 512.
+ * Banks must be TILED (moe_repack_bank).  Formats: AFFINE2/3/4/5/6/8_G64
+ * (hidden and inter multiples of 128), W4A16_SYM_G128 (multiples of 256);
+ * inter <= 512.  Every width computes sum_i q_i x_i on the exact integer
+ * codes with one fp32 accumulation order, so the same codes stored at any
+ * affine width give bit-identical results ([803-widen]).  The fused decode
+ * launch and the prefill tensor-core GEMMs read AFFINE3/4_G64 and W4A16; the
+ * other widths run the launch-per-step decode form at any n_tokens (the same
+ * results the fused launch would give).
  */
 moe_status moe_expert_mlp(const moe_expert_bank* bank, int expert, const void* x, int act,
                           int n_tokens, float* h_out, float* y_out, void* ws, size_t ws_bytes,
@@ -314,6 +331,19 @@ moe_status moe_pack_w4a16_g128(const int8_t* codes, int rows, int cols, uint32_t
                                cudaStream_t stream);
 moe_status moe_unpack_w4a16_g128(const uint32_t* packed, int rows, int cols, int8_t* codes,
                                  cudaStream_t stream);
+/* The other MLX affine widths ([803-fp64]): codes 0 .. 2^bits - 1. */
+moe_status moe_pack_affine2_g64(const uint8_t* codes, int rows, int cols, uint32_t* packed,
+                                cudaStream_t stream);
+moe_status moe_unpack_affine2_g64(const uint32_t* packed, int rows, int cols, uint8_t* codes,
+                                  cudaStream_t stream);
+moe_status moe_pack_affine5_g64(const uint8_t* codes, int rows, int cols, uint32_t* packed,
+                                cudaStream_t stream);
+moe_status moe_unpack_affine5_g64(const uint32_t* packed, int rows, int cols, uint8_t* codes,
+                                  cudaStream_t stream);
+moe_status moe_pack_affine6_g64(const uint8_t* codes, int rows, int cols, uint32_t* packed,
+                                cudaStream_t stream);
+moe_status moe_unpack_affine6_g64(const uint32_t* packed, int rows, int cols, uint8_t* codes,
+                                  cudaStream_t stream);
 
 /* Kernel-tiled expert layout.  The pages' engine likewise keeps its experts
  * in kernel tables of its own (gate and up interleaved per group, "Progress

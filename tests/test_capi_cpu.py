@@ -71,9 +71,9 @@ def _call_experts(capi, bank, T=2, k=2, ws=1 << 24, wsb=1 << 30):
 
 
 def test_refuses_unread_width_by_name(capi):
-    rc = _call_experts(capi, _bank("affine8_g64"))
+    rc = _call_experts(capi, _bank("bf16"))         # a dense type is not an expert format
     assert rc == 2
-    assert b"AFFINE8_G64" in capi.lib.moe_last_error()
+    assert b"BF16" in capi.lib.moe_last_error()
     S = capi.ExpertBankS
     rc = _call_experts(capi, S(42, 8, 128, 256, 1, 0, *[1 << 20] * 6))
     assert rc == 2
@@ -112,7 +112,7 @@ def test_tiled_bytes_equal_canonical_bytes(capi, fmt, bits, G, bias, E, I, H):
 
 def test_tiled_bytes_refuses_bad_shapes(capi):
     assert capi.lib.moe_tiled_bytes(capi.FMT["affine4_g64"], 8, 100, 256, 0) == 0
-    assert capi.lib.moe_tiled_bytes(capi.FMT["affine8_g64"], 8, 128, 256, 0) == 0
+    assert capi.lib.moe_tiled_bytes(capi.FMT["bf16"], 8, 128, 256, 0) == 0
     assert capi.lib.moe_tiled_bytes(capi.FMT["affine4_g64"], 8, 128, 256, 2) == 0
 
 
@@ -173,3 +173,15 @@ def test_route_static_limits(capi):
     rc = capi.lib.moe_route_static(ctypes.byref(r), None, None, P, 1, 32, 8, None, P, None, P,
                                    P, None)
     assert rc == 1   # NULL topk_idx, caught before the scratch is looked up
+
+
+@pytest.mark.parametrize("fmt,bits", [("affine2_g64", 2), ("affine3_g64", 3), ("affine4_g64", 4),
+                                      ("affine5_g64", 5), ("affine6_g64", 6), ("affine8_g64", 8)])
+def test_tiled_bytes_hold_exactly_the_canonical_bytes(capi, fmt, bits):
+    """A tiled bank at any affine width holds the codes at their width plus the
+    fp16 scale and bias of every 64-group, nothing more (no padding)."""
+    E, I, H = 3, 256, 512
+    for which, (rows, cols) in enumerate([(2 * I, H), (H, I)]):
+        n = rows * cols
+        assert capi.lib.moe_tiled_bytes(capi.FMT[fmt], E, I, H, which) == \
+            E * (n * bits // 8 + n // 64 * 4)

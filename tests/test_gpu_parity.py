@@ -19,7 +19,8 @@ from . import _harness as Hn
 
 pytestmark = pytest.mark.gpu
 
-FMTS = ["affine8_g64", "affine4_g64", "affine3_g64", "w4a16_g128"]
+FMTS = ["affine8_g64", "affine4_g64", "affine3_g64", "w4a16_g128", "affine2_g64", "affine5_g64",
+        "affine6_g64"]
 
 
 @pytest.fixture(scope="module")
@@ -51,7 +52,10 @@ def test_pack_unpack_bitexact(capi, fmt, shape):
     assert np.array_equal(out.cpu().numpy().astype(np.int32), codes)
 
 
-EXPERT_FMTS = ["affine4_g64", "affine3_g64", "w4a16_g128"]
+EXPERT_FMTS = ["affine4_g64", "affine3_g64", "w4a16_g128", "affine2_g64", "affine5_g64",
+               "affine6_g64", "affine8_g64"]
+BITS_OF = {"affine2_g64": 2, "affine3_g64": 3, "affine4_g64": 4, "affine5_g64": 5,
+           "affine6_g64": 6, "affine8_g64": 8, "w4a16_g128": 4}
 
 
 def _tiled_reference(fmt, mats, I, H, which):
@@ -63,14 +67,18 @@ def _tiled_reference(fmt, mats, I, H, which):
     ng, nch = CK // 64, K // CK
     nblk = H // 128 if which else I // 64
     w4 = fmt == "w4a16_g128"
+    bits = BITS_OF[fmt]
     out = bytearray()
     for m in mats:
-        codes = m.codes.astype(np.int64) + (8 if w4 else 0)          # nibble values
-        words = np.zeros((rows, K // 8), dtype=np.uint64)
+        codes = m.codes.astype(np.int64) + (8 if w4 else 0)          # stored values
+        words = np.zeros((rows, K // 8), dtype=np.uint64)            # low 4 bits
+        hiwords = np.zeros((rows, K // 8), dtype=np.uint64)          # bits 4..7
         for i in range(8):   # code i of a word in nibble (i & 1) * 4 + i // 2
             nib = (i & 1) * 4 + i // 2
-            words |= (codes[:, i::8].astype(np.uint64) << np.uint64(4 * nib))
+            words |= ((codes[:, i::8] & 15).astype(np.uint64) << np.uint64(4 * nib))
+            hiwords |= ((codes[:, i::8] >> 4).astype(np.uint64) << np.uint64(4 * nib))
         words = words.astype(np.uint32)
+        hiwords = hiwords.astype(np.uint32)
         sc = m.scales.view(np.uint16) if m.scales.dtype != np.uint16 else m.scales
         bi = None if w4 else (m.biases.view(np.uint16) if m.biases.dtype != np.uint16 else m.biases)
         for blk in range(nblk):
@@ -83,23 +91,44 @@ def _tiled_reference(fmt, mats, I, H, which):
                         base = blk * 64 + 16 * w if w < 4 else I + blk * 64 + 16 * (w - 4)
                     for G in range(ng):
                         lw = np.zeros((32, 4), dtype=np.uint32)
+                        hw = np.zeros((32, 4), dtype=np.uint32)
                         for lane in range(32):
                             g, t = lane // 4, lane % 4
                             k0 = c * CK + 64 * G + 16 * t
                             for j in range(4):
                                 r = base + g + 8 * (j >> 1)
                                 lw[lane, j] = words[r, (k0 + 8 * (j & 1)) // 8]
-                        if fmt == "affine3_g64":
+                                hw[lane, j] = hiwords[r, (k0 + 8 * (j & 1)) // 8]
+                        if bits in (2, 3):
                             m3 = np.uint32(0x33333333)
                             L01 = (lw[:, 0] & m3) | ((lw[:, 1] & m3) << np.uint32(2))
                             L23 = (lw[:, 2] & m3) | ((lw[:, 3] & m3) << np.uint32(2))
-                            Hb = (((lw[:, 0] >> np.uint32(2)) & np.uint32(0x11111111))
-                                  | ((lw[:, 1] >> np.uint32(1)) & np.uint32(0x22222222))
-                                  | (lw[:, 2] & np.uint32(0x44444444))
-                                  | ((lw[:, 3] << np.uint32(1)) & np.uint32(0x88888888)))
-                            item += np.concatenate([L01, L23, Hb]).astype("<u4").tobytes()
+                            planes = [L01, L23]
+                            if bits == 3:
+                                planes.append(
+                                    ((lw[:, 0] >> np.uint32(2)) & np.uint32(0x11111111))
+                                    | ((lw[:, 1] >> np.uint32(1)) & np.uint32(0x22222222))
+                                    | (lw[:, 2] & np.uint32(0x44444444))
+                                    | ((lw[:, 3] << np.uint32(1)) & np.uint32(0x88888888)))
+                            item += np.concatenate(planes).astype("<u4").tobytes()
                         else:
                             item += lw.astype("<u4").tobytes()
+                            # the bits above the low nibble, by the written
+                            # definitions of the 5-bit and 6-bit planes
+                            if bits in (5, 6):
+                                P = np.zeros((2, 32), dtype=np.uint64)
+                                for x in range(4):
+                                    for n in range(8):
+                                        hb = (hw[:, x] >> np.uint32(4 * n)).astype(np.uint64)
+                                        if bits == 5:
+                                            pos = 4 * x + (n & 3) + 16 * (n >> 2)
+                                            P[0] |= (hb & np.uint64(1)) << np.uint64(pos)
+                                        else:
+                                            pos = 2 * (4 * (x & 1) + (n & 3)) + 16 * (n >> 2)
+                                            P[x >> 1] |= (hb & np.uint64(3)) << np.uint64(pos)
+                                item += P[: 1 if bits == 5 else 2].astype("<u4").tobytes()
+                            if bits == 8:
+                                item += hw.astype("<u4").tobytes()
                 gs = 128 if w4 else 64
                 nsg = CK // gs
                 for w in range(8):
@@ -123,6 +152,8 @@ def _tiled_reference(fmt, mats, I, H, which):
 @pytest.mark.parametrize("fmt", EXPERT_FMTS)
 def test_tiled_layout_matches_definition(capi, fmt):
     I, H = (256, 512) if fmt == "w4a16_g128" else (128, 640)   # chunks 256/512 and 128/128
+    if fmt in ("affine5_g64", "affine6_g64", "affine8_g64"):
+        I, H = 128, 256
     bank = synth.gen_bank(np.random.default_rng(41), fmt, 2, I, H)
     tb = Hn.gpu_bank(bank)
     got13 = tb.tensors[0].cpu().numpy()
@@ -292,6 +323,11 @@ def test_bucket_bitexact(capi, T, k, E):
     ("w4a16_g128", "f16", 32, 2048, 512),
     ("w4a16_g128", "bf16", 3, 512, 256),
     ("affine4_g64", "f16", 9, 512, 128),
+    ("affine2_g64", "bf16", 6, 512, 256),
+    ("affine5_g64", "bf16", 11, 2048, 512),
+    ("affine6_g64", "f16", 7, 384, 128),
+    ("affine8_g64", "bf16", 8, 512, 128),
+    ("affine8_g64", "f16", 3, 256, 256),
 ])
 def test_expert_mlp_per_projection(capi, fmt, act, T, H, I):
     torch = Hn.torch()
@@ -404,6 +440,60 @@ def test_3bit_widened_to_4bit_bitexact(capi):
     assert Hn.torch().equal(out3, out4)
 
 
+def _rewidth(b, fmt):
+    """The same codes, scales and biases stored at another affine width."""
+    nb = synth.ExpertBank(fmt, b.E, b.I, b.H)
+    nb.w13 = [synth.QMatrix(fmt, m.rows, m.cols, codes=m.codes, scales=m.scales,
+                            biases=m.biases) for m in b.w13]
+    nb.w2 = [synth.QMatrix(fmt, m.rows, m.cols, codes=m.codes, scales=m.scales,
+                           biases=m.biases) for m in b.w2]
+    return nb
+
+
+@pytest.mark.parametrize("T", [5, 40])
+def test_codes_widened_across_all_widths_bitexact(capi, T):
+    """The widening control of "qwen3_5_moe on native CUDA with 3-bit routed
+    experts ... #803" (comment "The 3-bit width is up as #972") at every width
+    the expert kernels read: 2-bit codes stored as 2-, 3-, 4-, 5-, 6- and
+    8-bit banks give bit-identical layers (one accumulation order on the
+    exact integer codes), in the fused and the launch-per-step decode forms
+    (T=5) and in the decode form of a prefill-sized call (T=40)."""
+    torch = Hn.torch()
+    L = synth.gen_layer(T=T, E=16, k=8, H=512, I=256, expert_fmt="affine2_g64",
+                        shared_fmt="affine2_g64", gate_fmt="affine8_g64", seed=27)
+    flags = capi.MOE_FLAG_FORCE_DECODE
+    ref = None
+    for fmt in ["affine2_g64", "affine3_g64", "affine4_g64", "affine5_g64", "affine6_g64",
+                "affine8_g64"]:
+        L.experts = _rewidth(L.experts, fmt)
+        L.shared = _rewidth(L.shared, fmt)
+        g = Hn.GpuLayer(L)
+        outs = [g.forward(flags=flags)[0], g.forward(flags=flags | capi.MOE_FLAG_UNFUSED)[0]]
+        for o in outs:
+            if ref is None:
+                ref = o
+            assert torch.equal(o, ref), fmt
+    ref_o = Hn.oracle_layer(L, idx_override=g.forward(flags=flags)[1].cpu().numpy())
+    Hn.assert_layer_close(Hn.to_np(ref), ref_o["out"], out_type=L.act)
+
+
+@pytest.mark.parametrize("fmt", ["affine2_g64", "affine5_g64", "affine6_g64", "affine8_g64"])
+def test_other_widths_full_size(capi, fmt):
+    """MLX affine experts at the other widths the pages' loader reads
+    ("Affine experts at other widths"), at full size: decode batch 8 (E=256,
+    hidden 2048, inter 512, Zipf routing, a shared expert of the same width),
+    every output against the oracle, the routing against its fp64 routing up
+    to near ties."""
+    L = synth.workload("decode8_affine4_shared_zipf", expert_fmt=fmt, shared_fmt=fmt)
+    g = Hn.GpuLayer(L)
+    out, idx, _ = g.forward()
+    assert capi.moe_get_device_status(g.ws) == 0
+    idx = idx.cpu().numpy()
+    ref = Hn.oracle_layer(L, idx_override=idx)
+    Hn.assert_layer_close(Hn.to_np(out), ref["out"], out_type=L.act)
+    Hn.assert_routing_near_ties(L, idx, ref["logits"])
+
+
 def test_zero_tokens_and_zero_input(capi):
     L = synth.gen_layer(T=3, E=8, k=2, H=256, I=128, expert_fmt="affine4_g64",
                         shared_fmt="affine4_g64", gate_fmt="affine8_g64", seed=23)
@@ -439,10 +529,10 @@ def test_validation_errors(capi):
     with pytest.raises(capi.MoeError) as e:
         capi.moe_layer_forward(g.router, None, None, g.experts, None, g.x, 2, out, ws=small)
     assert e.value.status == 3
-    bad = capi.ExpertBank("affine8_g64", 8, 128, 256, *g.experts.tensors)
+    bad = capi.ExpertBank("bf16", 8, 128, 256, *g.experts.tensors)
     with pytest.raises(capi.MoeError) as e:
         capi.moe_layer_forward(g.router, None, None, bad, None, g.x, 2, out, ws=g.ws)
-    assert e.value.status == 2 and "AFFINE8_G64" in str(e.value)
+    assert e.value.status == 2 and "BF16" in str(e.value)
     assert capi.moe_get_device_status(g.ws) == 0
 
 
