@@ -333,34 +333,50 @@ bool use_prefill(const moe_expert_bank* b, int T, int flags) {
          prefill_smem(geo13(b).t, 0) > 0 && prefill_smem(geo2(b).t, 1) > 0;
 }
 
-// One expert of a bank over T tokens in the prefill form: h (bf16) into the
+// The prefill form's fp16 activation rows: x itself (fp16 activations) or
+// its fp16 copy in the workspace (bf16 activations, converted here).
+moe_status prefill_act(const void* x, bool f16, int T, int H, void* ws, const WsLayout& L,
+                       const uint16_t** out, cudaStream_t stream) {
+  if (f16) {
+    *out = static_cast<const uint16_t*>(x);
+    return MOE_OK;
+  }
+  uint16_t* xh = reinterpret_cast<uint16_t*>(wsp(ws, L.xh));
+  MOE_CUDA(launch_act_f16(static_cast<const uint16_t*>(x), long(T) * H, xh, static_cast<int*>(ws),
+                          stream),
+           "activation conversion");
+  *out = xh;
+  return MOE_OK;
+}
+
+// One expert of a bank over T tokens in the prefill form: h (fp16) into the
 // workspace, y (fp32) straight into y_out.
 moe_status run_expert_prefill(const moe_expert_bank* bank, int expert, const void* x, bool f16,
                               int T, float* y_out, void* ws, const WsLayout& L,
                               cudaStream_t stream) {
   const int H = bank->hidden, I = bank->inter;
   const MatGeo g13 = geo13(bank), g2 = geo2(bank);
+  const uint16_t* xa = nullptr;
+  if (moe_status s = prefill_act(x, f16, T, H, ws, L, &xa, stream)) return s;
   PrefillJob J{};
   J.g = g13.t;
   J.base = g13.base;
   J.fixed_e = expert;
   J.fixed_T = T;
-  J.B = static_cast<const uint16_t*>(x);
+  J.B = xa;
   J.ldB = H;
   J.h = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh));
-  J.hl = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hl));
   J.ldh = h_pitch(I);
   J.status = static_cast<int*>(ws);
-  MOE_CUDA(launch_prefill(J, 0, f16, sm_count(), stream), "prefill gate/up kernel");
+  MOE_CUDA(launch_prefill(J, 0, sm_count(), stream), "prefill gate/up kernel");
   PrefillJob D = J;
   D.g = g2.t;
   D.base = g2.base;
   D.B = J.h;
-  D.Blo = J.hl;
   D.ldB = h_pitch(I);
   D.y = y_out;
   D.ldy = H;
-  MOE_CUDA(launch_prefill(D, 1, false, sm_count(), stream), "prefill down kernel");
+  MOE_CUDA(launch_prefill(D, 1, sm_count(), stream), "prefill down kernel");
   return MOE_OK;
 }
 
@@ -400,6 +416,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
     case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED";
+    case MOE_ERR_RANGE: return "MOE_ERR_RANGE";
     default: return "MOE_ERR_UNKNOWN";
   }
 }
@@ -496,7 +513,10 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
   if (!bucket_offsets || (T > 0 && (!topk_idx || !topk_w || !bucket_perm)))
     return fail(MOE_ERR_INVALID_ARG, "routing outputs must not be NULL");
   const WsLayout L = ws_layout(T, E, top_k, H, 128);
-  if ((s = check_ws(ws, ws_bytes, L.idx))) return s;
+  // the logits, and above the decode sizes the router's k-slice sums
+  if ((s = check_ws(ws, ws_bytes, T > MOE_DECODE_MAX_TOKENS ? L.rpart + 16 * size_t(T) * (E + 1)
+                                                            : L.idx)))
+    return s;
   float* lg = logits ? logits : reinterpret_cast<float*>(wsp(ws, L.logits));
   float* gl = reinterpret_cast<float*>(wsp(ws, L.gate_logit));
   RouterJob R{};
@@ -519,6 +539,7 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
   R.logits = lg;
   R.gate_logit = gl;
   R.round_bf16 = rb;
+  R.part = T > MOE_DECODE_MAX_TOKENS ? reinterpret_cast<float*>(wsp(ws, L.rpart)) : nullptr;
   MOE_CUDA(launch_router(R, stream), "router kernel");
   MOE_CUDA(launch_topk(lg, shared_gate ? gl : nullptr, T, E, top_k, topk_idx, topk_w,
                        shared_gate ? shared_gate_w : nullptr, rb, stream),
@@ -597,6 +618,8 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
     MOE_CUDA(launch_subslots(bucket_offsets, E, nss, se, so, sc, stream, kMaxTok, 0, kPfLight),
              "sub-slot kernel");
     const MatGeo g13 = geo13(experts), g2 = geo2(experts);
+    const uint16_t* xa = nullptr;
+    if ((s = prefill_act(x, f16, T, H, ws, L, &xa, stream))) return s;
     PrefillJob J{};
     J.g = g13.t;
     J.base = g13.base;
@@ -604,35 +627,34 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
     J.te = te;
     J.toff = to;
     J.tcnt = tc;
-    J.B = static_cast<const uint16_t*>(x);
+    J.B = xa;
     J.ldB = H;
     J.gather = 1;
     J.perm = bucket_perm;
     J.k = top_k;
-    J.h = reinterpret_cast<uint16_t*>(wsp(ws, L.hh));
-    J.hl = reinterpret_cast<uint16_t*>(wsp(ws, L.hl));
+    J.h = reinterpret_cast<uint16_t*>(wsp(ws, L.hh));  // fp16 h rows of the tiled experts
     J.ldh = h_pitch(I);
     J.status = static_cast<int*>(ws);
-    MOE_CUDA(launch_prefill(J, 0, f16, sm_count(), stream), "prefill gate/up kernel");
+    MOE_CUDA(launch_prefill(J, 0, sm_count(), stream), "prefill gate/up kernel");
     PrefillJob D = J;
     D.g = g2.t;
     D.base = g2.base;
     D.B = J.h;
-    D.Blo = J.hl;
     D.ldB = h_pitch(I);
     D.gather = 0;
     D.y = y;
     D.ldy = H;
-    D.yzero = yhalf;
     D.scatter = 1;
-    MOE_CUDA(launch_prefill(D, 1, false, sm_count(), stream), "prefill down kernel");
+    MOE_CUDA(launch_prefill(D, 1, sm_count(), stream), "prefill down kernel");
     float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
     MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, f16, g13.t, xsum, stream),
              "activation sums");
     const SubSlots ss{nss, se, so, sc, 0, 0};
     s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
-                 bucket_perm, top_k, J.h, J.hl, reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr,
-                 y, yhalf, kRowsScatter, static_cast<int*>(ws), stream);
+                 bucket_perm, top_k, reinterpret_cast<uint16_t*>(wsp(ws, L.hh)),
+                 reinterpret_cast<uint16_t*>(wsp(ws, L.hl)),
+                 reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr, y, yhalf, kRowsScatter,
+                 static_cast<int*>(ws), stream);
     if (s) return s;
     CombineArgs C{};
     C.y = y;
@@ -647,6 +669,9 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
     C.H = H;
     C.f16 = f16;
     C.round_bf16 = rb;
+    C.idx = topk_idx;  // the tiled experts' y sits in plane 0 alone
+    C.offsets = bucket_offsets;
+    C.one_plane_max = kPfLight;
     MOE_CUDA(launch_combine(C, stream), "combine kernel");
     return ok();
   }

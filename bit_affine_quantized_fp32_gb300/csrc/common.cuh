@@ -54,6 +54,8 @@ struct WsLayout {
   size_t pt_e;        // i32 [maxss] expert of each tile
   size_t pt_off;      // i32 [maxss] first bucket position
   size_t pt_cnt;      // i32 [maxss] rows (1..128)
+  size_t xh;          // u16 [T][H] fp16 copy of bf16 activations (prefill form)
+  size_t rpart;       // f32 [4][T][E+1] k-slice sums of the router (prefill form)
   size_t total;
 };
 
@@ -107,6 +109,8 @@ inline WsLayout ws_layout(long T, long E, long k, long H, long I) {
   L.pt_e = take(4 * mss);
   L.pt_off = take(4 * mss);
   L.pt_cnt = take(4 * mss);
+  L.xh = take(2 * T * H);
+  L.rpart = take(4 * 4 * T * (E + 1));
   L.total = o;
   return L;
 }

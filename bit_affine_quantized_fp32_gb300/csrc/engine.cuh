@@ -1016,11 +1016,16 @@ __device__ void consumer_run(const EngineCfg& C, EngineSmem& E, const EngineMem&
 // output is issued before the chain starts (k <= kMaxTopK).  `nthr` threads.
 constexpr int kMaxTopK = 8;
 constexpr int kCombineRows = 64;  // columns of one combine piece
+// In the prefill form (one_plane set) an assignment whose expert has more
+// than one_plane_max assignments (by the bucket offsets) has its y in plane 0
+// alone (the tensor-core GEMMs); the second plane is then taken as 0.
 __device__ __forceinline__ void combine_rows(const float* y, size_t yhalf, const float* w,
                                              const float* ysh, const float* ysh2,
                                              const float* sg, uint16_t* out, int T, int k, int H,
                                              bool f16, int h0, int nh, int tid, int nthr,
-                                             bool rb = false) {
+                                             bool rb = false, const int32_t* idx = nullptr,
+                                             const int32_t* offsets = nullptr,
+                                             int one_plane_max = 0) {
   for (int v = tid; v < T * nh; v += nthr) {
     const int t = v / nh;
     const int h = h0 + (v - t * nh);
@@ -1030,7 +1035,12 @@ __device__ __forceinline__ void combine_rows(const float* y, size_t yhalf, const
       if (j < k) {
         const size_t a = (size_t)(t * k + j) * H + h;
         ya[j] = __ldcg(y + a);
-        if (yhalf) yb[j] = __ldcg(y + yhalf + a);
+        bool two = yhalf != 0;
+        if (two && idx) {
+          const int e = __ldg(idx + t * k + j);
+          two = __ldg(offsets + e + 1) - __ldg(offsets + e) <= one_plane_max;
+        }
+        yb[j] = two ? __ldcg(y + yhalf + a) : 0.f;
       }
     }
     float vs = 0.f;

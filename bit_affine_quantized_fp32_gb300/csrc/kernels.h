@@ -47,6 +47,9 @@ struct CombineArgs {
   uint16_t* out;     // [T][H]
   int T, k, H, f16;
   int round_bf16;    // w and sg rounded to bf16 before the sum
+  const int32_t* idx;      // prefill form (nullable): the assignments' experts [T][k]
+  const int32_t* offsets;  //   and bucket offsets [E+1]; experts with more than
+  int one_plane_max;       //   one_plane_max assignments have y in plane 0 only
 };
 cudaError_t launch_combine(const CombineArgs& A, cudaStream_t st);
 // *p = v, stream-ordered (a workspace control word)
@@ -80,6 +83,8 @@ struct RouterJob {
   float* logits;            // [T][E]
   float* gate_logit;        // [T] (when gq)
   int round_bf16;           // router and gate rows rounded to bf16 before the dot products
+  float* part;              // nullable scratch [4][T][E + 1]: the tensor-core router's
+                            // k-slice sums (used for T > 32)
 };
 int router_ks(int H);
 int router_blocks(int E, bool gate, int H);

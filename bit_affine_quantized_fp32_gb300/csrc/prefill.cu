@@ -3,27 +3,27 @@
 // For T > 32 tokens an expert sees up to hundreds of rows, so its weights are
 // dequantised once per tile of kPfTile rows and fed to the tensor cores:
 // D[128 weight rows x N tokens] += A[128 x 64] * B[N x 64]^T per 64-column
-// group, 16-bit operands in shared memory, fp32 accumulators in tensor memory.
+// group, fp16 operands in shared memory, fp32 accumulators in tensor memory.
 // One persistent CTA per SM, 15 warps:
 //   warps 0-3   epilogue: tensor memory -> registers (thread = weight row),
-//               SwiGLU -> bf16 h (mode 0) or fp32 y rows (mode 1);
+//               SwiGLU -> fp16 h (mode 0) or fp32 y rows (mode 1);
 //   warps 4-11  dequantisation: one weight item (128 rows x CK columns, the
 //               kernel-tiled layout) per raw stage, one 64-column group at a
-//               time into an A stage, w = fma(s, q, b) in fp32 split into a
-//               bf16 hi part and a bf16 lo part w - hi (fp16 for fp16
-//               activations);
+//               time into an A stage: w = fp16(s * q + b), one fused
+//               multiply-add of the fp16 scale, the exact code and the fp16
+//               bias (W4A16: s * u - 8 s), rounded once;
 //   warp 12     TMA bulk copies of the raw weight items (2 stages);
 //   warp 13     the operand rows of each group into a B stage (cp.async, 16 B
-//               pieces placed in the tensor core's K-major layout; h as hi
-//               and lo rows);
+//               pieces placed in the tensor core's K-major layout): fp16 x
+//               rows (mode 0) or fp16 h rows (mode 1);
 //   warp 14     allocates tensor memory and issues the MMAs (one thread);
 //               tcgen05.commit frees A/B stages and hands accumulators over.
-// Per 16 columns the MMAs add A_hi B + A_lo B (gate/up; x is exact) or
-// A_hi B_hi + A_hi B_lo + A_lo B_hi (down), so the operands carry ~16
-// significant bits.  Two accumulators of kPfTile columns let the epilogue of
-// one unit overlap the MMAs of the next.  Every wait is bounded (one second,
-// then the status word gets MOE_ERR_TIMEOUT and the remaining waits return at
-// once).
+// One MMA per 16 columns.  The activations enter as fp16: bf16 x is converted
+// once per call (exact in fp16's normal range; a value beyond it sets
+// MOE_ERR_RANGE), and h is stored as fp16 (likewise checked).  Two
+// accumulators of kPfTile columns let the epilogue of one unit overlap the
+// MMAs of the next.  Every wait is bounded (the workspace's limit, then the
+// status word gets MOE_ERR_TIMEOUT and the remaining waits return at once).
 //
 // Sources: "qwen3_5_moe on native CUDA with 3-bit routed experts ... #803"
 // (prefill windows through grouped expert GEMMs, SwiGLU epilogue).
@@ -41,13 +41,10 @@ constexpr int kPfRaw = 2;                    // raw weight-item stages
 constexpr int kPfA = 128 * 64 * 2;           // 128 rows x 64 columns, 16-bit
 constexpr int kPfB = kPfTile * 64 * 2;
 constexpr int kPfKBlk = 64;                  // columns per MMA group (4 x K16)
-constexpr int kPfStagesMax = 3;
-// A/B stages per mode: [A hi][A lo][B] (gate/up, 3 stages) or
-// [A hi][A lo][B hi][B lo] (down, 2 stages)
-__host__ __device__ constexpr int pf_stages(int mode) { return mode == 0 ? 3 : 2; }
-__host__ __device__ constexpr int pf_stage_bytes(int mode) {
-  return mode == 0 ? 2 * kPfA + kPfB : 2 * kPfA + 2 * kPfB;
-}
+constexpr int kPfStagesMax = 4;
+// A/B stages: [A][B], both fp16
+__host__ __device__ constexpr int pf_stages(int mode) { return mode == 0 ? 4 : 4; }
+__host__ __device__ constexpr int pf_stage_bytes(int mode) { return (void)mode, kPfA + kPfB; }
 
 __host__ __device__ inline int raw_stage_bytes(const TileGeo& g) {
   return (g.item_bytes + 1023) & ~1023;
@@ -87,39 +84,21 @@ __device__ __forceinline__ PfUnit pf_unit(const PrefillJob& J, int u) {
   return r;
 }
 
-// Two fp32 values -> a packed pair of 16-bit hi parts and of lo parts
-// (v - hi), bf16 or fp16.
-__device__ __forceinline__ void split2(float a, float b, bool f16, uint32_t& hi, uint32_t& lo) {
-  if (f16) {
-    const __half2 h = __floats2half2_rn(a, b);
-    const float2 hf = __half22float2(h);
-    const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
-    hi = *reinterpret_cast<const uint32_t*>(&h);
-    lo = *reinterpret_cast<const uint32_t*>(&l);
-  } else {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    const float2 hf = __bfloat1622float2(h);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
-    hi = *reinterpret_cast<const uint32_t*>(&h);
-    lo = *reinterpret_cast<const uint32_t*>(&l);
-  }
-}
-
-// One 8-code word (codes in nibble order [0 2 4 6 1 3 5 7]) -> 8 dequantised
-// values in column order, w = fma(s, 128 + q, b - 128 s) in fp32, as hi and
-// lo 16-bit parts.
-__device__ __forceinline__ void dequant_word(uint32_t w, float s, float b128, bool f16, uint4& hi,
-                                             uint4& lo) {
-  uint32_t h[4], l[4];
+// One 8-code word (codes in nibble order [0 2 4 6 1 3 5 7]) -> 8 fp16 weights
+// in column order: w = fma(s, q, b) in fp16 (the exact value rounded once;
+// q is exact as 1024 + q - 1024).
+__device__ __forceinline__ uint4 dequant_word16(uint32_t w, __half2 s2, __half2 b2) {
+  const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+  uint32_t h[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     uint32_t p;
-    asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;\n" : "=r"(p) : "r"(w >> (4 * j)));
-    const float c0 = __uint_as_float(p << 16), c1 = __uint_as_float(p & 0xFFFF0000u);
-    split2(fmaf(s, c0, b128), fmaf(s, c1, b128), f16, h[j], l[j]);
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;\n" : "=r"(p) : "r"(w >> (4 * j)));
+    const __half2 q = __hsub2(*reinterpret_cast<__half2*>(&p), k1024);
+    const __half2 v = __hfma2(s2, q, b2);
+    h[j] = *reinterpret_cast<const uint32_t*>(&v);
   }
-  hi = make_uint4(h[0], h[1], h[2], h[3]);
-  lo = make_uint4(l[0], l[1], l[2], l[3]);
+  return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
 // Group G of the raw item into an A stage: thread (tile w, lane l) converts
@@ -127,7 +106,7 @@ __device__ __forceinline__ void dequant_word(uint32_t w, float s, float b128, bo
 // the group -- into the K-major layout (one 16-byte piece per word).
 template <int FMT>
 __device__ __forceinline__ void dequant_group(const TileGeo& g, const uint8_t* raw, int G,
-                                              uint8_t* A, uint8_t* Alo, int w, int l, bool f16) {
+                                              uint8_t* A, int w, int l) {
   const int NG = g.ng;
   const int gq = l >> 2, t = l & 3;
   uint32_t W0, W1, W2, W3;
@@ -142,34 +121,29 @@ __device__ __forceinline__ void dequant_group(const TileGeo& g, const uint8_t* r
     W3 = v.w;
   }
   const uint8_t* sc = raw + g.code_bytes;
-  float s0, s1, b0, b1;
+  __half s0, s1, b0, b1;
   if constexpr (FMT == MOE_FMT_W4A16_SYM_G128) {
     const uint32_t sv =
         *reinterpret_cast<const uint32_t*>(sc + ((w * 8 + gq) * (NG / 2) + (G >> 1)) * 4);
-    const float2 sf = half2_bits_to_float2(sv);
-    s0 = sf.x;
-    s1 = sf.y;
-    b0 = -136.f * s0;  // w = s (u - 8) with the stored nibble u; operand is 128 + u
-    b1 = -136.f * s1;
+    s0 = __ushort_as_half(uint16_t(sv & 0xFFFF));
+    s1 = __ushort_as_half(uint16_t(sv >> 16));
+    // w = s (u - 8) for the stored nibble u: fma(s, u, -8 s), -8 s exact
+    b0 = __hmul(s0, __ushort_as_half(0xC800));
+    b1 = __hmul(s1, __ushort_as_half(0xC800));
   } else {
     const uint2 sv = *reinterpret_cast<const uint2*>(sc + ((w * 8 + gq) * NG + G) * 8);
-    const float2 p0 = half2_bits_to_float2(sv.x), p1 = half2_bits_to_float2(sv.y);
-    s0 = p0.x;
-    s1 = p1.x;
-    b0 = fmaf(-128.f, s0, p0.y);
-    b1 = fmaf(-128.f, s1, p1.y);
+    s0 = __ushort_as_half(uint16_t(sv.x & 0xFFFF));
+    b0 = __ushort_as_half(uint16_t(sv.x >> 16));
+    s1 = __ushort_as_half(uint16_t(sv.y & 0xFFFF));
+    b1 = __ushort_as_half(uint16_t(sv.y >> 16));
   }
+  const __half2 s02 = __halves2half2(s0, s0), s12 = __halves2half2(s1, s1);
+  const __half2 b02 = __halves2half2(b0, b0), b12 = __halves2half2(b1, b1);
   const int r0 = 16 * w + gq, r1 = r0 + 8;
-  const uint32_t WW[4] = {W0, W1, W2, W3};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = i < 2 ? r0 : r1;
-    uint4 hi, lo;
-    dequant_word(WW[i], i < 2 ? s0 : s1, i < 2 ? b0 : b1, f16, hi, lo);
-    const int o = umma_off(r, 16 * t + 8 * (i & 1), kPfKBlk);
-    *reinterpret_cast<uint4*>(A + o) = hi;
-    *reinterpret_cast<uint4*>(Alo + o) = lo;
-  }
+  *reinterpret_cast<uint4*>(A + umma_off(r0, 16 * t, kPfKBlk)) = dequant_word16(W0, s02, b02);
+  *reinterpret_cast<uint4*>(A + umma_off(r0, 16 * t + 8, kPfKBlk)) = dequant_word16(W1, s02, b02);
+  *reinterpret_cast<uint4*>(A + umma_off(r1, 16 * t, kPfKBlk)) = dequant_word16(W2, s12, b12);
+  *reinterpret_cast<uint4*>(A + umma_off(r1, 16 * t + 8, kPfKBlk)) = dequant_word16(W3, s12, b12);
 }
 
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
@@ -179,7 +153,7 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
 
-template <int FMT, int MODE, bool F16>
+template <int FMT, int MODE>
 __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant__ PrefillJob J) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ PfSmem S;
@@ -264,7 +238,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         if (ks >= NS)
           mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status, true);
         const int k0 = q * kPfKBlk;
-        uint8_t* B = stages + s * SB + 2 * kPfA;
+        uint8_t* B = stages + s * SB + kPfA;
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
           const int n = lane + 32 * i;
@@ -273,12 +247,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
               cp_async16(B + umma_off(n, ch * 8, kPfKBlk), src + ch * 8);
-            if (MODE == 1) {
-              const uint16_t* srl = J.Blo + rofs[i] + k0;
-#pragma unroll
-              for (int ch = 0; ch < 8; ++ch)
-                cp_async16(B + kPfB + umma_off(n, ch * 8, kPfKBlk), srl + ch * 8);
-            }
           }
         }
         cp_async_arrive_noinc(&S.b_full[s]);
@@ -295,9 +263,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         if (ui >= 2) mbar_wait_bounded(&S.acc_empty[a], ((ui >> 1) - 1) & 1, &S.wc, status, true);
         tmem_fence_after();
         const int N = max(16, (U.cnt + 15) & ~15);
-        const uint32_t idesc = (MODE == 0 && F16)
-                                   ? (umma_idesc_bf16(128, N) & ~((7u << 7) | (7u << 10)))
-                                   : umma_idesc_bf16(128, N);
+        // fp16 A and B: the format fields of the bf16 descriptor cleared
+        const uint32_t idesc = umma_idesc_bf16(128, N) & ~((7u << 7) | (7u << 10));
         const uint32_t d = tbase + uint32_t(a * kPfTile);
         constexpr uint32_t kSbo = (kPfKBlk / 8) * 128;
         for (int q = 0; q < nks; ++q, ++ks) {
@@ -306,16 +273,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
           mbar_wait_bounded(&S.b_full[s], (ks / NS) & 1, &S.wc, status, true);
           fence_proxy_async();
           tmem_fence_after();
-          const uint32_t ah = smem_u32(stages + s * SB), al = ah + kPfA;
-          const uint32_t bh = ah + 2 * kPfA, bl = bh + kPfB;
+          const uint32_t aa = smem_u32(stages + s * SB), ba = aa + kPfA;
 #pragma unroll
           for (int kk = 0; kk < kPfKBlk / 16; ++kk) {
             const uint32_t o = kk * 256;
-            const uint64_t dah = umma_desc(ah + o, 128, kSbo), dal = umma_desc(al + o, 128, kSbo);
-            const uint64_t dbh = umma_desc(bh + o, 128, kSbo);
-            umma_bf16(d, dah, dbh, idesc, q > 0 || kk > 0);
-            umma_bf16(d, dal, dbh, idesc, true);
-            if (MODE == 1) umma_bf16(d, dah, umma_desc(bl + o, 128, kSbo), idesc, true);
+            umma_bf16(d, umma_desc(aa + o, 128, kSbo), umma_desc(ba + o, 128, kSbo), idesc,
+                      q > 0 || kk > 0);
           }
           umma_commit(&S.ab_empty[s]);
         }
@@ -340,8 +303,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
           const int s = ks % NS;
           if (ks >= NS)
           mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status, true);
-          uint8_t* A = stages + s * SB;
-          dequant_group<FMT>(g, raw + rs * RB, Gi, A, A + kPfA, w, lane, MODE == 0 && F16);
+          dequant_group<FMT>(g, raw + rs * RB, Gi, stages + s * SB, w, lane);
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.a_full[s]);
@@ -377,10 +339,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
               if (n < U.cnt) {
                 const float ga = v[j], up = S.xch[r][j];
                 const float hv = ga / (1.f + expf(-ga)) * up;
-                const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
                 const size_t at = (size_t)(U.off + n) * J.ldh + 64 * U.m + r;
-                J.h[at] = __bfloat16_as_ushort(hb);
-                J.hl[at] = __bfloat16_as_ushort(__float2bfloat16_rn(hv - __bfloat162float(hb)));
+                J.h[at] = __half_as_ushort(__float2half_rn(hv));
+                if (!(fabsf(hv) <= 65504.f)) atomicExch(status, int(MOE_ERR_RANGE));
               }
             }
           }
@@ -393,7 +354,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
               const int row = J.scatter ? __ldg(J.perm + U.off + n) : U.off + n;
               const size_t at = (size_t)row * J.ldy + 128 * U.m + r;
               J.y[at] = v[j];
-              if (J.yzero) J.y[at + J.yzero] = 0.f;
             }
           }
         }
@@ -409,20 +369,40 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
   if (warp == 14) tmem_dealloc(tbase, 2 * kPfTile);
 }
 
-template <int FMT, int MODE, bool F16>
+template <int FMT, int MODE>
 cudaError_t launch_t(const PrefillJob& J, int sms, cudaStream_t st) {
   const int smem = prefill_smem(J.g, MODE);
   if (smem <= 0) return cudaErrorInvalidValue;
-  const cudaError_t e = ensure_dynamic_smem((const void*)k_prefill<FMT, MODE, F16>, smem);
+  const cudaError_t e = ensure_dynamic_smem((const void*)k_prefill<FMT, MODE>, smem);
   if (e != cudaSuccess) return e;
-  k_prefill<FMT, MODE, F16><<<sms, kPfThreads, smem, st>>>(J);
+  k_prefill<FMT, MODE><<<sms, kPfThreads, smem, st>>>(J);
   return cudaGetLastError();
 }
 
 template <int FMT>
-cudaError_t launch_fmt(const PrefillJob& J, int mode, bool f16a, int sms, cudaStream_t st) {
-  if (mode == 1) return launch_t<FMT, 1, false>(J, sms, st);
-  return f16a ? launch_t<FMT, 0, true>(J, sms, st) : launch_t<FMT, 0, false>(J, sms, st);
+cudaError_t launch_fmt(const PrefillJob& J, int mode, int sms, cudaStream_t st) {
+  return mode == 1 ? launch_t<FMT, 1>(J, sms, st) : launch_t<FMT, 0>(J, sms, st);
+}
+
+// bf16 activations -> fp16 (exact in fp16's normal range); a value outside
+// it sets MOE_ERR_RANGE in the status word
+__global__ void k_act_f16(const uint16_t* __restrict__ x, long n, uint16_t* __restrict__ xh,
+                          int* status) {
+  const long i = (long(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+  if (i >= n) return;
+  const uint4 v = *reinterpret_cast<const uint4*>(x + i);
+  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[4];
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float a = __uint_as_float(in[j] << 16), b = __uint_as_float(in[j] & 0xFFFF0000u);
+    bad |= !(fabsf(a) <= 65504.f) || !(fabsf(b) <= 65504.f);
+    const __half2 h = __floats2half2_rn(a, b);
+    out[j] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(xh + i) = make_uint4(out[0], out[1], out[2], out[3]);
+  if (bad) atomicExch(status, int(MOE_ERR_RANGE));
 }
 
 }  // namespace
@@ -433,13 +413,21 @@ int prefill_smem(const TileGeo& g, int mode) {
   return bytes + int(sizeof(PfSmem)) + 1024 <= kEngineSmemMax ? bytes : 0;
 }
 
-cudaError_t launch_prefill(const PrefillJob& J, int mode, bool f16a, int sms, cudaStream_t st) {
+cudaError_t launch_prefill(const PrefillJob& J, int mode, int sms, cudaStream_t st) {
   switch (J.g.fmt) {
-    case MOE_FMT_AFFINE4_G64: return launch_fmt<MOE_FMT_AFFINE4_G64>(J, mode, f16a, sms, st);
-    case MOE_FMT_AFFINE3_G64: return launch_fmt<MOE_FMT_AFFINE3_G64>(J, mode, f16a, sms, st);
-    case MOE_FMT_W4A16_SYM_G128: return launch_fmt<MOE_FMT_W4A16_SYM_G128>(J, mode, f16a, sms, st);
+    case MOE_FMT_AFFINE4_G64: return launch_fmt<MOE_FMT_AFFINE4_G64>(J, mode, sms, st);
+    case MOE_FMT_AFFINE3_G64: return launch_fmt<MOE_FMT_AFFINE3_G64>(J, mode, sms, st);
+    case MOE_FMT_W4A16_SYM_G128: return launch_fmt<MOE_FMT_W4A16_SYM_G128>(J, mode, sms, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_act_f16(const uint16_t* x, long n, uint16_t* xh, int* status,
+                           cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const long threads = (n + 7) / 8;
+  k_act_f16<<<unsigned((threads + 255) / 256), 256, 0, st>>>(x, n, xh, status);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

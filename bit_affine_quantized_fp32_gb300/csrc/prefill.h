@@ -14,13 +14,12 @@ constexpr int kPfLight = 40;
 
 // One prefill GEMM launch over a tile list: each tile is <= kPfTile rows of
 // one expert; every (tile, 128-row weight block) is a unit.
-//   mode 0 (gate/up): A = w13 blocks (64 gate + 64 up rows), B = activation
-//     rows, epilogue h = silu(gate) * up -> h rows off + n as bf16 hi + lo;
-//   mode 1 (down): A = w2 blocks (128 rows), B = h rows off + n (hi + lo),
+//   mode 0 (gate/up): A = w13 blocks (64 gate + 64 up rows), B = fp16
+//     activation rows, epilogue h = silu(gate) * up -> fp16 h rows off + n;
+//   mode 1 (down): A = w2 blocks (128 rows), B = fp16 h rows off + n,
 //     epilogue fp32 y rows (scattered by perm, or off + n).
-// The dequantised weights enter the MMA as bf16 hi + lo parts as well (fp16
-// for fp16 activations), so products carry ~16 significant bits and the sums
-// fp32 rounding only.
+// The dequantised weights enter the MMA as fp16, fma(s, q, b) rounded once;
+// accumulation is fp32.
 struct PrefillJob {
   TileGeo g;                 // tiled geometry of the matrix
   const uint8_t* base;       // tiled bank (expert 0, item 0)
@@ -30,26 +29,25 @@ struct PrefillJob {
   const int* tcnt;           //         rows (1..kPfTile)
   int fixed_e, fixed_T;
   int max_tiles;             // host bound (unused by the kernel)
-  const uint16_t* B;         // operand rows (x, or h hi), ldB elements apart
-  const uint16_t* Blo;       // mode 1: h lo rows
+  const uint16_t* B;         // fp16 operand rows (x, or h), ldB elements apart
   int ldB;
   int gather;                // mode 0: operand row = perm[off + n] / k (else off + n)
   const int* perm;
   int k;
-  uint16_t* h;               // mode 0 output: bf16 h hi, ldh elements apart
-  uint16_t* hl;              //                bf16 h lo (h - hi)
+  uint16_t* h;               // mode 0 output: fp16 h, ldh elements apart
   int ldh;
   float* y;                  // mode 1 output (fp32), ldy elements apart
   int ldy;
-  size_t yzero;              // mode 1: when > 0, 0 is also stored at y[i + yzero] (the
-                             //         second k-half plane the decode units would write)
   int scatter;               // mode 1: output row = perm[off + n] (else off + n)
   int* status;
 };
 
 // Shared memory of a launch for geometry g in mode 0/1 (0: not supported).
 int prefill_smem(const TileGeo& g, int mode);
-// mode 0/1 as above; f16a: fp16 activations (mode 0 only).
-cudaError_t launch_prefill(const PrefillJob& J, int mode, bool f16a, int sms, cudaStream_t st);
+cudaError_t launch_prefill(const PrefillJob& J, int mode, int sms, cudaStream_t st);
+// bf16 activations [n] -> fp16 (exact in fp16's normal range; outside it the
+// status word gets MOE_ERR_RANGE); n a multiple of 8, both 16-byte aligned
+cudaError_t launch_act_f16(const uint16_t* x, long n, uint16_t* xh, int* status,
+                           cudaStream_t st);
 
 }  // namespace moe

@@ -132,32 +132,6 @@ __device__ __forceinline__ float router_finalize(const float* p, size_t stride, 
   return s;
 }
 
-// Router block rb (8 warps): rows [rb*RPB, rb*RPB + RPB) of the router plus
-// the shared-gate row (row E), RPB = 8 / KS; warp (row, q) runs router_warp;
-// the KS partial sums of a row are finalised in split order.  Needs
-// blockDim.x == 256.  A token's logit does not depend on the other tokens.
-__device__ __forceinline__ void router_block(const RouterJob& J, int KS, int rb, float* part,
-                                             const uint16_t* xs, int t0, int tn) {
-  const int wid = threadIdx.x >> 5;
-  const int RPB = 8 / KS;
-  const int rl = wid / KS, q = wid - rl * KS;
-  const int row = rb * RPB + rl;
-  const int nrows = J.E + (J.gq ? 1 : 0);
-  if (row < nrows) router_warp_any(J, KS, row, q, xs, tn, part + wid * kRouterTT, 1);
-  __syncthreads();
-  for (int i = threadIdx.x; i < RPB * tn; i += blockDim.x) {
-    const int r2 = i / tn, tl = i - r2 * tn;
-    const int row2 = rb * RPB + r2;
-    if (row2 >= nrows) continue;
-    const float* p = part + (r2 * KS) * kRouterTT + tl;
-    if (row2 < J.E)
-      J.logits[size_t(t0 + tl) * J.E + row2] =
-          router_finalize(p, kRouterTT, KS, J.bias ? J.bias + row2 : nullptr);
-    else
-      J.gate_logit[t0 + tl] = router_finalize(p, kRouterTT, KS, nullptr);
-  }
-  __syncthreads();
-}
 
 // Split q of R consecutive router rows row0.. (rows >= nrows skipped; the
 // shared-gate row is row E) for all T tokens of J.x, by one warp: every
@@ -167,10 +141,12 @@ __device__ __forceinline__ void router_block(const RouterJob& J, int KS, int rb,
 // bits.  Lane 0 writes part[(r * KS + q) * T + t].
 template <int NI, int R>
 __device__ __forceinline__ void router_warp_rows(const RouterJob& J, int KS, int row0, int nrows,
-                                                 int q, float* part) {
+                                                 int q, float* part, const uint16_t* xs = nullptr,
+                                                 int tn = -1) {
   const int lane = threadIdx.x & 31;
   const int kq = q * (J.H / KS);
-  const int T = J.T;
+  const int T = tn < 0 ? J.T : tn;
+  if (!xs) xs = J.x;
   float w[R][NI][4];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -188,7 +164,7 @@ __device__ __forceinline__ void router_warp_rows(const RouterJob& J, int KS, int
     uint2 xv[8][NI];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const uint16_t* xr = J.x + size_t(min(tl + u, T - 1)) * J.H + kq + 4 * lane;
+      const uint16_t* xr = xs + size_t(min(tl + u, T - 1)) * J.H + kq + 4 * lane;
 #pragma unroll
       for (int i = 0; i < NI; ++i) xv[u][i] = *reinterpret_cast<const uint2*>(xr + 128 * i);
     }
@@ -245,11 +221,51 @@ __device__ __forceinline__ void router_warp_rows_any(const RouterJob& J, int KS,
   }
 }
 
+// Router block of the standalone kernel: rows [rb * R, rb * R + R) (the
+// shared-gate row is row E) for tokens [t0, t0 + tn), tn <= kRouterTT, with
+// warp q computing split q of all R rows (x loaded once per warp for the R
+// rows) into part [R * KS][kRouterTT], then every (row, token) finalised in
+// split order.  The same per-(row, token) arithmetic as router_warp, so the
+// same bits as the fused kernel's router.  Needs blockDim.x == 32 * KS.
+template <int R>
+__device__ __forceinline__ void router_block_rows(const RouterJob& J, int KS, int rb, float* part,
+                                                  int t0, int tn) {
+  const int wid = threadIdx.x >> 5;
+  const int nrows = J.E + (J.gq ? 1 : 0);
+  const int row0 = rb * R;
+  const int NI_ = J.H / (KS * 128);
+  const uint16_t* xs = J.x + size_t(t0) * J.H;
+  if (NI_ == 1)
+    router_warp_rows<1, R>(J, KS, row0, nrows, wid, part, xs, tn);
+  else if (NI_ == 2)
+    router_warp_rows<2, R>(J, KS, row0, nrows, wid, part, xs, tn);
+  else
+    for (int r = 0; r < R; ++r) {  // wide splits: one row at a time
+      if (NI_ == 3)
+        router_warp_rows<3, 1>(J, KS, row0 + r, nrows, wid, part + size_t(r) * KS * tn, xs, tn);
+      else
+        router_warp_rows<4, 1>(J, KS, row0 + r, nrows, wid, part + size_t(r) * KS * tn, xs, tn);
+    }
+  __syncthreads();
+  for (int i = threadIdx.x; i < R * tn; i += blockDim.x) {
+    const int r2 = i / tn, tl = i - r2 * tn;
+    const int row2 = row0 + r2;
+    if (row2 >= nrows) continue;
+    const float* p = part + (r2 * KS) * tn + tl;
+    if (row2 < J.E)
+      J.logits[size_t(t0 + tl) * J.E + row2] =
+          router_finalize(p, tn, KS, J.bias ? J.bias + row2 : nullptr);
+    else
+      J.gate_logit[t0 + tl] = router_finalize(p, tn, KS, nullptr);
+  }
+  __syncthreads();
+}
+
 // The fused kernel's router block rb: rows [rb*RPB, rb*RPB + RPB) (the
 // shared-gate row is row E), warp (r, q) computing split q of row r into
 // part [RPB * KS][T] (shared; RPB * KS * T <= 512 floats), then every
-// (row, token) finalised in split order (router_finalize, as router_block
-// does).  Threads 0..511 (the consumer warps) call it; it synchronises them
+// (row, token) finalised in split order (router_finalize, as
+// router_block_rows does).  Threads 0..511 (the consumer warps) call it; it synchronises them
 // with named barrier 2 only, so the CTA's other warps go on meanwhile.
 // With `tagged` set, each logit (and the shared-gate logit, row E) is
 // published instead as one 64-bit word tagged[t * TS + row] = gen << 32 |

@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(256) k_combine(const CombineArgs A) {
   combine_rows(A.y + t0 * kh, A.yhalf, A.w + t0 * A.k, A.ysh ? A.ysh + size_t(t0) * A.H : nullptr,
                A.ysh2 ? A.ysh2 + size_t(t0) * A.H : nullptr, A.sg ? A.sg + t0 : nullptr,
                A.out + size_t(t0) * A.H, Tn, A.k, A.H, A.f16 != 0, blockIdx.x * kCombineRows,
-               kCombineRows, threadIdx.x, blockDim.x, A.round_bf16 != 0);
+               kCombineRows, threadIdx.x, blockDim.x, A.round_bf16 != 0,
+               A.idx ? A.idx + t0 * A.k : nullptr, A.offsets, A.one_plane_max);
 }
 
 // dst = a + b elementwise (the two k-half planes of a down projection)

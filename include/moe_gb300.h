@@ -61,7 +61,9 @@ typedef enum moe_status {
   MOE_ERR_WORKSPACE = 3,           /* workspace missing or too small */
   MOE_ERR_CUDA = 4,                /* a CUDA runtime call failed */
   MOE_ERR_TIMEOUT = 5,             /* a bounded device-side wait gave up */
-  MOE_ERR_MISALIGNED = 6           /* a pointer is not 16-byte aligned */
+  MOE_ERR_MISALIGNED = 6,          /* a pointer is not 16-byte aligned */
+  MOE_ERR_RANGE = 7                /* device status: an activation or h value of the prefill
+                                      form lay outside fp16's range (its operands are fp16) */
 } moe_status;
 
 /* Storage formats.  Quantised formats hold packed codes in little-endian
@@ -154,9 +156,11 @@ typedef struct moe_expert_bank {
 /* The decode form (grouped GEMV on exact integer codes) serves n_tokens <=
  * MOE_DECODE_MAX_TOKENS; above it the prefill form runs the expert GEMMs on
  * the tensor cores (tcgen05) over tiles of up to 128 tokens of one expert,
- * with the dequantised weights and h as bf16 hi + lo parts (fp16 parts for
- * fp16 activations) and fp32 accumulation -- the same values to within the
- * layer's tolerance, not the same bits as the decode form. */
+ * with fp16 operands -- the dequantised weights fma(s, q, b) rounded once,
+ * the activations converted to fp16 (exact within fp16's normal range), h
+ * stored as fp16 -- and fp32 accumulation: the same values to within the
+ * layer's tolerance, not the same bits as the decode form.  Experts with at
+ * most 40 assignments in the call run the decode form's units. */
 #define MOE_DECODE_MAX_TOKENS 32
 
 /* Human-readable name of a status; never NULL. */
@@ -188,7 +192,10 @@ moe_status moe_workspace_set_wait_limit(void* ws, size_t ws_bytes, unsigned limi
                                         cudaStream_t stream);
 
 /* Read and clear the device status word of a workspace (synchronises the
- * stream).  *device_status receives MOE_OK or MOE_ERR_TIMEOUT. */
+ * stream).  *device_status receives MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_RANGE
+ * (the prefill form met an activation or h value beyond fp16's range; its
+ * outputs are then not valid -- the decode form, MOE_FLAG_FORCE_DECODE, has
+ * no such limit). */
 moe_status moe_get_device_status(void* ws, size_t ws_bytes, int* device_status,
                                  cudaStream_t stream);
 
