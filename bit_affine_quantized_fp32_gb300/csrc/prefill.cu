@@ -4,20 +4,28 @@
 // dequantised once per tile of kPfTile rows and fed to the tensor cores:
 // D[128 weight rows x N tokens] += A[128 x 64] * B[N x 64]^T per 64-column
 // group, fp16 operands in shared memory, fp32 accumulators in tensor memory.
-// One persistent CTA per SM, 15 warps:
-//   warps 0-3   epilogue: tensor memory -> registers (thread = weight row),
-//               SwiGLU -> fp16 h (mode 0) or fp32 y rows (mode 1);
+// One persistent CTA per SM, 18 warps:
+//   warps 0-3   epilogue: tensor memory -> registers, 32 columns a load
+//               (thread = accumulator lane = weight row), SwiGLU -> fp16 h
+//               (mode 0) or fp32 y rows (mode 1);
 //   warps 4-11  dequantisation: one weight item (128 rows x CK columns, the
 //               kernel-tiled layout) per raw stage, one 64-column group at a
 //               time into an A stage: w = fp16(s * q + b), one fused
 //               multiply-add of the fp16 scale, the exact code and the fp16
 //               bias (W4A16: s * u - 8 s), rounded once;
 //   warp 12     TMA bulk copies of the raw weight items (2 stages);
-//   warp 13     the operand rows of each group into a B stage (cp.async, 16 B
-//               pieces placed in the tensor core's K-major layout): fp16 x
-//               rows (mode 0) or fp16 h rows (mode 1);
-//   warp 14     allocates tensor memory and issues the MMAs (one thread);
-//               tcgen05.commit frees A/B stages and hands accumulators over.
+//   warp 13     allocates tensor memory and issues the MMAs (one thread);
+//               tcgen05.commit frees A/B stages and hands accumulators over;
+//   warps 14-17 the operand rows of each group into a B stage, 32 rows a
+//               warp (cp.async of 16-byte pieces; one instruction copies 4
+//               whole 128-byte rows): fp16 x rows (mode 0) or fp16 h rows
+//               (mode 1).
+// A and B stages use the K-major 128-byte-swizzled layout (umma.cuh), so the
+// dequantisation stores and the row copies write one shared-memory wavefront
+// per quarter warp.  In mode 0 the dequantisation places M-tile w of a w13
+// block (gate tiles 0-3, the matching up tiles 4-7) at accumulator lanes
+// 32 (w % 4) + 16 (w / 4) ..: each epilogue warp holds 16 gate rows and their
+// 16 up rows, and pairs them with one shuffle.
 // One MMA per 16 columns.  The activations enter as fp16: bf16 x is converted
 // once per call (exact in fp16's normal range; a value beyond it sets
 // MOE_ERR_RANGE), and h is stored as fp16 (likewise checked).  Two
@@ -42,6 +50,9 @@ constexpr int kPfA = 128 * 64 * 2;           // 128 rows x 64 columns, 16-bit
 constexpr int kPfB = kPfTile * 64 * 2;
 constexpr int kPfKBlk = 64;                  // columns per MMA group (4 x K16)
 constexpr int kPfStagesMax = 4;
+constexpr int kPfRawWarp = 12, kPfMmaWarp = 13, kPfBWarp0 = 14, kPfBWarps = 4;
+static_assert((kPfBWarp0 + kPfBWarps) * 32 == kPfThreads, "warp roles cover the block");
+static_assert(kPfBWarps * 32 == kPfTile, "one B warp per 32 tile rows");
 // A/B stages: [A][B], both fp16
 __host__ __device__ constexpr int pf_stages(int mode) { return mode == 0 ? 4 : 4; }
 __host__ __device__ constexpr int pf_stage_bytes(int mode) { return (void)mode, kPfA + kPfB; }
@@ -56,7 +67,6 @@ struct PfSmem {
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem;
   WaitCtl wc;
-  float xch[64][9];  // up rows handed to the gate rows in the SwiGLU epilogue
 };
 
 struct PfUnit {
@@ -101,10 +111,18 @@ __device__ __forceinline__ uint4 dequant_word16(uint32_t w, __half2 s2, __half2 
   return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
+// Accumulator lane (A row) of row i of M-tile w: in mode 0 the gate tile w
+// (w < 4) takes lanes 32 w + i and its up tile w + 4 lanes 32 w + 16 + i;
+// in mode 1 tile w takes lanes 16 w + i.
+template <int MODE>
+__device__ __forceinline__ int pf_arow(int w, int i) {
+  return MODE == 0 ? 32 * (w & 3) + 16 * (w >> 2) + i : 16 * w + i;
+}
+
 // Group G of the raw item into an A stage: thread (tile w, lane l) converts
-// its four words -- rows 16w + g and 16w + g + 8, columns 16t .. 16t + 15 of
-// the group -- into the K-major layout (one 16-byte piece per word).
-template <int FMT>
+// its four words -- tile rows g and g + 8, columns 16t .. 16t + 15 of the
+// group -- into the swizzled K-major layout (one 16-byte piece per word).
+template <int FMT, int MODE>
 __device__ __forceinline__ void dequant_group(const TileGeo& g, const uint8_t* raw, int G,
                                               uint8_t* A, int w, int l) {
   const int NG = g.ng;
@@ -139,11 +157,11 @@ __device__ __forceinline__ void dequant_group(const TileGeo& g, const uint8_t* r
   }
   const __half2 s02 = __halves2half2(s0, s0), s12 = __halves2half2(s1, s1);
   const __half2 b02 = __halves2half2(b0, b0), b12 = __halves2half2(b1, b1);
-  const int r0 = 16 * w + gq, r1 = r0 + 8;
-  *reinterpret_cast<uint4*>(A + umma_off(r0, 16 * t, kPfKBlk)) = dequant_word16(W0, s02, b02);
-  *reinterpret_cast<uint4*>(A + umma_off(r0, 16 * t + 8, kPfKBlk)) = dequant_word16(W1, s02, b02);
-  *reinterpret_cast<uint4*>(A + umma_off(r1, 16 * t, kPfKBlk)) = dequant_word16(W2, s12, b12);
-  *reinterpret_cast<uint4*>(A + umma_off(r1, 16 * t + 8, kPfKBlk)) = dequant_word16(W3, s12, b12);
+  const int r0 = pf_arow<MODE>(w, gq), r1 = r0 + 8;
+  *reinterpret_cast<uint4*>(A + umma_off_sw128(r0, 16 * t)) = dequant_word16(W0, s02, b02);
+  *reinterpret_cast<uint4*>(A + umma_off_sw128(r0, 16 * t + 8)) = dequant_word16(W1, s02, b02);
+  *reinterpret_cast<uint4*>(A + umma_off_sw128(r1, 16 * t)) = dequant_word16(W2, s12, b12);
+  *reinterpret_cast<uint4*>(A + umma_off_sw128(r1, 16 * t + 8)) = dequant_word16(W3, s12, b12);
 }
 
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
@@ -151,18 +169,18 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
-
 template <int FMT, int MODE>
 __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant__ PrefillJob J) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem_dyn[];
   __shared__ PfSmem S;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const TileGeo& g = J.g;
   constexpr int NS = pf_stages(MODE), SB = pf_stage_bytes(MODE);
   const int RB = raw_stage_bytes(g);
+  // the swizzled stages need 1024-byte alignment (the launch adds the slack)
+  uint8_t* smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
   uint8_t* raw = smem;
-  uint8_t* stages = smem + kPfRaw * RB;  // stage s: [A hi][A lo][B (hi)][B lo]
+  uint8_t* stages = smem + kPfRaw * RB;  // stage s: [A][B], RB a multiple of 1024
   if (tid == 0) {
     for (int i = 0; i < kPfRaw; ++i) {
       mbar_init(&S.raw_full[i], 1);
@@ -170,7 +188,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
     }
     for (int i = 0; i < NS; ++i) {
       mbar_init(&S.a_full[i], 8);
-      mbar_init(&S.b_full[i], 32);
+      mbar_init(&S.b_full[i], 32 * kPfBWarps);
       mbar_init(&S.ab_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -179,7 +197,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
     }
     wait_ctl_init(S.wc, J.status);
   }
-  if (warp == 14) tmem_alloc(&S.tmem, 2 * kPfTile);
+  if (warp == kPfMmaWarp) tmem_alloc(&S.tmem, 2 * kPfTile);
   fence_proxy_async();
   tmem_fence_before();
   __syncthreads();
@@ -190,7 +208,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
   const int NG = g.ng, nch = g.nch, nks = nch * NG;
   int* status = J.status;
 
-  if (warp == 12) {
+  if (warp == kPfRawWarp) {
     // ---- raw weight items
     int ri = 0;
     for (int u = blockIdx.x; u < nunits; u += G) {
@@ -199,7 +217,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         const int rs = ri % kPfRaw;
         if (lane == 0) {
           if (ri >= kPfRaw) {
-            mbar_wait_bounded(&S.raw_empty[rs], ((ri / kPfRaw) - 1) & 1, &S.wc, status, true);
+            mbar_wait_bounded(&S.raw_empty[rs], ((ri / kPfRaw) - 1) & 1, &S.wc, status);
             // the stage's previous copy has landed (immediate unless a timeout
             // let the consumers skip their wait): one copy per barrier phase
             mbar_drain(&S.raw_full[rs], ((ri / kPfRaw) - 1) & 1);
@@ -217,69 +235,62 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
     if (lane == 0)
       for (int i = max(0, ri - kPfRaw); i < ri; ++i)
         mbar_drain(&S.raw_full[i % kPfRaw], (i / kPfRaw) & 1);
-  } else if (warp == 13) {
-    // ---- operand rows, one 64-column group per stage; lane l copies rows
-    // l, l + 32, ... of the tile, their addresses resolved once per unit
-    constexpr int RPL = kPfTile / 32;
+  } else if (warp >= kPfBWarp0) {
+    // ---- operand rows, one 64-column group per stage.  B warp b owns tile
+    // rows 32 b .. 32 b + 31; instruction i copies rows 32 b + 4 i .. + 3,
+    // lane l piece l % 8 of row 32 b + 4 i + l / 8; the row addresses are
+    // resolved once per unit.
+    const int bw = warp - kPfBWarp0;
+    const int pc = lane & 7;
     int ks = 0;
     for (int u = blockIdx.x; u < nunits; u += G) {
       const PfUnit U = pf_unit(J, u);
-      size_t rofs[RPL];
+      const uint16_t* src[8];
 #pragma unroll
-      for (int i = 0; i < RPL; ++i) {
-        const int n = lane + 32 * i;
+      for (int i = 0; i < 8; ++i) {
+        const int n = 32 * bw + 4 * i + (lane >> 3);
         const int row = n < U.cnt ? ((MODE == 0 && J.gather) ? __ldg(J.perm + U.off + n) / J.k
                                                              : U.off + n)
                                   : 0;
-        rofs[i] = (size_t)row * J.ldB;
+        src[i] = J.B + (size_t)row * J.ldB + 8 * pc;
       }
       for (int q = 0; q < nks; ++q, ++ks) {
         const int s = ks % NS;
-        if (ks >= NS)
-          mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status, true);
+        if (ks >= NS) mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status);
         const int k0 = q * kPfKBlk;
         uint8_t* B = stages + s * SB + kPfA;
 #pragma unroll
-        for (int i = 0; i < RPL; ++i) {
-          const int n = lane + 32 * i;
-          if (n < U.cnt) {
-            const uint16_t* src = J.B + rofs[i] + k0;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              cp_async16(B + umma_off(n, ch * 8, kPfKBlk), src + ch * 8);
-          }
+        for (int i = 0; i < 8; ++i) {
+          const int n = 32 * bw + 4 * i + (lane >> 3);
+          if (n < U.cnt) cp_async16(B + umma_off_sw128(n, 8 * pc), src[i] + k0);
         }
         cp_async_arrive_noinc(&S.b_full[s]);
       }
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
-  } else if (warp == 14) {
+  } else if (warp == kPfMmaWarp) {
     // ---- MMA issue (one thread)
     if (lane == 0) {
       int ks = 0, ui = 0;
       for (int u = blockIdx.x; u < nunits; u += G, ++ui) {
         const PfUnit U = pf_unit(J, u);
         const int a = ui & 1;
-        if (ui >= 2) mbar_wait_bounded(&S.acc_empty[a], ((ui >> 1) - 1) & 1, &S.wc, status, true);
+        if (ui >= 2) mbar_wait_bounded(&S.acc_empty[a], ((ui >> 1) - 1) & 1, &S.wc, status);
         tmem_fence_after();
         const int N = max(16, (U.cnt + 15) & ~15);
-        // fp16 A and B: the format fields of the bf16 descriptor cleared
-        const uint32_t idesc = umma_idesc_bf16(128, N) & ~((7u << 7) | (7u << 10));
+        const uint32_t idesc = umma_idesc_f16(128, N);
         const uint32_t d = tbase + uint32_t(a * kPfTile);
-        constexpr uint32_t kSbo = (kPfKBlk / 8) * 128;
         for (int q = 0; q < nks; ++q, ++ks) {
           const int s = ks % NS;
-          mbar_wait_bounded(&S.a_full[s], (ks / NS) & 1, &S.wc, status, true);
-          mbar_wait_bounded(&S.b_full[s], (ks / NS) & 1, &S.wc, status, true);
+          mbar_wait_bounded(&S.a_full[s], (ks / NS) & 1, &S.wc, status);
+          mbar_wait_bounded(&S.b_full[s], (ks / NS) & 1, &S.wc, status);
           fence_proxy_async();
           tmem_fence_after();
           const uint32_t aa = smem_u32(stages + s * SB), ba = aa + kPfA;
 #pragma unroll
-          for (int kk = 0; kk < kPfKBlk / 16; ++kk) {
-            const uint32_t o = kk * 256;
-            umma_bf16(d, umma_desc(aa + o, 128, kSbo), umma_desc(ba + o, 128, kSbo), idesc,
-                      q > 0 || kk > 0);
-          }
+          for (int kk = 0; kk < kPfKBlk / 16; ++kk)
+            umma_f16(d, umma_desc_sw128(aa + 32 * kk), umma_desc_sw128(ba + 32 * kk), idesc,
+                     q > 0 || kk > 0);
           umma_commit(&S.ab_empty[s]);
         }
         umma_commit(&S.acc_full[a]);
@@ -298,12 +309,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       (void)U;
       for (int c = 0; c < nch; ++c, ++ri) {
         const int rs = ri % kPfRaw;
-        mbar_wait_bounded(&S.raw_full[rs], (ri / kPfRaw) & 1, &S.wc, status, true);
+        mbar_wait_bounded(&S.raw_full[rs], (ri / kPfRaw) & 1, &S.wc, status);
         for (int Gi = 0; Gi < NG; ++Gi, ++ks) {
           const int s = ks % NS;
-          if (ks >= NS)
-          mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status, true);
-          dequant_group<FMT>(g, raw + rs * RB, Gi, stages + s * SB, w, lane);
+          if (ks >= NS) mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status);
+          dequant_group<FMT, MODE>(g, raw + rs * RB, Gi, stages + s * SB, w, lane);
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.a_full[s]);
@@ -313,48 +323,48 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       }
     }
   } else {
-    // ---- epilogue: thread r = tensor-memory lane r = weight row r of the block
-    const int r = tid;
+    // ---- epilogue: thread (warp q, lane l) = accumulator lane 32 q + l
     int ui = 0;
     for (int u = blockIdx.x; u < nunits; u += G, ++ui) {
       const PfUnit U = pf_unit(J, u);
       const int a = ui & 1;
-      mbar_wait_bounded(&S.acc_full[a], (ui >> 1) & 1, &S.wc, status, true);
+      mbar_wait_bounded(&S.acc_full[a], (ui >> 1) & 1, &S.wc, status);
       tmem_fence_after();
       const uint32_t tl = tbase + (uint32_t(32 * warp) << 16) + uint32_t(a * kPfTile);
-      for (int c8 = 0; c8 < U.cnt; c8 += 8) {
-        float v[8];
-        tmem_ld8(tl + uint32_t(c8), v);
+      for (int c0 = 0; c0 < U.cnt; c0 += 32) {
         if (MODE == 0) {
-          // rows 0-63 are gate rows 64 m + r, rows 64-127 the matching up rows
-          if (r >= 64) {
+          // lanes 0-15: gate rows 64 m + 16 q + l, lanes 16-31 the matching
+          // up rows; lane l < 16 finishes tokens c0 .. c0 + 15 of its
+          // column, lane l + 16 tokens c0 + 16 .. c0 + 31
+          float v[32];
+          tmem_ld32(tl + uint32_t(c0), v);
+          const bool hi = lane >= 16;
+          const size_t col = 64 * size_t(U.m) + 16 * warp + (lane & 15);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) S.xch[r - 64][j] = v[j];
-          }
-          epi_bar();
-          if (r < 64) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int n = c8 + j;
-              if (n < U.cnt) {
-                const float ga = v[j], up = S.xch[r][j];
-                const float hv = ga / (1.f + expf(-ga)) * up;
-                const size_t at = (size_t)(U.off + n) * J.ldh + 64 * U.m + r;
-                J.h[at] = __half_as_ushort(__float2half_rn(hv));
-                if (!(fabsf(hv) <= 65504.f)) atomicExch(status, int(MOE_ERR_RANGE));
-              }
-            }
-          }
-          epi_bar();
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int n = c8 + j;
+          for (int jj = 0; jj < 16; ++jj) {
+            const float recv = __shfl_xor_sync(0xffffffffu, hi ? v[jj] : v[16 + jj], 16);
+            const float ga = hi ? recv : v[jj];
+            const float up = hi ? v[16 + jj] : recv;
+            const int n = c0 + jj + (hi ? 16 : 0);
             if (n < U.cnt) {
-              const int row = J.scatter ? __ldg(J.perm + U.off + n) : U.off + n;
-              const size_t at = (size_t)row * J.ldy + 128 * U.m + r;
-              J.y[at] = v[j];
+              const float hv = ga / (1.f + expf(-ga)) * up;
+              J.h[(size_t)(U.off + n) * J.ldh + col] = __half_as_ushort(__float2half_rn(hv));
+              if (!(fabsf(hv) <= 65504.f)) atomicExch(status, int(MOE_ERR_RANGE));
             }
+          }
+        } else {
+          // output rows of tokens c0 .. c0 + 31, one per lane, then one
+          // 128-byte row piece a token
+          const int nl = c0 + lane;
+          const int orow =
+              nl < U.cnt ? (J.scatter ? __ldg(J.perm + U.off + nl) : U.off + nl) : 0;
+          float v[32];
+          tmem_ld32(tl + uint32_t(c0), v);
+          const size_t col = 128 * size_t(U.m) + 32 * warp + lane;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int row = __shfl_sync(0xffffffffu, orow, j);
+            if (c0 + j < U.cnt) J.y[(size_t)row * J.ldy + col] = v[j];
           }
         }
       }
@@ -366,7 +376,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
-  if (warp == 14) tmem_dealloc(tbase, 2 * kPfTile);
+  if (warp == kPfMmaWarp) tmem_dealloc(tbase, 2 * kPfTile);
 }
 
 template <int FMT, int MODE>
@@ -409,7 +419,8 @@ __global__ void k_act_f16(const uint16_t* __restrict__ x, long n, uint16_t* __re
 
 int prefill_smem(const TileGeo& g, int mode) {
   if (g.K % kPfKBlk != 0) return 0;
-  const int bytes = kPfRaw * raw_stage_bytes(g) + pf_stages(mode) * pf_stage_bytes(mode);
+  // + 1024: slack to align the stages to the swizzle atom
+  const int bytes = kPfRaw * raw_stage_bytes(g) + pf_stages(mode) * pf_stage_bytes(mode) + 1024;
   return bytes + int(sizeof(PfSmem)) + 1024 <= kEngineSmemMax ? bytes : 0;
 }
 

@@ -6,7 +6,7 @@
 namespace moe {
 
 constexpr int kPfTile = 128;   // tokens per N tile (tensor-memory columns per accumulator)
-constexpr int kPfThreads = 480;
+constexpr int kPfThreads = 576;
 // Experts with at most this many assignments in a prefill call go to the
 // decode units instead (each tensor-core unit dequantises a whole weight
 // block whatever its rows; the decode units cost per 8 rows).

@@ -1,14 +1,17 @@
 // umma.cuh -- 5th-generation tensor core (tcgen05) helpers for sm_103a:
-// tensor-memory allocation, shared-memory matrix descriptors, the bf16 MMA
+// tensor-memory allocation, shared-memory matrix descriptors, the 16-bit MMA
 // with fp32 accumulation in tensor memory, its completion barrier and the
 // tensor-memory loads of the epilogue.  Inline PTX only.
 //
-// Operand tiles live in shared memory in the K-major layout without swizzle:
-// 8-row x 16-byte core matrices (8 rows x 8 bf16 along K), one core matrix
-// = 128 contiguous bytes, row r of it at byte 16 r.  A tile of R rows and
-// KT columns stores core matrix (row block i, k block j) at
-//   i * sbo + j * lbo        with lbo = 128 and sbo = (KT / 8) * 128,
-// i.e. the K blocks of one 8-row block are contiguous.
+// Operand tiles live in shared memory in the K-major layout with the 128-byte
+// swizzle: a tile of 64 16-bit columns stores row r as 128 contiguous bytes
+// at 128 r, its 16-byte piece c (columns 8c .. 8c + 7) at slot c ^ (r & 7);
+// eight rows make a 1024-byte swizzle atom, atoms 1024 bytes apart (the
+// stride byte offset).  The tile base is 1024-byte aligned, since the
+// swizzle acts on the address bits themselves; the K slice kk (16 columns)
+// of an MMA starts 32 kk bytes after the tile base.  Eight 16-byte stores
+// to the eight pieces of one row, or to pieces whose (c ^ (r & 7)) differ,
+// fall in eight distinct bank groups (one shared-memory wavefront).
 #pragma once
 
 #include <stdint.h>
@@ -17,35 +20,40 @@
 
 namespace moe {
 
-// Byte offset of element (r, k) of a K-major no-swizzle tile with KT columns.
-__host__ __device__ inline int umma_off(int r, int k, int KT) {
-  return (r >> 3) * (KT / 8) * 128 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+constexpr int kUmmaRowBytes = 128;    // 64 16-bit columns
+constexpr int kUmmaAtomBytes = 1024;  // 8 rows
+
+// Byte offset of 16-bit element (r, k) (k < 64) of a K-major 128-byte-swizzled
+// tile.
+__host__ __device__ inline int umma_off_sw128(int r, int k) {
+  return r * kUmmaRowBytes + ((((k >> 3) ^ (r & 7)) & 7) << 4) + (k & 7) * 2;
 }
 
-// Shared-memory matrix descriptor: start address, leading (K) and stride
-// (M/N) byte offsets, descriptor version 1, no swizzle.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor of a K-major 128-byte-swizzled tile (or of
+// its K slice at saddr = base + 32 kk): start address, leading byte offset
+// 16 (unused by this layout), stride byte offset 1024, descriptor version 1,
+// base offset 0, layout type 2 (128-byte swizzle) in bits 61..63.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
   uint64_t d = 0;
   d |= uint64_t((saddr & 0x3FFFFu) >> 4);
-  d |= uint64_t((lbo & 0x3FFFFu) >> 4) << 16;
-  d |= uint64_t((sbo & 0x3FFFFu) >> 4) << 32;
-  d |= uint64_t(1) << 46;  // version
-  return d;                // base offset 0, relative LBO mode, no swizzle
+  d |= uint64_t(16 >> 4) << 16;
+  d |= uint64_t(kUmmaAtomBytes >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and an
-// fp32 accumulator, shape M x N.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+// Instruction descriptor of kind::f16 with fp16 A and B (both K-major, the
+// A and B format fields 0) and an fp32 accumulator, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
   return (1u << 4)                       // D format: f32
-         | (1u << 7)                     // A format: bf16
-         | (1u << 10)                    // B format: bf16
          | (uint32_t(N >> 3) << 17)      // N / 8
          | (uint32_t(M >> 4) << 24);     // M / 16
 }
 
 // D[tmem] (+)= A * B^T over K = 16, issued by one thread.
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, bool accumulate) {
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, bool accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
@@ -98,6 +106,25 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane (the lane
+// rule of tmem_ld8).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 }  // namespace moe
