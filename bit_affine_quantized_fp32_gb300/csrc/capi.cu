@@ -333,6 +333,15 @@ bool use_prefill(const moe_expert_bank* b, int T, int flags) {
          prefill_smem(geo13(b).t, 0) > 0 && prefill_smem(geo2(b).t, 1) > 0;
 }
 
+// The shared expert joins the routed experts' prefill launches when both
+// take the prefill form with one tiled geometry (same format; the shapes
+// are equal by the layer's checks).
+bool prefill_pair(const moe_expert_bank* experts, const moe_expert_bank* shared, int T,
+                  int flags) {
+  return use_prefill(experts, T, flags) && use_prefill(shared, T, flags) &&
+         shared->fmt == experts->fmt;
+}
+
 // The prefill form's fp16 activation rows: x itself (fp16 activations) or
 // its fp16 copy in the workspace (bf16 activations, converted here).
 moe_status prefill_act(const void* x, bool f16, int T, int H, void* ws, const WsLayout& L,
@@ -401,6 +410,143 @@ moe_status run_expert_mlp(const moe_expert_bank* bank, int expert, const void* x
   if (y_out)
     MOE_CUDA(launch_add_planes(ysh, ysh + half, y_out, long(half), stream), "plane sum");
   return MOE_OK;
+}
+
+// The routed experts (validated) and, when `shared` is given, the shared
+// expert folded into the same prefill launches (its output into L.ysh, which
+// is then the combine's shared row): see prefill_pair.
+moe_status experts_run(const moe_expert_bank* experts, const moe_expert_bank* shared,
+                       const void* x, bool f16, int T, int top_k, const int32_t* topk_idx,
+                       const float* topk_w, const int32_t* bucket_offsets,
+                       const int32_t* bucket_perm, const float* y_shared,
+                       const float* shared_gate_w, void* out, int flags, void* ws,
+                       const WsLayout& L, cudaStream_t stream) {
+  moe_status s;
+  const int E = experts->n_experts, H = experts->hidden, I = experts->inter;
+  const bool rb = (flags & MOE_FLAG_ROUND_BF16) != 0;
+  if (use_prefill(experts, T, flags)) {
+    // Experts with more than kPfLight assignments: tiles of up to kPfTile
+    // bucket positions through the tensor-core GEMMs (second y plane set to
+    // 0); the others: sub-slots of 8 through the decode units.  One combine
+    // over the two y planes.
+    float* y = reinterpret_cast<float*>(wsp(ws, L.y));
+    const size_t yhalf = size_t(T) * top_k * H;
+    int* nt = reinterpret_cast<int*>(wsp(ws, L.pt_n));
+    int* te = reinterpret_cast<int*>(wsp(ws, L.pt_e));
+    int* to = reinterpret_cast<int*>(wsp(ws, L.pt_off));
+    int* tc = reinterpret_cast<int*>(wsp(ws, L.pt_cnt));
+    MOE_CUDA(launch_subslots(bucket_offsets, E, nt, te, to, tc, stream, kPfTile, kPfLight),
+             "tile kernel");
+    int* nss = reinterpret_cast<int*>(wsp(ws, L.nss));
+    int* se = reinterpret_cast<int*>(wsp(ws, L.ss_e));
+    int* so = reinterpret_cast<int*>(wsp(ws, L.ss_off));
+    int* sc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
+    MOE_CUDA(launch_subslots(bucket_offsets, E, nss, se, so, sc, stream, kMaxTok, 0, kPfLight),
+             "sub-slot kernel");
+    const MatGeo g13 = geo13(experts), g2 = geo2(experts);
+    const uint16_t* xa = nullptr;
+    if ((s = prefill_act(x, f16, T, H, ws, L, &xa, stream))) return s;
+    PrefillJob J{};
+    J.g = g13.t;
+    J.base = g13.base;
+    J.n_tiles = nt;
+    J.te = te;
+    J.toff = to;
+    J.tcnt = tc;
+    J.B = xa;
+    J.ldB = H;
+    J.gather = 1;
+    J.perm = bucket_perm;
+    J.k = top_k;
+    J.h = reinterpret_cast<uint16_t*>(wsp(ws, L.hh));  // fp16 h rows of the tiled experts
+    J.ldh = h_pitch(I);
+    J.status = static_cast<int*>(ws);
+    if (shared) {
+      J.sh_base = geo13(shared).base;
+      J.sh_T = T;
+      J.sh_B = xa;
+      J.sh_h = reinterpret_cast<uint16_t*>(wsp(ws, L.sh_hh));
+      y_shared = reinterpret_cast<float*>(wsp(ws, L.ysh));
+    }
+    MOE_CUDA(launch_prefill(J, 0, sm_count(), stream), "prefill gate/up kernel");
+    PrefillJob D = J;
+    D.g = g2.t;
+    D.base = g2.base;
+    D.B = J.h;
+    D.ldB = h_pitch(I);
+    D.gather = 0;
+    D.y = y;
+    D.ldy = H;
+    D.scatter = 1;
+    if (shared) {
+      D.sh_base = geo2(shared).base;
+      D.sh_B = J.sh_h;
+      D.sh_h = nullptr;
+      D.sh_y = const_cast<float*>(y_shared);
+    }
+    MOE_CUDA(launch_prefill(D, 1, sm_count(), stream), "prefill down kernel");
+    float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
+    MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, f16, g13.t, xsum, stream),
+             "activation sums");
+    const SubSlots ss{nss, se, so, sc, 0, 0};
+    s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
+                 bucket_perm, top_k, reinterpret_cast<uint16_t*>(wsp(ws, L.hh)),
+                 reinterpret_cast<uint16_t*>(wsp(ws, L.hl)),
+                 reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr, y, yhalf, kRowsScatter,
+                 static_cast<int*>(ws), stream);
+    if (s) return s;
+    CombineArgs C{};
+    C.y = y;
+    C.yhalf = yhalf;
+    C.w = topk_w;
+    C.ysh = y_shared;
+    C.ysh2 = nullptr;
+    C.sg = shared_gate_w;
+    C.out = static_cast<uint16_t*>(out);
+    C.T = T;
+    C.k = top_k;
+    C.H = H;
+    C.f16 = f16;
+    C.round_bf16 = rb;
+    C.idx = topk_idx;  // the tiled experts' y sits in plane 0 alone
+    C.offsets = bucket_offsets;
+    C.one_plane_max = kPfLight;
+    MOE_CUDA(launch_combine(C, stream), "combine kernel");
+    return ok();
+  }
+  float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
+  MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, f16, geo13(experts).t, xsum,
+                       stream),
+           "activation sums");
+  int* nss = reinterpret_cast<int*>(wsp(ws, L.nss));
+  int* se = reinterpret_cast<int*>(wsp(ws, L.ss_e));
+  int* so = reinterpret_cast<int*>(wsp(ws, L.ss_off));
+  int* sc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
+  MOE_CUDA(launch_subslots(bucket_offsets, E, nss, se, so, sc, stream), "sub-slot kernel");
+  const SubSlots ss{nss, se, so, sc, 0, 0};
+  float* y = reinterpret_cast<float*>(wsp(ws, L.y));
+  const size_t yhalf = size_t(T) * top_k * H;
+  s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
+               bucket_perm, top_k, reinterpret_cast<uint16_t*>(wsp(ws, L.hh)),
+               reinterpret_cast<uint16_t*>(wsp(ws, L.hl)),
+               reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr, y, yhalf, kRowsScatter,
+               static_cast<int*>(ws), stream);
+  if (s) return s;
+  CombineArgs C{};
+  C.y = y;
+  C.yhalf = yhalf;
+  C.w = topk_w;
+  C.ysh = y_shared;
+  C.ysh2 = nullptr;
+  C.sg = shared_gate_w;
+  C.out = static_cast<uint16_t*>(out);
+  C.T = T;
+  C.k = top_k;
+  C.H = H;
+  C.f16 = f16;
+  C.round_bf16 = rb;
+  MOE_CUDA(launch_combine(C, stream), "combine kernel");
+  return ok();
 }
 
 }  // namespace
@@ -589,7 +735,6 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
     return fail(MOE_ERR_INVALID_ARG, "top_k=%d not in 1..min(8, n_experts)", top_k);
   if (flags & ~(MOE_FLAG_FORCE_DECODE | MOE_FLAG_ROUND_BF16))
     return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
-  const bool rb = (flags & MOE_FLAG_ROUND_BF16) != 0;
   if (T == 0) return ok();
   if (!x || !topk_idx || !topk_w || !bucket_offsets || !bucket_perm || !out)
     return fail(MOE_ERR_INVALID_ARG, "x, routing and out pointers must not be NULL");
@@ -597,117 +742,9 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
     return fail(MOE_ERR_MISALIGNED, "x/out/y_shared must be 16-byte aligned");
   const WsLayout L = ws_layout(T, E, top_k, H, I);
   if ((s = check_ws(ws, ws_bytes, L.total))) return s;
-  const bool f16 = act == MOE_FMT_F16;
-  if (use_prefill(experts, T, flags)) {
-    // Experts with more than kPfLight assignments: tiles of up to kPfTile
-    // bucket positions through the tensor-core GEMMs (second y plane set to
-    // 0); the others: sub-slots of 8 through the decode units.  One combine
-    // over the two y planes.
-    float* y = reinterpret_cast<float*>(wsp(ws, L.y));
-    const size_t yhalf = size_t(T) * top_k * H;
-    int* nt = reinterpret_cast<int*>(wsp(ws, L.pt_n));
-    int* te = reinterpret_cast<int*>(wsp(ws, L.pt_e));
-    int* to = reinterpret_cast<int*>(wsp(ws, L.pt_off));
-    int* tc = reinterpret_cast<int*>(wsp(ws, L.pt_cnt));
-    MOE_CUDA(launch_subslots(bucket_offsets, E, nt, te, to, tc, stream, kPfTile, kPfLight),
-             "tile kernel");
-    int* nss = reinterpret_cast<int*>(wsp(ws, L.nss));
-    int* se = reinterpret_cast<int*>(wsp(ws, L.ss_e));
-    int* so = reinterpret_cast<int*>(wsp(ws, L.ss_off));
-    int* sc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
-    MOE_CUDA(launch_subslots(bucket_offsets, E, nss, se, so, sc, stream, kMaxTok, 0, kPfLight),
-             "sub-slot kernel");
-    const MatGeo g13 = geo13(experts), g2 = geo2(experts);
-    const uint16_t* xa = nullptr;
-    if ((s = prefill_act(x, f16, T, H, ws, L, &xa, stream))) return s;
-    PrefillJob J{};
-    J.g = g13.t;
-    J.base = g13.base;
-    J.n_tiles = nt;
-    J.te = te;
-    J.toff = to;
-    J.tcnt = tc;
-    J.B = xa;
-    J.ldB = H;
-    J.gather = 1;
-    J.perm = bucket_perm;
-    J.k = top_k;
-    J.h = reinterpret_cast<uint16_t*>(wsp(ws, L.hh));  // fp16 h rows of the tiled experts
-    J.ldh = h_pitch(I);
-    J.status = static_cast<int*>(ws);
-    MOE_CUDA(launch_prefill(J, 0, sm_count(), stream), "prefill gate/up kernel");
-    PrefillJob D = J;
-    D.g = g2.t;
-    D.base = g2.base;
-    D.B = J.h;
-    D.ldB = h_pitch(I);
-    D.gather = 0;
-    D.y = y;
-    D.ldy = H;
-    D.scatter = 1;
-    MOE_CUDA(launch_prefill(D, 1, sm_count(), stream), "prefill down kernel");
-    float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
-    MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, f16, g13.t, xsum, stream),
-             "activation sums");
-    const SubSlots ss{nss, se, so, sc, 0, 0};
-    s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
-                 bucket_perm, top_k, reinterpret_cast<uint16_t*>(wsp(ws, L.hh)),
-                 reinterpret_cast<uint16_t*>(wsp(ws, L.hl)),
-                 reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr, y, yhalf, kRowsScatter,
-                 static_cast<int*>(ws), stream);
-    if (s) return s;
-    CombineArgs C{};
-    C.y = y;
-    C.yhalf = yhalf;
-    C.w = topk_w;
-    C.ysh = y_shared;
-    C.ysh2 = nullptr;
-    C.sg = shared_gate_w;
-    C.out = static_cast<uint16_t*>(out);
-    C.T = T;
-    C.k = top_k;
-    C.H = H;
-    C.f16 = f16;
-    C.round_bf16 = rb;
-    C.idx = topk_idx;  // the tiled experts' y sits in plane 0 alone
-    C.offsets = bucket_offsets;
-    C.one_plane_max = kPfLight;
-    MOE_CUDA(launch_combine(C, stream), "combine kernel");
-    return ok();
-  }
-  float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
-  MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, f16, geo13(experts).t, xsum,
-                       stream),
-           "activation sums");
-  int* nss = reinterpret_cast<int*>(wsp(ws, L.nss));
-  int* se = reinterpret_cast<int*>(wsp(ws, L.ss_e));
-  int* so = reinterpret_cast<int*>(wsp(ws, L.ss_off));
-  int* sc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
-  MOE_CUDA(launch_subslots(bucket_offsets, E, nss, se, so, sc, stream), "sub-slot kernel");
-  const SubSlots ss{nss, se, so, sc, 0, 0};
-  float* y = reinterpret_cast<float*>(wsp(ws, L.y));
-  const size_t yhalf = size_t(T) * top_k * H;
-  s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
-               bucket_perm, top_k, reinterpret_cast<uint16_t*>(wsp(ws, L.hh)),
-               reinterpret_cast<uint16_t*>(wsp(ws, L.hl)),
-               reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr, y, yhalf, kRowsScatter,
-               static_cast<int*>(ws), stream);
-  if (s) return s;
-  CombineArgs C{};
-  C.y = y;
-  C.yhalf = yhalf;
-  C.w = topk_w;
-  C.ysh = y_shared;
-  C.ysh2 = nullptr;
-  C.sg = shared_gate_w;
-  C.out = static_cast<uint16_t*>(out);
-  C.T = T;
-  C.k = top_k;
-  C.H = H;
-  C.f16 = f16;
-  C.round_bf16 = rb;
-  MOE_CUDA(launch_combine(C, stream), "combine kernel");
-  return ok();
+  return experts_run(experts, nullptr, x, act == MOE_FMT_F16, T, top_k, topk_idx, topk_w,
+                     bucket_offsets, bucket_perm, y_shared, shared_gate_w, out, flags, ws, L,
+                     stream);
 }
 
 moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
@@ -815,6 +852,17 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
                 shared_gate ? sgw : nullptr, offs, perm, flags & MOE_FLAG_ROUND_BF16, ws, ws_bytes,
                 stream);
   if (s) return s;
+  const int ef = flags & (MOE_FLAG_FORCE_DECODE | MOE_FLAG_ROUND_BF16);
+  if (shared && prefill_pair(experts, shared, T, ef)) {
+    // one pair of prefill launches for the routed and the shared expert
+    if ((s = check_act(act))) return s;
+    if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x/out is NULL");
+    if (!aligned16(x) || !aligned16(out))
+      return fail(MOE_ERR_MISALIGNED, "x/out must be 16-byte aligned");
+    s = experts_run(experts, shared, x, act == MOE_FMT_F16, T, top_k, idx, w, offs, perm,
+                    nullptr, shared_gate ? sgw : nullptr, out, ef, ws, L, stream);
+    return s ? s : ok();
+  }
   float* ysh = nullptr;
   if (shared) {
     ysh = reinterpret_cast<float*>(wsp(ws, L.ysh));
@@ -822,9 +870,7 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
     if (s) return s;
   }
   return moe_experts_forward(experts, x, act, T, top_k, idx, w, offs, perm, ysh,
-                             shared && shared_gate ? sgw : nullptr, out,
-                             flags & (MOE_FLAG_FORCE_DECODE | MOE_FLAG_ROUND_BF16), ws, ws_bytes,
-                             stream);
+                             shared && shared_gate ? sgw : nullptr, out, ef, ws, ws_bytes, stream);
 }
 
 #define MOE_PACK_PAIR(NAME, FMT, CT)                                                           \

@@ -3,35 +3,45 @@
 // For T > 32 tokens an expert sees up to hundreds of rows, so its weights are
 // dequantised once per tile of kPfTile rows and fed to the tensor cores:
 // D[128 weight rows x N tokens] += A[128 x 64] * B[N x 64]^T per 64-column
-// group, fp16 operands in shared memory, fp32 accumulators in tensor memory.
+// group, fp16 operands, fp32 accumulators in tensor memory.  A (the
+// dequantised weights) is written straight into tensor memory; B (the
+// activation rows) is staged in shared memory.
 // One persistent CTA per SM, 18 warps:
 //   warps 0-3   epilogue: tensor memory -> registers, 32 columns a load
 //               (thread = accumulator lane = weight row), SwiGLU -> fp16 h
-//               (mode 0) or fp32 y rows (mode 1);
+//               (mode 0; the fast exponential and division, a few ulp of
+//               fp32, far below the fp16 rounding of h) or fp32 y rows
+//               (mode 1);
 //   warps 4-11  dequantisation: one weight item (128 rows x CK columns, the
 //               kernel-tiled layout) per raw stage, one 64-column group at a
-//               time into an A stage: w = fp16(s * q + b), one fused
-//               multiply-add of the fp16 scale, the exact code and the fp16
-//               bias (W4A16: s * u - 8 s), rounded once;
-//   warp 12     TMA bulk copies of the raw weight items (2 stages);
+//               time into a tensor-memory A stage: w = fp16(s * q + b), one
+//               fused multiply-add of the fp16 scale, the exact code and the
+//               fp16 bias (W4A16: s * u - 8 s), rounded once;
+//   warp 12     TMA bulk copies of the raw weight items (3 stages);
 //   warp 13     allocates tensor memory and issues the MMAs (one thread);
 //               tcgen05.commit frees A/B stages and hands accumulators over;
 //   warps 14-17 the operand rows of each group into a B stage, 32 rows a
 //               warp (cp.async of 16-byte pieces; one instruction copies 4
 //               whole 128-byte rows): fp16 x rows (mode 0) or fp16 h rows
 //               (mode 1).
-// A and B stages use the K-major 128-byte-swizzled layout (umma.cuh), so the
-// dequantisation stores and the row copies write one shared-memory wavefront
-// per quarter warp.  In mode 0 the dequantisation places M-tile w of a w13
-// block (gate tiles 0-3, the matching up tiles 4-7) at accumulator lanes
-// 32 (w % 4) + 16 (w / 4) ..: each epilogue warp holds 16 gate rows and their
-// 16 up rows, and pairs them with one shuffle.
+// Dequantisation warp w takes M-tile w of the block and places it at
+// tensor-memory lanes 32 (w % 4) + 16 (w / 4) .. + 15, inside its own lane
+// quarter: in mode 0 (gate tiles 0-3, the matching up tiles 4-7) each
+// epilogue warp then holds 16 gate rows and their 16 up rows and pairs them
+// with one shuffle.  A lane's four code words (rows g, g + 8; 16 columns
+// each) are transposed within its quad so that the 16x256b tensor-memory
+// stores put every element at its own column (the packed layout keeps 16
+// consecutive columns per lane; the store shape wants 4 runs of 4).
+// B stages use the K-major 128-byte-swizzled layout (umma.cuh): the row
+// copies write one shared-memory wavefront per quarter warp.
 // One MMA per 16 columns.  The activations enter as fp16: bf16 x is converted
 // once per call (exact in fp16's normal range; a value beyond it sets
 // MOE_ERR_RANGE), and h is stored as fp16 (likewise checked).  Two
 // accumulators of kPfTile columns let the epilogue of one unit overlap the
 // MMAs of the next.  Every wait is bounded (the workspace's limit, then the
-// status word gets MOE_ERR_TIMEOUT and the remaining waits return at once).
+// status word gets MOE_ERR_TIMEOUT and the remaining waits return at once);
+// the dequantisation and MMA roles poll, the long waits of the copy and
+// epilogue roles let the hardware suspend the warp.
 //
 // Sources: "qwen3_5_moe on native CUDA with 3-bit routed experts ... #803"
 // (prefill windows through grouped expert GEMMs, SwiGLU epilogue).
@@ -45,17 +55,21 @@ namespace moe {
 
 namespace {
 
-constexpr int kPfRaw = 2;                    // raw weight-item stages
-constexpr int kPfA = 128 * 64 * 2;           // 128 rows x 64 columns, 16-bit
-constexpr int kPfB = kPfTile * 64 * 2;
+constexpr int kPfRaw = 3;                    // raw weight-item stages
+constexpr int kPfB = kPfTile * 64 * 2;       // B stage: kPfTile rows x 64 fp16
 constexpr int kPfKBlk = 64;                  // columns per MMA group (4 x K16)
-constexpr int kPfStagesMax = 4;
+constexpr int kPfStages = 6;                 // A/B stages
 constexpr int kPfRawWarp = 12, kPfMmaWarp = 13, kPfBWarp0 = 14, kPfBWarps = 4;
 static_assert((kPfBWarp0 + kPfBWarps) * 32 == kPfThreads, "warp roles cover the block");
 static_assert(kPfBWarps * 32 == kPfTile, "one B warp per 32 tile rows");
-// A/B stages: [A][B], both fp16
-__host__ __device__ constexpr int pf_stages(int mode) { return mode == 0 ? 4 : 4; }
-__host__ __device__ constexpr int pf_stage_bytes(int mode) { return (void)mode, kPfA + kPfB; }
+// tensor memory: two accumulators of kPfTile fp32 columns, then the A stages
+// (64 fp16 columns = 32 columns each)
+constexpr int kPfACol0 = 2 * kPfTile;
+constexpr int kPfACols = kPfKBlk / 2;
+constexpr int kPfTmemCols = 512;
+static_assert(kPfACol0 + kPfStages * kPfACols <= kPfTmemCols, "tensor memory budget");
+__host__ __device__ constexpr int pf_stages(int mode) { return (void)mode, kPfStages; }
+__host__ __device__ constexpr int pf_stage_bytes(int mode) { return (void)mode, kPfB; }
 
 __host__ __device__ inline int raw_stage_bytes(const TileGeo& g) {
   return (g.item_bytes + 1023) & ~1023;
@@ -63,7 +77,7 @@ __host__ __device__ inline int raw_stage_bytes(const TileGeo& g) {
 
 struct PfSmem {
   uint64_t raw_full[kPfRaw], raw_empty[kPfRaw];
-  uint64_t a_full[kPfStagesMax], b_full[kPfStagesMax], ab_empty[kPfStagesMax];
+  uint64_t a_full[kPfStages], b_full[kPfStages], ab_empty[kPfStages];
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem;
   WaitCtl wc;
@@ -71,16 +85,33 @@ struct PfSmem {
 
 struct PfUnit {
   int e, off, cnt, m;
+  bool sh;  // a unit of the second (shared-expert) bank
 };
 
 __device__ __forceinline__ int pf_tiles(const PrefillJob& J) {
   return J.n_tiles ? __ldcg(J.n_tiles) : (J.fixed_T + kPfTile - 1) / kPfTile;
 }
 
+// units of the second bank (they come first)
+__device__ __forceinline__ int pf_sh_units(const PrefillJob& J) {
+  return J.sh_base ? (J.sh_T + kPfTile - 1) / kPfTile * J.g.nblk : 0;
+}
+
 __device__ __forceinline__ PfUnit pf_unit(const PrefillJob& J, int u) {
   const int nblk = J.g.nblk;
-  const int t = u / nblk;
+  const int nsh = pf_sh_units(J);
   PfUnit r;
+  r.sh = u < nsh;
+  if (r.sh) {
+    const int t = u / nblk;
+    r.m = u - t * nblk;
+    r.e = 0;
+    r.off = kPfTile * t;
+    r.cnt = min(kPfTile, J.sh_T - kPfTile * t);
+    return r;
+  }
+  u -= nsh;
+  const int t = u / nblk;
   r.m = u - t * nblk;
   if (J.n_tiles) {
     r.e = __ldcg(J.te + t);
@@ -111,20 +142,42 @@ __device__ __forceinline__ uint4 dequant_word16(uint32_t w, __half2 s2, __half2 
   return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
-// Accumulator lane (A row) of row i of M-tile w: in mode 0 the gate tile w
-// (w < 4) takes lanes 32 w + i and its up tile w + 4 lanes 32 w + 16 + i;
-// in mode 1 tile w takes lanes 16 w + i.
-template <int MODE>
-__device__ __forceinline__ int pf_arow(int w, int i) {
-  return MODE == 0 ? 32 * (w & 3) + 16 * (w >> 2) + i : 16 * w + i;
+// Accumulator lane (A row) of row i of M-tile w: lanes 32 (w % 4) + 16 (w / 4)
+// + i, in the lane quarter of dequantisation warp 4 + w.  In mode 0 the gate
+// tile w (w < 4) and its up tile w + 4 share quarter w.
+__device__ __forceinline__ int pf_arow(int w, int i) { return 32 * (w & 3) + 16 * (w >> 2) + i; }
+
+// Quad transpose of one row's codes.  Lane t of a quad holds the row's
+// 4-code blocks 4t .. 4t + 3 (of the 16 in a 64-column group): Wa blocks 4t,
+// 4t + 1 and Wb blocks 4t + 2, 4t + 3, block 2i + p of a word in its bytes p
+// and p + 2 (the nibble order of the packed words).  Afterwards Na holds
+// blocks t, 4 + t and Nb blocks 8 + t, 12 + t in the same word format.
+// Round r brings lane t the word of lane t ^ r that holds block 4 (t ^ r) + t.
+__device__ __forceinline__ void quad_transpose(uint32_t Wa, uint32_t Wb, int t, uint32_t& Na,
+                                               uint32_t& Nb) {
+  const bool hi = t >= 2;
+  uint32_t v[4];
+  v[0] = hi ? Wb : Wa;
+#pragma unroll
+  for (int r = 1; r < 4; ++r) v[r] = __shfl_xor_sync(0xffffffffu, ((t ^ r) >= 2) ? Wb : Wa, r);
+  // v[r] holds block 4 (t ^ r) + t in bytes p, p + 2 (p = t & 1); it goes to
+  // word (t ^ r) / 2 at position (t ^ r) & 1
+  const uint32_t sel = (t & 1) ? 0x3715u : 0x6240u;
+  uint32_t X, Y;
+  asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(X) : "r"(v[0]), "r"(v[1]), "r"(sel));
+  asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(Y) : "r"(v[2]), "r"(v[3]), "r"(sel));
+  Na = hi ? Y : X;
+  Nb = hi ? X : Y;
 }
 
-// Group G of the raw item into an A stage: thread (tile w, lane l) converts
-// its four words -- tile rows g and g + 8, columns 16t .. 16t + 15 of the
-// group -- into the swizzled K-major layout (one 16-byte piece per word).
-template <int FMT, int MODE>
+// Group G of the raw item into the tensor-memory A stage at column ta_col:
+// thread (tile w, lane l = 4 g + t) converts the codes of tile rows g and
+// g + 8 -- after the quad transpose, columns 16 j + 4 t .. + 3 (j = 0..3) --
+// and stores them with four 16x256b stores (store j: columns 8 j .. 8 j + 7
+// of the stage, two fp16 a column).
+template <int FMT>
 __device__ __forceinline__ void dequant_group(const TileGeo& g, const uint8_t* raw, int G,
-                                              uint8_t* A, int w, int l) {
+                                              uint32_t ta, int w, int l) {
   const int NG = g.ng;
   const int gq = l >> 2, t = l & 3;
   uint32_t W0, W1, W2, W3;
@@ -157,11 +210,15 @@ __device__ __forceinline__ void dequant_group(const TileGeo& g, const uint8_t* r
   }
   const __half2 s02 = __halves2half2(s0, s0), s12 = __halves2half2(s1, s1);
   const __half2 b02 = __halves2half2(b0, b0), b12 = __halves2half2(b1, b1);
-  const int r0 = pf_arow<MODE>(w, gq), r1 = r0 + 8;
-  *reinterpret_cast<uint4*>(A + umma_off_sw128(r0, 16 * t)) = dequant_word16(W0, s02, b02);
-  *reinterpret_cast<uint4*>(A + umma_off_sw128(r0, 16 * t + 8)) = dequant_word16(W1, s02, b02);
-  *reinterpret_cast<uint4*>(A + umma_off_sw128(r1, 16 * t)) = dequant_word16(W2, s12, b12);
-  *reinterpret_cast<uint4*>(A + umma_off_sw128(r1, 16 * t + 8)) = dequant_word16(W3, s12, b12);
+  uint32_t N0, N1, N2, N3;
+  quad_transpose(W0, W1, t, N0, N1);  // row g
+  quad_transpose(W2, W3, t, N2, N3);  // row g + 8
+  const uint4 q0 = dequant_word16(N0, s02, b02), q1 = dequant_word16(N1, s02, b02);
+  const uint4 q2 = dequant_word16(N2, s12, b12), q3 = dequant_word16(N3, s12, b12);
+  tmem_st_16x256b(ta + 0, q0.x, q0.y, q2.x, q2.y);
+  tmem_st_16x256b(ta + 8, q0.z, q0.w, q2.z, q2.w);
+  tmem_st_16x256b(ta + 16, q1.x, q1.y, q3.x, q3.y);
+  tmem_st_16x256b(ta + 24, q1.z, q1.w, q3.z, q3.w);
 }
 
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
@@ -180,7 +237,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
   // the swizzled stages need 1024-byte alignment (the launch adds the slack)
   uint8_t* smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
   uint8_t* raw = smem;
-  uint8_t* stages = smem + kPfRaw * RB;  // stage s: [A][B], RB a multiple of 1024
+  uint8_t* stages = smem + kPfRaw * RB;  // B stage s at s * kPfB; RB a multiple of 1024
   if (tid == 0) {
     for (int i = 0; i < kPfRaw; ++i) {
       mbar_init(&S.raw_full[i], 1);
@@ -197,13 +254,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
     }
     wait_ctl_init(S.wc, J.status);
   }
-  if (warp == kPfMmaWarp) tmem_alloc(&S.tmem, 2 * kPfTile);
+  if (warp == kPfMmaWarp) tmem_alloc(&S.tmem, kPfTmemCols);
   fence_proxy_async();
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
   const uint32_t tbase = S.tmem;
-  const int nunits = pf_tiles(J) * g.nblk;
+  const int nunits = pf_sh_units(J) + pf_tiles(J) * g.nblk;
   const int G = gridDim.x;
   const int NG = g.ng, nch = g.nch, nks = nch * NG;
   int* status = J.status;
@@ -217,14 +274,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         const int rs = ri % kPfRaw;
         if (lane == 0) {
           if (ri >= kPfRaw) {
-            mbar_wait_bounded(&S.raw_empty[rs], ((ri / kPfRaw) - 1) & 1, &S.wc, status);
+            mbar_wait_bounded(&S.raw_empty[rs], ((ri / kPfRaw) - 1) & 1, &S.wc, status, true);
             // the stage's previous copy has landed (immediate unless a timeout
             // let the consumers skip their wait): one copy per barrier phase
             mbar_drain(&S.raw_full[rs], ((ri / kPfRaw) - 1) & 1);
           }
           mbar_expect_tx(&S.raw_full[rs], unsigned(g.item_bytes));
           bulk_g2s(raw + rs * RB,
-                   J.base + (size_t)U.e * g.expert_bytes +
+                   (U.sh ? J.sh_base : J.base) + (size_t)U.e * g.expert_bytes +
                        (size_t)(U.m * nch + c) * g.item_bytes,
                    unsigned(g.item_bytes), &S.raw_full[rs]);
         }
@@ -249,16 +306,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int n = 32 * bw + 4 * i + (lane >> 3);
-        const int row = n < U.cnt ? ((MODE == 0 && J.gather) ? __ldg(J.perm + U.off + n) / J.k
-                                                             : U.off + n)
-                                  : 0;
-        src[i] = J.B + (size_t)row * J.ldB + 8 * pc;
+        const int row =
+            n < U.cnt ? ((MODE == 0 && J.gather && !U.sh) ? __ldg(J.perm + U.off + n) / J.k
+                                                          : U.off + n)
+                      : 0;
+        src[i] = (U.sh ? J.sh_B : J.B) + (size_t)row * J.ldB + 8 * pc;
       }
       for (int q = 0; q < nks; ++q, ++ks) {
         const int s = ks % NS;
-        if (ks >= NS) mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status);
+        if (ks >= NS)
+          mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status, true);
         const int k0 = q * kPfKBlk;
-        uint8_t* B = stages + s * SB + kPfA;
+        uint8_t* B = stages + s * SB;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int n = 32 * bw + 4 * i + (lane >> 3);
@@ -284,13 +343,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
           const int s = ks % NS;
           mbar_wait_bounded(&S.a_full[s], (ks / NS) & 1, &S.wc, status);
           mbar_wait_bounded(&S.b_full[s], (ks / NS) & 1, &S.wc, status);
-          fence_proxy_async();
-          tmem_fence_after();
-          const uint32_t aa = smem_u32(stages + s * SB), ba = aa + kPfA;
+          fence_proxy_async();  // the cp.async rows of B
+          tmem_fence_after();   // the tensor-memory stores of A
+          const uint32_t ta = tbase + uint32_t(kPfACol0 + s * kPfACols);
+          const uint32_t ba = smem_u32(stages + s * SB);
 #pragma unroll
           for (int kk = 0; kk < kPfKBlk / 16; ++kk)
-            umma_f16(d, umma_desc_sw128(aa + 32 * kk), umma_desc_sw128(ba + 32 * kk), idesc,
-                     q > 0 || kk > 0);
+            umma_f16_tmem_a(d, ta + 8 * kk, umma_desc_sw128(ba + 32 * kk), idesc,
+                            q > 0 || kk > 0);
           umma_commit(&S.ab_empty[s]);
         }
         umma_commit(&S.acc_full[a]);
@@ -303,6 +363,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
   } else if (warp >= 4) {
     // ---- dequantisation: warp 4 + w takes M-tile w
     const int w = warp - 4;
+    const uint32_t tw = tbase + (uint32_t(pf_arow(w, 0)) << 16);
     int ri = 0, ks = 0;
     for (int u = blockIdx.x; u < nunits; u += G) {
       const PfUnit U = pf_unit(J, u);
@@ -313,8 +374,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         for (int Gi = 0; Gi < NG; ++Gi, ++ks) {
           const int s = ks % NS;
           if (ks >= NS) mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status);
-          dequant_group<FMT, MODE>(g, raw + rs * RB, Gi, stages + s * SB, w, lane);
-          fence_proxy_async();
+          dequant_group<FMT>(g, raw + rs * RB, Gi, tw + uint32_t(kPfACol0 + s * kPfACols), w,
+                             lane);
+          tmem_wait_st();
+          tmem_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.a_full[s]);
         }
@@ -328,7 +391,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
     for (int u = blockIdx.x; u < nunits; u += G, ++ui) {
       const PfUnit U = pf_unit(J, u);
       const int a = ui & 1;
-      mbar_wait_bounded(&S.acc_full[a], (ui >> 1) & 1, &S.wc, status);
+      mbar_wait_bounded(&S.acc_full[a], (ui >> 1) & 1, &S.wc, status, true);
       tmem_fence_after();
       const uint32_t tl = tbase + (uint32_t(32 * warp) << 16) + uint32_t(a * kPfTile);
       for (int c0 = 0; c0 < U.cnt; c0 += 32) {
@@ -340,6 +403,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
           tmem_ld32(tl + uint32_t(c0), v);
           const bool hi = lane >= 16;
           const size_t col = 64 * size_t(U.m) + 16 * warp + (lane & 15);
+          uint16_t* hout = U.sh ? J.sh_h : J.h;
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const float recv = __shfl_xor_sync(0xffffffffu, hi ? v[jj] : v[16 + jj], 16);
@@ -347,24 +411,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
             const float up = hi ? v[16 + jj] : recv;
             const int n = c0 + jj + (hi ? 16 : 0);
             if (n < U.cnt) {
-              const float hv = ga / (1.f + expf(-ga)) * up;
-              J.h[(size_t)(U.off + n) * J.ldh + col] = __half_as_ushort(__float2half_rn(hv));
+              const float hv = __fdividef(ga, 1.f + __expf(-ga)) * up;
+              hout[(size_t)(U.off + n) * J.ldh + col] = __half_as_ushort(__float2half_rn(hv));
               if (!(fabsf(hv) <= 65504.f)) atomicExch(status, int(MOE_ERR_RANGE));
             }
           }
         } else {
-          // output rows of tokens c0 .. c0 + 31, one per lane, then one
-          // 128-byte row piece a token
+          // output rows of tokens c0 .. c0 + 31, one per lane, then two
+          // 64-byte row pieces a token
           const int nl = c0 + lane;
           const int orow =
-              nl < U.cnt ? (J.scatter ? __ldg(J.perm + U.off + nl) : U.off + nl) : 0;
+              nl < U.cnt ? ((J.scatter && !U.sh) ? __ldg(J.perm + U.off + nl) : U.off + nl) : 0;
           float v[32];
           tmem_ld32(tl + uint32_t(c0), v);
-          const size_t col = 128 * size_t(U.m) + 32 * warp + lane;
+          // lane 32 q + l holds row l % 16 of M-tile q + 4 (l / 16)
+          const size_t col = 128 * size_t(U.m) + 16 * (warp + 4 * (lane >> 4)) + (lane & 15);
+          float* yout = U.sh ? J.sh_y : J.y;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int row = __shfl_sync(0xffffffffu, orow, j);
-            if (c0 + j < U.cnt) J.y[(size_t)row * J.ldy + col] = v[j];
+            if (c0 + j < U.cnt) yout[(size_t)row * J.ldy + col] = v[j];
           }
         }
       }
@@ -376,7 +442,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
-  if (warp == kPfMmaWarp) tmem_dealloc(tbase, 2 * kPfTile);
+  if (warp == kPfMmaWarp) tmem_dealloc(tbase, kPfTmemCols);
 }
 
 template <int FMT, int MODE>

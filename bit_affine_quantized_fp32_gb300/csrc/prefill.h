@@ -10,7 +10,7 @@ constexpr int kPfThreads = 576;
 // Experts with at most this many assignments in a prefill call go to the
 // decode units instead (each tensor-core unit dequantises a whole weight
 // block whatever its rows; the decode units cost per 8 rows).
-constexpr int kPfLight = 40;
+constexpr int kPfLight = 16;
 
 // One prefill GEMM launch over a tile list: each tile is <= kPfTile rows of
 // one expert; every (tile, 128-row weight block) is a unit.
@@ -40,6 +40,15 @@ struct PrefillJob {
   int ldy;
   int scatter;               // mode 1: output row = perm[off + n] (else off + n)
   int* status;
+  // Optional second bank of the same geometry (the shared expert, expert 0
+  // of sh_base) run in the same launch: its units come first, fixed tiles
+  // over sh_T rows, operand rows sh_B + row * ldB (never gathered), outputs
+  // sh_h (mode 0, ldh) or sh_y (mode 1, ldy; never scattered).
+  const uint8_t* sh_base;    // nullptr: none
+  int sh_T;
+  const uint16_t* sh_B;
+  uint16_t* sh_h;
+  float* sh_y;
 };
 
 // Shared memory of a launch for geometry g in mode 0/1 (0: not supported).

@@ -61,6 +61,18 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B^T over K = 16: A from tensor memory (lane m =
+// row m, column c = K elements 2c (low half) and 2c + 1), B from shared
+// memory, issued by one thread.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                                uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1 : 0)
+      : "memory");
+}
+
 // Arrive once on the mbarrier when every MMA issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -106,6 +118,23 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// One 16-lane x 8-column block of tensor memory from registers (shape
+// 16x256b, one repeat): thread l of the warp writes lanes L + l / 4 (r0, r1)
+// and L + 8 + l / 4 (r2, r3), columns C + 2 (l % 4) (r0, r2) and
+// C + 2 (l % 4) + 1 (r1, r3), where taddr = (L << 16) | C and the lanes
+// L .. L + 15 lie in this warp's quarter (32 (warp % 4) ..).  Asynchronous:
+// tmem_wait_st orders it before later reads by other threads.
+__device__ __forceinline__ void tmem_st_16x256b(uint32_t taddr, uint32_t r0, uint32_t r1,
+                                                uint32_t r2, uint32_t r3) {
+  asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(taddr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's tensor-memory lane (the lane
