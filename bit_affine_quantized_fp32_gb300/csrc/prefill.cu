@@ -2,8 +2,9 @@
 //
 // For T > 32 tokens an expert sees up to hundreds of rows, so its weights are
 // dequantised once per tile of kPfTile rows and fed to the tensor cores:
-// D[128 weight rows x N tokens] += A[128 x 64] * B[N x 64]^T per 64-column
-// group, fp16 operands, fp32 accumulators in tensor memory.  A (the
+// D[128 weight rows x N tokens] += A[128 x 128] * B[N x 128]^T per stage of
+// 128 columns (two 64-column code groups, eight K16 MMAs behind one
+// hand-off), fp16 operands, fp32 accumulators in tensor memory.  A (the
 // dequantised weights) is written straight into tensor memory; B (the
 // activation rows) is staged in shared memory.
 // One persistent CTA per SM, 18 warps:
@@ -13,17 +14,19 @@
 //               fp32, far below the fp16 rounding of h) or fp32 y rows
 //               (mode 1);
 //   warps 4-11  dequantisation: one weight item (128 rows x CK columns, the
-//               kernel-tiled layout) per raw stage, one 64-column group at a
-//               time into a tensor-memory A stage: w = fp16(s * q + b), one
+//               kernel-tiled layout) per raw stage, two 64-column groups at
+//               a time into a tensor-memory A stage: w = fp16(s * q + b), one
 //               fused multiply-add of the fp16 scale, the exact code and the
 //               fp16 bias (W4A16: s * u - 8 s), rounded once;
-//   warp 12     TMA bulk copies of the raw weight items (3 stages);
+//   warp 12     TMA bulk copies of the raw weight items (2 stages);
 //   warp 13     allocates tensor memory and issues the MMAs (one thread);
 //               tcgen05.commit frees A/B stages and hands accumulators over;
-//   warps 14-17 the operand rows of each group into a B stage, 32 rows a
+//   warps 14-17 the operand rows of each stage into a B stage, 32 rows a
 //               warp (cp.async of 16-byte pieces; one instruction copies 4
-//               whole 128-byte rows): fp16 x rows (mode 0) or fp16 h rows
-//               (mode 1).
+//               whole 128-byte rows of a 64-column half): fp16 x rows
+//               (mode 0) or fp16 h rows (mode 1).
+// A stage is complete when the eight dequantisation warps and the 128 copy
+// threads have arrived on its barrier (one wait for the MMA thread).
 // Dequantisation warp w takes M-tile w of the block and places it at
 // tensor-memory lanes 32 (w % 4) + 16 (w / 4) .. + 15, inside its own lane
 // quarter: in mode 0 (gate tiles 0-3, the matching up tiles 4-7) each
@@ -32,8 +35,9 @@
 // each) are transposed within its quad so that the 16x256b tensor-memory
 // stores put every element at its own column (the packed layout keeps 16
 // consecutive columns per lane; the store shape wants 4 runs of 4).
-// B stages use the K-major 128-byte-swizzled layout (umma.cuh): the row
-// copies write one shared-memory wavefront per quarter warp.
+// B stages hold two 64-column halves in the K-major 128-byte-swizzled layout
+// (umma.cuh): the row copies write one shared-memory wavefront per quarter
+// warp.
 // One MMA per 16 columns.  The activations enter as fp16: bf16 x is converted
 // once per call (exact in fp16's normal range; a value beyond it sets
 // MOE_ERR_RANGE), and h is stored as fp16 (likewise checked).  Two
@@ -55,15 +59,17 @@ namespace moe {
 
 namespace {
 
-constexpr int kPfRaw = 3;                    // raw weight-item stages
-constexpr int kPfB = kPfTile * 64 * 2;       // B stage: kPfTile rows x 64 fp16
-constexpr int kPfKBlk = 64;                  // columns per MMA group (4 x K16)
-constexpr int kPfStages = 6;                 // A/B stages
+constexpr int kPfRaw = 2;                    // raw weight-item stages
+constexpr int kPfGrp = 64;                   // columns per code group / swizzle half
+constexpr int kPfKBlk = 2 * kPfGrp;          // columns per stage (8 x K16)
+constexpr int kPfHalf = kPfTile * kPfGrp * 2;  // one 64-column half of a B stage
+constexpr int kPfB = 2 * kPfHalf;            // B stage: kPfTile rows x 128 fp16
+constexpr int kPfStages = 4;                 // A/B stages
 constexpr int kPfRawWarp = 12, kPfMmaWarp = 13, kPfBWarp0 = 14, kPfBWarps = 4;
 static_assert((kPfBWarp0 + kPfBWarps) * 32 == kPfThreads, "warp roles cover the block");
 static_assert(kPfBWarps * 32 == kPfTile, "one B warp per 32 tile rows");
 // tensor memory: two accumulators of kPfTile fp32 columns, then the A stages
-// (64 fp16 columns = 32 columns each)
+// (128 fp16 columns = 64 columns each)
 constexpr int kPfACol0 = 2 * kPfTile;
 constexpr int kPfACols = kPfKBlk / 2;
 constexpr int kPfTmemCols = 512;
@@ -77,7 +83,7 @@ __host__ __device__ inline int raw_stage_bytes(const TileGeo& g) {
 
 struct PfSmem {
   uint64_t raw_full[kPfRaw], raw_empty[kPfRaw];
-  uint64_t a_full[kPfStages], b_full[kPfStages], ab_empty[kPfStages];
+  uint64_t full[kPfStages], ab_empty[kPfStages];
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem;
   WaitCtl wc;
@@ -170,11 +176,11 @@ __device__ __forceinline__ void quad_transpose(uint32_t Wa, uint32_t Wb, int t, 
   Nb = hi ? X : Y;
 }
 
-// Group G of the raw item into the tensor-memory A stage at column ta_col:
-// thread (tile w, lane l = 4 g + t) converts the codes of tile rows g and
-// g + 8 -- after the quad transpose, columns 16 j + 4 t .. + 3 (j = 0..3) --
-// and stores them with four 16x256b stores (store j: columns 8 j .. 8 j + 7
-// of the stage, two fp16 a column).
+// Group G of the raw item into the 32 tensor-memory columns at ta (lane
+// field: the tile's first lane): thread (tile w, lane l = 4 g + t) converts
+// the codes of tile rows g and g + 8 -- after the quad transpose, columns
+// 16 j + 4 t .. + 3 (j = 0..3) -- and stores them with four 16x256b stores
+// (store j: columns 8 j .. 8 j + 7, two fp16 a column).
 template <int FMT>
 __device__ __forceinline__ void dequant_group(const TileGeo& g, const uint8_t* raw, int G,
                                               uint32_t ta, int w, int l) {
@@ -244,8 +250,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       mbar_init(&S.raw_empty[i], 8);
     }
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&S.a_full[i], 8);
-      mbar_init(&S.b_full[i], 32 * kPfBWarps);
+      mbar_init(&S.full[i], 8 + 32 * kPfBWarps);  // dequantisation warps + copy threads
       mbar_init(&S.ab_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
   const uint32_t tbase = S.tmem;
   const int nunits = pf_sh_units(J) + pf_tiles(J) * g.nblk;
   const int G = gridDim.x;
-  const int NG = g.ng, nch = g.nch, nks = nch * NG;
+  const int NG = g.ng, nch = g.nch, nks = nch * NG / 2;  // stages per unit
   int* status = J.status;
 
   if (warp == kPfRawWarp) {
@@ -319,11 +324,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         const int k0 = q * kPfKBlk;
         uint8_t* B = stages + s * SB;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int n = 32 * bw + 4 * i + (lane >> 3);
-          if (n < U.cnt) cp_async16(B + umma_off_sw128(n, 8 * pc), src[i] + k0);
-        }
-        cp_async_arrive_noinc(&S.b_full[s]);
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int n = 32 * bw + 4 * i + (lane >> 3);
+            if (n < U.cnt)
+              cp_async16(B + h * kPfHalf + umma_off_sw128(n, 8 * pc), src[i] + k0 + kPfGrp * h);
+          }
+        cp_async_arrive_noinc(&S.full[s]);
       }
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
@@ -341,15 +349,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
         const uint32_t d = tbase + uint32_t(a * kPfTile);
         for (int q = 0; q < nks; ++q, ++ks) {
           const int s = ks % NS;
-          mbar_wait_bounded(&S.a_full[s], (ks / NS) & 1, &S.wc, status);
-          mbar_wait_bounded(&S.b_full[s], (ks / NS) & 1, &S.wc, status);
+          mbar_wait_bounded(&S.full[s], (ks / NS) & 1, &S.wc, status);
           fence_proxy_async();  // the cp.async rows of B
           tmem_fence_after();   // the tensor-memory stores of A
           const uint32_t ta = tbase + uint32_t(kPfACol0 + s * kPfACols);
           const uint32_t ba = smem_u32(stages + s * SB);
 #pragma unroll
           for (int kk = 0; kk < kPfKBlk / 16; ++kk)
-            umma_f16_tmem_a(d, ta + 8 * kk, umma_desc_sw128(ba + 32 * kk), idesc,
+            umma_f16_tmem_a(d, ta + 8 * kk,
+                            umma_desc_sw128(ba + (kk >> 2) * kPfHalf + 32 * (kk & 3)), idesc,
                             q > 0 || kk > 0);
           umma_commit(&S.ab_empty[s]);
         }
@@ -371,15 +379,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill(const __grid_constant
       for (int c = 0; c < nch; ++c, ++ri) {
         const int rs = ri % kPfRaw;
         mbar_wait_bounded(&S.raw_full[rs], (ri / kPfRaw) & 1, &S.wc, status);
-        for (int Gi = 0; Gi < NG; ++Gi, ++ks) {
+        for (int Gi = 0; Gi < NG; Gi += 2, ++ks) {
           const int s = ks % NS;
           if (ks >= NS) mbar_wait_bounded(&S.ab_empty[s], ((ks / NS) - 1) & 1, &S.wc, status);
-          dequant_group<FMT>(g, raw + rs * RB, Gi, tw + uint32_t(kPfACol0 + s * kPfACols), w,
-                             lane);
+          const uint32_t ta = tw + uint32_t(kPfACol0 + s * kPfACols);
+          dequant_group<FMT>(g, raw + rs * RB, Gi, ta, w, lane);
+          dequant_group<FMT>(g, raw + rs * RB, Gi + 1, ta + kPfGrp / 2, w, lane);
           tmem_wait_st();
           tmem_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&S.a_full[s]);
+          if (lane == 0) mbar_arrive(&S.full[s]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.raw_empty[rs]);
