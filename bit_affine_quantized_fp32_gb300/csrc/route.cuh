@@ -494,33 +494,51 @@ __device__ __forceinline__ void topk_warp_tagged(const unsigned long long* tagge
   topk_select(key, t, k, idx, w, sg, has_gate, gl, idx2, w2, rb);
 }
 
-// Shared memory of bucket_cta for NW warps.
+// Shared memory of bucket_cta (up to 32 warps, up to 256 experts).
 struct BucketSmem {
-  int cnt[256];
-  int cur[256];
-  int wsum[32];
-  int wc[32][256];
+  int wc[32][256];  // per-warp counts, then per-warp cursors
+  int base[256];    // first bucket position of each expert
+  int wsum[8];
 };
 
-// Stable counting sort of the N assignment ids by expert (one CTA of NW
-// warps): histogram, exclusive prefix sum over <= 256 experts, then chunks of
-// 32*NW assignments in order, ranked inside a chunk with warp match + per-warp
-// counts.  Ids outside 0..E-1 are skipped.
+// Stable counting sort of the N assignment ids by expert (one CTA of 32
+// warps): warp w owns a contiguous range of assignments, taken in rounds of
+// 32 in order.  Pass 1 counts each expert per warp (warp match: one add per
+// expert and round), then every expert's counts are prefix-summed over the
+// warps and its total over the experts (the bucket offsets), and pass 2 puts
+// each assignment at base[e] + (earlier assignments of e in earlier warps and
+// rounds) + (its rank among this round's lanes with expert e).  Ids outside
+// 0..E-1 are skipped.
 __device__ __forceinline__ void bucket_cta(const int32_t* idx, int N, int E, int32_t* offsets,
                                            int32_t* perm, BucketSmem& S) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int NT = blockDim.x, NW = NT >> 5;
-  for (int i = tid; i < 256; i += NT) S.cnt[i] = 0;
-  __syncthreads();
-  for (int a = tid; a < N; a += NT) {
-    const int e = __ldcg(idx + a);
-    if (e >= 0 && e < E) atomicAdd(&S.cnt[e], 1);
+  const int NW = blockDim.x >> 5;
+  const int C = (((N + NW - 1) / NW) + 31) & ~31;  // assignments per warp
+  const int a0 = min(N, wid * C), a1 = min(N, a0 + C);
+  for (int i = lane; i < 256; i += 32) S.wc[wid][i] = 0;
+  __syncwarp();
+  for (int b = a0; b < a1; b += 32) {
+    const int a = b + lane;
+    int e = a < a1 ? __ldcg(idx + a) : -1;
+    if (e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (__ffs(peers) - 1) == lane) S.wc[wid][e] += __popc(peers);
+    __syncwarp();
   }
   __syncthreads();
-  // exclusive scan of cnt[0..255] by the first 8 warps
-  int incl = 0;
+  // thread e: exclusive prefix of expert e's counts over the warps (in place)
+  int tot = 0;
   if (tid < 256) {
-    incl = tid < E ? S.cnt[tid] : 0;
+    for (int w = 0; w < NW; ++w) {
+      const int c = S.wc[w][tid];
+      S.wc[w][tid] = tot;
+      tot += c;
+    }
+    if (tid >= E) tot = 0;
+  }
+  // exclusive scan of the totals over the experts (the first 8 warps)
+  int incl = tot;
+  if (tid < 256) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -533,35 +551,20 @@ __device__ __forceinline__ void bucket_cta(const int32_t* idx, int N, int E, int
     int pre = 0;
     for (int i = 0; i < wid; ++i) pre += S.wsum[i];
     incl += pre;
-    const int c = tid < E ? S.cnt[tid] : 0;
-    S.cur[tid] = incl - c;
+    S.base[tid] = incl - tot;
     if (tid < E) offsets[tid + 1] = incl;
     if (tid == 0) offsets[0] = 0;
   }
   __syncthreads();
-  for (int base = 0; base < N; base += NT) {
-    for (int i = lane; i < 256; i += 32) S.wc[wid][i] = 0;
-    __syncwarp();
-    const int a = base + tid;
-    int e = a < N ? __ldcg(idx + a) : -1;
+  for (int b = a0; b < a1; b += 32) {
+    const int a = b + lane;
+    int e = a < a1 ? __ldcg(idx + a) : -1;
     if (e >= E) e = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    const bool leader = (__ffs(peers) - 1) == lane;
-    if (e >= 0 && leader) S.wc[wid][e] = __popc(peers);
-    __syncthreads();
-    if (e >= 0) {
-      int pre = 0;
-      for (int i = 0; i < wid; ++i) pre += S.wc[i][e];
-      perm[S.cur[e] + pre + rank] = a;
-    }
-    __syncthreads();
-    for (int x = tid; x < E; x += NT) {
-      int tot = 0;
-      for (int i = 0; i < NW; ++i) tot += S.wc[i][x];
-      S.cur[x] += tot;
-    }
-    __syncthreads();
+    if (e >= 0) perm[S.base[e] + S.wc[wid][e] + __popc(peers & ((1u << lane) - 1u))] = a;
+    __syncwarp();
+    if (e >= 0 && (__ffs(peers) - 1) == lane) S.wc[wid][e] += __popc(peers);
+    __syncwarp();
   }
 }
 

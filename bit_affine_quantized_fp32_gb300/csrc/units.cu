@@ -86,17 +86,88 @@ __global__ void k_xsum(const uint16_t* __restrict__ x, int T, int H, int f16, Ti
   xsum_task(x, H, f16 != 0, g13, xsum, task);
 }
 
-// blockIdx.x: 64-column piece, blockIdx.y: run of kCombineTok tokens
-constexpr int kCombineTok = 16;
-__global__ void __launch_bounds__(256) k_combine(const CombineArgs A) {
-  const int t0 = blockIdx.y * kCombineTok;
-  const int Tn = min(kCombineTok, A.T - t0);
-  const size_t kh = size_t(A.k) * A.H;
-  combine_rows(A.y + t0 * kh, A.yhalf, A.w + t0 * A.k, A.ysh ? A.ysh + size_t(t0) * A.H : nullptr,
-               A.ysh2 ? A.ysh2 + size_t(t0) * A.H : nullptr, A.sg ? A.sg + t0 : nullptr,
-               A.out + size_t(t0) * A.H, Tn, A.k, A.H, A.f16 != 0, blockIdx.x * kCombineRows,
-               kCombineRows, threadIdx.x, blockDim.x, A.round_bf16 != 0,
-               A.idx ? A.idx + t0 * A.k : nullptr, A.offsets, A.one_plane_max);
+// The combine of combine_rows, element for element the same arithmetic, laid
+// out for streaming: a block takes kCmbTok tokens x kCmbCols columns; the
+// tokens' slot weights (bf16-rounded in the chain), the second-plane flags and
+// the shared weights are read once into shared memory, then each thread reads
+// four consecutive columns of every slot row with 16-byte loads.
+constexpr int kCmbTok = 4, kCmbCols = 512, kCmbThreads = kCmbCols / 4;
+__global__ void __launch_bounds__(kCmbThreads) k_combine(const CombineArgs A) {
+  __shared__ float sw[kCmbTok][kMaxTopK];
+  __shared__ int stwo[kCmbTok][kMaxTopK];
+  __shared__ float ssg[kCmbTok];
+  const int t0 = blockIdx.y * kCmbTok;
+  const int Tn = min(kCmbTok, A.T - t0);
+  const int tid = threadIdx.x;
+  const bool rb = A.round_bf16 != 0;
+  if (tid < kCmbTok * kMaxTopK) {
+    const int tt = tid / kMaxTopK, j = tid - tt * kMaxTopK;
+    float wv = 0.f;
+    int two = 0;
+    if (tt < Tn && j < A.k) {
+      const int t = t0 + tt;
+      wv = A.w[t * A.k + j];
+      if (rb) wv = round_bf16(wv);
+      two = A.yhalf != 0;
+      if (two && A.idx) {
+        const int e = __ldg(A.idx + t * A.k + j);
+        two = __ldg(A.offsets + e + 1) - __ldg(A.offsets + e) <= A.one_plane_max;
+      }
+    }
+    sw[tt][j] = wv;
+    stwo[tt][j] = two;
+  }
+  if (tid < kCmbTok) {
+    float v = 1.f;
+    if (A.sg && tid < Tn) v = rb ? round_bf16(A.sg[t0 + tid]) : A.sg[t0 + tid];
+    ssg[tid] = v;
+  }
+  __syncthreads();
+  const int h = blockIdx.x * kCmbCols + 4 * tid;
+  if (h >= A.H) return;
+  for (int tt = 0; tt < Tn; ++tt) {
+    const int t = t0 + tt;
+    float4 ya[kMaxTopK], yb[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < A.k) {
+        const size_t a = (size_t)(t * A.k + j) * A.H + h;
+        ya[j] = __ldcg(reinterpret_cast<const float4*>(A.y + a));
+        yb[j] = stwo[tt][j] ? __ldcg(reinterpret_cast<const float4*>(A.y + A.yhalf + a))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float4 vs = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (A.ysh) {
+      const size_t a = (size_t)t * A.H + h;
+      vs = __ldcg(reinterpret_cast<const float4*>(A.ysh + a));
+      if (A.ysh2) {
+        const float4 v2 = __ldcg(reinterpret_cast<const float4*>(A.ysh2 + a));
+        vs = make_float4(vs.x + v2.x, vs.y + v2.y, vs.z + v2.z, vs.w + v2.w);
+      }
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < A.k) {
+        const float wj = sw[tt][j];
+        const float y4[4] = {ya[j].x, ya[j].y, ya[j].z, ya[j].w};
+        const float b4[4] = {yb[j].x, yb[j].y, yb[j].z, yb[j].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c] = fmaf(wj, A.yhalf ? y4[c] + b4[c] : y4[c], acc[c]);
+      }
+    if (A.ysh) {
+      const float v4[4] = {vs.x, vs.y, vs.z, vs.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[c] = fmaf(ssg[tt], v4[c], acc[c]);
+    }
+    const bool f16 = A.f16 != 0;
+    const uint32_t lo = uint32_t(float_to_act_bits(acc[0], f16)) |
+                        (uint32_t(float_to_act_bits(acc[1], f16)) << 16);
+    const uint32_t hi = uint32_t(float_to_act_bits(acc[2], f16)) |
+                        (uint32_t(float_to_act_bits(acc[3], f16)) << 16);
+    *reinterpret_cast<uint2*>(A.out + (size_t)t * A.H + h) = make_uint2(lo, hi);
+  }
 }
 
 // dst = a + b elementwise (the two k-half planes of a down projection)
@@ -185,7 +256,8 @@ cudaError_t launch_store_word(int* p, int v, cudaStream_t st) {
 
 cudaError_t launch_combine(const CombineArgs& A, cudaStream_t st) {
   if (A.T <= 0) return cudaSuccess;
-  k_combine<<<dim3(A.H / kCombineRows, (A.T + kCombineTok - 1) / kCombineTok), 256, 0, st>>>(A);
+  k_combine<<<dim3((A.H + kCmbCols - 1) / kCmbCols, (A.T + kCmbTok - 1) / kCmbTok), kCmbThreads, 0,
+              st>>>(A);
   return cudaGetLastError();
 }
 
