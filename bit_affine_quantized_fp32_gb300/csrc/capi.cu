@@ -659,9 +659,10 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
   if (!bucket_offsets || (T > 0 && (!topk_idx || !topk_w || !bucket_perm)))
     return fail(MOE_ERR_INVALID_ARG, "routing outputs must not be NULL");
   const WsLayout L = ws_layout(T, E, top_k, H, 128);
-  // the logits, and above the decode sizes the router's k-slice sums
-  if ((s = check_ws(ws, ws_bytes, T > MOE_DECODE_MAX_TOKENS ? L.rpart + 16 * size_t(T) * (E + 1)
-                                                            : L.idx)))
+  // the logits, and above the decode sizes the router's k-slice sums and
+  // bf16 parts
+  if ((s = check_ws(ws, ws_bytes,
+                    T > MOE_DECODE_MAX_TOKENS ? L.rsplit + 2 * router_split_elems(T, E, H) : L.idx)))
     return s;
   float* lg = logits ? logits : reinterpret_cast<float*>(wsp(ws, L.logits));
   float* gl = reinterpret_cast<float*>(wsp(ws, L.gate_logit));
@@ -686,6 +687,7 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
   R.gate_logit = gl;
   R.round_bf16 = rb;
   R.part = T > MOE_DECODE_MAX_TOKENS ? reinterpret_cast<float*>(wsp(ws, L.rpart)) : nullptr;
+  R.split = T > MOE_DECODE_MAX_TOKENS ? reinterpret_cast<uint16_t*>(wsp(ws, L.rsplit)) : nullptr;
   MOE_CUDA(launch_router(R, stream), "router kernel");
   MOE_CUDA(launch_topk(lg, shared_gate ? gl : nullptr, T, E, top_k, topk_idx, topk_w,
                        shared_gate ? shared_gate_w : nullptr, rb, stream),

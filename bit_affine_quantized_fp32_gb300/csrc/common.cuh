@@ -56,6 +56,8 @@ struct WsLayout {
   size_t pt_cnt;      // i32 [maxss] rows (1..128)
   size_t xh;          // u16 [T][H] fp16 copy of bf16 activations (prefill form)
   size_t rpart;       // f32 [4][T][E+1] k-slice sums of the router (prefill form)
+  size_t rsplit;      // u16 [3][E+1][H] + [2][T][H] bf16 parts of the router rows and of
+                      //     fp16 x (prefill form)
   size_t total;
 };
 
@@ -111,6 +113,7 @@ inline WsLayout ws_layout(long T, long E, long k, long H, long I) {
   L.pt_cnt = take(4 * mss);
   L.xh = take(2 * T * H);
   L.rpart = take(4 * 4 * T * (E + 1));
+  L.rsplit = take(2 * (3 * (E + 1) * H + 2 * T * H));
   L.total = o;
   return L;
 }

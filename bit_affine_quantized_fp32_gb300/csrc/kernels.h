@@ -85,7 +85,11 @@ struct RouterJob {
   int round_bf16;           // router and gate rows rounded to bf16 before the dot products
   float* part;              // nullable scratch [4][T][E + 1]: the tensor-core router's
                             // k-slice sums (used for T > 32)
+  uint16_t* split;          // scratch with part: bf16 parts of the weights [3][E + 1][H]
+                            // then of fp16 x [2][T][H]
 };
+// elements of RouterJob::split for T tokens, E experts (+ 1 gate row), H columns
+inline size_t router_split_elems(long T, long E, long H) { return size_t(3 * (E + 1) * H + 2 * T * H); }
 int router_ks(int H);
 int router_blocks(int E, bool gate, int H);
 cudaError_t launch_router(const RouterJob& J, cudaStream_t st);

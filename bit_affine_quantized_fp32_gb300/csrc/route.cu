@@ -2,6 +2,7 @@
 // bucketing, slots) over the device functions of route.cuh.
 
 #include "route.cuh"
+#include "host.h"
 
 namespace moe {
 
@@ -50,11 +51,18 @@ __global__ void __launch_bounds__(256) k_subslots(const int32_t* __restrict__ of
 // exactly into three bf16 parts w = w1 + w2 + w3 (8 significant bits each, the
 // remainders exact in fp32); bf16 activations are exact operands, fp16 ones
 // split exactly into two bf16 parts.  So every product is exact and the sums
-// are fp32 (mma.sync m16n8k16, fp32 accumulation).  A block computes a tile of
-// 32 tokens x 32 rows over 64-column chunks of H staged in shared memory; warp
-// w takes tokens 16 (w & 1) .. and rows 16 (w >> 1) .. (two 8-row n-tiles).
-constexpr int kRtTok = 32, kRtRows = 32, kRtK = 64, kRtPitch = kRtK + 8;  // bf16 elements
-constexpr int kRtSplit = 4;  // k-slices per tile, summed in order by k_router_sum
+// are fp32 (mma.sync m16n8k16, fp32 accumulation).  k_router_split writes the
+// parts once per call (workspace); a k_router_tc block computes a tile of 64
+// tokens x 32 rows over a k-slice of H, streaming 64-column chunks of the
+// parts through a ring of kRtStages shared-memory stages (cp.async); warp w
+// takes tokens 32 (w & 1) .. (two 16-row m-tiles) and rows 16 (w >> 1) ..
+// (two 8-row n-tiles): four accumulator chains, each fragment loaded once
+// for two or three MMAs.
+constexpr int kRtTok = 64, kRtRows = 32, kRtK = 64, kRtPitch = kRtK + 8;  // bf16 elements
+constexpr int kRtSplit = 4;   // k-slices per tile, summed in order by k_router_sum
+constexpr int kRtStages = 4;  // chunks in flight per block
+constexpr int kRtXPart = kRtTok * kRtPitch;   // elements of one x-part tile
+constexpr int kRtWPart = kRtRows * kRtPitch;  // elements of one weight-part tile
 
 __device__ __forceinline__ void split3_bf16(float v, uint16_t& a, uint16_t& b, uint16_t& c) {
   const __nv_bfloat16 h1 = __float2bfloat16_rn(v);
@@ -66,104 +74,172 @@ __device__ __forceinline__ void split3_bf16(float v, uint16_t& a, uint16_t& b, u
   c = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
 }
 
+// rows whose weights are one exact bf16 part (the chain's bf16 rows, or bf16
+// router rows without a gate row of another format)
+__host__ __device__ inline bool router_one_part(const RouterJob& J) {
+  return J.round_bf16 || (!J.gq && J.fmt == MOE_FMT_BF16);
+}
+
+// wp[p][r][k] (p < 3, r < E + gate) = part p of weight (r, k); for fp16
+// activations xp[p][t][k] (p < 2) = part p of x (t, k).  Thread: 4 columns.
+__global__ void k_router_split(const RouterJob J, uint16_t* __restrict__ wp,
+                               uint16_t* __restrict__ xp) {
+  const int nrows = J.E + (J.gq ? 1 : 0);
+  const int q4 = J.H / 4;
+  const long nw = long(nrows) * q4;
+  const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < nw) {
+    const int r = int(i / q4), k = int(i - long(r) * q4) * 4;
+    float w[4];
+    if (r >= J.E)
+      router_load_w4(J.gfmt, J.gq, J.gs, J.gb, 0, J.H, k, w, J.round_bf16 != 0);
+    else
+      router_load_w4(J.fmt, J.q, J.s, J.b, r, J.H, k, w, J.round_bf16 != 0);
+    uint16_t a[4], b[4], c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) split3_bf16(w[j], a[j], b[j], c[j]);
+    const size_t o = size_t(r) * J.H + k, ps = size_t(nrows) * J.H;
+    auto put = [&](uint16_t* dst, const uint16_t (&v)[4]) {
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(uint32_t(v[0]) | (uint32_t(v[1]) << 16), uint32_t(v[2]) | (uint32_t(v[3]) << 16));
+    };
+    put(wp + o, a);
+    put(wp + ps + o, b);
+    put(wp + 2 * ps + o, c);
+    return;
+  }
+  if (!J.f16) return;
+  const long j = i - nw;
+  if (j >= long(J.T) * q4) return;
+  const int t = int(j / q4), k = int(j - long(t) * q4) * 4;
+  const uint2 v = *reinterpret_cast<const uint2*>(J.x + size_t(t) * J.H + k);
+  const uint32_t in[2] = {v.x, v.y};
+  uint32_t hi[2], lo[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&in[h]));
+    const __nv_bfloat162 bh = __floats2bfloat162_rn(f.x, f.y);
+    const float2 fh = __bfloat1622float2(bh);
+    const __nv_bfloat162 bl = __floats2bfloat162_rn(f.x - fh.x, f.y - fh.y);
+    hi[h] = *reinterpret_cast<const uint32_t*>(&bh);
+    lo[h] = *reinterpret_cast<const uint32_t*>(&bl);
+  }
+  const size_t o = size_t(t) * J.H + k;
+  *reinterpret_cast<uint2*>(xp + o) = make_uint2(hi[0], hi[1]);
+  *reinterpret_cast<uint2*>(xp + size_t(J.T) * J.H + o) = make_uint2(lo[0], lo[1]);
+}
+
+// Shared memory of one k_router_tc stage: px x-part tiles then nwp weight-part
+// tiles.
+__host__ __device__ inline int router_stage_elems(const RouterJob& J) {
+  return (J.f16 ? 2 : 1) * kRtXPart + (router_one_part(J) ? 1 : 3) * kRtWPart;
+}
+
 // blockIdx.z: k-slice of H; the slice's sums go to part[z][T][E + 1]
-__global__ void __launch_bounds__(128) k_router_tc(const RouterJob J, float* part) {
-  __shared__ __align__(16) uint16_t xs[2][kRtTok][kRtPitch];
-  __shared__ __align__(16) uint16_t wsm[3][kRtRows][kRtPitch];
+__global__ void __launch_bounds__(128) k_router_tc(const RouterJob J, const uint16_t* __restrict__ wp,
+                                                   const uint16_t* __restrict__ xp,
+                                                   float* __restrict__ part) {
+  extern __shared__ __align__(16) uint16_t rt_smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int t0 = blockIdx.x * kRtTok, r0 = blockIdx.y * kRtRows;
   const int nrows = J.E + (J.gq ? 1 : 0);
-  const int px = J.f16 ? 2 : 1;  // bf16 parts of x
-  const bool w1part = J.round_bf16 || (!J.gq && J.fmt == MOE_FMT_BF16);
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  const int kslice = J.H / kRtSplit;
-  for (int k0 = blockIdx.z * kslice; k0 < (blockIdx.z + 1) * kslice; k0 += kRtK) {
-    // x chunk: 32 tokens x 64 columns, 16 values per thread
-    {
-      const int tk = tid >> 2, c = (tid & 3) * 16;
-      const int tok = t0 + tk;
+  const int px = J.f16 ? 2 : 1;                 // bf16 parts of x
+  const int nwp = router_one_part(J) ? 1 : 3;   // bf16 parts of the weights
+  const int SE = px * kRtXPart + nwp * kRtWPart;  // elements per stage
+  const size_t ps = size_t(nrows) * J.H;
+  const int kslice = J.H / kRtSplit, nchunk = kslice / kRtK, kbeg = blockIdx.z * kslice;
+  // chunk c -> stage c % kRtStages: 16-byte pieces (row piece >> 3, columns
+  // 8 (piece & 7) ..), thread tid taking pieces tid + 128 i; rows past T or
+  // E + gate are left as they are (their products only reach sums that are
+  // not written)
+  auto issue = [&](int c) {
+    uint16_t* S = rt_smem + (c % kRtStages) * SE;
+    const int k0 = kbeg + c * kRtK;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (tok < J.T) v = *reinterpret_cast<const uint4*>(J.x + size_t(tok) * J.H + k0 + c + 8 * h);
-        if (!J.f16) {
-          *reinterpret_cast<uint4*>(&xs[0][tk][c + 8 * h]) = v;
-        } else {  // fp16 -> exact bf16 hi + lo
-          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&in[j]));
-            const __nv_bfloat162 bh = __floats2bfloat162_rn(f.x, f.y);
-            const float2 fh = __bfloat1622float2(bh);
-            const __nv_bfloat162 bl = __floats2bfloat162_rn(f.x - fh.x, f.y - fh.y);
-            hi[j] = *reinterpret_cast<const uint32_t*>(&bh);
-            lo[j] = *reinterpret_cast<const uint32_t*>(&bl);
-          }
-          *reinterpret_cast<uint4*>(&xs[0][tk][c + 8 * h]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(&xs[1][tk][c + 8 * h]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    for (int h = 0; h < kRtTok * 8 / 128; ++h) {
+      const int pc = tid + 128 * h, rr = pc >> 3, c8 = (pc & 7) * 8;
+      for (int p = 0; p < px; ++p)
+        if (t0 + rr < J.T) {
+          const uint16_t* src = (J.f16 ? xp + size_t(p) * J.T * J.H : J.x) +
+                                size_t(t0 + rr) * J.H + k0 + c8;
+          cp_async16(S + p * kRtXPart + rr * kRtPitch + c8, src);
         }
-      }
     }
-    // weight chunk: 32 rows x 64 columns, 16 values per thread, split in 3
-    {
-      const int rr = tid >> 2, c = (tid & 3) * 16;
-      const int row = r0 + rr;
+    uint16_t* W = S + px * kRtXPart;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float w[4] = {0.f, 0.f, 0.f, 0.f};
-        const int k = k0 + c + 4 * q4;
-        if (row < nrows) {
-          if (row >= J.E)
-            router_load_w4(J.gfmt, J.gq, J.gs, J.gb, 0, J.H, k, w, J.round_bf16 != 0);
-          else
-            router_load_w4(J.fmt, J.q, J.s, J.b, row, J.H, k, w, J.round_bf16 != 0);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          split3_bf16(w[j], wsm[0][rr][c + 4 * q4 + j], wsm[1][rr][c + 4 * q4 + j],
-                      wsm[2][rr][c + 4 * q4 + j]);
-      }
+    for (int h = 0; h < kRtRows * 8 / 128; ++h) {
+      const int pc = tid + 128 * h, rr = pc >> 3, c8 = (pc & 7) * 8;
+      for (int p = 0; p < nwp; ++p)
+        if (r0 + rr < nrows)
+          cp_async16(W + p * kRtWPart + rr * kRtPitch + c8,
+                     wp + p * ps + size_t(r0 + rr) * J.H + k0 + c8);
     }
+  };
+  float acc[2][2][4] = {};
+  for (int c = 0; c < kRtStages - 1; ++c) {
+    if (c < nchunk) issue(c);
+    cp_async_commit();
+  }
+  const int tb = 32 * (warp & 1), rb = 16 * (warp >> 1);
+  for (int c = 0; c < nchunk; ++c) {
+    if (c + kRtStages - 1 < nchunk) issue(c + kRtStages - 1);
+    cp_async_commit();
+    cp_async_wait<kRtStages - 1>();  // chunk c has landed (this thread's pieces)
     __syncthreads();
-    const int tb = 16 * (warp & 1), rb = 16 * (warp >> 1);
+    const uint16_t* S = rt_smem + (c % kRtStages) * SE;
 #pragma unroll
     for (int kk = 0; kk < kRtK; kk += 16) {
+      uint32_t bw[3][2][2];  // [part][n-tile][reg]
 #pragma unroll
-      for (int xp = 0; xp < 2; ++xp) {
-        if (xp >= px) break;
-        const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&xs[xp][tb + g][kk + 2 * t4]);
-        const uint32_t a1 = *reinterpret_cast<const uint32_t*>(&xs[xp][tb + g + 8][kk + 2 * t4]);
-        const uint32_t a2 = *reinterpret_cast<const uint32_t*>(&xs[xp][tb + g][kk + 2 * t4 + 8]);
-        const uint32_t a3 =
-            *reinterpret_cast<const uint32_t*>(&xs[xp][tb + g + 8][kk + 2 * t4 + 8]);
+      for (int wq = 0; wq < 3; ++wq) {
+        if (wq >= nwp) break;
+        const uint16_t* W = S + px * kRtXPart + wq * kRtWPart;
 #pragma unroll
-        for (int wp = 0; wp < 3; ++wp) {
-          if (wp > 0 && w1part) break;
+        for (int nt = 0; nt < 2; ++nt) {
+          const int rw = rb + 8 * nt + g;
+          bw[wq][nt][0] = *reinterpret_cast<const uint32_t*>(W + rw * kRtPitch + kk + 2 * t4);
+          bw[wq][nt][1] = *reinterpret_cast<const uint32_t*>(W + rw * kRtPitch + kk + 2 * t4 + 8);
+        }
+      }
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const int rw = rb + 8 * nt + g;
-            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&wsm[wp][rw][kk + 2 * t4]);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&wsm[wp][rw][kk + 2 * t4 + 8]);
-            mma16816<false>(acc[nt], a0, a1, a2, a3, b0, b1);
+      for (int xq = 0; xq < 2; ++xq) {
+        if (xq >= px) break;
+        const uint16_t* X = S + xq * kRtXPart;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int tr = tb + 16 * mt + g;
+          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(X + tr * kRtPitch + kk + 2 * t4);
+          const uint32_t a1 =
+              *reinterpret_cast<const uint32_t*>(X + (tr + 8) * kRtPitch + kk + 2 * t4);
+          const uint32_t a2 =
+              *reinterpret_cast<const uint32_t*>(X + tr * kRtPitch + kk + 2 * t4 + 8);
+          const uint32_t a3 =
+              *reinterpret_cast<const uint32_t*>(X + (tr + 8) * kRtPitch + kk + 2 * t4 + 8);
+#pragma unroll
+          for (int wq = 0; wq < 3; ++wq) {
+            if (wq >= nwp) break;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+              mma16816<false>(acc[mt][nt], a0, a1, a2, a3, bw[wq][nt][0], bw[wq][nt][1]);
           }
         }
       }
     }
-    __syncthreads();
+    __syncthreads();  // the stage is refilled by a later issue
   }
-  // acc[nt]: (token tb + g, rows rb + 8 nt + 2 t4, +1), (token tb + g + 8, same rows)
-  const int tb = 16 * (warp & 1), rb = 16 * (warp >> 1);
+  // acc[mt][nt]: (token tb + 16 mt + g, rows rb + 8 nt + 2 t4, +1), (token + 8, same rows)
   float* pz = part + size_t(blockIdx.z) * J.T * nrows;
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+  for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int tok = t0 + tb + g + 8 * (i >> 1);
-      const int row = r0 + rb + 8 * nt + 2 * t4 + (i & 1);
-      if (tok < J.T && row < nrows) pz[size_t(tok) * nrows + row] = acc[nt][i];
-    }
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int tok = t0 + tb + 16 * mt + g + 8 * (i >> 1);
+        const int row = r0 + rb + 8 * nt + 2 * t4 + (i & 1);
+        if (tok < J.T && row < nrows) pz[size_t(tok) * nrows + row] = acc[mt][nt][i];
+      }
 }
 
 // logits = the k-slices' sums added in slice order, plus the bias
@@ -206,9 +282,15 @@ cudaError_t launch_router(const RouterJob& J, cudaStream_t st) {
   const int KS = router_ks(J.H);
   if (KS == 0) return cudaErrorInvalidValue;
   const int rows = J.E + (J.gq ? 1 : 0);
-  if (J.T > kRouterTensorMin && J.part && J.H % (kRtK * kRtSplit) == 0) {
+  if (J.T > kRouterTensorMin && J.part && J.split && J.H % (kRtK * kRtSplit) == 0) {
+    const long n_split = long(rows) * (J.H / 4) + (J.f16 ? long(J.T) * (J.H / 4) : 0);
+    k_router_split<<<unsigned((n_split + 255) / 256), 256, 0, st>>>(J, J.split,
+                                                                    J.split + 3 * size_t(rows) * J.H);
+    const int smem = kRtStages * router_stage_elems(J) * 2;
+    const cudaError_t e = ensure_dynamic_smem((const void*)k_router_tc, smem);
+    if (e != cudaSuccess) return e;
     k_router_tc<<<dim3((J.T + kRtTok - 1) / kRtTok, (rows + kRtRows - 1) / kRtRows, kRtSplit), 128,
-                  0, st>>>(J, J.part);
+                  smem, st>>>(J, J.split, J.split + 3 * size_t(rows) * J.H, J.part);
     const long n = long(J.T) * rows;
     k_router_sum<<<unsigned((n + 255) / 256), 256, 0, st>>>(J, J.part);
   } else
