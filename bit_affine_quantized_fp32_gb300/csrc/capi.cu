@@ -435,17 +435,27 @@ moe_status experts_run(const moe_expert_bank* experts, const moe_expert_bank* sh
     int* te = reinterpret_cast<int*>(wsp(ws, L.pt_e));
     int* to = reinterpret_cast<int*>(wsp(ws, L.pt_off));
     int* tc = reinterpret_cast<int*>(wsp(ws, L.pt_cnt));
-    MOE_CUDA(launch_subslots(bucket_offsets, E, nt, te, to, tc, stream, kPfTile, kPfLight),
-             "tile kernel");
     int* nss = reinterpret_cast<int*>(wsp(ws, L.nss));
     int* se = reinterpret_cast<int*>(wsp(ws, L.ss_e));
     int* so = reinterpret_cast<int*>(wsp(ws, L.ss_off));
     int* sc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
-    MOE_CUDA(launch_subslots(bucket_offsets, E, nss, se, so, sc, stream, kMaxTok, 0, kPfLight),
-             "sub-slot kernel");
+    MOE_CUDA(launch_subslots_pair(bucket_offsets, E, kPfLight, SubslotTable{nt, te, to, tc},
+                                  kPfTile, SubslotTable{nss, se, so, sc}, kMaxTok, stream),
+             "tile and sub-slot kernel");
     const MatGeo g13 = geo13(experts), g2 = geo2(experts);
-    const uint16_t* xa = nullptr;
-    if ((s = prefill_act(x, f16, T, H, ws, L, &xa, stream))) return s;
+    // the fp16 operand rows and the per-64-group sums of x (decode units)
+    float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
+    const uint16_t* xa = static_cast<const uint16_t*>(x);
+    if (f16) {
+      MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, true, g13.t, xsum, stream),
+               "activation sums");
+    } else {
+      uint16_t* xh = reinterpret_cast<uint16_t*>(wsp(ws, L.xh));
+      MOE_CUDA(launch_xsum_f16(static_cast<const uint16_t*>(x), T, H, g13.t, xsum, xh,
+                               static_cast<int*>(ws), stream),
+               "activation sums and conversion");
+      xa = xh;
+    }
     PrefillJob J{};
     J.g = g13.t;
     J.base = g13.base;
@@ -485,9 +495,6 @@ moe_status experts_run(const moe_expert_bank* experts, const moe_expert_bank* sh
       D.sh_y = const_cast<float*>(y_shared);
     }
     MOE_CUDA(launch_prefill(D, 1, sm_count(), stream), "prefill down kernel");
-    float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
-    MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, f16, g13.t, xsum, stream),
-             "activation sums");
     const SubSlots ss{nss, se, so, sc, 0, 0};
     s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
                  bucket_perm, top_k, reinterpret_cast<uint16_t*>(wsp(ws, L.hh)),

@@ -36,6 +36,10 @@ struct UnitJob {
 cudaError_t launch_units(const UnitJob& J, bool f16a, int sms, cudaStream_t st);
 cudaError_t launch_xsum(const uint16_t* x, int T, int H, bool f16, const TileGeo& g13,
                         float* xsum, cudaStream_t st);
+// launch_xsum over bf16 activations that also writes their fp16 copy xh
+// (MOE_ERR_RANGE in *status for a value outside fp16's range)
+cudaError_t launch_xsum_f16(const uint16_t* x, int T, int H, const TileGeo& g13, float* xsum,
+                            uint16_t* xh, int* status, cudaStream_t st);
 
 struct CombineArgs {
   const float* y;    // [2][T*k][H] k-half planes
@@ -102,6 +106,18 @@ cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offs
 // more than cmin and at most cmax assignments.
 cudaError_t launch_subslots(const int32_t* offsets, int E, int* nss, int* se, int* so, int* sc,
                             cudaStream_t st, int run = kMaxTok, int cmin = 0, int cmax = 1 << 30);
+// A sub-slot table in device memory: count, then expert / first position /
+// rows of each entry.
+struct SubslotTable {
+  int* n;
+  int* e;
+  int* off;
+  int* cnt;
+};
+// Table A: runs of run_a positions of the experts with more than `split`
+// assignments; table B: runs of run_b of the experts with 1..split.
+cudaError_t launch_subslots_pair(const int32_t* offsets, int E, int split, const SubslotTable& A,
+                                 int run_a, const SubslotTable& B, int run_b, cudaStream_t st);
 
 // formats
 cudaError_t launch_pack(int fmt, const uint8_t* codes, int rows, int cols, uint32_t* packed,

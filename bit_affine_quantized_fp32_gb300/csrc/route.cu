@@ -44,6 +44,17 @@ __global__ void __launch_bounds__(256) k_subslots(const int32_t* __restrict__ of
   subslots_cta(offsets, E, nss, se, so, sc, wcount, run, cmin, cmax);
 }
 
+// Both tables of a prefill call in one launch: runs of `run_a` positions of
+// the experts with more than `split` assignments, runs of `run_b` of the
+// others (as two k_subslots launches).
+__global__ void __launch_bounds__(256) k_subslots_pair(const int32_t* __restrict__ offsets, int E,
+                                                       int split, SubslotTable A, int run_a,
+                                                       SubslotTable B, int run_b) {
+  __shared__ int wcount[8];
+  subslots_cta(offsets, E, A.n, A.e, A.off, A.cnt, wcount, run_a, split, 1 << 30);
+  subslots_cta(offsets, E, B.n, B.e, B.off, B.cnt, wcount, run_b, 0, split);
+}
+
 // ---------------------------------------------------------------------------
 // Router logits of a prefill window on the tensor cores: a dense contraction
 // logits[T, E + 1] = x[T, H] * W[E + 1, H]^T (row E the shared-gate row).
@@ -314,6 +325,12 @@ cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offs
 cudaError_t launch_subslots(const int32_t* offsets, int E, int* nss, int* se, int* so, int* sc,
                             cudaStream_t st, int run, int cmin, int cmax) {
   k_subslots<<<1, 256, 0, st>>>(offsets, E, nss, se, so, sc, run, cmin, cmax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_subslots_pair(const int32_t* offsets, int E, int split, const SubslotTable& A,
+                                 int run_a, const SubslotTable& B, int run_b, cudaStream_t st) {
+  k_subslots_pair<<<1, 256, 0, st>>>(offsets, E, split, A, run_a, B, run_b);
   return cudaGetLastError();
 }
 

@@ -86,6 +86,28 @@ __global__ void k_xsum(const uint16_t* __restrict__ x, int T, int H, int f16, Ti
   xsum_task(x, H, f16 != 0, g13, xsum, task);
 }
 
+// xsum_task over bf16 activations plus their fp16 copy (exact in fp16's
+// normal range; a value beyond it sets MOE_ERR_RANGE): lane l of the warp of
+// (token, 128 columns) converts the 4 columns it sums.
+__global__ void k_xsum_f16(const uint16_t* __restrict__ x, int T, int H, TileGeo g13,
+                           float* __restrict__ xsum, uint16_t* __restrict__ xh, int* status) {
+  const int task = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (task >= T * (H >> 7)) return;
+  xsum_task(x, H, false, g13, xsum, task);
+  const int lane = threadIdx.x & 31, nb = H >> 7;
+  const int t = task / nb, q = task - t * nb;
+  const size_t at = (size_t)t * H + q * 128 + 4 * lane;
+  const uint2 v = *reinterpret_cast<const uint2*>(x + at);
+  const float f0 = __uint_as_float(v.x << 16), f1 = __uint_as_float(v.x & 0xFFFF0000u);
+  const float f2 = __uint_as_float(v.y << 16), f3 = __uint_as_float(v.y & 0xFFFF0000u);
+  const __half2 h01 = __floats2half2_rn(f0, f1), h23 = __floats2half2_rn(f2, f3);
+  *reinterpret_cast<uint2*>(xh + at) = make_uint2(*reinterpret_cast<const uint32_t*>(&h01),
+                                                  *reinterpret_cast<const uint32_t*>(&h23));
+  if (!(fabsf(f0) <= 65504.f) || !(fabsf(f1) <= 65504.f) || !(fabsf(f2) <= 65504.f) ||
+      !(fabsf(f3) <= 65504.f))
+    atomicExch(status, int(MOE_ERR_RANGE));
+}
+
 // The combine of combine_rows, element for element the same arithmetic, laid
 // out for streaming: a block takes kCmbTok tokens x kCmbCols columns; the
 // tokens' slot weights (bf16-rounded in the chain), the second-plane flags and
@@ -239,6 +261,14 @@ cudaError_t launch_xsum(const uint16_t* x, int T, int H, bool f16, const TileGeo
   const int tasks = T * (H >> 7);
   if (tasks <= 0) return cudaSuccess;
   k_xsum<<<(tasks + 7) / 8, 256, 0, st>>>(x, T, H, f16 ? 1 : 0, g13, xsum);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_xsum_f16(const uint16_t* x, int T, int H, const TileGeo& g13, float* xsum,
+                            uint16_t* xh, int* status, cudaStream_t st) {
+  const int tasks = T * (H >> 7);
+  if (tasks <= 0) return cudaSuccess;
+  k_xsum_f16<<<(tasks + 7) / 8, 256, 0, st>>>(x, T, H, g13, xsum, xh, status);
   return cudaGetLastError();
 }
 
