@@ -269,12 +269,17 @@ def step_flops(cfg: dict, T: int) -> float:
 
 def launches_per_step(cfg: dict, T: int) -> int:
     # one persistent launch per decode call (T <= 32); the prefill form:
-    # routing (router, top-k, bucket), the shared expert's two tensor-core
-    # GEMMs, tiles and sub-slots (2), the routed tensor-core GEMMs (2),
-    # activation sums, decode units for the light experts (2), combine
+    # routing (weight split, tensor-core router, top-k, bucket), the tile and
+    # sub-slot tables (1), activation sums with the fp16 copy (1), the
+    # tensor-core gate/up and down GEMMs (2; the shared expert folded in when
+    # it has the experts' format, else its own conversion and two GEMMs), the
+    # decode units of the light experts (2) and the combine (1)
     if T <= 32:
         return 1
-    return 3 + (2 if cfg["shared_fmt"] else 0) + 8
+    n = 4 + 1 + 1 + 2 + 2 + 1
+    if cfg["shared_fmt"] and cfg["shared_fmt"] != cfg["expert_fmt"]:
+        n += 3
+    return n
 
 
 def measure(name: str, steps: int, warmup: int, nbanks: int, ws_world: int, rank: int,
@@ -505,12 +510,18 @@ def metric_name(T: int, fmt: str) -> str:
                                                T, fmt)
 
 
+def dtype_of(T: int, act: str) -> str:
+    # the decode form multiplies the activations as given; the prefill GEMMs
+    # take fp16 operands
+    return act if T <= 32 else "f16"
+
+
 def arith_note(T: int, act: str) -> str:
     if T <= 32:
         return ("%s activations times the exact integer codes (mma.sync), fp32 accumulation, "
                 "per-group scale and bias in fp32" % act)
-    return ("dequantised weights and h as 16-bit hi + lo parts (tcgen05), fp32 accumulation "
-            "in tensor memory")
+    return ("fp16 operands (weights fp16(s*q+b) rounded once, x and h in fp16) on tcgen05 "
+            "with fp32 accumulation in tensor memory; exact-product bf16-split router")
 
 
 def run_gpu(args, ws_world, rank, local):
@@ -533,6 +544,8 @@ def run_gpu(args, ws_world, rank, local):
         others[name] = {"metric": metric_name(r["T"], r["cfg"]["expert_fmt"]),
                         "value": round(r["value"], 1), "unit": "tokens/s",
                         "ms_per_step": round(r["ms_per_step"], 6), "steps": n,
+                        "dtype": dtype_of(r["T"], r["cfg"]["act"]),
+                        "arith": arith_note(r["T"], r["cfg"]["act"]),
                         "roofline": r["roofline"], "e2e": r["e2e"],
                         "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
                         "config": r["config"]}
@@ -547,7 +560,7 @@ def run_gpu(args, ws_world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": head["cfg"]["act"],
+        "dtype": dtype_of(head["T"], head["cfg"]["act"]),
         "arith": arith_note(head["T"], head["cfg"]["act"]),
         "data": "synthetic (seeded; random-init weights of the layer's shapes)",
         "config": head["config"],

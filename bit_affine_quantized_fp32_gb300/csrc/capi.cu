@@ -695,10 +695,8 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
   R.round_bf16 = rb;
   R.part = T > MOE_DECODE_MAX_TOKENS ? reinterpret_cast<float*>(wsp(ws, L.rpart)) : nullptr;
   R.split = T > MOE_DECODE_MAX_TOKENS ? reinterpret_cast<uint16_t*>(wsp(ws, L.rsplit)) : nullptr;
-  MOE_CUDA(launch_router(R, stream), "router kernel");
-  MOE_CUDA(launch_topk(lg, shared_gate ? gl : nullptr, T, E, top_k, topk_idx, topk_w,
-                       shared_gate ? shared_gate_w : nullptr, rb, stream),
-           "top-k kernel");
+  MOE_CUDA(launch_router_topk(R, top_k, topk_idx, topk_w, shared_gate_w, rb, stream),
+           "router and top-k kernels");
   MOE_CUDA(launch_bucket(topk_idx, T, top_k, E, bucket_offsets, bucket_perm, stream),
            "bucket kernel");
   return ok();

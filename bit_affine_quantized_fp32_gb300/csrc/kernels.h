@@ -96,8 +96,14 @@ struct RouterJob {
 inline size_t router_split_elems(long T, long E, long H) { return size_t(3 * (E + 1) * H + 2 * T * H); }
 int router_ks(int H);
 int router_blocks(int E, bool gate, int H);
+// the SIMT router (logits and gate logit of every token)
 cudaError_t launch_router(const RouterJob& J, cudaStream_t st);
 // round_bf16: slot weights bf16(w) and shared weight bf16(sigmoid(bf16(g)))
+// launch_router then launch_topk (same results); above 32 tokens the
+// tensor-core router's k-slice sums feed the top-k directly (logits and gate
+// logit still written).  sg is used only with a gate row.
+cudaError_t launch_router_topk(const RouterJob& J, int k, int32_t* idx, float* w, float* sg,
+                               bool round_bf16, cudaStream_t st);
 cudaError_t launch_topk(const float* logits, const float* gate_logit, int T, int E, int k,
                         int32_t* idx, float* w, float* sg, bool round_bf16, cudaStream_t st);
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets,

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(256) k_subslots_pair(const int32_t* __restrict
 // (two 8-row n-tiles): four accumulator chains, each fragment loaded once
 // for two or three MMAs.
 constexpr int kRtTok = 64, kRtRows = 32, kRtK = 64, kRtPitch = kRtK + 8;  // bf16 elements
-constexpr int kRtSplit = 4;   // k-slices per tile, summed in order by k_router_sum
+constexpr int kRtSplit = 4;   // k-slices per tile, summed in order by k_topk_parts
 constexpr int kRtStages = 4;  // chunks in flight per block
 constexpr int kRtXPart = kRtTok * kRtPitch;   // elements of one x-part tile
 constexpr int kRtWPart = kRtRows * kRtPitch;  // elements of one weight-part tile
@@ -253,20 +253,40 @@ __global__ void __launch_bounds__(128) k_router_tc(const RouterJob J, const uint
       }
 }
 
-// logits = the k-slices' sums added in slice order, plus the bias
-__global__ void k_router_sum(const RouterJob J, const float* __restrict__ part) {
+// Top-k of token t (one warp) from the k-slice sums: each logit is the
+// slices' sums added in slice order, plus the bias; it is written to
+// J.logits (and the gate logit to J.gate_logit) on the way.
+__global__ void k_topk_parts(const RouterJob J, const float* __restrict__ part, int k,
+                             int32_t* __restrict__ idx, float* __restrict__ w,
+                             float* __restrict__ sg, int rb) {
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= J.T) return;
+  const int lane = threadIdx.x & 31;
   const int nrows = J.E + (J.gq ? 1 : 0);
-  const long i = long(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= long(J.T) * nrows) return;
-  const int tok = int(i / nrows), row = int(i - long(tok) * nrows);
   const size_t stride = size_t(J.T) * nrows;
-  float v = part[i];
+  const float* row = part + size_t(t) * nrows;
+  unsigned long long key[8];
 #pragma unroll
-  for (int z = 1; z < kRtSplit; ++z) v += part[i + z * stride];
-  if (row < J.E)
-    J.logits[size_t(tok) * J.E + row] = v + (J.bias ? J.bias[row] : 0.f);
-  else
-    J.gate_logit[tok] = v;
+  for (int i = 0; i < 8; ++i) {
+    const int e = 8 * lane + i;
+    key[i] = 0ull;
+    if (e < J.E) {
+      float v = __ldcg(row + e);
+#pragma unroll
+      for (int z = 1; z < kRtSplit; ++z) v += __ldcg(row + z * stride + e);
+      v = v + (J.bias ? J.bias[e] : 0.f);
+      J.logits[size_t(t) * J.E + e] = v;
+      key[i] = rank_key(v, e);
+    }
+  }
+  float gl = 0.f;
+  if (J.gq) {
+    gl = __ldcg(row + J.E);
+#pragma unroll
+    for (int z = 1; z < kRtSplit; ++z) gl += __ldcg(row + z * stride + J.E);
+    if (lane == 0) J.gate_logit[t] = gl;
+  }
+  topk_select(key, t, k, idx, w, sg, J.gq != nullptr, gl, nullptr, nullptr, rb != 0);
 }
 
 }  // namespace
@@ -293,7 +313,19 @@ cudaError_t launch_router(const RouterJob& J, cudaStream_t st) {
   const int KS = router_ks(J.H);
   if (KS == 0) return cudaErrorInvalidValue;
   const int rows = J.E + (J.gq ? 1 : 0);
-  if (J.T > kRouterTensorMin && J.part && J.split && J.H % (kRtK * kRtSplit) == 0) {
+  k_router<1><<<dim3(rows, (J.T + kRouterTT - 1) / kRouterTT), 32 * KS, 0, st>>>(J, KS);
+  return cudaGetLastError();
+}
+
+// Router and top-k: above kRouterTensorMin tokens (with the scratch) the
+// tensor-core router's k-slice sums go straight into the top-k, else the SIMT
+// router's logits through k_topk.
+cudaError_t launch_router_topk(const RouterJob& J, int k, int32_t* idx, float* w, float* sg,
+                               bool round_bf16, cudaStream_t st) {
+  if (J.T <= 0) return cudaSuccess;
+  const int rows = J.E + (J.gq ? 1 : 0);
+  if (J.T > kRouterTensorMin && J.part && J.split && J.H % (kRtK * kRtSplit) == 0 &&
+      router_ks(J.H) != 0) {
     const long n_split = long(rows) * (J.H / 4) + (J.f16 ? long(J.T) * (J.H / 4) : 0);
     k_router_split<<<unsigned((n_split + 255) / 256), 256, 0, st>>>(J, J.split,
                                                                     J.split + 3 * size_t(rows) * J.H);
@@ -302,11 +334,14 @@ cudaError_t launch_router(const RouterJob& J, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     k_router_tc<<<dim3((J.T + kRtTok - 1) / kRtTok, (rows + kRtRows - 1) / kRtRows, kRtSplit), 128,
                   smem, st>>>(J, J.split, J.split + 3 * size_t(rows) * J.H, J.part);
-    const long n = long(J.T) * rows;
-    k_router_sum<<<unsigned((n + 255) / 256), 256, 0, st>>>(J, J.part);
-  } else
-    k_router<1><<<dim3(rows, (J.T + kRouterTT - 1) / kRouterTT), 32 * KS, 0, st>>>(J, KS);
-  return cudaGetLastError();
+    k_topk_parts<<<(J.T + 7) / 8, 256, 0, st>>>(J, J.part, k, idx, w, J.gq ? sg : nullptr,
+                                                round_bf16 ? 1 : 0);
+    return cudaGetLastError();
+  }
+  cudaError_t e = launch_router(J, st);
+  if (e != cudaSuccess) return e;
+  return launch_topk(J.logits, J.gq ? J.gate_logit : nullptr, J.T, J.E, k, idx, w,
+                     J.gq ? sg : nullptr, round_bf16, st);
 }
 
 cudaError_t launch_topk(const float* logits, const float* gate_logit, int T, int E, int k,
