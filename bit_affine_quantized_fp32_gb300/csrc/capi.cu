@@ -80,6 +80,41 @@ cudaError_t ensure_dynamic_smem(const void* func, int bytes) {
   return cudaSuccess;
 }
 
+// A second stream with fork and join events, per CUDA context and caller
+// stream, for the part of a call that may run beside the work on the
+// caller's stream (fork: an event on the caller's stream that the side
+// stream waits for; join: the reverse).  Created on first use and kept for
+// the life of the process; the events carry no timing.
+struct SideStream {
+  cudaStream_t s;
+  cudaEvent_t fork, join;
+};
+
+cudaError_t side_stream(cudaStream_t user, SideStream* out) {
+  struct Entry {
+    unsigned long long ctx;
+    cudaStream_t user;
+    SideStream side;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  const unsigned long long ctx = current_context_id();
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (e.ctx == ctx && e.user == user) {
+      *out = e.side;
+      return cudaSuccess;
+    }
+  SideStream side{};
+  cudaError_t err = cudaStreamCreateWithFlags(&side.s, cudaStreamNonBlocking);
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&side.fork, cudaEventDisableTiming);
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&side.join, cudaEventDisableTiming);
+  if (err != cudaSuccess) return err;
+  cache.push_back(Entry{ctx ? ctx : current_context_id(), user, side});
+  *out = side;
+  return cudaSuccess;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -456,6 +491,23 @@ moe_status experts_run(const moe_expert_bank* experts, const moe_expert_bank* sh
                "activation sums and conversion");
       xa = xh;
     }
+    // the light experts (decode units, y planes 0 and 1 of their own rows, h
+    // rows of their own bucket positions) on a side stream, beside the
+    // tensor-core GEMMs of the others; joined before the combine
+    SideStream side{};
+    MOE_CUDA(side_stream(stream, &side), "side stream");
+    MOE_CUDA(cudaEventRecord(side.fork, stream), "fork event");
+    MOE_CUDA(cudaStreamWaitEvent(side.s, side.fork, 0), "fork wait");
+    {
+      const SubSlots ss{nss, se, so, sc, 0, 0};
+      s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
+                   bucket_perm, top_k, reinterpret_cast<uint16_t*>(wsp(ws, L.hh)),
+                   reinterpret_cast<uint16_t*>(wsp(ws, L.hl)),
+                   reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr, y, yhalf, kRowsScatter,
+                   static_cast<int*>(ws), side.s);
+      if (s) return s;
+    }
+    MOE_CUDA(cudaEventRecord(side.join, side.s), "join event");
     PrefillJob J{};
     J.g = g13.t;
     J.base = g13.base;
@@ -495,13 +547,7 @@ moe_status experts_run(const moe_expert_bank* experts, const moe_expert_bank* sh
       D.sh_y = const_cast<float*>(y_shared);
     }
     MOE_CUDA(launch_prefill(D, 1, sm_count(), stream), "prefill down kernel");
-    const SubSlots ss{nss, se, so, sc, 0, 0};
-    s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
-                 bucket_perm, top_k, reinterpret_cast<uint16_t*>(wsp(ws, L.hh)),
-                 reinterpret_cast<uint16_t*>(wsp(ws, L.hl)),
-                 reinterpret_cast<float*>(wsp(ws, L.hsum)), nullptr, y, yhalf, kRowsScatter,
-                 static_cast<int*>(ws), stream);
-    if (s) return s;
+    MOE_CUDA(cudaStreamWaitEvent(stream, side.join, 0), "join wait");
     CombineArgs C{};
     C.y = y;
     C.yhalf = yhalf;
