@@ -160,7 +160,10 @@ typedef struct moe_expert_bank {
  * the activations converted to fp16 (exact within fp16's normal range), h
  * stored as fp16 -- and fp32 accumulation: the same values to within the
  * layer's tolerance, not the same bits as the decode form.  Experts with at
- * most 40 assignments in the call run the decode form's units. */
+ * most 16 assignments in the call run the decode form's units, on a second
+ * stream (one per CUDA context and caller stream, created on first use)
+ * that forks from the caller's stream with an event and joins it again
+ * before the combine, so the call stays capturable in a CUDA graph. */
 #define MOE_DECODE_MAX_TOKENS 32
 
 /* Human-readable name of a status; never NULL. */
@@ -219,6 +222,11 @@ moe_status moe_get_device_status(void* ws, size_t ws_bytes, int* device_status,
  *   logits       nullable [T, E] fp32 output
  *   topk_idx [T, k] int32, topk_w [T, k] fp32, shared_gate_w nullable [T]
  *   flags        0 or MOE_FLAG_ROUND_BF16 (the engine's bf16 rounding chain)
+ * Above MOE_DECODE_MAX_TOKENS the logits come from the tensor cores: each
+ * router (and gate) weight split exactly into three bf16 parts, fp16
+ * activations into two, so every product is exact and the sums are fp32
+ * (four k-slices added in order); below it a SIMT fp32 dot product.  Both
+ * lie within the fp32 dot-product bound of the exact logits.
  */
 moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
                      const moe_qmatrix* shared_gate, const void* x, int act, int n_tokens,
@@ -308,7 +316,9 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
  * cooperative launch (one CTA per SM) whose phases synchronise through
  * counters in the workspace; every wait is bounded and reports
  * MOE_ERR_TIMEOUT in the workspace status word instead of hanging.  The
- * results are bit-identical to the multi-launch path (MOE_FLAG_UNFUSED). */
+ * results are bit-identical to the multi-launch path (MOE_FLAG_UNFUSED).
+ * Above it, a shared expert of the routed experts' format runs inside the
+ * routed experts' two tensor-core GEMM launches (its units first). */
 moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
                              const moe_qmatrix* shared_gate, const moe_expert_bank* experts,
                              const moe_expert_bank* shared, const void* x, int act,
