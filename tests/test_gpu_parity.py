@@ -584,9 +584,10 @@ def test_fused_alternating_shapes(capi):
 
 
 # ---------------------------------------------------------------------------
-# Prefill form (T > 32): the tcgen05 expert GEMMs with bf16 hi + lo operands
-# and fp32 accumulation; the tolerance is the layer's (the operands carry about
-# 16 significant bits, far inside it).
+# Prefill form (T > 32): the tcgen05 expert GEMMs with single fp16 operands
+# (weights fp16(s*q + b) rounded once, x and h in fp16) and fp32
+# accumulation; the tolerance is the layer's (a CPU emulation of the
+# full-size window puts the operands' rounding at about a fifth of it).
 
 PREFILL_CASES = [
     # Zipf routing: the busiest experts take more than one 128-token tile
@@ -616,6 +617,45 @@ def test_prefill_layer(capi, cfg):
     out_d, idx_d, _ = g.forward(flags=1)
     assert Hn.torch().equal(idx, idx_d)
     Hn.assert_layer_close(Hn.to_np(out_d), ref["out"], out_type=L.act)
+
+
+def test_prefill_graph_capture_with_side_stream(capi):
+    """The prefill form forks the light experts' decode units onto a side
+    stream and joins them before the combine: captured into a CUDA graph on
+    the caller's stream and replayed, the call gives the eager call's bits
+    (and the oracle's values), the light experts included."""
+    torch = Hn.torch()
+    L = synth.gen_layer(T=300, E=64, k=4, H=256, I=128, expert_fmt="affine4_g64",
+                        shared_fmt="affine4_g64", gate_fmt="affine8_g64", zipf=True, seed=46)
+    g = Hn.GpuLayer(L)
+    out, idx, w = g.forward()
+    counts = np.bincount(idx.cpu().numpy().ravel(), minlength=L.E)
+    assert ((counts > 0) & (counts <= 16)).any() and (counts > 16).any()  # both kinds
+    out_g = torch.empty_like(out)
+    idx_g = torch.empty_like(idx)
+    w_g = torch.empty_like(w)
+    from bit_affine_quantized_fp32_gb300 import capi as C
+
+    def call():
+        C.moe_layer_forward(g.router, g.bias, g.gate, g.experts, g.shared, g.x, L.k, out_g,
+                            idx_g, w_g, 0, g.ws)
+
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):  # the library's per-stream state is made outside capture
+        call()
+    cap.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        call()
+    for _ in range(3):
+        out_g.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_g, out) and torch.equal(idx_g, idx) and torch.equal(w_g, w)
+    ref = Hn.oracle_layer(L, idx_override=idx.cpu().numpy())
+    Hn.assert_layer_close(Hn.to_np(out_g), ref["out"], out_type=L.act)
+    assert capi.moe_get_device_status(g.ws) == 0
 
 
 def test_prefill_full_size(capi):
