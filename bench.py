@@ -269,17 +269,17 @@ def step_flops(cfg: dict, T: int) -> float:
 
 def launches_per_step(cfg: dict, T: int) -> int:
     # one persistent launch per decode call (T <= 32); the prefill form:
-    # routing (weight split, tensor-core router, top-k, bucket), the tile and
-    # sub-slot tables (1), activation sums with the fp16 copy (1), the
-    # tensor-core gate/up and down GEMMs (2; the shared expert folded in when
-    # it has the experts' format, else its own conversion and two GEMMs), the
-    # decode units of the light experts (2) and the combine (1)
+    # routing (weight split, tensor-core router, top-k, bucket sort with the
+    # tile and sub-slot tables), activation sums with the fp16 copy (1, on the
+    # side stream), the tensor-core gate/up and down GEMMs (2, the shared
+    # expert folded in), the decode units of the light experts (2) and the
+    # combine (1); a shared expert of another format runs its own conversion
+    # and two GEMMs, and the tables then take a launch of their own
     if T <= 32:
         return 1
-    n = 4 + 1 + 1 + 2 + 2 + 1
     if cfg["shared_fmt"] and cfg["shared_fmt"] != cfg["expert_fmt"]:
-        n += 3
-    return n
+        return 4 + 3 + 1 + 1 + 2 + 2 + 1
+    return 4 + 1 + 2 + 2 + 1
 
 
 def measure(name: str, steps: int, warmup: int, nbanks: int, ws_world: int, rank: int,

@@ -88,6 +88,7 @@ cudaError_t ensure_dynamic_smem(const void* func, int bytes) {
 struct SideStream {
   cudaStream_t s;
   cudaEvent_t fork, join;
+  cudaEvent_t xready, tables;  // the layer's early fork: x prepared (side), tables built (caller)
 };
 
 cudaError_t side_stream(cudaStream_t user, SideStream* out) {
@@ -109,6 +110,8 @@ cudaError_t side_stream(cudaStream_t user, SideStream* out) {
   cudaError_t err = cudaStreamCreateWithFlags(&side.s, cudaStreamNonBlocking);
   if (err == cudaSuccess) err = cudaEventCreateWithFlags(&side.fork, cudaEventDisableTiming);
   if (err == cudaSuccess) err = cudaEventCreateWithFlags(&side.join, cudaEventDisableTiming);
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&side.xready, cudaEventDisableTiming);
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&side.tables, cudaEventDisableTiming);
   if (err != cudaSuccess) return err;
   cache.push_back(Entry{ctx ? ctx : current_context_id(), user, side});
   *out = side;
@@ -368,6 +371,16 @@ bool use_prefill(const moe_expert_bank* b, int T, int flags) {
          prefill_smem(geo13(b).t, 0) > 0 && prefill_smem(geo2(b).t, 1) > 0;
 }
 
+// The prefill form's activation pass: the per-64-group sums of x (decode
+// units) and, for bf16 activations, x's fp16 copy in the workspace (L.xh).
+cudaError_t launch_prepare_x(const void* x, bool f16, int T, int H, const TileGeo& g13,
+                             float* xsum, void* ws, const WsLayout& L, cudaStream_t stream) {
+  if (f16) return launch_xsum(static_cast<const uint16_t*>(x), T, H, true, g13, xsum, stream);
+  return launch_xsum_f16(static_cast<const uint16_t*>(x), T, H, g13, xsum,
+                         reinterpret_cast<uint16_t*>(wsp(ws, L.xh)), static_cast<int*>(ws),
+                         stream);
+}
+
 // The shared expert joins the routed experts' prefill launches when both
 // take the prefill form with one tiled geometry (same format; the shapes
 // are equal by the layer's checks).
@@ -455,7 +468,8 @@ moe_status experts_run(const moe_expert_bank* experts, const moe_expert_bank* sh
                        const float* topk_w, const int32_t* bucket_offsets,
                        const int32_t* bucket_perm, const float* y_shared,
                        const float* shared_gate_w, void* out, int flags, void* ws,
-                       const WsLayout& L, cudaStream_t stream) {
+                       const WsLayout& L, cudaStream_t stream,
+                       const SideStream* early = nullptr) {
   moe_status s;
   const int E = experts->n_experts, H = experts->hidden, I = experts->inter;
   const bool rb = (flags & MOE_FLAG_ROUND_BF16) != 0;
@@ -474,30 +488,29 @@ moe_status experts_run(const moe_expert_bank* experts, const moe_expert_bank* sh
     int* se = reinterpret_cast<int*>(wsp(ws, L.ss_e));
     int* so = reinterpret_cast<int*>(wsp(ws, L.ss_off));
     int* sc = reinterpret_cast<int*>(wsp(ws, L.ss_cnt));
-    MOE_CUDA(launch_subslots_pair(bucket_offsets, E, kPfLight, SubslotTable{nt, te, to, tc},
-                                  kPfTile, SubslotTable{nss, se, so, sc}, kMaxTok, stream),
-             "tile and sub-slot kernel");
     const MatGeo g13 = geo13(experts), g2 = geo2(experts);
-    // the fp16 operand rows and the per-64-group sums of x (decode units)
     float* xsum = reinterpret_cast<float*>(wsp(ws, L.xsum));
-    const uint16_t* xa = static_cast<const uint16_t*>(x);
-    if (f16) {
-      MOE_CUDA(launch_xsum(static_cast<const uint16_t*>(x), T, H, true, g13.t, xsum, stream),
-               "activation sums");
-    } else {
-      uint16_t* xh = reinterpret_cast<uint16_t*>(wsp(ws, L.xh));
-      MOE_CUDA(launch_xsum_f16(static_cast<const uint16_t*>(x), T, H, g13.t, xsum, xh,
-                               static_cast<int*>(ws), stream),
-               "activation sums and conversion");
-      xa = xh;
-    }
+    const uint16_t* xa =
+        f16 ? static_cast<const uint16_t*>(x) : reinterpret_cast<uint16_t*>(wsp(ws, L.xh));
     // the light experts (decode units, y planes 0 and 1 of their own rows, h
     // rows of their own bucket positions) on a side stream, beside the
     // tensor-core GEMMs of the others; joined before the combine
     SideStream side{};
-    MOE_CUDA(side_stream(stream, &side), "side stream");
-    MOE_CUDA(cudaEventRecord(side.fork, stream), "fork event");
-    MOE_CUDA(cudaStreamWaitEvent(side.s, side.fork, 0), "fork wait");
+    if (early) {
+      // the layer already built the tables with the bucket sort and started
+      // the side stream on x (prepare_x_early): hand it the tables
+      side = *early;
+      MOE_CUDA(cudaEventRecord(side.tables, stream), "tables event");
+      MOE_CUDA(cudaStreamWaitEvent(side.s, side.tables, 0), "tables wait");
+    } else {
+      MOE_CUDA(launch_subslots_pair(bucket_offsets, E, kPfLight, SubslotTable{nt, te, to, tc},
+                                    kPfTile, SubslotTable{nss, se, so, sc}, kMaxTok, stream),
+               "tile and sub-slot kernel");
+      MOE_CUDA(launch_prepare_x(x, f16, T, H, g13.t, xsum, ws, L, stream), "activation sums");
+      MOE_CUDA(side_stream(stream, &side), "side stream");
+      MOE_CUDA(cudaEventRecord(side.fork, stream), "fork event");
+      MOE_CUDA(cudaStreamWaitEvent(side.s, side.fork, 0), "fork wait");
+    }
     {
       const SubSlots ss{nss, se, so, sc, 0, 0};
       s = run_bank(experts, ss, int(max_subslots(T, E, top_k)), x, f16, xsum, kRowsGather,
@@ -508,6 +521,7 @@ moe_status experts_run(const moe_expert_bank* experts, const moe_expert_bank* sh
       if (s) return s;
     }
     MOE_CUDA(cudaEventRecord(side.join, side.s), "join event");
+    if (early) MOE_CUDA(cudaStreamWaitEvent(stream, side.xready, 0), "x wait");
     PrefillJob J{};
     J.g = g13.t;
     J.base = g13.base;
@@ -600,6 +614,78 @@ moe_status experts_run(const moe_expert_bank* experts, const moe_expert_bank* sh
   C.round_bf16 = rb;
   MOE_CUDA(launch_combine(C, stream), "combine kernel");
   return ok();
+}
+
+// moe_route's argument checks (router, gate, activations, sizes).
+moe_status route_check(const moe_qmatrix* router, const moe_qmatrix* shared_gate, const void* x,
+                       int act, int T, int top_k) {
+  moe_status s;
+  const int E = router->rows, H = router->cols;
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "n_tokens=%d < 0", T);
+  if (E < 1 || E > 256) return fail(MOE_ERR_INVALID_ARG, "router rows (experts)=%d not in 1..256", E);
+  if (top_k < 1 || top_k > 8 || top_k > E)
+    return fail(MOE_ERR_INVALID_ARG, "top_k=%d not in 1..min(8, experts)", top_k);
+  if ((s = check_hidden(H))) return s;
+  if ((s = check_router_matrix(router, "router", E, H))) return s;
+  if (shared_gate && (s = check_router_matrix(shared_gate, "shared_gate", 1, H))) return s;
+  if ((s = check_act(act))) return s;
+  if (T > 0 && !x) return fail(MOE_ERR_INVALID_ARG, "x is NULL");
+  if (x && !aligned16(x)) return fail(MOE_ERR_MISALIGNED, "x not 16-byte aligned");
+  return MOE_OK;
+}
+
+// The prefill form's tile and sub-slot tables, built by the bucket launch.
+struct PrefillTables {
+  int split;
+  SubslotTable A;
+  int run_a;
+  SubslotTable B;
+  int run_b;
+};
+
+// moe_route's launches (checked arguments) on workspace layout L: router and
+// top-k, then the bucket sort (with `tables`, also the prefill tables).
+moe_status route_run(const moe_qmatrix* router, const float* logit_bias,
+                     const moe_qmatrix* shared_gate, const void* x, bool f16, int T, int top_k,
+                     float* logits, int32_t* topk_idx, float* topk_w, float* shared_gate_w,
+                     int32_t* bucket_offsets, int32_t* bucket_perm, bool rb, void* ws,
+                     const WsLayout& L, const PrefillTables* tables, cudaStream_t stream) {
+  const int E = router->rows, H = router->cols;
+  float* lg = logits ? logits : reinterpret_cast<float*>(wsp(ws, L.logits));
+  float* gl = reinterpret_cast<float*>(wsp(ws, L.gate_logit));
+  RouterJob R{};
+  R.fmt = router->fmt;
+  R.q = router->qweight;
+  R.s = static_cast<const uint16_t*>(router->scales);
+  R.b = static_cast<const uint16_t*>(router->biases);
+  if (shared_gate) {
+    R.gfmt = shared_gate->fmt;
+    R.gq = shared_gate->qweight;
+    R.gs = static_cast<const uint16_t*>(shared_gate->scales);
+    R.gb = static_cast<const uint16_t*>(shared_gate->biases);
+  }
+  R.bias = logit_bias;
+  R.x = static_cast<const uint16_t*>(x);
+  R.f16 = f16;
+  R.T = T;
+  R.E = E;
+  R.H = H;
+  R.logits = lg;
+  R.gate_logit = gl;
+  R.round_bf16 = rb;
+  R.part = T > MOE_DECODE_MAX_TOKENS ? reinterpret_cast<float*>(wsp(ws, L.rpart)) : nullptr;
+  R.split = T > MOE_DECODE_MAX_TOKENS ? reinterpret_cast<uint16_t*>(wsp(ws, L.rsplit)) : nullptr;
+  MOE_CUDA(launch_router_topk(R, top_k, topk_idx, topk_w, shared_gate_w, rb, stream),
+           "router and top-k kernels");
+  if (tables)
+    MOE_CUDA(launch_bucket_tables(topk_idx, T, top_k, E, bucket_offsets, bucket_perm,
+                                  tables->split, tables->A, tables->run_a, tables->B,
+                                  tables->run_b, stream),
+             "bucket and table kernel");
+  else
+    MOE_CUDA(launch_bucket(topk_idx, T, top_k, E, bucket_offsets, bucket_perm, stream),
+             "bucket kernel");
+  return MOE_OK;
 }
 
 }  // namespace
@@ -697,18 +783,8 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
   moe_status s;
   if (!router) return fail(MOE_ERR_INVALID_ARG, "router is NULL");
   if (flags & ~MOE_FLAG_ROUND_BF16) return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
-  const bool rb = (flags & MOE_FLAG_ROUND_BF16) != 0;
   const int E = router->rows, H = router->cols, T = n_tokens;
-  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "n_tokens=%d < 0", T);
-  if (E < 1 || E > 256) return fail(MOE_ERR_INVALID_ARG, "router rows (experts)=%d not in 1..256", E);
-  if (top_k < 1 || top_k > 8 || top_k > E)
-    return fail(MOE_ERR_INVALID_ARG, "top_k=%d not in 1..min(8, experts)", top_k);
-  if ((s = check_hidden(H))) return s;
-  if ((s = check_router_matrix(router, "router", E, H))) return s;
-  if (shared_gate && (s = check_router_matrix(shared_gate, "shared_gate", 1, H))) return s;
-  if ((s = check_act(act))) return s;
-  if (T > 0 && !x) return fail(MOE_ERR_INVALID_ARG, "x is NULL");
-  if (x && !aligned16(x)) return fail(MOE_ERR_MISALIGNED, "x not 16-byte aligned");
+  if ((s = route_check(router, shared_gate, x, act, T, top_k))) return s;
   if (!bucket_offsets || (T > 0 && (!topk_idx || !topk_w || !bucket_perm)))
     return fail(MOE_ERR_INVALID_ARG, "routing outputs must not be NULL");
   const WsLayout L = ws_layout(T, E, top_k, H, 128);
@@ -717,35 +793,10 @@ moe_status moe_route(const moe_qmatrix* router, const float* logit_bias,
   if ((s = check_ws(ws, ws_bytes,
                     T > MOE_DECODE_MAX_TOKENS ? L.rsplit + 2 * router_split_elems(T, E, H) : L.idx)))
     return s;
-  float* lg = logits ? logits : reinterpret_cast<float*>(wsp(ws, L.logits));
-  float* gl = reinterpret_cast<float*>(wsp(ws, L.gate_logit));
-  RouterJob R{};
-  R.fmt = router->fmt;
-  R.q = router->qweight;
-  R.s = static_cast<const uint16_t*>(router->scales);
-  R.b = static_cast<const uint16_t*>(router->biases);
-  if (shared_gate) {
-    R.gfmt = shared_gate->fmt;
-    R.gq = shared_gate->qweight;
-    R.gs = static_cast<const uint16_t*>(shared_gate->scales);
-    R.gb = static_cast<const uint16_t*>(shared_gate->biases);
-  }
-  R.bias = logit_bias;
-  R.x = static_cast<const uint16_t*>(x);
-  R.f16 = act == MOE_FMT_F16;
-  R.T = T;
-  R.E = E;
-  R.H = H;
-  R.logits = lg;
-  R.gate_logit = gl;
-  R.round_bf16 = rb;
-  R.part = T > MOE_DECODE_MAX_TOKENS ? reinterpret_cast<float*>(wsp(ws, L.rpart)) : nullptr;
-  R.split = T > MOE_DECODE_MAX_TOKENS ? reinterpret_cast<uint16_t*>(wsp(ws, L.rsplit)) : nullptr;
-  MOE_CUDA(launch_router_topk(R, top_k, topk_idx, topk_w, shared_gate_w, rb, stream),
-           "router and top-k kernels");
-  MOE_CUDA(launch_bucket(topk_idx, T, top_k, E, bucket_offsets, bucket_perm, stream),
-           "bucket kernel");
-  return ok();
+  s = route_run(router, logit_bias, shared_gate, x, act == MOE_FMT_F16, T, top_k, logits,
+                topk_idx, topk_w, shared_gate_w, bucket_offsets, bucket_perm,
+                (flags & MOE_FLAG_ROUND_BF16) != 0, ws, L, nullptr, stream);
+  return s ? s : ok();
 }
 
 moe_status moe_expert_mlp(const moe_expert_bank* bank, int expert, const void* x, int act,
@@ -901,21 +952,47 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
   float* sgw = reinterpret_cast<float*>(wsp(ws, L.sgw));
   int32_t* offs = reinterpret_cast<int32_t*>(wsp(ws, L.offsets));
   int32_t* perm = reinterpret_cast<int32_t*>(wsp(ws, L.perm));
+  const int ef = flags & (MOE_FLAG_FORCE_DECODE | MOE_FLAG_ROUND_BF16);
+  const bool fold = shared && prefill_pair(experts, shared, T, ef);
+  if (use_prefill(experts, T, ef) && (!shared || fold)) {
+    // The prefill form in one pass over the workspace layout L: the side
+    // stream starts on x (sums and fp16 copy) at once, beside the routing,
+    // whose bucket launch also builds the tile and sub-slot tables; the
+    // experts then run with the shared expert folded into their launches.
+    if ((s = route_check(router, shared_gate, x, act, T, top_k))) return s;
+    if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x/out is NULL");
+    if (!aligned16(out)) return fail(MOE_ERR_MISALIGNED, "out must be 16-byte aligned");
+    const bool f16 = act == MOE_FMT_F16;
+    SideStream side{};
+    MOE_CUDA(side_stream(stream, &side), "side stream");
+    MOE_CUDA(cudaEventRecord(side.fork, stream), "fork event");
+    MOE_CUDA(cudaStreamWaitEvent(side.s, side.fork, 0), "fork wait");
+    MOE_CUDA(launch_prepare_x(x, f16, T, H, geo13(experts).t,
+                              reinterpret_cast<float*>(wsp(ws, L.xsum)), ws, L, side.s),
+             "activation sums");
+    MOE_CUDA(cudaEventRecord(side.xready, side.s), "x event");
+    const PrefillTables tb{
+        kPfLight,
+        SubslotTable{reinterpret_cast<int*>(wsp(ws, L.pt_n)), reinterpret_cast<int*>(wsp(ws, L.pt_e)),
+                     reinterpret_cast<int*>(wsp(ws, L.pt_off)),
+                     reinterpret_cast<int*>(wsp(ws, L.pt_cnt))},
+        kPfTile,
+        SubslotTable{reinterpret_cast<int*>(wsp(ws, L.nss)), reinterpret_cast<int*>(wsp(ws, L.ss_e)),
+                     reinterpret_cast<int*>(wsp(ws, L.ss_off)),
+                     reinterpret_cast<int*>(wsp(ws, L.ss_cnt))},
+        kMaxTok};
+    s = route_run(router, logit_bias, shared_gate, x, f16, T, top_k, nullptr, idx, w,
+                  shared_gate ? sgw : nullptr, offs, perm, (ef & MOE_FLAG_ROUND_BF16) != 0, ws, L,
+                  &tb, stream);
+    if (s) return s;
+    s = experts_run(experts, fold ? shared : nullptr, x, f16, T, top_k, idx, w, offs, perm,
+                    nullptr, fold && shared_gate ? sgw : nullptr, out, ef, ws, L, stream, &side);
+    return s ? s : ok();
+  }
   s = moe_route(router, logit_bias, shared_gate, x, act, T, top_k, nullptr, idx, w,
                 shared_gate ? sgw : nullptr, offs, perm, flags & MOE_FLAG_ROUND_BF16, ws, ws_bytes,
                 stream);
   if (s) return s;
-  const int ef = flags & (MOE_FLAG_FORCE_DECODE | MOE_FLAG_ROUND_BF16);
-  if (shared && prefill_pair(experts, shared, T, ef)) {
-    // one pair of prefill launches for the routed and the shared expert
-    if ((s = check_act(act))) return s;
-    if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x/out is NULL");
-    if (!aligned16(x) || !aligned16(out))
-      return fail(MOE_ERR_MISALIGNED, "x/out must be 16-byte aligned");
-    s = experts_run(experts, shared, x, act == MOE_FMT_F16, T, top_k, idx, w, offs, perm,
-                    nullptr, shared_gate ? sgw : nullptr, out, ef, ws, L, stream);
-    return s ? s : ok();
-  }
   float* ysh = nullptr;
   if (shared) {
     ysh = reinterpret_cast<float*>(wsp(ws, L.ysh));

@@ -124,6 +124,10 @@ struct SubslotTable {
 // assignments; table B: runs of run_b of the experts with 1..split.
 cudaError_t launch_subslots_pair(const int32_t* offsets, int E, int split, const SubslotTable& A,
                                  int run_a, const SubslotTable& B, int run_b, cudaStream_t st);
+// launch_bucket then launch_subslots_pair, in one launch
+cudaError_t launch_bucket_tables(const int32_t* idx, int T, int k, int E, int32_t* offsets,
+                                 int32_t* perm, int split, const SubslotTable& A, int run_a,
+                                 const SubslotTable& B, int run_b, cudaStream_t st);
 
 // formats
 cudaError_t launch_pack(int fmt, const uint8_t* codes, int rows, int cols, uint32_t* packed,

@@ -37,6 +37,22 @@ __global__ void __launch_bounds__(1024) k_bucket(const int32_t* __restrict__ idx
   bucket_cta(idx, N, E, offsets, perm, S);
 }
 
+// k_bucket followed, in the same block, by the two tables of k_subslots_pair
+// (the offsets it reads are the block's own writes, visible after the
+// barrier).
+__global__ void __launch_bounds__(1024) k_bucket_tables(const int32_t* __restrict__ idx, int N,
+                                                        int E, int32_t* __restrict__ offsets,
+                                                        int32_t* __restrict__ perm, int split,
+                                                        SubslotTable A, int run_a, SubslotTable B,
+                                                        int run_b) {
+  __shared__ BucketSmem S;
+  __shared__ int wcount[8];
+  bucket_cta(idx, N, E, offsets, perm, S);
+  __syncthreads();
+  subslots_cta(offsets, E, A.n, A.e, A.off, A.cnt, wcount, run_a, split, 1 << 30);
+  subslots_cta(offsets, E, B.n, B.e, B.off, B.cnt, wcount, run_b, 0, split);
+}
+
 __global__ void __launch_bounds__(256) k_subslots(const int32_t* __restrict__ offsets, int E,
                                                   int* nss, int* se, int* so, int* sc,
                                                   int run, int cmin, int cmax) {
@@ -360,6 +376,13 @@ cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offs
 cudaError_t launch_subslots(const int32_t* offsets, int E, int* nss, int* se, int* so, int* sc,
                             cudaStream_t st, int run, int cmin, int cmax) {
   k_subslots<<<1, 256, 0, st>>>(offsets, E, nss, se, so, sc, run, cmin, cmax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bucket_tables(const int32_t* idx, int T, int k, int E, int32_t* offsets,
+                                 int32_t* perm, int split, const SubslotTable& A, int run_a,
+                                 const SubslotTable& B, int run_b, cudaStream_t st) {
+  k_bucket_tables<<<1, 1024, 0, st>>>(idx, T * k, E, offsets, perm, split, A, run_a, B, run_b);
   return cudaGetLastError();
 }
 
