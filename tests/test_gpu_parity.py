@@ -658,6 +658,54 @@ def test_prefill_graph_capture_with_side_stream(capi):
     assert capi.moe_get_device_status(g.ws) == 0
 
 
+def test_prefill_standalone_calls_equal_the_layer(capi):
+    """moe_route, moe_shared_expert and moe_experts_forward above 32 tokens
+    (the standalone prefill flow: its own tables launch and activation pass,
+    the light experts on the side stream) give the layer's bits; the layer
+    builds its tables in the bucket launch and folds the shared expert into
+    the routed experts' GEMM launches."""
+    torch = Hn.torch()
+    L = synth.gen_layer(T=300, E=64, k=4, H=256, I=128, expert_fmt="affine4_g64",
+                        shared_fmt="affine4_g64", gate_fmt="affine8_g64", zipf=True, seed=47)
+    g = Hn.GpuLayer(L)
+    out, idx, w = g.forward()
+    r = g.route()
+    assert torch.equal(r["idx"], idx) and torch.equal(r["w"], w)
+    ysh = torch.empty((L.T, L.H), dtype=torch.float32, device="cuda")
+    capi.moe_shared_expert(g.shared, g.x, ysh, g.ws)
+    out2 = torch.empty_like(out)
+    capi.moe_experts_forward(g.experts, g.x, L.k, r["idx"], r["w"], r["offsets"], r["perm"], ysh,
+                             r["sg"], out2, 0, g.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, out)
+    ref = Hn.oracle_layer(L, idx_override=idx.cpu().numpy())
+    Hn.assert_layer_close(Hn.to_np(out2), ref["out"], out_type=L.act)
+    assert capi.moe_get_device_status(g.ws) == 0
+
+
+def test_prefill_range_status(capi):
+    """The prefill form's operands are fp16: a bf16 activation beyond fp16's
+    range (2^17 here) sets MOE_ERR_RANGE in the workspace status word; the
+    decode form of the same tokens does not, and after the workspace is
+    re-initialised an in-range call reads 0."""
+    torch = Hn.torch()
+    L = synth.gen_layer(T=40, E=8, k=2, H=256, I=128, expert_fmt="affine4_g64", seed=48)
+    g = Hn.GpuLayer(L)
+    out, _, _ = g.forward()
+    assert capi.moe_get_device_status(g.ws) == 0
+    xbig = g.x.clone()
+    xbig[3, 5] = 131072.0
+    g.forward(xbig)
+    torch.cuda.synchronize()
+    assert capi.moe_get_device_status(g.ws) == 7  # MOE_ERR_RANGE
+    capi.moe_workspace_init(g.ws)
+    g.forward(xbig[:32].contiguous())  # the decode form (T <= 32): no fp16 operands
+    assert capi.moe_get_device_status(g.ws) == 0
+    out2, _, _ = g.forward()
+    assert capi.moe_get_device_status(g.ws) == 0
+    assert torch.equal(out2, out)
+
+
 def test_prefill_full_size(capi):
     """The 512-token prefill window at full size (E=256, hidden 2048, inter
     512, Zipf routing, shared expert): every output of every token against the
