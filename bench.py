@@ -34,8 +34,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "decode8_affine4_shared_zipf"
+# A sweep runs a prompt of `windows` x T tokens of a base workload as that
+# many consecutive layer calls of T tokens (one step = the whole prompt).
+SWEEPS = {"prefill4096_affine4_zipf_sweep": ("prefill512_affine4_zipf", 8)}
 OTHER_WORKLOADS = ["decode1_affine4", "decode4_affine3", "decode32_w4a16",
-                   "prefill512_affine4_zipf"]
+                   "prefill512_affine4_zipf", "prefill4096_affine4_zipf_sweep"]
 E, K_TOP, H, I = 256, 8, 2048, 512
 
 
@@ -282,47 +285,65 @@ def launches_per_step(cfg: dict, T: int) -> int:
     return 4 + 1 + 2 + 2 + 1
 
 
+def workload_cfg(name: str):
+    """(config of one layer call, tokens per call, calls per step) of a
+    workload or a sweep."""
+    from bit_affine_quantized_fp32_gb300 import synth
+    base, nwin = SWEEPS.get(name, (name, 1))
+    cfg = dict(synth.WORKLOADS[base])
+    return cfg, cfg["T"], nwin
+
+
 def measure(name: str, steps: int, warmup: int, nbanks: int, ws_world: int, rank: int,
             device, keep: bool = False) -> dict:
-    """Time `steps` layer calls of workload `name` (after `warmup`), device-only
-    and end to end; returns the figures of one JSON line (and, with keep, the
-    banks and inputs for the CPU baseline)."""
+    """Time `steps` steps of workload `name` (after `warmup`), device-only and
+    end to end; a step is one layer call, or for a sweep the prompt's
+    consecutive calls.  Returns the figures of one JSON line (and, with keep,
+    the banks and inputs for the CPU baseline)."""
     import torch
     from bit_affine_quantized_fp32_gb300 import capi, synth
 
-    cfg = dict(synth.WORKLOADS[name])
-    T = cfg["T"]
+    cfg, Tw, nwin = workload_cfg(name)
+    T = Tw * nwin                     # tokens per step
     act = cfg["act"]
     banks = [Bank(cfg, b, device) for b in range(nbanks)]
     n_in = 16
     xs = [synth.device_x(T, H, act, 500 + 31 * i + rank, device) for i in range(n_in)]
-    wsb = capi.moe_workspace_bytes(T, E, K_TOP, H, I)
+    wsb = capi.moe_workspace_bytes(Tw, E, K_TOP, H, I)
     ws = torch.empty(wsb, dtype=torch.uint8, device=device)
     capi.moe_workspace_init(ws)
     out = torch.empty((T, H), dtype=xs[0].dtype, device=device)
 
     def step(i, x=None, o=None):
         bk = banks[i % len(banks)]
-        capi.moe_layer_forward(bk.router, bk.bias, bk.gate, bk.experts, bk.shared,
-                               xs[i % n_in] if x is None else x, K_TOP,
-                               out if o is None else o, None, None, 0, ws)
+        xx = xs[i % n_in] if x is None else x
+        oo = out if o is None else o
+        for w in range(nwin):  # consecutive windows of the prompt, one workspace
+            capi.moe_layer_forward(bk.router, bk.bias, bk.gate, bk.experts, bk.shared,
+                                   xx[w * Tw:(w + 1) * Tw], K_TOP, oo[w * Tw:(w + 1) * Tw],
+                                   None, None, 0, ws)
 
-    # experts touched per (bank, batch): from the library's own routing
+    # experts touched per (bank, batch, window): from the library's own routing
     pairs = math.lcm(len(banks), n_in)
-    U = []
-    offs = torch.empty(E + 1, dtype=torch.int32, device=device)
-    perm = torch.empty(T * K_TOP, dtype=torch.int32, device=device)
-    idx = torch.empty((T, K_TOP), dtype=torch.int32, device=device)
-    wt = torch.empty((T, K_TOP), dtype=torch.float32, device=device)
-    for i in range(pairs):
-        bk = banks[i % len(banks)]
-        capi.moe_route(bk.router, bk.bias, bk.gate, xs[i % n_in], K_TOP, None, idx, wt, None,
-                       offs, perm, ws)
-        U.append(int((offs[1:] - offs[:-1] > 0).sum().item()))
     eb = expert_bytes(cfg["expert_fmt"])
     fixed = (matrix_bytes(cfg["router_fmt"], E, H) + matrix_bytes(cfg["gate_fmt"], 1, H) +
-             (expert_bytes(cfg["shared_fmt"]) if cfg["shared_fmt"] else 0) + 2 * T * H * 2)
-    step_bytes = [u * eb + fixed for u in U]
+             (expert_bytes(cfg["shared_fmt"]) if cfg["shared_fmt"] else 0) + 2 * Tw * H * 2)
+    U = []
+    step_bytes = []
+    offs = torch.empty(E + 1, dtype=torch.int32, device=device)
+    perm = torch.empty(Tw * K_TOP, dtype=torch.int32, device=device)
+    idx = torch.empty((Tw, K_TOP), dtype=torch.int32, device=device)
+    wt = torch.empty((Tw, K_TOP), dtype=torch.float32, device=device)
+    for i in range(pairs):
+        bk = banks[i % len(banks)]
+        sb = 0
+        for w in range(nwin):
+            capi.moe_route(bk.router, bk.bias, bk.gate, xs[i % n_in][w * Tw:(w + 1) * Tw], K_TOP,
+                           None, idx, wt, None, offs, perm, ws)
+            u = int((offs[1:] - offs[:-1] > 0).sum().item())
+            U.append(u)
+            sb += u * eb + fixed
+        step_bytes.append(sb)
 
     def bytes_for(n):
         return sum(step_bytes[i % pairs] for i in range(n))
@@ -465,13 +486,13 @@ def measure(name: str, steps: int, warmup: int, nbanks: int, ws_world: int, rank
     else:
         tf = float(peaks.get("bf16_tflops", 1900.0))
         tf_sus = float(peaks.get("bf16_tflops_sustained", tf))
-        fl = step_flops(cfg, T)
+        fl = step_flops(cfg, Tw) * nwin
         tfs = fl / (step_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(tfs, 2), "peak": tf, "unit": "TFLOP/s",
                 "frac": round(tfs / tf, 4), "frac_of_sustained": round(tfs / tf_sus, 4),
                 "traffic": captured_traffic(name),
-                "kernel": "whole step (all launches of one layer call; the tcgen05 expert "
-                          "GEMMs lead)",
+                "kernel": "whole step (all launches of the step's layer calls; the tcgen05 "
+                          "expert GEMMs lead)",
                 "peak_source": "measured" if "bf16_tflops" in peaks else "fallback",
                 "target_frac": 0.50, "algorithmic_flops_per_step": fl,
                 "hbm": {"achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
@@ -484,7 +505,7 @@ def measure(name: str, steps: int, warmup: int, nbanks: int, ws_world: int, rank
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
                 "copies": "pinned host x in and out back every step, on two copy streams "
                           "overlapping the neighbouring steps' layer calls"},
-        "gpu_launches": launches_per_step(cfg, T) * steps,
+        "gpu_launches": launches_per_step(cfg, Tw) * nwin * steps,
         "clocks": clk,
         "config": {"workload": name, "tokens": T, "experts": E, "top_k": K_TOP,
                    "hidden": H, "inter": I, "expert_fmt": cfg["expert_fmt"],
@@ -495,6 +516,9 @@ def measure(name: str, steps: int, warmup: int, nbanks: int, ws_world: int, rank
                        len(banks), len(banks) * (E * eb + fixed) / 1e9),
                    "experts_touched_mean": round(float(np.mean(U)), 2)},
     }
+    if nwin > 1:
+        res["config"]["tokens_per_call"] = Tw
+        res["config"]["calls_per_step"] = nwin
     if keep:
         res["banks"], res["xs"] = banks, xs
     else:
@@ -505,7 +529,11 @@ def measure(name: str, steps: int, warmup: int, nbanks: int, ws_world: int, rank
     return res
 
 
-def metric_name(T: int, fmt: str) -> str:
+def metric_name(T: int, fmt: str, name: str = "") -> str:
+    if name in SWEEPS:
+        _, nwin = SWEEPS[name]
+        return "MoE-layer tokens/s (prefill sweep of %d tokens in %d-token windows, %s)" % (
+            T, T // nwin, fmt)
     return "MoE-layer tokens/s (%s %d, %s)" % ("decode batch" if T <= 32 else "prefill window",
                                                T, fmt)
 
@@ -537,11 +565,10 @@ def run_gpu(args, ws_world, rank, local):
     for name in ([] if args.also == "none" else args.also.split(",")):
         if name == args.workload or not name:
             continue
-        T = int(__import__("bit_affine_quantized_fp32_gb300.synth",
-                           fromlist=["WORKLOADS"]).WORKLOADS[name]["T"])
-        n = args.other_steps if T <= 32 else max(64, args.other_steps // 4)
+        _, Tw, nwin = workload_cfg(name)
+        n = args.other_steps if Tw <= 32 else max(64, args.other_steps // (4 * nwin))
         r = measure(name, n, args.warmup, args.banks, ws_world, rank, device)
-        others[name] = {"metric": metric_name(r["T"], r["cfg"]["expert_fmt"]),
+        others[name] = {"metric": metric_name(r["T"], r["cfg"]["expert_fmt"], name),
                         "value": round(r["value"], 1), "unit": "tokens/s",
                         "ms_per_step": round(r["ms_per_step"], 6), "steps": n,
                         "dtype": dtype_of(r["T"], r["cfg"]["act"]),
@@ -550,7 +577,7 @@ def run_gpu(args, ws_world, rank, local):
                         "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
                         "config": r["config"]}
     line = {
-        "metric": metric_name(head["T"], head["cfg"]["expert_fmt"]),
+        "metric": metric_name(head["T"], head["cfg"]["expert_fmt"], head["name"]),
         "value": round(head["value"], 1),
         "unit": "tokens/s",
         "n_gpus": ws_world,
@@ -652,8 +679,7 @@ def run_reference(args, ws_world, rank, local):
     is not used."""
     import torch
     from bit_affine_quantized_fp32_gb300 import synth
-    cfg = dict(synth.WORKLOADS[args.workload])
-    T = cfg["T"]
+    cfg, T, _ = workload_cfg(args.workload)  # a sweep's oracle sample: tokens of one window
     have_gpu = torch.cuda.is_available()
     device = torch.device("cuda", local) if have_gpu else torch.device("cpu")
     if have_gpu:

@@ -117,3 +117,15 @@ def test_clock_record_parsing():
     assert r["reasons"] == ["sw_thermal_slowdown"] and r["sm_mhz"] == (1500 + 2070) / 2
     assert bench.parse_clock_lines([]) == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
                                            "samples": 0}
+
+
+def test_sweep_workload_is_consecutive_windows():
+    # the 4096-token prompt of the prefill configuration: eight consecutive
+    # 512-token layer calls per step, reported beside the other workloads
+    cfg, Tw, nwin = bench.workload_cfg("prefill4096_affine4_zipf_sweep")
+    assert (Tw, nwin) == (512, 8) and cfg["expert_fmt"] == "affine4_g64" and cfg["zipf"]
+    assert "prefill4096_affine4_zipf_sweep" in bench.OTHER_WORKLOADS
+    assert bench.workload_cfg("decode8_affine4_shared_zipf")[1:] == (8, 1)
+    assert bench.metric_name(4096, "affine4_g64", "prefill4096_affine4_zipf_sweep") == (
+        "MoE-layer tokens/s (prefill sweep of 4096 tokens in 512-token windows, affine4_g64)")
+
