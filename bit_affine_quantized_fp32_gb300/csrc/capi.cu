@@ -497,8 +497,8 @@ moe_status experts_run(const moe_expert_bank* experts, const moe_expert_bank* sh
     // tensor-core GEMMs of the others; joined before the combine
     SideStream side{};
     if (early) {
-      // the layer already built the tables with the bucket sort and started
-      // the side stream on x (prepare_x_early): hand it the tables
+      // moe_layer_forward already built the tables with the bucket sort and
+      // started the side stream on x (launch_prepare_x): hand it the tables
       side = *early;
       MOE_CUDA(cudaEventRecord(side.tables, stream), "tables event");
       MOE_CUDA(cudaStreamWaitEvent(side.s, side.tables, 0), "tables wait");

@@ -1,7 +1,8 @@
 // umma.cuh -- 5th-generation tensor core (tcgen05) helpers for sm_103a:
 // tensor-memory allocation, shared-memory matrix descriptors, the 16-bit MMA
-// with fp32 accumulation in tensor memory, its completion barrier and the
-// tensor-memory loads of the epilogue.  Inline PTX only.
+// (A from tensor memory, B from shared memory) with fp32 accumulation in
+// tensor memory, its completion barrier, and the tensor-memory stores and
+// loads around it.  Inline PTX only.
 //
 // Operand tiles live in shared memory in the K-major layout with the 128-byte
 // swizzle: a tile of 64 16-bit columns stores row r as 128 contiguous bytes
@@ -51,16 +52,6 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
          | (uint32_t(M >> 4) << 24);     // M / 16
 }
 
-// D[tmem] (+)= A * B^T over K = 16, issued by one thread.
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1 : 0)
-      : "memory");
-}
-
 // D[tmem] (+)= A[tmem] * B^T over K = 16: A from tensor memory (lane m =
 // row m, column c = K elements 2c (low half) and 2c + 1), B from shared
 // memory, issued by one thread.
@@ -104,22 +95,6 @@ __device__ __forceinline__ void tmem_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 }
 
-// 8 consecutive fp32 columns of this thread's tensor-memory lane: warp w of a
-// warpgroup reads lanes 32 (w % 4) .. + 31, thread l lane 32 (w % 4) + l.
-// taddr carries the lane base in bits 16..31 and the column in bits 0..15.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // One 16-lane x 8-column block of tensor memory from registers (shape
 // 16x256b, one repeat): thread l of the warp writes lanes L + l / 4 (r0, r1)
 // and L + 8 + l / 4 (r2, r3), columns C + 2 (l % 4) (r0, r2) and
@@ -137,8 +112,9 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's tensor-memory lane (the lane
-// rule of tmem_ld8).
+// 32 consecutive fp32 columns of this thread's tensor-memory lane: warp w of
+// a warpgroup reads lanes 32 (w % 4) .. + 31, thread l lane 32 (w % 4) + l;
+// taddr carries the lane base in bits 16..31 and the column in bits 0..15.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
