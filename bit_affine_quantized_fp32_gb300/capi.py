@@ -23,6 +23,7 @@ PACKED = ("affine8_g64", "affine4_g64", "affine3_g64", "w4a16_g128", "affine2_g6
 MOE_FLAG_FORCE_DECODE = 1
 MOE_FLAG_UNFUSED = 2
 MOE_FLAG_ROUND_BF16 = 4
+MOE_FLAG_FORCE_PREFILL = 8
 MOE_DECODE_MAX_TOKENS = 32
 
 EXPORTS = [

@@ -364,11 +364,26 @@ moe_status run_bank(const moe_expert_bank* bank, const SubSlots& ss, int max_ss,
 // the given workspace layout: activation sums -> gate/up units (SwiGLU) ->
 // down units into the two planes of the workspace's shared-expert output
 // (L.ysh); y_out (nullable) receives their sum.
-// The prefill form (tcgen05 expert GEMMs) serves T > MOE_DECODE_MAX_TOKENS
-// unless the caller forces the decode form or the shape does not fit it.
+// The prefill form (tcgen05 expert GEMMs) serves T > MOE_DECODE_MAX_TOKENS,
+// or any T with MOE_FLAG_FORCE_PREFILL, unless the caller forces the decode
+// form or the shape does not fit it.
 bool use_prefill(const moe_expert_bank* b, int T, int flags) {
-  return T > MOE_DECODE_MAX_TOKENS && !(flags & MOE_FLAG_FORCE_DECODE) && fused_format(b->fmt) &&
+  return (T > MOE_DECODE_MAX_TOKENS || (T > 0 && (flags & MOE_FLAG_FORCE_PREFILL))) &&
+         !(flags & MOE_FLAG_FORCE_DECODE) && fused_format(b->fmt) &&
          prefill_smem(geo13(b).t, 0) > 0 && prefill_smem(geo2(b).t, 1) > 0;
+}
+
+// MOE_FLAG_FORCE_PREFILL: not with MOE_FLAG_FORCE_DECODE, and only for the
+// formats the tensor-core GEMMs read.
+moe_status check_force_prefill(const moe_expert_bank* b, int flags) {
+  if (!(flags & MOE_FLAG_FORCE_PREFILL)) return MOE_OK;
+  if (flags & MOE_FLAG_FORCE_DECODE)
+    return fail(MOE_ERR_INVALID_ARG, "MOE_FLAG_FORCE_PREFILL with MOE_FLAG_FORCE_DECODE");
+  if (!fused_format(b->fmt))
+    return fail(MOE_ERR_UNSUPPORTED_FORMAT,
+                "MOE_FLAG_FORCE_PREFILL: the prefill GEMMs do not read %s experts",
+                fmt_name(b->fmt));
+  return MOE_OK;
 }
 
 // The prefill form's activation pass: the per-64-group sums of x (decode
@@ -837,8 +852,9 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
   if (T < 0) return fail(MOE_ERR_INVALID_ARG, "n_tokens=%d < 0", T);
   if (top_k < 1 || top_k > 8 || top_k > E)
     return fail(MOE_ERR_INVALID_ARG, "top_k=%d not in 1..min(8, n_experts)", top_k);
-  if (flags & ~(MOE_FLAG_FORCE_DECODE | MOE_FLAG_ROUND_BF16))
+  if (flags & ~(MOE_FLAG_FORCE_DECODE | MOE_FLAG_FORCE_PREFILL | MOE_FLAG_ROUND_BF16))
     return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if ((s = check_force_prefill(experts, flags))) return s;
   if (T == 0) return ok();
   if (!x || !topk_idx || !topk_w || !bucket_offsets || !bucket_perm || !out)
     return fail(MOE_ERR_INVALID_ARG, "x, routing and out pointers must not be NULL");
@@ -873,10 +889,13 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
   const WsLayout L = ws_layout(T, E, top_k, H, I);
   if ((s = check_ws(ws, ws_bytes, L.total))) return s;
   if (T == 0) return ok();
-  if (flags & ~(MOE_FLAG_FORCE_DECODE | MOE_FLAG_UNFUSED | MOE_FLAG_ROUND_BF16))
+  if (flags &
+      ~(MOE_FLAG_FORCE_DECODE | MOE_FLAG_FORCE_PREFILL | MOE_FLAG_UNFUSED | MOE_FLAG_ROUND_BF16))
     return fail(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if ((s = check_force_prefill(experts, flags))) return s;
   const bool rb = (flags & MOE_FLAG_ROUND_BF16) != 0;
-  if (!(flags & MOE_FLAG_UNFUSED) && T <= MOE_DECODE_MAX_TOKENS && fused_format(experts->fmt) &&
+  if (!(flags & (MOE_FLAG_UNFUSED | MOE_FLAG_FORCE_PREFILL)) && T <= MOE_DECODE_MAX_TOKENS &&
+      fused_format(experts->fmt) &&
       (!shared || fused_format(shared->fmt))) {
     // validate what moe_route / moe_experts_forward would, then one launch
     if ((s = check_hidden(H))) return s;
@@ -952,7 +971,7 @@ moe_status moe_layer_forward(const moe_qmatrix* router, const float* logit_bias,
   float* sgw = reinterpret_cast<float*>(wsp(ws, L.sgw));
   int32_t* offs = reinterpret_cast<int32_t*>(wsp(ws, L.offsets));
   int32_t* perm = reinterpret_cast<int32_t*>(wsp(ws, L.perm));
-  const int ef = flags & (MOE_FLAG_FORCE_DECODE | MOE_FLAG_ROUND_BF16);
+  const int ef = flags & (MOE_FLAG_FORCE_DECODE | MOE_FLAG_FORCE_PREFILL | MOE_FLAG_ROUND_BF16);
   const bool fold = shared && prefill_pair(experts, shared, T, ef);
   if (use_prefill(experts, T, ef) && (!shared || fold)) {
     // The prefill form in one pass over the workspace layout L: the side

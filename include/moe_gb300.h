@@ -141,6 +141,10 @@ typedef struct moe_expert_bank {
 #define MOE_FLAG_FORCE_DECODE 1   /* use the decode (grouped GEMV) form at any T */
 #define MOE_FLAG_UNFUSED 2        /* moe_layer_forward: one launch per step instead of the
                                      single persistent decode launch (same results) */
+#define MOE_FLAG_FORCE_PREFILL 8  /* use the prefill form (tcgen05 expert GEMMs) at any
+                                     T >= 1; experts in AFFINE3/4_G64 or W4A16 only
+                                     (others: MOE_ERR_UNSUPPORTED_FORMAT); not together
+                                     with MOE_FLAG_FORCE_DECODE */
 /* The engine's bf16 rounding chain ([803-gate]: router and combine checked
  * byte-equal against a host reference, weights within a bf16 step).  In
  * moe_route and moe_layer_forward: the router and shared-gate rows are
@@ -295,8 +299,8 @@ moe_status moe_shared_expert(const moe_expert_bank* shared, const void* x, int a
  * the activation type.  y_shared/shared_gate_w nullable (no shared slot when
  * y_shared is NULL; weight 1 when only shared_gate_w is NULL).
  * Routing inputs are moe_route's outputs (or any valid equivalent).
- * flags: MOE_FLAG_FORCE_DECODE, MOE_FLAG_ROUND_BF16 (weights rounded to bf16
- * before the sum).
+ * flags: MOE_FLAG_FORCE_DECODE, MOE_FLAG_FORCE_PREFILL, MOE_FLAG_ROUND_BF16
+ * (weights rounded to bf16 before the sum).
  * In the decode form every token's output row depends only on that token's
  * inputs: a row is bit-identical whatever the other rows of the call
  * ([547-win]); the prefill form (T > 32) matches it to within the layer's
@@ -311,7 +315,8 @@ moe_status moe_experts_forward(const moe_expert_bank* experts, const void* x, in
 /* The whole layer in one call: route, shared expert, routed experts, combine.
  * shared (nullable) is a one-expert bank; shared_gate nullable.
  * topk_idx/topk_w nullable outputs [T, k].
- * flags: MOE_FLAG_FORCE_DECODE, MOE_FLAG_UNFUSED, MOE_FLAG_ROUND_BF16.
+ * flags: MOE_FLAG_FORCE_DECODE, MOE_FLAG_FORCE_PREFILL, MOE_FLAG_UNFUSED,
+ * MOE_FLAG_ROUND_BF16.
  * For n_tokens <= MOE_DECODE_MAX_TOKENS the layer runs as ONE persistent
  * cooperative launch (one CTA per SM) whose phases synchronise through
  * counters in the workspace; every wait is bounded and reports

@@ -150,6 +150,23 @@ def test_route_validation(capi):
     assert rc == 1 and b"flags" in capi.lib.moe_last_error()
 
 
+def test_force_prefill_flag_validation(capi):
+    # MOE_FLAG_FORCE_PREFILL with MOE_FLAG_FORCE_DECODE is refused, and so is
+    # a format the tensor-core GEMMs do not read (checked before any launch)
+    P = 1 << 21
+
+    def call(bank, flags):
+        return capi.lib.moe_experts_forward(ctypes.byref(bank), P, 1, 4, 2, P, P, P, P, None,
+                                            None, P, flags, 1 << 24, 1 << 30, None)
+
+    rc = call(_bank("affine4_g64"), capi.MOE_FLAG_FORCE_PREFILL | capi.MOE_FLAG_FORCE_DECODE)
+    assert rc == 1 and b"FORCE_DECODE" in capi.lib.moe_last_error()
+    rc = call(_bank("affine2_g64"), capi.MOE_FLAG_FORCE_PREFILL)
+    assert rc == 2 and b"AFFINE2" in capi.lib.moe_last_error()
+    rc = call(_bank("affine4_g64"), 16)  # unknown flag
+    assert rc == 1 and b"flags" in capi.lib.moe_last_error()
+
+
 def test_wait_limit_validation(capi):
     assert capi.lib.moe_workspace_set_wait_limit(None, 1 << 20, 5, None) == 3
     assert capi.lib.moe_workspace_set_wait_limit(1 << 21, 1 << 20, 1 << 31, None) == 1

@@ -706,6 +706,24 @@ def test_prefill_range_status(capi):
     assert torch.equal(out2, out)
 
 
+@pytest.mark.parametrize("name", ["decode8_affine4_shared_zipf", "decode4_affine3",
+                                  "decode32_w4a16"])
+def test_force_prefill_at_decode_sizes(capi, name):
+    """MOE_FLAG_FORCE_PREFILL runs the prefill form (tensor-core GEMMs for the
+    experts above the light threshold, the shared expert folded in) at a
+    decode batch: every output against the oracle at full size, the routing
+    equal to the decode form's."""
+    torch = Hn.torch()
+    L = synth.workload(name)
+    g = Hn.GpuLayer(L)
+    out_d, idx_d, w_d = g.forward()
+    out, idx, w = g.forward(flags=capi.MOE_FLAG_FORCE_PREFILL)
+    assert torch.equal(idx, idx_d) and torch.equal(w, w_d)
+    ref = Hn.oracle_layer(L, idx_override=idx.cpu().numpy())
+    Hn.assert_layer_close(Hn.to_np(out), ref["out"], out_type=L.act)
+    assert capi.moe_get_device_status(g.ws) == 0
+
+
 def test_prefill_full_size(capi):
     """The 512-token prefill window at full size (E=256, hidden 2048, inter
     512, Zipf routing, shared expert): every output of every token against the
